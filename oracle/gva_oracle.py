@@ -1,0 +1,199 @@
+"""FP64 CPU oracle for the gapped variable-length attention forward and its LSE merge.
+
+TEST INFRASTRUCTURE ONLY. This module is the correctness reference that the CUDA
+path is checked against. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` may import it; the library itself
+never does, and it shares no code with the library.
+
+What it computes (plain definition, FP64 throughout, bf16 inputs widened exactly):
+
+cosmos-framework PR #302 ("fix(mot): gapped replay on GPUs FlashAttention-4 has no
+kernels for (sm120)"), section "What": every segment ``b`` has query rows
+``cu_q[b] .. cu_q[b+1]`` and key rows ``cu_k[b] .. cu_k[b+1]``; only the first
+``used_q[b]`` query rows attend, and only to the first ``used_k[b]`` keys. Rows past
+a segment's used length are left as they are; a segment with no keys gets a zero
+output and a log-sum-exp of -inf. Its "Tests" section names the check used here:
+a per-segment FP64 reference.
+
+For query head ``h`` of a row ``r < cu_q[b] + used_q[b]`` (KV head ``h // (Hq/Hkv)``,
+the contiguous GQA grouping):
+
+    x_j   = s * <Q[r, h], K[cu_k[b] + j, h_kv]>      for j < used_k[b]
+    M     = max_j x_j,   l = sum_j exp(x_j - M)
+    O[r,h]= sum_j exp(x_j - M) V[cu_k[b] + j, h_kv] / l
+    LSE[h, r] = M + ln l                             (natural log of scaled logits)
+
+with ``s = 1/sqrt(d)`` unless given. Zero-padded keys are never part of the sum:
+each one would add exp(0) = 1 to ``l`` (TensorRT-LLM issue #18687, "actual
+behavior").
+
+The LSE merge (cosmos-framework PR #312, "Problem and behavior": visibility
+partitions combined by an FP32 LSE merge) combines partial results of disjoint key
+sets of the same query rows:
+
+    L = max_p lse_p;   if L = -inf:  O = 0, lse = -inf
+    else  w_p = exp(lse_p - L),  lse = L + ln sum_p w_p,  O = sum_p w_p O_p / sum_p w_p
+
+Score blocks are sized from a byte budget rather than a fixed row count (the
+review of PR #302 on the FP32 fallback's score block), so long segments do not
+materialise a huge score matrix.
+
+Every function here is pinned by ``tests/test_oracle.py`` against brute force,
+closed forms, library routines and invariants.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional, Sequence
+
+import numpy as np
+
+__all__ = ["attention_forward", "attention_rows", "lse_merge", "used_flops"]
+
+DEFAULT_BUDGET_BYTES = 1 << 30
+
+
+def _as_f64(x) -> np.ndarray:
+    if hasattr(x, "detach"):  # a torch tensor: widen through float32 (exact for bf16)
+        x = x.detach().cpu().float().numpy()
+    return np.asarray(x)
+
+
+def used_flops(used_q, used_k, num_heads_q: int, head_dim: int) -> float:
+    """Useful FLOPs: 2*d per score for QK^T and 2*d per score for PV."""
+    uq = np.asarray(used_q, np.float64)
+    uk = np.asarray(used_k, np.float64)
+    return 4.0 * head_dim * num_heads_q * float(np.sum(uq * uk))
+
+
+def _segment_attention(qs: np.ndarray, ks: np.ndarray, vs: np.ndarray, scale: float,
+                       budget_bytes: int):
+    """Softmax attention of ``qs`` [n, d] over ``ks``/``vs`` [m, d], FP64, m >= 1.
+
+    Returns (O [n, d], LSE [n]). The score block holds at most ``budget_bytes``."""
+    n, m = qs.shape[0], ks.shape[0]
+    rows = max(1, int(budget_bytes) // (8 * max(m, 1)))
+    o = np.empty((n, vs.shape[1]), np.float64)
+    lse = np.empty(n, np.float64)
+    kt = ks.T
+    for r0 in range(0, n, rows):
+        r1 = min(n, r0 + rows)
+        x = (qs[r0:r1] @ kt) * scale  # [rows, m]
+        mx = x.max(axis=1)
+        e = np.exp(x - mx[:, None])
+        l = e.sum(axis=1)
+        o[r0:r1] = (e @ vs) / l[:, None]
+        lse[r0:r1] = mx + np.log(l)
+    return o, lse
+
+
+def attention_forward(q, k, v, cu_q, used_q, cu_k, used_k, *, scale: Optional[float] = None,
+                      out=None, lse=None, num_heads_kv: Optional[int] = None,
+                      budget_bytes: int = DEFAULT_BUDGET_BYTES, segments: Optional[Sequence[int]] = None):
+    """Gapped varlen attention forward over packed Q [total_q, Hq, d], K/V [total_k, Hkv, d].
+
+    ``out`` ([total_q, Hq, d]) and ``lse`` ([Hq, total_q]) give the buffers' prior
+    contents; rows past a segment's used length keep them (default: zeros). Returns
+    FP64 (out, lse). ``segments`` restricts the work to a subset of segments."""
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    total_q, hq, d = q.shape
+    hkv = k.shape[1] if num_heads_kv is None else num_heads_kv
+    if hq % hkv:
+        raise ValueError(f"Hq={hq} is not a multiple of Hkv={hkv}")
+    g = hq // hkv
+    s = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    cu_q = np.asarray(cu_q, np.int64)
+    cu_k = np.asarray(cu_k, np.int64)
+    used_q = np.asarray(used_q, np.int64)
+    used_k = np.asarray(used_k, np.int64)
+    o_out = np.zeros((total_q, hq, v.shape[2]), np.float64) if out is None else _as_f64(out).astype(np.float64, copy=True)
+    l_out = np.zeros((hq, total_q), np.float64) if lse is None else _as_f64(lse).astype(np.float64, copy=True)
+    segs = range(len(used_q)) if segments is None else segments
+    for b in segs:
+        r0, nq = int(cu_q[b]), int(used_q[b])
+        k0, nk = int(cu_k[b]), int(used_k[b])
+        if nq == 0:
+            continue
+        if nk == 0:  # keyless segment: zero output, -inf LSE on used rows only
+            o_out[r0:r0 + nq] = 0.0
+            l_out[:, r0:r0 + nq] = -np.inf
+            continue
+        for hk in range(hkv):
+            # the g query heads sharing KV head hk, folded into one row block
+            qs = q[r0:r0 + nq, hk * g:(hk + 1) * g, :].astype(np.float64).reshape(nq * g, d)
+            ks = k[k0:k0 + nk, hk, :].astype(np.float64)
+            vs = v[k0:k0 + nk, hk, :].astype(np.float64)
+            ob, lb = _segment_attention(qs, ks, vs, s, budget_bytes)
+            o_out[r0:r0 + nq, hk * g:(hk + 1) * g, :] = ob.reshape(nq, g, -1)
+            l_out[hk * g:(hk + 1) * g, r0:r0 + nq] = lb.reshape(nq, g).T
+    return o_out, l_out
+
+
+def attention_rows(q, k, v, cu_q, used_q, cu_k, used_k, rows: Sequence[int], *,
+                   scale: Optional[float] = None, num_heads_kv: Optional[int] = None,
+                   budget_bytes: int = DEFAULT_BUDGET_BYTES):
+    """The same definition evaluated for a list of global query rows (all heads).
+
+    For spot checks of launches too large to evaluate in full. Every row must be a
+    used row. Returns (O [n, Hq, d], LSE [Hq, n]) in FP64."""
+    hq, d = q.shape[1], q.shape[2]
+    hkv = k.shape[1] if num_heads_kv is None else num_heads_kv
+    g = hq // hkv
+    s = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    cu_q = np.asarray(cu_q, np.int64)
+    cu_k = np.asarray(cu_k, np.int64)
+    used_q = np.asarray(used_q, np.int64)
+    used_k = np.asarray(used_k, np.int64)
+    o = np.zeros((len(rows), hq, v.shape[2]), np.float64)
+    l = np.zeros((hq, len(rows)), np.float64)
+    for i, r in enumerate(rows):
+        b = int(np.searchsorted(cu_q, r, side="right")) - 1  # last segment starting at or before r
+        if not (cu_q[b] <= r < cu_q[b] + used_q[b]):
+            raise ValueError(f"row {r} is not a used row")
+        k0, nk = int(cu_k[b]), int(used_k[b])
+        if nk == 0:
+            l[:, i] = -np.inf
+            continue
+        for hk in range(hkv):
+            qs = _as_f64(q[r, hk * g:(hk + 1) * g, :]).astype(np.float64)
+            ks = _as_f64(k[k0:k0 + nk, hk, :]).astype(np.float64)
+            vs = _as_f64(v[k0:k0 + nk, hk, :]).astype(np.float64)
+            ob, lb = _segment_attention(qs, ks, vs, s, budget_bytes)
+            o[i, hk * g:(hk + 1) * g] = ob
+            l[hk * g:(hk + 1) * g, i] = lb
+    return o, l
+
+
+def lse_merge(outs: Sequence, lses: Sequence, cu_q, used_q, *, out=None, lse=None):
+    """Combine partial results of disjoint key partitions of the same query rows.
+
+    ``outs[p]`` is [total_q, Hq, d] and ``lses[p]`` is [Hq, total_q]. Only used rows
+    are merged; the others keep ``out`` / ``lse`` (default zeros). FP64."""
+    outs = [_as_f64(o).astype(np.float64) for o in outs]
+    lses = [_as_f64(x).astype(np.float64) for x in lses]
+    if len(outs) < 1 or len(outs) != len(lses):
+        raise ValueError("need at least one partition, with one LSE per output")
+    total_q, hq, d = outs[0].shape
+    o_out = np.zeros((total_q, hq, d), np.float64) if out is None else _as_f64(out).astype(np.float64, copy=True)
+    l_out = np.zeros((hq, total_q), np.float64) if lse is None else _as_f64(lse).astype(np.float64, copy=True)
+    cu_q = np.asarray(cu_q, np.int64)
+    used_q = np.asarray(used_q, np.int64)
+    for b in range(len(used_q)):
+        r0, r1 = int(cu_q[b]), int(cu_q[b]) + int(used_q[b])
+        if r1 == r0:
+            continue
+        ls = np.stack([x[:, r0:r1] for x in lses])  # [P, Hq, n]
+        big = ls.max(axis=0)  # [Hq, n]
+        dead = np.isneginf(big)
+        safe = np.where(dead, 0.0, big)
+        w = np.where(np.isneginf(ls), 0.0, np.exp(ls - safe[None]))  # [P, Hq, n]
+        tot = w.sum(axis=0)
+        merged_lse = np.where(dead, -np.inf, safe + np.log(np.where(dead, 1.0, tot)))
+        acc = np.zeros((r1 - r0, hq, d), np.float64)
+        for p, o in enumerate(outs):
+            wp = np.where(dead, 0.0, w[p] / np.where(dead, 1.0, tot)).T[:, :, None]  # [n, Hq, 1]
+            # a partition with zero weight (no keys for the row) contributes nothing
+            acc += np.where(wp > 0.0, wp * np.where(wp > 0.0, o[r0:r1], 0.0), 0.0)
+        o_out[r0:r1] = acc
+        l_out[:, r0:r1] = merged_lse
+    return o_out, l_out

@@ -1,0 +1,308 @@
+"""Pins for the FP64 oracle: each check ties it to something other than itself.
+
+* brute force on tiny inputs (pure-Python scalar loops with ``math.fsum``);
+* closed forms: all-zero keys, a single key, the dilution worked example;
+* exact special cases: keyless segments, untouched gap rows, pad invariance;
+* a library routine: equal-length gap-free segments against
+  ``torch.nn.functional.scaled_dot_product_attention`` in float64;
+* invariants: GQA = repeated K/V, key permutation, merge of disjoint key
+  partitions = attention over their union.
+
+``test_pins_catch_planted_mistakes`` plants plausible mistakes in a copy of the
+oracle's source and checks that at least one pin fails for each.
+"""
+import inspect
+import json
+import math
+import os
+import types
+
+import numpy as np
+import pytest
+import torch
+
+from gapped_varlen_attention_gb300 import workloads as W
+from oracle import gva_oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ------------------------------------------------------------------------------------
+# Independent brute force: scalar Python, no numpy arithmetic.
+# ------------------------------------------------------------------------------------
+
+def brute_force(q, k, v, cu_q, used_q, cu_k, used_k, scale, fill_o, fill_l):
+    total_q, hq, d = q.shape
+    hkv = k.shape[1]
+    g = hq // hkv
+    o = [[[fill_o for _ in range(d)] for _ in range(hq)] for _ in range(total_q)]
+    l = [[fill_l for _ in range(total_q)] for _ in range(hq)]
+    for b in range(len(used_q)):
+        for i in range(int(used_q[b])):
+            r = int(cu_q[b]) + i
+            for h in range(hq):
+                hk = h // g
+                keys = range(int(cu_k[b]), int(cu_k[b]) + int(used_k[b]))
+                if len(keys) == 0:
+                    o[r][h] = [0.0] * d
+                    l[h][r] = -math.inf
+                    continue
+                x = [scale * math.fsum(float(q[r, h, t]) * float(k[j, hk, t]) for t in range(d)) for j in keys]
+                m = max(x)
+                e = [math.exp(xi - m) for xi in x]
+                den = math.fsum(e)
+                o[r][h] = [math.fsum(e[n] * float(v[j, hk, t]) for n, j in enumerate(keys)) / den for t in range(d)]
+                l[h][r] = m + math.log(den)
+    return np.array(o), np.array(l)
+
+
+def _rand(rng, *shape):
+    return rng.standard_normal(shape)
+
+
+# ------------------------------------------------------------------------------------
+# Pins, parameterised on the oracle module so planted mistakes can be checked.
+# ------------------------------------------------------------------------------------
+
+def pin_bruteforce(orc):
+    rng = np.random.default_rng(7)
+    for trial in range(4):
+        hq, hkv = [(2, 1), (4, 2), (3, 3), (6, 2)][trial]
+        d = [4, 8, 5, 6][trial]
+        g = W.random_geometry(rng, 4, 5, 6, hq, hkv, d)
+        q = _rand(rng, g.total_q, hq, d)
+        k = _rand(rng, g.total_k, hkv, d)
+        v = _rand(rng, g.total_k, hkv, d)
+        scale = 0.3 + trial * 0.2
+        o_ref, l_ref = brute_force(q, k, v, g.cu_q, g.used_q, g.cu_k, g.used_k, scale, 0.5, 0.25)
+        o, l = orc.attention_forward(q, k, v, g.cu_q, g.used_q, g.cu_k, g.used_k, scale=scale,
+                                     out=np.full(q.shape, 0.5), lse=np.full((hq, g.total_q), 0.25))
+        np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(l, l_ref, rtol=0, atol=1e-12)
+
+
+def pin_default_scale(orc):
+    rng = np.random.default_rng(8)
+    g = W.random_geometry(rng, 2, 4, 5, 2, 1, 9, allow_empty=False)
+    q, k, v = _rand(rng, g.total_q, 2, 9), _rand(rng, g.total_k, 1, 9), _rand(rng, g.total_k, 1, 9)
+    o_ref, l_ref = brute_force(q, k, v, g.cu_q, g.used_q, g.cu_k, g.used_k, 1.0 / 3.0, 0.0, 0.0)
+    o, l = orc.attention_forward(q, k, v, g.cu_q, g.used_q, g.cu_k, g.used_k)
+    np.testing.assert_allclose(o, o_ref, atol=1e-12)
+    np.testing.assert_allclose(l, l_ref, atol=1e-12)
+
+
+def pin_dilution_golden(orc):
+    with open(os.path.join(GOLDEN, "dilution_worked_example.json")) as f:
+        ex = json.load(f)
+    q = np.array(ex["q"])[:, None, :]
+    k = np.array(ex["k"])[:, None, :]
+    v = np.array(ex["v"])[:, None, :]
+    cap = k.shape[0]
+    for used, eo, el in [(ex["used_k"], ex["expected_o"], ex["expected_lse_exp"]),
+                         (ex["diluted_used_k"], ex["diluted_o"], ex["diluted_lse_exp"])]:
+        o, l = orc.attention_forward(q, k, v, [0, 1], [1], [0, cap], [used], scale=ex["scale"])
+        np.testing.assert_allclose(o[0, 0], eo, rtol=0, atol=1e-14)
+        assert abs(l[0, 0] - math.log(el)) < 1e-14
+
+
+def pin_zero_keys_closed_form(orc):
+    """All used keys zero: every logit is 0, so O = mean of the used values and
+    LSE = ln(used_k), whatever the query."""
+    rng = np.random.default_rng(9)
+    for uk in [1, 3, 17]:
+        q = _rand(rng, 5, 4, 8)
+        k = np.zeros((uk + 4, 2, 8))
+        v = _rand(rng, uk + 4, 2, 8)
+        o, l = orc.attention_forward(q, k, v, [0, 5], [5], [0, uk + 4], [uk])
+        mean = v[:uk].mean(axis=0)  # [2, 8]
+        for h in range(4):
+            np.testing.assert_allclose(o[:, h, :], np.broadcast_to(mean[h // 2], (5, 8)), atol=1e-13)
+        np.testing.assert_allclose(l, math.log(uk), atol=1e-13)
+
+
+def pin_single_key(orc):
+    rng = np.random.default_rng(10)
+    q = _rand(rng, 3, 2, 6)
+    k = _rand(rng, 2, 1, 6)
+    v = _rand(rng, 2, 1, 6)
+    o, l = orc.attention_forward(q, k, v, [0, 3], [3], [0, 2], [1], scale=0.7)
+    for r in range(3):
+        for h in range(2):
+            np.testing.assert_allclose(o[r, h], v[0, 0], atol=1e-14)
+            x0 = 0.7 * math.fsum(q[r, h, t] * k[0, 0, t] for t in range(6))
+            assert abs(l[h, r] - x0) < 1e-13
+
+
+def pin_keyless_and_gap_rows(orc):
+    """The tiny workload: 7.0 sentinels survive on gap rows bit for bit; the keyless
+    segment's used rows get +0.0 and -inf."""
+    g = W.tiny()
+    q, k, v = (t.float().numpy() for t in W.make_qkv(g, 1001))
+    o0 = np.full(q.shape, W.TINY_SENTINEL)
+    l0 = np.full((g.num_heads_q, g.total_q), W.TINY_SENTINEL)
+    o, l = orc.attention_forward(q, k, v, g.cu_q, g.used_q, g.cu_k, g.used_k, out=o0, lse=l0)
+    gap = W.gap_rows(g.cu_q, g.used_q)
+    assert np.array_equal(o[gap], o0[gap]) and np.array_equal(l[:, gap], l0[:, gap])
+    r0 = int(g.cu_q[2])
+    keyless = slice(r0, r0 + int(g.used_q[2]))
+    assert np.all(o[keyless] == 0.0) and not np.any(np.signbit(o[keyless]))
+    assert np.all(np.isneginf(l[:, keyless]))
+    keyed = ~gap
+    keyed[keyless] = False
+    assert np.all(np.isfinite(o[~gap])) and np.all(np.isfinite(l[:, keyed]))
+
+
+def pin_pad_invariance(orc):
+    """Appending zero or NaN K/V rows past the used keys (growing the capacity)
+    leaves O and LSE bit-identical."""
+    rng = np.random.default_rng(11)
+    q = _rand(rng, 6, 2, 8)
+    k = _rand(rng, 5, 2, 8)
+    v = _rand(rng, 5, 2, 8)
+    base = orc.attention_forward(q, k, v, [0, 6], [6], [0, 5], [5])
+    for pad, fill in [(3, 0.0), (40, 0.0), (7, np.nan), (2, np.inf)]:
+        kp = np.concatenate([k, np.full((pad, 2, 8), fill)])
+        vp = np.concatenate([v, np.full((pad, 2, 8), fill)])
+        got = orc.attention_forward(q, kp, vp, [0, 6], [6], [0, 5 + pad], [5])
+        assert np.array_equal(got[0], base[0]) and np.array_equal(got[1], base[1])
+
+
+def pin_sdpa_equal_lengths(orc):
+    """Equal-length, gap-free segments are a dense batch: compare with PyTorch's
+    float64 scaled_dot_product_attention (GQA via enable_gqa)."""
+    rng = np.random.default_rng(12)
+    B, L, S, hq, hkv, d = 3, 7, 9, 6, 2, 16
+    q = _rand(rng, B * L, hq, d)
+    k = _rand(rng, B * S, hkv, d)
+    v = _rand(rng, B * S, hkv, d)
+    cu_q = np.arange(B + 1) * L
+    cu_k = np.arange(B + 1) * S
+    o, _ = orc.attention_forward(q, k, v, cu_q, [L] * B, cu_k, [S] * B, scale=0.2)
+    tq = torch.from_numpy(q).view(B, L, hq, d).transpose(1, 2)
+    tk = torch.from_numpy(k).view(B, S, hkv, d).transpose(1, 2)
+    tv = torch.from_numpy(v).view(B, S, hkv, d).transpose(1, 2)
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=0.2, enable_gqa=True)
+    np.testing.assert_allclose(o, ref.transpose(1, 2).reshape(B * L, hq, d).numpy(), atol=1e-12)
+
+
+def pin_gqa_repeat(orc):
+    rng = np.random.default_rng(13)
+    g = W.random_geometry(rng, 3, 6, 7, 6, 3, 5, allow_empty=False)
+    q = _rand(rng, g.total_q, 6, 5)
+    k = _rand(rng, g.total_k, 3, 5)
+    v = _rand(rng, g.total_k, 3, 5)
+    a = orc.attention_forward(q, k, v, g.cu_q, g.used_q, g.cu_k, g.used_k)
+    b = orc.attention_forward(q, np.repeat(k, 2, axis=1), np.repeat(v, 2, axis=1),
+                              g.cu_q, g.used_q, g.cu_k, g.used_k)
+    np.testing.assert_allclose(a[0], b[0], atol=1e-13)
+    np.testing.assert_allclose(a[1], b[1], atol=1e-13)
+
+
+def pin_key_permutation(orc):
+    rng = np.random.default_rng(14)
+    q = _rand(rng, 4, 2, 8)
+    k = _rand(rng, 9, 1, 8)
+    v = _rand(rng, 9, 1, 8)
+    a = orc.attention_forward(q, k, v, [0, 4], [4], [0, 9], [7])
+    perm = np.concatenate([rng.permutation(7), np.arange(7, 9)])
+    b = orc.attention_forward(q, k[perm], v[perm], [0, 4], [4], [0, 9], [7])
+    np.testing.assert_allclose(a[0], b[0], atol=1e-13)
+    np.testing.assert_allclose(a[1], b[1], atol=1e-13)
+
+
+def pin_merge_union(orc):
+    """Attention over disjoint key partitions, merged, equals attention over the union;
+    a keyless partition makes the merge the identity; all-keyless gives 0 / -inf."""
+    rng = np.random.default_rng(15)
+    g = W.random_geometry(rng, 5, 8, 12, 4, 2, 8, allow_empty=False)
+    q = _rand(rng, g.total_q, 4, 8)
+    k = _rand(rng, g.total_k, 2, 8)
+    v = _rand(rng, g.total_k, 2, 8)
+    # split strictly inside where possible, and one segment entirely on each side
+    sigma = np.array([rng.integers(1, u) if u >= 2 else u for u in g.used_k])
+    sigma[0], sigma[1] = 0, g.used_k[1]
+    assert np.any((sigma > 0) & (sigma < g.used_k))
+    parts = W.split_keys(g, sigma)
+    res = [orc.attention_forward(q, k, v, p.cu_q, p.used_q, p.cu_k, p.used_k) for p in parts]
+    union = orc.attention_forward(q, k, v, g.cu_q, g.used_q, g.cu_k, g.used_k)
+    o, l = orc.lse_merge([r[0] for r in res], [r[1] for r in res], g.cu_q, g.used_q)
+    np.testing.assert_allclose(o, union[0], atol=1e-12)
+    assert np.array_equal(np.isneginf(l), np.isneginf(union[1]))
+    fin = np.isfinite(union[1])
+    np.testing.assert_allclose(l[fin], union[1][fin], atol=1e-12)
+    # a keyless partition: identity, bit for bit
+    empty = g.with_keys(g.cu_k, np.zeros_like(g.used_k))
+    e = orc.attention_forward(q, k, v, empty.cu_q, empty.used_q, empty.cu_k, empty.used_k)
+    o2, l2 = orc.lse_merge([union[0], e[0]], [union[1], e[1]], g.cu_q, g.used_q)
+    used = ~W.gap_rows(g.cu_q, g.used_q)
+    assert np.array_equal(o2[used], union[0][used]) and np.array_equal(l2[:, used], union[1][:, used])
+    o3, l3 = orc.lse_merge([e[0], e[0]], [e[1], e[1]], g.cu_q, g.used_q)
+    assert np.all(o3[used] == 0.0) and np.all(np.isneginf(l3[:, used]))
+
+
+def pin_rows_match(orc):
+    g = W.tiny()
+    q, k, v = (t.float().numpy() for t in W.make_qkv(g, 1001))
+    o, l = orc.attention_forward(q, k, v, g.cu_q, g.used_q, g.cu_k, g.used_k)
+    rows = [0, 39, 48, 64, 96, 107]
+    o2, l2 = orc.attention_rows(q, k, v, g.cu_q, g.used_q, g.cu_k, g.used_k, rows)
+    assert np.array_equal(o2, o[rows]) and np.array_equal(l2, l[:, rows])
+
+
+PINS = [pin_bruteforce, pin_default_scale, pin_dilution_golden, pin_zero_keys_closed_form,
+        pin_single_key, pin_keyless_and_gap_rows, pin_pad_invariance, pin_sdpa_equal_lengths,
+        pin_gqa_repeat, pin_key_permutation, pin_merge_union, pin_rows_match]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
+def test_oracle_pin(pin):
+    pin(gva_oracle)
+
+
+def test_budgeted_blocks_agree():
+    """A tiny score-block budget (one row per block) gives the same result."""
+    g = W.tiny()
+    q, k, v = (t.float().numpy() for t in W.make_qkv(g, 1001))
+    a = gva_oracle.attention_forward(q, k, v, g.cu_q, g.used_q, g.cu_k, g.used_k)
+    b = gva_oracle.attention_forward(q, k, v, g.cu_q, g.used_q, g.cu_k, g.used_k, budget_bytes=8)
+    np.testing.assert_allclose(a[0], b[0], atol=1e-13)
+    np.testing.assert_allclose(a[1], b[1], atol=1e-13)
+
+
+# ------------------------------------------------------------------------------------
+# Planted mistakes: each must be caught by at least one pin.
+# ------------------------------------------------------------------------------------
+
+MUTANTS = {
+    "dropped_scale": ("x = (qs[r0:r1] @ kt) * scale", "x = (qs[r0:r1] @ kt)"),
+    "log2_lse": ("lse[r0:r1] = mx + np.log(l)", "lse[r0:r1] = mx + np.log2(l)"),
+    "no_normalisation": ("o[r0:r1] = (e @ vs) / l[:, None]", "o[r0:r1] = (e @ vs)"),
+    "pad_key_attended": ("ks = k[k0:k0 + nk, hk, :].astype", "ks = k[k0:k0 + nk + 1, hk, :].astype"),
+    "interleaved_gqa": ("qs = q[r0:r0 + nq, hk * g:(hk + 1) * g, :]", "qs = q[r0:r0 + nq, hk::hkv, :]"),
+    "gap_row_written": ("o_out[r0:r0 + nq] = 0.0", "o_out[r0:r0 + nq + 1] = 0.0"),
+    "keyless_lse_plus_inf": ("l_out[:, r0:r0 + nq] = -np.inf", "l_out[:, r0:r0 + nq] = np.inf"),
+    "transposed_lse": ("lb.reshape(nq, g).T", "lb.reshape(g, nq)"),
+    "merge_weight_sign": ("np.exp(ls - safe[None])", "np.exp(safe[None] - ls)"),
+    "sqrt_d_scale": ("1.0 / math.sqrt(d) if scale is None", "1.0 / d if scale is None"),
+}
+
+
+def _mutant(name):
+    src = inspect.getsource(gva_oracle)
+    old, new = MUTANTS[name]
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    mod = types.ModuleType(f"oracle_mutant_{name}")
+    exec(compile(src.replace(old, new), f"<mutant {name}>", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistakes(name):
+    mod = _mutant(name)
+    caught = []
+    for pin in PINS:
+        try:
+            pin(mod)
+        except Exception:  # any assertion or shape error counts as caught
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught the planted mistake {name}"
