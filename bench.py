@@ -1,0 +1,474 @@
+"""Throughput of the gapped varlen attention forward on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input: the
+forward launch(es) and, for partitioned workloads, the LSE merge. The default workload
+is the long joint video + LiDAR replay (4 segments x 32768 query rows, 65536 keys each,
+seeded used fractions; Hq=32, Hkv=8, d=128, bf16), the largest single-GPU workload.
+
+Metric: useful TFLOP/s over used rows (4 * d * Hq * sum_b used_q[b] * used_k[b] per
+launch) divided by the device time per step (CUDA events on the launching stream).
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl gva|reference] [--workload NAME]
+
+With torchrun (N > 1) every rank runs its own copy of the workload on its own GPU (the
+path shards by independent problems; there is no data-path collective), and the value
+is the total work of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "gapped-varlen attn fwd TFLOP/s (used rows) & % of GB300 BF16 peak; ms/launch"
+UNIT = "TFLOP/s"
+FWD_SOURCE = os.path.join(ROOT, "gapped_varlen_attention_gb300", "csrc", "gva_fwd.cu")
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "gva_fwd_kernel_long_replay.md")
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+# --------------------------------------------------------------------------------------
+# Workloads: each returns (description, setup(device) -> step callable, flops per step,
+# launches per step, host/device byte counts).
+# --------------------------------------------------------------------------------------
+
+def _describe(g):
+    return {"segments": g.num_segments, "total_q": g.total_q, "total_k": g.total_k,
+            "used_q": [int(x) for x in g.used_q], "used_k": [int(x) for x in g.used_k],
+            "heads_q": g.num_heads_q, "heads_kv": g.num_heads_kv, "head_dim": g.head_dim}
+
+
+class Workload:
+    """Device-resident inputs and outputs of one workload, and its step."""
+
+    def __init__(self, name: str, seed_offset: int = 0):
+        import gapped_varlen_attention_gb300 as gva
+        from gapped_varlen_attention_gb300 import workloads as W
+        self.name = name
+        self.gva = gva
+        dev = "cuda"
+        if name == "long_replay":
+            g = W.long_replay()
+            self.geoms = [g]
+            self.q, self.k, self.v = W.make_qkv(g, 1005 + seed_offset, device=dev)
+            self.parts = None
+            self.label = ("long joint video+LiDAR replay: 4 segments x 32768 q rows (used 60-100%) x 65536 keys "
+                          "(used 50-100%), Hq=32, Hkv=8, d=128, bf16, non-causal")
+        elif name == "cfg_text_cross":
+            g = W.cfg_text_cross()
+            self.geoms = [g]
+            self.q, self.k, self.v = W.make_qkv(g, 1002 + seed_offset, device=dev, k_pad_fill=0.0)
+            self.parts = None
+            self.label = "CFG B=2 text cross-attention: 2 x 4096 q rows, text keys 700 / 20 of 1024, Hq=16, Hkv=8"
+        elif name == "multiview_causal":
+            full, parts = W.multiview_causal()
+            self.geoms = parts
+            self.q, self.k, self.v = W.make_qkv(full, 1003 + seed_offset, device=dev)
+            self.parts = full
+            self.label = "multiview causal gapped replay: 7 segments, 2 visibility partitions + FP32 LSE merge"
+        elif name == "tiny":
+            g = W.tiny()
+            self.geoms = [g]
+            self.q, self.k, self.v = W.make_qkv(g, 1001 + seed_offset, device=dev)
+            self.parts = None
+            self.label = "tiny: 3 segments, Hq=4, Hkv=2, d=64"
+        else:
+            raise SystemExit(f"unknown workload {name}")
+        self.plans = [gva.Plan.from_geometry(g) for g in self.geoms]
+        g0 = self.geoms[0]
+        if self.parts is None:
+            self.out, self.lse = W.make_outputs(g0, 0.0, device=dev)
+            self.partials = None
+        else:
+            self.merge_plan = gva.Plan.from_geometry(self.parts)
+            self.out, self.lse = W.make_outputs(self.parts, 0.0, device=dev)
+            self.partials = [W.make_outputs(p, 0.0, device=dev, out_dtype=torch.float32) for p in self.geoms]
+        self.flops = float(sum(g.used_flops() for g in self.geoms))
+        self.launches_per_step = len(self.geoms) + (0 if self.parts is None else 1)
+
+    def step(self, q=None, k=None, v=None):
+        gva = self.gva
+        q = self.q if q is None else q
+        k = self.k if k is None else k
+        v = self.v if v is None else v
+        if self.partials is None:
+            gva.forward(self.plans[0], q, k, v, self.out, self.lse)
+        else:
+            for plan, (o, l) in zip(self.plans, self.partials):
+                gva.forward(plan, q, k, v, o, l)
+            gva.lse_merge(self.merge_plan, [p[0] for p in self.partials], [p[1] for p in self.partials],
+                          self.out, self.lse)
+
+    def check(self):
+        for p in self.plans:
+            self.gva.device_status(p)
+
+    def config(self):
+        geom = self.parts if self.parts is not None else self.geoms[0]
+        return {"workload": self.name, "description": self.label, **_describe(geom),
+                "useful_flops_per_step": self.flops,
+                "l2": "inputs larger than L2 (no flush needed)" if self.input_bytes() > 2 * 129e6
+                else "L2 flushed between steps (256 MB write)"}
+
+    def input_bytes(self):
+        return sum(t.numel() * t.element_size() for t in (self.q, self.k, self.v))
+
+    def output_bytes(self):
+        return self.out.numel() * self.out.element_size() + self.lse.numel() * self.lse.element_size()
+
+
+# --------------------------------------------------------------------------------------
+# Measurement helpers
+# --------------------------------------------------------------------------------------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def fwd_source_hash():
+    with open(FWD_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current forward kernel source; else None."""
+    if workload != "long_replay" or not os.path.exists(TRAFFIC_SUMMARY):
+        return None
+    text = open(TRAFFIC_SUMMARY).read()
+    h = re.search(r"kernel source sha256\[:16\]:\s*`?([0-9a-f]{16})", text)
+    t = re.search(r"dram bytes per full launch:\s*`?([0-9.eE+]+)", text)
+    if not h or not t or h.group(1) != fwd_source_hash():
+        return None
+    return float(t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[3:7]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def time_steps(fn, steps: int, stream) -> float:
+    """Device milliseconds for `steps` calls of fn, CUDA events on `stream`."""
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end)
+
+
+# --------------------------------------------------------------------------------------
+# CPU oracle timing (the reported baseline)
+# --------------------------------------------------------------------------------------
+
+def oracle_sample_rate(wl, budget_s: float, seed: int = 0):
+    """Run the FP64 oracle on a seeded sample of used rows of the workload for about
+    `budget_s` seconds; return (TFLOP/s, description, rows, seconds)."""
+    from oracle import gva_oracle
+    geoms = wl.geoms
+    rng = np.random.default_rng(seed)
+    q = wl.q.cpu()
+    k = wl.k.cpu()
+    v = wl.v.cpu()
+    done_flops = 0.0
+    rows_done = 0
+    t0 = time.perf_counter()
+    while True:
+        for g in geoms:
+            b = int(rng.choice(np.flatnonzero(g.used_q > 0)))
+            rows = [int(g.cu_q[b]) + int(x) for x in rng.integers(0, int(g.used_q[b]), size=4)]
+            gva_oracle.attention_rows(q, k, v, g.cu_q, g.used_q, g.cu_k, g.used_k, rows)
+            done_flops += 4.0 * g.head_dim * g.num_heads_q * float(g.used_k[b]) * len(rows)
+            rows_done += len(rows)
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    desc = (f"{rows_done} seeded used rows (all {geoms[0].num_heads_q} heads, every used key of their "
+            f"segment) of the {wl.name} workload, FP64 NumPy oracle")
+    return done_flops / el / 1e12, desc, rows_done, el
+
+
+# --------------------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gva", "reference"], default="gva")
+    ap.add_argument("--workload", default="long_replay",
+                    choices=["long_replay", "cfg_text_cross", "multiview_causal", "tiny"])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.warmup < 3 and args.impl == "gva":
+        args.warmup = 3
+
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    import gapped_varlen_attention_gb300 as gva
+    if rank == 0 or world == 1:
+        gva.build()
+    if dist is not None:
+        dist.barrier()
+    gva.load_library()
+
+    wl = Workload(args.workload, seed_offset=rank)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    wl.check()
+
+    flush = None
+    if wl.input_bytes() <= 2 * 129e6:
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def one():
+        if flush is not None:
+            flush.fill_(1)
+        wl.step()
+
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clocks:
+        ms = time_steps(one, args.steps, stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms_step = ms / args.steps
+    # kernel-only time of the dominant launch (the forward) over the same kind of region
+    fwd_only = lambda: wl.gva.forward(wl.plans[0], wl.q, wl.k, wl.v, *(wl.partials[0] if wl.partials else  # noqa
+                                                                       (wl.out, wl.lse)))
+    fwd_ms = time_steps(fwd_only, max(3, args.steps // 2), stream) / max(3, args.steps // 2)
+    wl.check()
+
+    # end to end through the public API: pinned host inputs -> device, step, result -> host
+    hq = [t.cpu().pin_memory() for t in (wl.q, wl.k, wl.v)]
+    dq = [torch.empty_like(t) for t in (wl.q, wl.k, wl.v)]
+    ho = torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory()
+    hl = torch.empty(wl.lse.shape, dtype=wl.lse.dtype).pin_memory()
+
+    def e2e_step():
+        for d, h in zip(dq, hq):
+            d.copy_(h, non_blocking=True)
+        wl.step(*dq)
+        ho.copy_(wl.out, non_blocking=True)
+        hl.copy_(wl.lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = time_steps(e2e_step, args.e2e_steps, stream) / args.e2e_steps
+    barrier()
+
+    t = torch.tensor([ms_step, fwd_ms, e2e_ms], dtype=torch.float64, device="cuda")
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_step, fwd_ms, e2e_ms = (float(x) for x in t.tolist())
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    sustained = args.steps * ms_step > 1000.0
+    peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    value = world * wl.flops / (ms_step * 1e-3) / 1e12
+    fwd_flops = wl.geoms[0].used_flops()
+    achieved = fwd_flops / (fwd_ms * 1e-3) / 1e12
+    traffic = recorded_traffic(args.workload)
+    cpu_rate, cpu_desc, _, _ = oracle_sample_rate(wl, args.cpu_budget_s)
+    e2e_value = world * wl.flops / (e2e_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, the pages' segment shapes)",
+        "config": {**wl.config(), "parallelism": f"replicas x{world} (independent problems per GPU)"},
+        "pct_of_bf16_peak": round(100.0 * value / world / peak, 2),
+        "roofline": {
+            "bound": "tensor",
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "kernel": "gva_fwd_kernel",
+            "ms_per_launch": round(fwd_ms, 4),
+            "peak_source": f"{peak_src} {'sustained' if sustained else 'burst'} dense bf16 (cuBLAS)",
+        },
+        "e2e": {"value": round(e2e_value, 3), "unit": UNIT,
+                "h2d_bytes_per_step": int(wl.input_bytes()), "d2h_bytes_per_step": int(wl.output_bytes()),
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": args.steps * wl.launches_per_step,
+        "clocks": clocks.summary(),
+        "cpu_baseline": {"value": round(cpu_rate, 6), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": cpu_desc},
+    }
+    print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_reference(args, world, rank):
+    """The oracle, timed as it stands on the host cores, on bounded samples of the same
+    workload: each step is a seeded sample of used rows sized to ~budget seconds."""
+    if rank != 0:
+        return
+    from gapped_varlen_attention_gb300 import workloads as W
+
+    class HostWorkload:
+        pass
+
+    wl = HostWorkload()
+    wl.name = args.workload
+    if args.workload == "long_replay":
+        g = W.long_replay()
+        wl.geoms = [g]
+        seed = 1005
+    elif args.workload == "cfg_text_cross":
+        g = W.cfg_text_cross()
+        wl.geoms = [g]
+        seed = 1002
+    elif args.workload == "multiview_causal":
+        g, parts = W.multiview_causal()
+        wl.geoms = parts
+        seed = 1003
+    else:
+        g = W.tiny()
+        wl.geoms = [g]
+        seed = 1001
+    wl.q, wl.k, wl.v = W.make_qkv(g, seed)
+    budget = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup):
+        oracle_sample_rate(wl, budget, seed=i)
+    rates, descs, secs = [], [], 0.0
+    for i in range(args.steps):
+        r, d, _, el = oracle_sample_rate(wl, budget, seed=100 + i)
+        rates.append(r)
+        descs.append(d)
+        secs += el
+    value = float(np.mean(rates))
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * secs / args.steps, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16 widened to f64)",
+        "config": {"workload": args.workload},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": descs[-1] + f"; {budget:.1f} s per step"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

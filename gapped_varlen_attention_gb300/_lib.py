@@ -1,0 +1,201 @@
+"""ctypes binding of libgva.so (include/gva.h): argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module checks
+shapes and dtypes, hands over device pointers and the current torch stream, and turns
+status codes into exceptions. There is no fallback: if the library is missing or the
+device is unsupported, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+_PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG_DIR, "libgva.so")
+
+GVA_OK, GVA_ERR_INVALID_ARG, GVA_ERR_UNSUPPORTED, GVA_ERR_CUDA, GVA_ERR_DEVICE_CHECK = range(5)
+GVA_BF16, GVA_FP32 = 0, 1
+
+# Every symbol include/gva.h declares.
+EXPORTS = ("gva_plan", "gva_forward", "gva_lse_merge", "gva_plan_destroy", "gva_plan_get_info",
+           "gva_device_status", "gva_status_string", "gva_last_error")
+
+
+class GvaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("num_segments", ctypes.c_int32), ("num_heads_q", ctypes.c_int32),
+                ("num_heads_kv", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("total_q", ctypes.c_int64), ("total_k", ctypes.c_int64),
+                ("num_work_items", ctypes.c_int32), ("num_merge_units", ctypes.c_int32),
+                ("grid_ctas", ctypes.c_int32), ("sm_count", ctypes.c_int32),
+                ("used_flops", ctypes.c_double)]
+
+
+_lib = None
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libgva.so (built by ``__graft_entry__.build()``); raises if it is absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(p)
+    i32, vp, f32 = ctypes.c_int32, ctypes.c_void_p, ctypes.c_float
+    pi32 = ctypes.POINTER(ctypes.c_int32)
+    lib.gva_plan.argtypes = [pi32, pi32, pi32, pi32, i32, i32, i32, i32, ctypes.POINTER(vp)]
+    lib.gva_forward.argtypes = [vp, vp, vp, vp, vp, i32, vp, f32, vp]
+    lib.gva_lse_merge.argtypes = [vp, i32, ctypes.POINTER(vp), i32, ctypes.POINTER(vp), vp, i32, vp, vp]
+    lib.gva_plan_destroy.argtypes = [vp]
+    lib.gva_plan_get_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
+    lib.gva_device_status.argtypes = [vp]
+    lib.gva_status_string.argtypes = [i32]
+    lib.gva_status_string.restype = ctypes.c_char_p
+    lib.gva_last_error.argtypes = []
+    lib.gva_last_error.restype = ctypes.c_char_p
+    for name in ("gva_plan", "gva_forward", "gva_lse_merge", "gva_plan_destroy", "gva_plan_get_info",
+                 "gva_device_status"):
+        getattr(lib, name).restype = i32
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(lib, status: int, what: str):
+    if status != GVA_OK:
+        name = lib.gva_status_string(status).decode()
+        detail = lib.gva_last_error().decode()
+        raise GvaError(status, f"{what}: {name}: {detail}")
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+class Plan:
+    """A validated segment geometry with its device work list (``gva_plan``)."""
+
+    def __init__(self, cu_seqlens_q, seqused_q, cu_seqlens_k, seqused_k, num_heads_q: int, num_heads_kv: int,
+                 head_dim: int):
+        self._lib = load_library()
+        self.cu_q, self.used_q = _i32(cu_seqlens_q), _i32(seqused_q)
+        self.cu_k, self.used_k = _i32(cu_seqlens_k), _i32(seqused_k)
+        n = int(self.used_q.shape[0])
+        if self.cu_q.shape[0] != n + 1 or self.cu_k.shape[0] != n + 1 or self.used_k.shape[0] != n:
+            raise ValueError("cu_seqlens must have num_segments + 1 entries and seqused num_segments")
+        ptr = ctypes.c_void_p()
+        as_p = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))  # noqa: E731
+        st = self._lib.gva_plan(as_p(self.cu_q), as_p(self.used_q), as_p(self.cu_k), as_p(self.used_k), n,
+                                int(num_heads_q), int(num_heads_kv), int(head_dim), ctypes.byref(ptr))
+        _check(self._lib, st, "gva_plan")
+        self._handle = ptr
+        self.num_heads_q, self.num_heads_kv, self.head_dim = int(num_heads_q), int(num_heads_kv), int(head_dim)
+        self.total_q, self.total_k = int(self.cu_q[-1]), int(self.cu_k[-1])
+
+    @classmethod
+    def from_geometry(cls, g) -> "Plan":
+        return cls(g.cu_q, g.used_q, g.cu_k, g.used_k, g.num_heads_q, g.num_heads_kv, g.head_dim)
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        if self._handle is None:
+            raise RuntimeError("plan was destroyed")
+        return self._handle
+
+    def info(self) -> dict:
+        inf = PlanInfo()
+        _check(self._lib, self._lib.gva_plan_get_info(self.handle, ctypes.byref(inf)), "gva_plan_get_info")
+        return {name: getattr(inf, name) for name, _ in PlanInfo._fields_}
+
+    def close(self):
+        if getattr(self, "_handle", None) is not None:
+            self._lib.gva_plan_destroy(self._handle)
+            self._handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _stream_ptr(stream) -> ctypes.c_void_p:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev_ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def forward(plan: Plan, q, k, v, out, lse, softmax_scale: float = 0.0, stream=None):
+    """``gva_forward``: write O and LSE of the used rows into ``out`` / ``lse``.
+
+    q [total_q, Hq, d] bf16, k / v [total_k, Hkv, d] bf16, out [total_q, Hq, d] bf16
+    or fp32, lse [Hq, total_q] fp32, all contiguous CUDA tensors."""
+    import torch
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise TypeError("q, k and v must be bfloat16")
+    if out.dtype not in (torch.bfloat16, torch.float32) or lse.dtype != torch.float32:
+        raise TypeError("out must be bfloat16 or float32 and lse float32")
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("lse", lse)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    hq, hkv, d = plan.num_heads_q, plan.num_heads_kv, plan.head_dim
+    if tuple(q.shape) != (plan.total_q, hq, d) or tuple(out.shape) != (plan.total_q, hq, d):
+        raise ValueError(f"q / out must be [{plan.total_q}, {hq}, {d}]")
+    if tuple(k.shape) != (plan.total_k, hkv, d) or tuple(v.shape) != (plan.total_k, hkv, d):
+        raise ValueError(f"k / v must be [{plan.total_k}, {hkv}, {d}]")
+    if tuple(lse.shape) != (hq, plan.total_q):
+        raise ValueError(f"lse must be [{hq}, {plan.total_q}]")
+    lib = plan._lib
+    st = lib.gva_forward(plan.handle, _dev_ptr(q), _dev_ptr(k), _dev_ptr(v), _dev_ptr(out),
+                         GVA_FP32 if out.dtype == torch.float32 else GVA_BF16, _dev_ptr(lse),
+                         float(softmax_scale), _stream_ptr(stream))
+    _check(lib, st, "gva_forward")
+    return out, lse
+
+
+def lse_merge(plan: Plan, outs: Sequence, lses: Sequence, out, lse, stream=None):
+    """``gva_lse_merge``: combine partial results of disjoint key sets of plan's rows."""
+    import torch
+    if len(outs) != len(lses) or not outs:
+        raise ValueError("need one LSE per partial output and at least one partition")
+    in_dtype = outs[0].dtype
+    for o, l in zip(outs, lses):
+        if o.dtype != in_dtype or o.dtype not in (torch.bfloat16, torch.float32) or l.dtype != torch.float32:
+            raise TypeError("partials must share one dtype (bf16 or fp32) with fp32 LSEs")
+        if tuple(o.shape) != (plan.total_q, plan.num_heads_q, plan.head_dim) or tuple(l.shape) != (
+                plan.num_heads_q, plan.total_q):
+            raise ValueError("partial shapes do not match the plan")
+        if not (o.is_cuda and l.is_cuda and o.is_contiguous() and l.is_contiguous()):
+            raise ValueError("partials must be contiguous CUDA tensors")
+    if tuple(out.shape) != tuple(outs[0].shape) or tuple(lse.shape) != tuple(lses[0].shape):
+        raise ValueError("out / lse shapes do not match the plan")
+    if not (out.is_cuda and lse.is_cuda and out.is_contiguous() and lse.is_contiguous()):
+        raise ValueError("out / lse must be contiguous CUDA tensors")
+    n = len(outs)
+    po = (ctypes.c_void_p * n)(*[o.data_ptr() for o in outs])
+    pl = (ctypes.c_void_p * n)(*[l.data_ptr() for l in lses])
+    lib = plan._lib
+    st = lib.gva_lse_merge(plan.handle, n, po, GVA_FP32 if in_dtype == torch.float32 else GVA_BF16, pl,
+                           _dev_ptr(out), GVA_FP32 if out.dtype == torch.float32 else GVA_BF16, _dev_ptr(lse),
+                           _stream_ptr(stream))
+    _check(lib, st, "gva_lse_merge")
+    return out, lse
+
+
+def device_status(plan: Plan):
+    """Synchronise and raise if a kernel of this plan recorded a device-side failure."""
+    _check(plan._lib, plan._lib.gva_device_status(plan.handle), "gva_device_status")

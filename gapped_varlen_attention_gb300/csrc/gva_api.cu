@@ -1,0 +1,348 @@
+// C ABI of the gapped varlen attention library: plan construction on the host, tensor
+// maps, launches, status reporting. See include/gva.h for the contract.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "gva.h"
+#include "gva_internal.h"
+
+struct gva_plan {
+  int device = -1;
+  int sm_count = 0;
+  int32_t num_segments = 0, num_heads_q = 0, num_heads_kv = 0, head_dim = 0, group = 0;
+  int64_t total_q = 0, total_k = 0;
+  int32_t num_items = 0, num_units = 0, grid = 0, merge_grid = 0;
+  double used_flops = 0.0;
+  gva::WorkItem* d_items = nullptr;
+  gva::MergeUnit* d_units = nullptr;
+  int* d_error = nullptr;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+gva_status fail(gva_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+gva_status ok() {
+  g_last_error.clear();
+  return GVA_OK;
+}
+
+gva_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(GVA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+  }
+  return fn;
+}
+
+// A 3-D bf16 tensor map over a packed [rows, heads, d] tensor, viewed as
+// (d, rows, heads) so that a box of (64, box_rows, box_heads) lands in shared memory
+// head-major: smem row = head_in_box * box_rows + row_in_box, 128 bytes per row.
+gva_status make_map(CUtensorMap* map, const void* base, int64_t rows, int32_t heads, int32_t d, uint32_t box_rows,
+                    uint32_t box_heads, const char* name) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return fail(GVA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(heads) * d * 2, static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[3] = {64, box_rows, box_heads};
+  cuuint32_t elem[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, elem,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(GVA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name, (int)r);
+  return GVA_OK;
+}
+
+gva_status validate_offsets(const int32_t* cu, const int32_t* used, int32_t n, const char* name) {
+  if (cu[0] != 0) return fail(GVA_ERR_INVALID_ARG, "cu_seqlens_%s[0] = %d, expected 0", name, cu[0]);
+  for (int32_t b = 0; b < n; ++b) {
+    if (cu[b + 1] < cu[b])
+      return fail(GVA_ERR_INVALID_ARG, "cu_seqlens_%s decreases at segment %d (%d -> %d)", name, b, cu[b], cu[b + 1]);
+    const int32_t cap = cu[b + 1] - cu[b];
+    if (used[b] < 0 || used[b] > cap)
+      return fail(GVA_ERR_INVALID_ARG, "seqused_%s[%d] = %d outside [0, capacity %d]", name, b, used[b], cap);
+  }
+  return GVA_OK;
+}
+
+void free_plan(struct gva_plan* p) {
+  if (p == nullptr) return;
+  if (p->d_items) cudaFree(p->d_items);
+  if (p->d_units) cudaFree(p->d_units);
+  if (p->d_error) cudaFree(p->d_error);
+  delete p;
+}
+
+}  // namespace
+
+extern "C" {
+
+gva_status gva_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, const int32_t* cu_seqlens_k,
+                    const int32_t* seqused_k, int32_t num_segments, int32_t num_heads_q, int32_t num_heads_kv,
+                    int32_t head_dim, gva_plan_t* out_plan) {
+  if (out_plan == nullptr) return fail(GVA_ERR_INVALID_ARG, "out_plan is NULL");
+  *out_plan = nullptr;
+  // ---- host-only validation (no CUDA call before this block passes)
+  if (num_segments < 0) return fail(GVA_ERR_INVALID_ARG, "num_segments = %d < 0", num_segments);
+  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr || (num_segments > 0 && (seqused_q == nullptr || seqused_k == nullptr)))
+    return fail(GVA_ERR_INVALID_ARG, "a geometry array is NULL");
+  if (num_heads_q <= 0 || num_heads_kv <= 0)
+    return fail(GVA_ERR_INVALID_ARG, "head counts must be positive (Hq=%d, Hkv=%d)", num_heads_q, num_heads_kv);
+  if (num_heads_q % num_heads_kv != 0)
+    return fail(GVA_ERR_INVALID_ARG, "num_heads_q=%d is not divisible by num_heads_kv=%d", num_heads_q, num_heads_kv);
+  const int32_t group = num_heads_q / num_heads_kv;
+  if (gva::kTileRows % group != 0)
+    return fail(GVA_ERR_UNSUPPORTED, "query heads per KV head (%d) must divide %d", group, gva::kTileRows);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(GVA_ERR_UNSUPPORTED, "head_dim=%d is not supported (64 or 128)", head_dim);
+  if (num_heads_q * gva::kMergeRows * gva::kMaxMergeParts * 4 > 200 * 1024)
+    return fail(GVA_ERR_UNSUPPORTED, "num_heads_q=%d is too large", num_heads_q);
+  gva_status s = validate_offsets(cu_seqlens_q, seqused_q, num_segments, "q");
+  if (s != GVA_OK) return s;
+  s = validate_offsets(cu_seqlens_k, seqused_k, num_segments, "k");
+  if (s != GVA_OK) return s;
+
+  // ---- work list: (segment, KV head, 2 x 128 folded rows), keyless items epilogue-only
+  const int32_t tokens_per_tile = gva::kTileRows / group;
+  const int32_t tokens_per_item = tokens_per_tile * gva::kTilesPerItem;
+  std::vector<gva::WorkItem> items;
+  std::vector<int64_t> cost;
+  std::vector<gva::MergeUnit> units;
+  double flops = 0.0;
+  for (int32_t b = 0; b < num_segments; ++b) {
+    const int32_t uq = seqused_q[b], uk = seqused_k[b];
+    flops += 4.0 * head_dim * num_heads_q * static_cast<double>(uq) * static_cast<double>(uk);
+    for (int32_t r0 = 0; r0 < uq; r0 += gva::kMergeRows)
+      units.push_back({cu_seqlens_q[b] + r0, std::min(gva::kMergeRows, uq - r0)});
+    const int64_t nblk = (uk + gva::kBlockKeys - 1) / gva::kBlockKeys;
+    for (int32_t hk = 0; hk < num_heads_kv; ++hk) {
+      for (int32_t t0 = 0; t0 < uq; t0 += tokens_per_item) {
+        gva::WorkItem it{};
+        it.q_row0 = cu_seqlens_q[b] + t0;
+        it.q_rows = std::min(tokens_per_item, uq - t0);
+        it.k_row0 = cu_seqlens_k[b];
+        it.k_len = uk;
+        it.head_kv = hk;
+        it.n_tiles = it.q_rows > tokens_per_tile ? 2 : 1;
+        items.push_back(it);
+        cost.push_back(nblk * it.n_tiles * 4 + it.n_tiles);
+      }
+    }
+  }
+  std::vector<int32_t> order(items.size());
+  for (size_t i = 0; i < order.size(); ++i) order[i] = static_cast<int32_t>(i);
+  std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t c) { return cost[a] > cost[c]; });
+  std::vector<gva::WorkItem> sorted(items.size());
+  for (size_t i = 0; i < order.size(); ++i) sorted[i] = items[order[i]];
+
+  // ---- device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(GVA_ERR_UNSUPPORTED, "no usable CUDA device: %s", cudaGetErrorString(e));
+  int major = 0, minor = 0, sms = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (major != 10 || minor != 3)
+    return fail(GVA_ERR_UNSUPPORTED, "this library is built for sm_103a (GB300); device %d is sm_%d%d", dev, major,
+                minor);
+
+  struct gva_plan* p = new struct gva_plan();
+  p->device = dev;
+  p->sm_count = sms;
+  p->num_segments = num_segments;
+  p->num_heads_q = num_heads_q;
+  p->num_heads_kv = num_heads_kv;
+  p->head_dim = head_dim;
+  p->group = group;
+  p->total_q = cu_seqlens_q[num_segments];
+  p->total_k = cu_seqlens_k[num_segments];
+  p->num_items = static_cast<int32_t>(sorted.size());
+  p->num_units = static_cast<int32_t>(units.size());
+  p->grid = std::min(p->num_items, sms);
+  p->merge_grid = std::min(p->num_units, sms * 8);
+  p->used_flops = flops;
+  if ((e = cudaMalloc(&p->d_error, sizeof(int))) != cudaSuccess || (e = cudaMemset(p->d_error, 0, sizeof(int))) != cudaSuccess) {
+    free_plan(p);
+    return cuda_fail(e, "allocating the plan's error word");
+  }
+  if (!sorted.empty()) {
+    if ((e = cudaMalloc(&p->d_items, sorted.size() * sizeof(gva::WorkItem))) != cudaSuccess ||
+        (e = cudaMemcpy(p->d_items, sorted.data(), sorted.size() * sizeof(gva::WorkItem), cudaMemcpyHostToDevice)) !=
+            cudaSuccess) {
+      free_plan(p);
+      return cuda_fail(e, "uploading the work list");
+    }
+  }
+  if (!units.empty()) {
+    if ((e = cudaMalloc(&p->d_units, units.size() * sizeof(gva::MergeUnit))) != cudaSuccess ||
+        (e = cudaMemcpy(p->d_units, units.data(), units.size() * sizeof(gva::MergeUnit), cudaMemcpyHostToDevice)) !=
+            cudaSuccess) {
+      free_plan(p);
+      return cuda_fail(e, "uploading the merge units");
+    }
+  }
+  *out_plan = p;
+  return ok();
+}
+
+gva_status gva_forward(gva_plan_t plan, const void* q, const void* k, const void* v, void* out, gva_dtype out_dtype,
+                       float* lse, float softmax_scale, cudaStream_t stream) {
+  if (plan == nullptr) return fail(GVA_ERR_INVALID_ARG, "plan is NULL");
+  if (out_dtype != GVA_BF16 && out_dtype != GVA_FP32) return fail(GVA_ERR_INVALID_ARG, "bad out_dtype %d", (int)out_dtype);
+  if (plan->num_items == 0) return ok();  // no used rows: nothing to write
+  // With no keys at all (every item keyless) K and V are never read and may be empty.
+  const bool has_keys = plan->total_k > 0;
+  if (!has_keys) k = v = q;
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || lse == nullptr)
+    return fail(GVA_ERR_INVALID_ARG, "a tensor pointer is NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return fail(GVA_ERR_INVALID_ARG, "q, k, v, out and lse must be 16-byte aligned");
+  if (!(softmax_scale == softmax_scale) || std::isinf(softmax_scale))
+    return fail(GVA_ERR_INVALID_ARG, "softmax_scale is not finite");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != plan->device)
+    return fail(GVA_ERR_INVALID_ARG, "the plan was built on device %d, the current device is %d", plan->device, dev);
+  const int32_t tokens_per_tile = gva::kTileRows / plan->group;
+  CUtensorMap mq, mk, mv;
+  gva_status s;
+  const int64_t krows = has_keys ? plan->total_k : 1;
+  if ((s = make_map(&mq, q, plan->total_q, plan->num_heads_q, plan->head_dim, tokens_per_tile, plan->group, "Q")) != GVA_OK)
+    return s;
+  if ((s = make_map(&mk, k, krows, plan->num_heads_kv, plan->head_dim, gva::kBlockKeys, 1, "K")) != GVA_OK) return s;
+  if ((s = make_map(&mv, v, krows, plan->num_heads_kv, plan->head_dim, gva::kBlockKeys, 1, "V")) != GVA_OK) return s;
+  const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(plan->head_dim));
+  gva::FwdParams prm{};
+  prm.items = plan->d_items;
+  prm.num_items = plan->num_items;
+  prm.out = out;
+  prm.lse = lse;
+  prm.total_q = plan->total_q;
+  prm.num_heads_q = plan->num_heads_q;
+  prm.group = plan->group;
+  prm.tokens_per_tile = tokens_per_tile;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.error_flag = plan->d_error;
+  e = gva::launch_forward(plan->head_dim, out_dtype == GVA_FP32, prm, mq, mk, mv, plan->grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launching the forward kernel");
+  return ok();
+}
+
+gva_status gva_lse_merge(gva_plan_t plan, int32_t num_parts, const void* const* outs, gva_dtype in_dtype,
+                         const float* const* lses, void* out, gva_dtype out_dtype, float* lse, cudaStream_t stream) {
+  if (plan == nullptr) return fail(GVA_ERR_INVALID_ARG, "plan is NULL");
+  if (num_parts < 1 || num_parts > gva::kMaxMergeParts)
+    return fail(GVA_ERR_INVALID_ARG, "num_parts=%d outside [1, %d]", num_parts, gva::kMaxMergeParts);
+  if ((in_dtype != GVA_BF16 && in_dtype != GVA_FP32) || (out_dtype != GVA_BF16 && out_dtype != GVA_FP32))
+    return fail(GVA_ERR_INVALID_ARG, "bad dtype");
+  if (outs == nullptr || lses == nullptr) return fail(GVA_ERR_INVALID_ARG, "outs / lses is NULL");
+  if (plan->num_units == 0) return ok();
+  gva::MergeParams prm{};
+  for (int i = 0; i < num_parts; ++i) {
+    if (outs[i] == nullptr || lses[i] == nullptr) return fail(GVA_ERR_INVALID_ARG, "partition %d has a NULL pointer", i);
+    if (!aligned16(outs[i])) return fail(GVA_ERR_INVALID_ARG, "outs[%d] must be 16-byte aligned", i);
+    if ((reinterpret_cast<uintptr_t>(lses[i]) & 3u) != 0) return fail(GVA_ERR_INVALID_ARG, "lses[%d] misaligned", i);
+    prm.outs[i] = outs[i];
+    prm.lses[i] = lses[i];
+  }
+  if (out == nullptr || lse == nullptr) return fail(GVA_ERR_INVALID_ARG, "out / lse is NULL");
+  if (!aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return fail(GVA_ERR_INVALID_ARG, "out must be 16-byte aligned and lse 4-byte aligned");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != plan->device)
+    return fail(GVA_ERR_INVALID_ARG, "the plan was built on device %d, the current device is %d", plan->device, dev);
+  prm.units = plan->d_units;
+  prm.num_units = plan->num_units;
+  prm.num_parts = num_parts;
+  prm.out = out;
+  prm.lse = lse;
+  prm.total_q = plan->total_q;
+  prm.num_heads_q = plan->num_heads_q;
+  prm.head_dim = plan->head_dim;
+  e = gva::launch_merge(in_dtype == GVA_FP32, out_dtype == GVA_FP32, prm, plan->merge_grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launching the LSE merge kernel");
+  return ok();
+}
+
+gva_status gva_plan_destroy(gva_plan_t plan) {
+  free_plan(plan);
+  return ok();
+}
+
+gva_status gva_plan_get_info(gva_plan_t plan, gva_plan_info* info) {
+  if (plan == nullptr || info == nullptr) return fail(GVA_ERR_INVALID_ARG, "plan or info is NULL");
+  info->num_segments = plan->num_segments;
+  info->num_heads_q = plan->num_heads_q;
+  info->num_heads_kv = plan->num_heads_kv;
+  info->head_dim = plan->head_dim;
+  info->total_q = plan->total_q;
+  info->total_k = plan->total_k;
+  info->num_work_items = plan->num_items;
+  info->num_merge_units = plan->num_units;
+  info->grid_ctas = plan->grid;
+  info->sm_count = plan->sm_count;
+  info->used_flops = plan->used_flops;
+  return ok();
+}
+
+gva_status gva_device_status(gva_plan_t plan) {
+  if (plan == nullptr) return fail(GVA_ERR_INVALID_ARG, "plan is NULL");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  int word = 0;
+  if ((e = cudaMemcpy(&word, plan->d_error, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "reading the device error word");
+  if (word != 0) {
+    cudaMemset(plan->d_error, 0, sizeof(int));
+    return fail(GVA_ERR_DEVICE_CHECK, "a kernel recorded device error bits 0x%x (1 = bounded wait timed out)", word);
+  }
+  return ok();
+}
+
+const char* gva_status_string(gva_status status) {
+  switch (status) {
+    case GVA_OK: return "GVA_OK";
+    case GVA_ERR_INVALID_ARG: return "GVA_ERR_INVALID_ARG";
+    case GVA_ERR_UNSUPPORTED: return "GVA_ERR_UNSUPPORTED";
+    case GVA_ERR_CUDA: return "GVA_ERR_CUDA";
+    case GVA_ERR_DEVICE_CHECK: return "GVA_ERR_DEVICE_CHECK";
+  }
+  return "GVA_UNKNOWN_STATUS";
+}
+
+const char* gva_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

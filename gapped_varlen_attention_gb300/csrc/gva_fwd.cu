@@ -1,0 +1,516 @@
+// Gapped variable-length attention forward, sm_103a.
+//
+// Computes, for every used query row of every segment and every query head, softmax
+// attention over the segment's used keys, writing O and the natural-log LSE; rows past
+// a segment's used length are not touched, and keyless segments get O = 0, LSE = -inf
+// (cosmos-framework PR #302, "What"). Keys past the used length never enter the
+// softmax (TensorRT-LLM issue #18687, "actual behavior": each attended zero key would
+// add exp(0) = 1 to the denominator).
+//
+// Design (one persistent CTA per SM, 10 warps):
+//   warp 0      TMA producer: the item's two Q tiles, then K and V blocks of 128 keys
+//               into a ring of shared-memory stages (128-byte swizzle).
+//   warp 1      TMEM allocator and MMA issuer (one thread): S_t = Q_t K^T into TMEM,
+//               O_t += P_t V with P_t read from TMEM (tcgen05 "A from TMEM" form).
+//   warps 2-5   softmax + epilogue of Q tile 0; warps 6-9 of Q tile 1. One thread owns
+//               one tile row (= one TMEM lane), so the row max and row sum are plain
+//               register reductions with no shuffles or shared memory.
+// A work item is (segment, KV head, 2 x 128 folded rows): the g = Hq/Hkv query heads
+// of one KV head are folded into the tile's rows (128/g tokens x g heads), so each K/V
+// block feeds 256 rows. Two tiles ping-pong: while the softmax warps of one tile work,
+// the tensor core runs the other tile's PV and next QK^T.
+//
+// TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 [384,384+d).
+// P_t (bf16, two per 32-bit column) overwrites the first 64 columns of S_t once S_t is
+// in registers.
+//
+// The running max is kept in log2 units of the scaled logits. O is rescaled only when
+// a row's max grows by more than 2^8 over the max its P values were computed with;
+// the final O / l and LSE use the same max, so the result is exact up to rounding.
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "gva_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace gva {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kWarpTma = 0;
+constexpr int kWarpMma = 1;
+constexpr int kFirstSoftmaxWarp = 2;
+constexpr uint32_t kTmemCols = 512;
+// TMEM column of S_t (and P_t) and of O_t.
+__host__ __device__ constexpr uint32_t col_s(int t) { return 128u * t; }
+__host__ __device__ constexpr uint32_t col_o(int t) { return 256u + 128u * t; }
+constexpr float kRescaleThreshold = 8.0f;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
+constexpr float kLn2 = 0.693147180559945309f;
+
+template <int D>
+struct Cfg {
+  static constexpr int kChunks = D / 64;                 // 128-byte rows per operand row
+  static constexpr int kQBytes = kTileRows * D * 2;      // one Q tile
+  static constexpr int kKVBytes = kBlockKeys * D * 2;    // one K or V block
+  static constexpr int kQChunkBytes = kTileRows * 128;   // one 64-column chunk of a Q tile
+  static constexpr int kKVChunkBytes = kBlockKeys * 128;
+  static constexpr int kStages = D == 64 ? 3 : 2;        // K stages; V has as many
+  static constexpr int kSmem = kTilesPerItem * kQBytes + 2 * kStages * kKVBytes;
+  static constexpr int kSmemAlloc = kSmem + 1024;        // slack for 1024-byte alignment
+  static_assert(kSmemAlloc <= 227 * 1024, "shared memory budget");
+};
+
+struct Ctrl {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Wait for the phase of `bar` with parity `parity` to complete. Gives up (returning
+// false) when another role has aborted or after kWaitLimitNs, recording the timeout.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicOr(err, kErrWaitTimeout);
+      return false;
+    }
+  }
+}
+
+// Same, ignoring the abort flag: used to drain copies and MMAs already in flight.
+__device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, int* err) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(err, kErrWaitTimeout);
+      return;
+    }
+  }
+}
+
+// Persistent schedule: the items are sorted by decreasing cost; CTA c takes item
+// r * grid + c in even rounds and r * grid + (grid - 1 - c) in odd ones.
+__device__ __forceinline__ int item_index(int round, int cta, int grid) {
+  return (round & 1) ? round * grid + (grid - 1 - cta) : round * grid + cta;
+}
+
+__device__ __forceinline__ WorkItem load_item(const WorkItem* items, int idx) {
+  const int4* p = reinterpret_cast<const int4*>(items + idx);
+  const int4 a = __ldg(p), b = __ldg(p + 1);
+  WorkItem it;
+  it.q_row0 = a.x; it.q_rows = a.y; it.k_row0 = a.z; it.k_len = a.w;
+  it.head_kv = b.x; it.n_tiles = b.y; it.pad0 = b.z; it.pad1 = b.w;
+  return it;
+}
+
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t s_col, uint32_t q_smem, uint32_t k_smem) {
+  constexpr uint32_t idesc = make_idesc_bf16(kTileRows, kBlockKeys, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off_q = (kk / 4) * Cfg<D>::kQChunkBytes + (kk % 4) * 32;
+    const uint32_t off_k = (kk / 4) * Cfg<D>::kKVChunkBytes + (kk % 4) * 32;
+    umma_bf16_ss(tmem + s_col, make_smem_desc_sw128(q_smem + off_q, 16, 1024),
+                 make_smem_desc_sw128(k_smem + off_k, 16, 1024), idesc, kk > 0);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t s_col, uint32_t o_col, uint32_t v_smem,
+                                         bool accumulate) {
+  constexpr uint32_t idesc = make_idesc_bf16(kTileRows, D, true);
+#pragma unroll
+  for (int kk = 0; kk < kBlockKeys / 16; ++kk) {
+    umma_bf16_ts(tmem + o_col, tmem + s_col + kk * 8,
+                 make_smem_desc_sw128(v_smem + kk * 16 * 128, Cfg<D>::kKVChunkBytes, 1024), idesc,
+                 (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <typename TOut>
+__device__ __forceinline__ void store_row32(TOut* dst, const float (&x)[32]);
+
+template <>
+__device__ __forceinline__ void store_row32<__nv_bfloat16>(__nv_bfloat16* dst, const float (&x)[32]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    d[i] = make_uint4(pack_bf16x2(x[8 * i + 0], x[8 * i + 1]), pack_bf16x2(x[8 * i + 2], x[8 * i + 3]),
+                      pack_bf16x2(x[8 * i + 4], x[8 * i + 5]), pack_bf16x2(x[8 * i + 6], x[8 * i + 7]));
+  }
+}
+
+template <>
+__device__ __forceinline__ void store_row32<float>(float* dst, const float (&x)[32]) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) d[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+}
+
+template <int D, typename TOut>
+__global__ void __launch_bounds__(kThreads, 1)
+    gva_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                   const __grid_constant__ CUtensorMap map_v, const FwdParams p) {
+  using C = Cfg<D>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Ctrl ctrl;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;                                          // 2 tiles
+  uint8_t* sK = sQ + kTilesPerItem * C::kQBytes;               // S stages
+  uint8_t* sV = sK + S * C::kKVBytes;                          // S stages
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile int* abort_flag = &ctrl.abort;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&ctrl.q_full, 1);
+    mbar_init(&ctrl.q_empty, 1);
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&ctrl.k_full[i], 1);
+      mbar_init(&ctrl.k_empty[i], 1);
+      mbar_init(&ctrl.v_full[i], 1);
+      mbar_init(&ctrl.v_empty[i], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&ctrl.s_full[t], 1);
+      mbar_init(&ctrl.p_full[t], 128);
+      mbar_init(&ctrl.o_full[t], 1);
+    }
+    mbar_init(&ctrl.mma_done, 1);
+    ctrl.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(&ctrl.tmem_base, kTmemCols);
+    tmem_relinquish_alloc_permit();
+  }
+  tcgen05_fence_before();
+  __syncthreads();
+  tcgen05_fence_after();
+  const uint32_t tmem = ctrl.tmem_base;
+  const int T = p.tokens_per_tile;
+  const int G = p.group;
+
+  if (warp == kWarpTma) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&map_q);
+      tma_prefetch_desc(&map_k);
+      tma_prefetch_desc(&map_v);
+      uint32_t q_it = 0, kb = 0, vb = 0;
+      for (int round = 0;; ++round) {
+        const int idx = item_index(round, blockIdx.x, gridDim.x);
+        if (idx >= p.num_items) break;
+        const WorkItem it = load_item(p.items, idx);
+        if (it.k_len == 0) continue;
+        const int nblk = (it.k_len + kBlockKeys - 1) / kBlockKeys;
+        if (!wait_bar(&ctrl.q_empty, (q_it & 1) ^ 1, abort_flag, p.error_flag)) break;
+        mbar_arrive_expect_tx(&ctrl.q_full, it.n_tiles * C::kQBytes);
+        for (int t = 0; t < it.n_tiles; ++t)
+#pragma unroll
+          for (int ch = 0; ch < C::kChunks; ++ch)
+            tma_load_3d(sQ + t * C::kQBytes + ch * C::kQChunkBytes, &map_q, &ctrl.q_full, ch * 64,
+                        it.q_row0 + t * T, it.head_kv * G);
+        ++q_it;
+        bool ok = true;
+        for (int j = 0; j < nblk && ok; ++j) {
+          const int key0 = it.k_row0 + j * kBlockKeys;
+          const uint32_t ks = kb % S, vs = vb % S;
+          ok = wait_bar(&ctrl.k_empty[ks], ((kb / S) & 1) ^ 1, abort_flag, p.error_flag);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&ctrl.k_full[ks], C::kKVBytes);
+#pragma unroll
+          for (int ch = 0; ch < C::kChunks; ++ch)
+            tma_load_3d(sK + ks * C::kKVBytes + ch * C::kKVChunkBytes, &map_k, &ctrl.k_full[ks], ch * 64, key0,
+                        it.head_kv);
+          ++kb;
+          ok = wait_bar(&ctrl.v_empty[vs], ((vb / S) & 1) ^ 1, abort_flag, p.error_flag);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&ctrl.v_full[vs], C::kKVBytes);
+#pragma unroll
+          for (int ch = 0; ch < C::kChunks; ++ch)
+            tma_load_3d(sV + vs * C::kKVBytes + ch * C::kKVChunkBytes, &map_v, &ctrl.v_full[vs], ch * 64, key0,
+                        it.head_kv);
+          ++vb;
+        }
+        if (!ok) break;
+      }
+      // Drain: every copy this thread issued has landed before the CTA may exit.
+      if (q_it > 0) drain_bar(&ctrl.q_full, (q_it - 1) & 1, p.error_flag);
+      for (uint32_t i = (kb > (uint32_t)S ? kb - S : 0); i < kb; ++i) drain_bar(&ctrl.k_full[i % S], (i / S) & 1, p.error_flag);
+      for (uint32_t i = (vb > (uint32_t)S ? vb - S : 0); i < vb; ++i) drain_bar(&ctrl.v_full[i % S], (i / S) & 1, p.error_flag);
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t q_base = smem_addr(sQ);
+      const uint32_t k_base = smem_addr(sK);
+      const uint32_t v_base = smem_addr(sV);
+      uint32_t q_it = 0, kb = 0, vb = 0, pc0 = 0, pc1 = 0;
+      bool ok = true;
+      for (int round = 0; ok; ++round) {
+        const int idx = item_index(round, blockIdx.x, gridDim.x);
+        if (idx >= p.num_items) break;
+        const WorkItem it = load_item(p.items, idx);
+        if (it.k_len == 0) continue;
+        const int nblk = (it.k_len + kBlockKeys - 1) / kBlockKeys;
+        const bool two = it.n_tiles == 2;
+        ok = wait_bar(&ctrl.q_full, q_it & 1, abort_flag, p.error_flag);
+        if (!ok) break;
+        ++q_it;
+        uint32_t ks = kb % S;
+        ok = wait_bar(&ctrl.k_full[ks], (kb / S) & 1, abort_flag, p.error_flag);
+        if (!ok) break;
+        tcgen05_fence_after();
+        issue_qk<D>(tmem, col_s(0), q_base, k_base + ks * C::kKVBytes);
+        umma_commit(&ctrl.s_full[0]);
+        if (two) {
+          issue_qk<D>(tmem, col_s(1), q_base + C::kQBytes, k_base + ks * C::kKVBytes);
+          umma_commit(&ctrl.s_full[1]);
+        }
+        umma_commit(&ctrl.k_empty[ks]);
+        ++kb;
+        if (nblk == 1) umma_commit(&ctrl.q_empty);
+        for (int j = 0; j < nblk; ++j) {
+          const bool more = j + 1 < nblk;
+          const uint32_t vs = vb % S;
+          ks = kb % S;
+          ok = wait_bar(&ctrl.v_full[vs], (vb / S) & 1, abort_flag, p.error_flag);
+          if (ok && more) ok = wait_bar(&ctrl.k_full[ks], (kb / S) & 1, abort_flag, p.error_flag);
+          if (ok) ok = wait_bar(&ctrl.p_full[0], pc0 & 1, abort_flag, p.error_flag);
+          if (!ok) break;
+          ++pc0;
+          tcgen05_fence_after();
+          issue_pv<D>(tmem, col_s(0), col_o(0), v_base + vs * C::kKVBytes, j > 0);
+          if (!more) umma_commit(&ctrl.o_full[0]);
+          if (more) {
+            issue_qk<D>(tmem, col_s(0), q_base, k_base + ks * C::kKVBytes);
+            umma_commit(&ctrl.s_full[0]);
+          }
+          if (two) {
+            ok = wait_bar(&ctrl.p_full[1], pc1 & 1, abort_flag, p.error_flag);
+            if (!ok) break;
+            ++pc1;
+            tcgen05_fence_after();
+            issue_pv<D>(tmem, col_s(1), col_o(1), v_base + vs * C::kKVBytes, j > 0);
+            if (!more) umma_commit(&ctrl.o_full[1]);
+            if (more) {
+              issue_qk<D>(tmem, col_s(1), q_base + C::kQBytes, k_base + ks * C::kKVBytes);
+              umma_commit(&ctrl.s_full[1]);
+            }
+          }
+          umma_commit(&ctrl.v_empty[vs]);
+          ++vb;
+          if (more) {
+            umma_commit(&ctrl.k_empty[ks]);
+            ++kb;
+            if (j + 2 == nblk) umma_commit(&ctrl.q_empty);
+          }
+        }
+      }
+      // Every MMA issued so far completes before TMEM is released.
+      umma_commit(&ctrl.mma_done);
+      drain_bar(&ctrl.mma_done, 0, p.error_flag);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ softmax + epilogue
+    const int t = (warp - kFirstSoftmaxWarp) >> 2;      // Q tile of this warpgroup
+    const int lane_base = (warp & 3) * 32;              // TMEM lane quarter of this warp
+    const int row = lane_base + lane;                   // tile row = TMEM lane
+    const int hl = row / T;                             // folded head within the KV group
+    const int tok = row - hl * T;                       // token within the tile
+    const uint32_t s_addr = tmem_addr(tmem, lane_base, col_s(t));
+    const uint32_t o_addr = tmem_addr(tmem, lane_base, col_o(t));
+    const float c = p.scale_log2;
+    TOut* out = reinterpret_cast<TOut*>(p.out);
+    uint32_t sc = 0, oc = 0, vb = 0;
+    bool ok = true;
+    for (int round = 0; ok; ++round) {
+      const int idx = item_index(round, blockIdx.x, gridDim.x);
+      if (idx >= p.num_items) break;
+      const WorkItem it = load_item(p.items, idx);
+      if (it.n_tiles <= t) continue;
+      const bool valid = tok < it.q_rows - t * T;
+      const int64_t token = static_cast<int64_t>(it.q_row0) + t * T + tok;
+      const int head = it.head_kv * G + hl;
+      TOut* orow = out + (token * p.num_heads_q + head) * D;
+      float* lrow = p.lse + static_cast<int64_t>(head) * p.total_q + token;
+      if (it.k_len == 0) {
+        if (valid) {
+          float z[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) z[i] = 0.0f;
+#pragma unroll
+          for (int ch = 0; ch < D / 32; ++ch) store_row32<TOut>(orow + ch * 32, z);
+          *lrow = -CUDART_INF_F;
+        }
+        continue;
+      }
+      const int nblk = (it.k_len + kBlockKeys - 1) / kBlockKeys;
+      float m_used = -CUDART_INF_F;
+      float l = 0.0f;
+      for (int j = 0; j < nblk; ++j) {
+        ok = __all_sync(0xffffffffu, wait_bar(&ctrl.s_full[t], sc & 1, abort_flag, p.error_flag));
+        if (!ok) break;
+        ++sc;
+        tcgen05_fence_after();
+        uint32_t raw[128];
+        tmem_ld128_sync(s_addr, raw);
+        float s[128];
+#pragma unroll
+        for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(raw[i]);
+        const int rem = it.k_len - j * kBlockKeys;  // used keys in this block (>= 1)
+        if (rem < kBlockKeys) {
+#pragma unroll
+          for (int i = 0; i < 128; ++i) s[i] = (i < rem) ? s[i] : -CUDART_INF_F;
+        }
+        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+        for (int i = 4; i < 128; i += 4) {
+          mx0 = fmaxf(mx0, s[i]);
+          mx1 = fmaxf(mx1, s[i + 1]);
+          mx2 = fmaxf(mx2, s[i + 2]);
+          mx3 = fmaxf(mx3, s[i + 3]);
+        }
+        const float m_new = fmaxf(m_used, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c);
+        if (j == 0) {
+          m_used = m_new;
+        } else if (__any_sync(0xffffffffu, m_new > m_used + kRescaleThreshold)) {
+          // Rescale this row's O accumulator (complete: the S MMA just waited for was
+          // issued after the previous PV of this tile).
+          const float f = ex2_approx(m_used - m_new);
+          l *= f;
+          m_used = m_new;
+#pragma unroll
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t o[32];
+            tmem_ld32_sync(o_addr + ch * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+            tmem_st32(o_addr + ch * 32, o);
+          }
+        }
+        const float neg_m = -m_used;
+        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+        uint32_t pk_lo[32], pk_hi[32];  // P as bf16 pairs: column i holds keys 2i, 2i+1
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float p0 = ex2_approx(fmaf(s[2 * i + 0], c, neg_m));
+          const float p1 = ex2_approx(fmaf(s[2 * i + 1], c, neg_m));
+          const float p2 = ex2_approx(fmaf(s[2 * i + 2], c, neg_m));
+          const float p3 = ex2_approx(fmaf(s[2 * i + 3], c, neg_m));
+          l0 += p0;
+          l1 += p1;
+          l2 += p2;
+          l3 += p3;
+          pk_lo[i] = pack_bf16x2(p0, p1);
+          pk_lo[i + 1] = pack_bf16x2(p2, p3);
+        }
+        tmem_st32(s_addr, pk_lo);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float p0 = ex2_approx(fmaf(s[64 + 2 * i + 0], c, neg_m));
+          const float p1 = ex2_approx(fmaf(s[64 + 2 * i + 1], c, neg_m));
+          const float p2 = ex2_approx(fmaf(s[64 + 2 * i + 2], c, neg_m));
+          const float p3 = ex2_approx(fmaf(s[64 + 2 * i + 3], c, neg_m));
+          l0 += p0;
+          l1 += p1;
+          l2 += p2;
+          l3 += p3;
+          pk_hi[i] = pack_bf16x2(p0, p1);
+          pk_hi[i + 1] = pack_bf16x2(p2, p3);
+        }
+        tmem_st32(s_addr + 32, pk_hi);
+        l += (l0 + l1) + (l2 + l3);
+        if (t == 0 && rem < kBlockKeys) {
+          // Keys past the used length in this V block (gap, padding or another
+          // segment) get P = 0, but 0 * NaN would still poison O: zero those rows of
+          // the staged V block before the PV MMA reads it.
+          const uint32_t vblk = vb + j;
+          ok = __all_sync(0xffffffffu,
+                          wait_bar(&ctrl.v_full[vblk % S], (vblk / S) & 1, abort_flag, p.error_flag));
+          if (!ok) break;
+          uint8_t* vbase = sV + (vblk % S) * C::kKVBytes;
+          const int n16 = (kBlockKeys - rem) * C::kChunks * 8;  // 16-byte pieces to clear
+          for (int i = row; i < n16; i += 128) {
+            const int r = rem + i / (C::kChunks * 8);
+            const int rest = i % (C::kChunks * 8);
+            *reinterpret_cast<uint4*>(vbase + (rest / 8) * C::kKVChunkBytes + r * 128 + (rest % 8) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        tmem_wait_st();
+        tcgen05_fence_before();
+        mbar_arrive(&ctrl.p_full[t]);
+      }
+      if (!ok) break;
+      if (t == 0) vb += nblk;
+      ok = __all_sync(0xffffffffu, wait_bar(&ctrl.o_full[t], oc & 1, abort_flag, p.error_flag));
+      if (!ok) break;
+      ++oc;
+      tcgen05_fence_after();
+      const float inv_l = 1.0f / l;
+      const float lse_val = (m_used + log2f(l)) * kLn2;
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t o[32];
+        tmem_ld32_sync(o_addr + ch * 32, o);
+        float x[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(o[i]) * inv_l;
+        if (valid) store_row32<TOut>(orow + ch * 32, x);
+      }
+      if (valid) *lrow = lse_val;
+    }
+    tmem_wait_st();
+  }
+
+  tcgen05_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tcgen05_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D, typename TOut>
+cudaError_t launch_impl(const FwdParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                        int grid, cudaStream_t stream) {
+  auto kern = gva_fwd_kernel<D, TOut>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemAlloc);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, Cfg<D>::kSmemAlloc, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int forward_smem_bytes(int head_dim) {
+  return head_dim == 64 ? Cfg<64>::kSmemAlloc : Cfg<128>::kSmemAlloc;
+}
+
+cudaError_t launch_forward(int head_dim, bool out_f32, const FwdParams& p, const CUtensorMap& map_q,
+                           const CUtensorMap& map_k, const CUtensorMap& map_v, int grid, cudaStream_t stream) {
+  if (head_dim == 128) {
+    return out_f32 ? launch_impl<128, float>(p, map_q, map_k, map_v, grid, stream)
+                   : launch_impl<128, __nv_bfloat16>(p, map_q, map_k, map_v, grid, stream);
+  }
+  return out_f32 ? launch_impl<64, float>(p, map_q, map_k, map_v, grid, stream)
+                 : launch_impl<64, __nv_bfloat16>(p, map_q, map_k, map_v, grid, stream);
+}
+
+}  // namespace gva

@@ -1,0 +1,70 @@
+// Internal types shared by the host API and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace gva {
+
+// Rows of one Q tile (one TMEM lane per row), keys per K/V block, Q tiles per work item.
+constexpr int kTileRows = 128;
+constexpr int kBlockKeys = 128;
+constexpr int kTilesPerItem = 2;
+// Used rows of one segment handled by one merge work unit.
+constexpr int kMergeRows = 16;
+constexpr int kMaxMergeParts = 8;
+
+// One forward work item: up to 2 x 128 folded rows (tokens x the query heads of one KV
+// head) of one segment, attending the segment's used keys.
+struct alignas(16) WorkItem {
+  int32_t q_row0;   // global token row of the item's first token
+  int32_t q_rows;   // used tokens covered by the item (1 .. 2 * tokens_per_tile)
+  int32_t k_row0;   // global key row of the segment's first key
+  int32_t k_len;    // used keys of the segment (0: keyless, epilogue only)
+  int32_t head_kv;  // KV head; query heads head_kv * group .. + group - 1
+  int32_t n_tiles;  // 1 or 2 Q tiles with used rows
+  int32_t pad0, pad1;
+};
+
+struct alignas(8) MergeUnit {
+  int32_t row0;   // global token row of the first row
+  int32_t rows;   // used rows in this unit (1 .. kMergeRows)
+};
+
+struct FwdParams {
+  const WorkItem* items;
+  int32_t num_items;
+  void* out;
+  float* lse;
+  int64_t total_q;
+  int32_t num_heads_q;
+  int32_t group;            // Hq / Hkv
+  int32_t tokens_per_tile;  // kTileRows / group
+  float scale_log2;         // softmax scale * log2(e)
+  int* error_flag;
+};
+
+struct MergeParams {
+  const MergeUnit* units;
+  int32_t num_units;
+  int32_t num_parts;
+  const void* outs[kMaxMergeParts];
+  const float* lses[kMaxMergeParts];
+  void* out;
+  float* lse;
+  int64_t total_q;
+  int32_t num_heads_q;
+  int32_t head_dim;
+};
+
+// Device error word bits.
+constexpr int kErrWaitTimeout = 1;
+
+// Launchers (defined in gva_fwd.cu / gva_merge.cu). They return the launch error.
+cudaError_t launch_forward(int head_dim, bool out_f32, const FwdParams& p, const CUtensorMap& map_q,
+                           const CUtensorMap& map_k, const CUtensorMap& map_v, int grid, cudaStream_t stream);
+cudaError_t launch_merge(bool in_f32, bool out_f32, const MergeParams& p, int grid, cudaStream_t stream);
+int forward_smem_bytes(int head_dim);
+
+}  // namespace gva

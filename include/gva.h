@@ -1,0 +1,164 @@
+/*
+ * gva.h - C ABI of the gapped variable-length attention forward for GB300 (sm_103a).
+ *
+ * The operation (cosmos-framework PR #302 "fix(mot): gapped replay on GPUs
+ * FlashAttention-4 has no kernels for (sm120)", section "What"; the FA4 varlen
+ * forward with seqused_q / seqused_k it replaces):
+ *
+ *   Segment b owns query rows cu_seqlens_q[b] .. cu_seqlens_q[b+1] and key rows
+ *   cu_seqlens_k[b] .. cu_seqlens_k[b+1]. Only its first seqused_q[b] query rows
+ *   attend, and only to its first seqused_k[b] keys. For every such row r and query
+ *   head h (KV head h / (Hq/Hkv), contiguous GQA groups):
+ *       O[r,h,:]  = softmax_j(s * <Q[r,h,:], K[j,hkv,:]>) . V[j,hkv,:]
+ *       LSE[h,r]  = ln sum_j exp(s * <Q[r,h,:], K[j,hkv,:]>)     (natural log, FP32)
+ *   Rows past a segment's used length are not written (O and LSE). A segment with
+ *   seqused_k[b] = 0 gets O = +0 and LSE = -inf on its used rows. Keys past
+ *   seqused_k[b] (gap or zero padding) never enter the softmax: each attended zero
+ *   key would add exp(0) = 1 to the denominator (TensorRT-LLM issue #18687,
+ *   "actual behavior").
+ *
+ * Layouts (all tensors contiguous, row-major, device memory):
+ *   Q, O : [total_q, Hq, d]      Q bf16; O bf16 or fp32 (gva_dtype)
+ *   K, V : [total_k, Hkv, d]     bf16
+ *   LSE  : [Hq, total_q]         fp32 (the PyTorch unpadded-varlen LSE layout named
+ *                                in the review of PR #302)
+ *   total_q = cu_seqlens_q[B], total_k = cu_seqlens_k[B].
+ *
+ * Conventions:
+ *   - Every function returns a gva_status and never throws. On failure,
+ *     gva_last_error() gives a human-readable reason (thread-local).
+ *   - gva_forward and gva_lse_merge are asynchronous on `stream`, allocate nothing,
+ *     and do not synchronise the host. gva_plan allocates and uploads a small device
+ *     work list once per geometry (from host ints: no device-to-host read).
+ *   - The caller owns every tensor. A plan owns only its device work list and is
+ *     released by gva_plan_destroy; no launch that uses it may still be in flight.
+ *   - Two launches that share a plan may run concurrently: a plan holds no per-call
+ *     state except a device error word (see gva_device_status).
+ */
+#ifndef GVA_H_
+#define GVA_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define GVA_API __attribute__((visibility("default")))
+#else
+#define GVA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GVA_OK = 0,
+  GVA_ERR_INVALID_ARG = 1,  /* bad geometry, null / misaligned pointer, bad count */
+  GVA_ERR_UNSUPPORTED = 2,  /* head_dim, head grouping or device not supported */
+  GVA_ERR_CUDA = 3,         /* a CUDA runtime or driver call failed */
+  GVA_ERR_DEVICE_CHECK = 4  /* a kernel reported a device-side check failure */
+} gva_status;
+
+typedef enum { GVA_BF16 = 0, GVA_FP32 = 1 } gva_dtype;
+
+typedef struct gva_plan* gva_plan_t;
+
+/* Geometry summary of a plan (for tests and benchmarks). */
+typedef struct {
+  int32_t num_segments, num_heads_q, num_heads_kv, head_dim;
+  int64_t total_q, total_k;
+  int32_t num_work_items;   /* forward work items (segment, kv head, 2 x 128-row Q tiles) */
+  int32_t num_merge_units;  /* merge work units (up to 16 used rows of one segment) */
+  int32_t grid_ctas;        /* persistent CTAs one forward launch uses */
+  int32_t sm_count;
+  double used_flops;        /* 4 * d * Hq * sum_b seqused_q[b] * seqused_k[b] */
+} gva_plan_info;
+
+/*
+ * gva_plan - validate one launch's segment geometry and build its work list.
+ *
+ * Cites: PR #302 "What" (cu_seqlens / seqused semantics) and its review (build the
+ * gather plan from the runtime's host ints, with no device sync inside the op).
+ *
+ *   cu_seqlens_q, cu_seqlens_k : HOST int32 [num_segments + 1], start at 0,
+ *                                non-decreasing (segment capacities are differences)
+ *   seqused_q, seqused_k       : HOST int32 [num_segments], 0 <= used <= capacity
+ *   num_heads_q % num_heads_kv == 0 and 128 % (num_heads_q / num_heads_kv) == 0
+ *   head_dim in {64, 128}
+ *
+ * The plan is bound to the current CUDA device, which must be sm_103 (GB300).
+ * Errors: GVA_ERR_INVALID_ARG for bad geometry (checked before any CUDA call),
+ * GVA_ERR_UNSUPPORTED for head_dim / grouping / device, GVA_ERR_CUDA if the upload
+ * fails. On error *out_plan is set to NULL.
+ */
+GVA_API gva_status gva_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, const int32_t* cu_seqlens_k,
+                    const int32_t* seqused_k, int32_t num_segments, int32_t num_heads_q, int32_t num_heads_kv,
+                    int32_t head_dim, gva_plan_t* out_plan);
+
+/*
+ * gva_forward - the gapped varlen attention forward of one launch (one kernel).
+ *
+ * Cites: PR #302 "What" (used rows attend used keys; rows past the used length left
+ * as they are; a keyless segment gets zero output and -inf LSE), TensorRT-LLM issue
+ * #18687 "actual behavior" (padded keys must not enter the softmax denominator).
+ *
+ *   q, k, v   : DEVICE bf16, layouts above, 16-byte aligned, must not alias out/lse
+ *   out       : DEVICE, out_dtype (GVA_BF16 or GVA_FP32), [total_q, Hq, d]
+ *   lse       : DEVICE fp32 [Hq, total_q]
+ *   softmax_scale : s in the formula; <= 0 selects 1/sqrt(head_dim)
+ *   stream    : CUDA stream the kernel is enqueued on
+ *
+ * Only used rows of out / lse are written. Asynchronous; returns GVA_ERR_CUDA if the
+ * launch fails. Device-side waits are bounded; a timeout is recorded in the plan's
+ * error word (gva_device_status) instead of hanging.
+ */
+GVA_API gva_status gva_forward(gva_plan_t plan, const void* q, const void* k, const void* v, void* out,
+                       gva_dtype out_dtype, float* lse, float softmax_scale, cudaStream_t stream);
+
+/*
+ * gva_lse_merge - combine partial forwards over disjoint key sets of the same rows.
+ *
+ * Cites: cosmos-framework PR #312, "Problem and behavior" (visibility partitions are
+ * combined by an FP32 LSE merge). For every used row r and head h of `plan`'s query
+ * geometry:
+ *   L = max_p lses[p][h,r];  L = -inf  ->  out = +0, lse = -inf
+ *   else w_p = exp(lses[p][h,r] - L), lse = L + ln sum_p w_p,
+ *        out[r,h,:] = sum_p w_p outs[p][r,h,:] / sum_p w_p
+ * A partition whose lse is -inf contributes nothing (its output is not read).
+ *
+ *   num_parts : 1 .. 8
+ *   outs      : HOST array of num_parts DEVICE pointers, in_dtype, [total_q, Hq, d]
+ *   lses      : HOST array of num_parts DEVICE fp32 pointers, [Hq, total_q]
+ *   out, lse  : DEVICE outputs (out_dtype / fp32); out may alias outs[0] and lse may
+ *               alias lses[0] (each element is read before it is written by the same
+ *               thread); rows past the used length are not written.
+ * Computed in FP32. Asynchronous on `stream`.
+ */
+GVA_API gva_status gva_lse_merge(gva_plan_t plan, int32_t num_parts, const void* const* outs, gva_dtype in_dtype,
+                         const float* const* lses, void* out, gva_dtype out_dtype, float* lse,
+                         cudaStream_t stream);
+
+/* Release a plan's device memory. NULL is accepted. Synchronous with respect to the
+ * host only through cudaFree. */
+GVA_API gva_status gva_plan_destroy(gva_plan_t plan);
+
+/* Fill *info with the plan's geometry summary. */
+GVA_API gva_status gva_plan_get_info(gva_plan_t plan, gva_plan_info* info);
+
+/* Synchronise the device, read and clear the plan's device error word. Returns
+ * GVA_ERR_DEVICE_CHECK if a kernel of this plan recorded a bounded-wait timeout or a
+ * check failure since the last call, GVA_OK otherwise. For tests and debugging; it
+ * is not needed on the fast path. */
+GVA_API gva_status gva_device_status(gva_plan_t plan);
+
+/* Static description of a status code. */
+GVA_API const char* gva_status_string(gva_status status);
+
+/* Detail of the last error returned on the calling thread ("" if none). */
+GVA_API const char* gva_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GVA_H_ */

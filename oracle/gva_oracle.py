@@ -135,7 +135,8 @@ def attention_rows(q, k, v, cu_q, used_q, cu_k, used_k, rows: Sequence[int], *,
     """The same definition evaluated for a list of global query rows (all heads).
 
     For spot checks of launches too large to evaluate in full. Every row must be a
-    used row. Returns (O [n, Hq, d], LSE [Hq, n]) in FP64."""
+    used row. Rows of one segment are evaluated together, with the segment's keys
+    widened once per KV head. Returns (O [n, Hq, d], LSE [Hq, n]) in FP64."""
     hq, d = q.shape[1], q.shape[2]
     hkv = k.shape[1] if num_heads_kv is None else num_heads_kv
     g = hq // hkv
@@ -144,23 +145,28 @@ def attention_rows(q, k, v, cu_q, used_q, cu_k, used_k, rows: Sequence[int], *,
     cu_k = np.asarray(cu_k, np.int64)
     used_q = np.asarray(used_q, np.int64)
     used_k = np.asarray(used_k, np.int64)
+    rows = [int(r) for r in rows]
     o = np.zeros((len(rows), hq, v.shape[2]), np.float64)
     l = np.zeros((hq, len(rows)), np.float64)
+    by_segment = {}
     for i, r in enumerate(rows):
         b = int(np.searchsorted(cu_q, r, side="right")) - 1  # last segment starting at or before r
-        if not (cu_q[b] <= r < cu_q[b] + used_q[b]):
+        if not (0 <= b < len(used_q) and cu_q[b] <= r < cu_q[b] + used_q[b]):
             raise ValueError(f"row {r} is not a used row")
+        by_segment.setdefault(b, []).append(i)
+    for b, idx in by_segment.items():
         k0, nk = int(cu_k[b]), int(used_k[b])
         if nk == 0:
-            l[:, i] = -np.inf
+            l[:, idx] = -np.inf
             continue
+        sel = [rows[i] for i in idx]
         for hk in range(hkv):
-            qs = _as_f64(q[r, hk * g:(hk + 1) * g, :]).astype(np.float64)
+            qs = np.concatenate([_as_f64(q[r, hk * g:(hk + 1) * g, :]) for r in sel]).astype(np.float64)
             ks = _as_f64(k[k0:k0 + nk, hk, :]).astype(np.float64)
             vs = _as_f64(v[k0:k0 + nk, hk, :]).astype(np.float64)
             ob, lb = _segment_attention(qs, ks, vs, s, budget_bytes)
-            o[i, hk * g:(hk + 1) * g] = ob
-            l[hk * g:(hk + 1) * g, i] = lb
+            o[idx, hk * g:(hk + 1) * g] = ob.reshape(len(sel), g, -1)
+            l[hk * g:(hk + 1) * g, idx] = lb.reshape(len(sel), g).T
     return o, l
 
 
