@@ -83,7 +83,7 @@ gva_status make_map(CUtensorMap* map, const void* base, int64_t rows, int32_t he
 }
 
 gva_status validate_offsets(const int32_t* cu, const int32_t* used, int32_t n, const char* name) {
-  if (cu[0] != 0) return fail(GVA_ERR_INVALID_ARG, "cu_seqlens_%s[0] = %d, expected 0", name, cu[0]);
+  if (cu[0] < 0) return fail(GVA_ERR_INVALID_ARG, "cu_seqlens_%s[0] = %d is negative", name, cu[0]);
   for (int32_t b = 0; b < n; ++b) {
     if (cu[b + 1] < cu[b])
       return fail(GVA_ERR_INVALID_ARG, "cu_seqlens_%s decreases at segment %d (%d -> %d)", name, b, cu[b], cu[b + 1]);

@@ -165,6 +165,17 @@ def long_replay(seed: int = 1005) -> Geometry:
     return _geom(_cum([cq] * B), uq, _cum([ck] * B), uk, 32, 8, 128)
 
 
+def long_replay_small(seed: int = 1006) -> Geometry:
+    """A reduced long replay for profiling captures: 2 segments of 8192 query rows and
+    32768 keys with the same seeded used fractions; Hq=32, Hkv=8, d=128 (Q + K + V about
+    0.4 GB, above the 129 MB L2)."""
+    rng = np.random.default_rng(seed)
+    B, cq, ck = 2, 8192, 32768
+    uq = np.floor(rng.uniform(0.6, 1.0, size=B) * cq).astype(np.int64)
+    uk = np.floor(rng.uniform(0.5, 1.0, size=B) * ck).astype(np.int64)
+    return _geom(_cum([cq] * B), uq, _cum([ck] * B), uk, 32, 8, 128)
+
+
 def random_geometry(rng: np.random.Generator, num_segments: int, max_q: int, max_k: int,
                     num_heads_q: int, num_heads_kv: int, head_dim: int,
                     allow_empty: bool = True) -> Geometry:

@@ -22,7 +22,7 @@
  *   K, V : [total_k, Hkv, d]     bf16
  *   LSE  : [Hq, total_q]         fp32 (the PyTorch unpadded-varlen LSE layout named
  *                                in the review of PR #302)
- *   total_q = cu_seqlens_q[B], total_k = cu_seqlens_k[B].
+ *   total_q = cu_seqlens_q[B], total_k = cu_seqlens_k[B] (rows of the buffers).
  *
  * Conventions:
  *   - Every function returns a gva_status and never throws. On failure,
@@ -80,8 +80,10 @@ typedef struct {
  * Cites: PR #302 "What" (cu_seqlens / seqused semantics) and its review (build the
  * gather plan from the runtime's host ints, with no device sync inside the op).
  *
- *   cu_seqlens_q, cu_seqlens_k : HOST int32 [num_segments + 1], start at 0,
- *                                non-decreasing (segment capacities are differences)
+ *   cu_seqlens_q, cu_seqlens_k : HOST int32 [num_segments + 1], non-negative and
+ *                                non-decreasing (segment capacities are differences;
+ *                                a first offset above 0 lets a visibility partition
+ *                                address a sub-range of the same K/V buffers)
  *   seqused_q, seqused_k       : HOST int32 [num_segments], 0 <= used <= capacity
  *   num_heads_q % num_heads_kv == 0 and 128 % (num_heads_q / num_heads_kv) == 0
  *   head_dim in {64, 128}

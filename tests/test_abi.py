@@ -63,7 +63,7 @@ def _plan_status(lib, cu_q, uq, cu_k, uk, hq=4, hkv=2, d=64):
 
 
 BAD = [
-    ("cu_q does not start at 0", ([1, 48], [10], [0, 48], [10], 4, 2, 64), 1, "cu_seqlens_q[0]"),
+    ("negative cu_q start", ([-1, 48], [10], [0, 48], [10], 4, 2, 64), 1, "cu_seqlens_q[0]"),
     ("decreasing cu_k", ([0, 48, 96], [1, 1], [0, 48, 40], [1, 1], 4, 2, 64), 1, "decreases"),
     ("used_q > capacity", ([0, 48], [49], [0, 48], [1], 4, 2, 64), 1, "seqused_q"),
     ("negative used_k", ([0, 48], [4], [0, 48], [-1], 4, 2, 64), 1, "seqused_k"),

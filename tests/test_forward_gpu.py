@@ -118,10 +118,12 @@ def test_random_gapped_geometries(hq, hkv, d, dtype, seed):
 
 @pytest.mark.parametrize("scale", [0.02, 0.25])
 def test_explicit_softmax_scale(scale):
+    """A sharper softmax concentrates O on few values of |v| up to ~4, where rounding O
+    itself to bf16 costs up to 1.6e-2; fp32 output measures the kernel's arithmetic."""
     rng = np.random.default_rng(31)
     g = W.random_geometry(rng, 3, 300, 500, 8, 2, 128, allow_empty=False)
     q, k, v = W.make_qkv(g, 31)
-    o, l = gpu_forward(g, q, k, v, scale=scale)
+    o, l = gpu_forward(g, q, k, v, scale=scale, out_dtype=torch.float32)
     o_ref, l_ref = oracle_forward(g, q, k, v, scale=scale)
     check_full(g, o, l, o_ref, l_ref, W.TINY_SENTINEL)
 

@@ -56,8 +56,9 @@ def test_merge_matches_oracle(parts, in_dtype, out_dtype, hq, d):
     assert np.array_equal(np.isneginf(lg[:, used]), np.isneginf(l_ref[:, used]))
     fin = np.isfinite(l_ref) & used[None, :]
     assert np.abs(lg[fin] - l_ref[fin]).max() <= 1e-5
-    tol = 1e-2 if out_dtype == torch.bfloat16 else 1e-5
-    assert np.abs(og[used] - o_ref[used]).max() <= tol
+    # fp32 output: FP32 arithmetic only; bf16 output: plus its own rounding (<= 2^-9 relative)
+    rel = 2.0 ** -8 if out_dtype == torch.bfloat16 else 0.0
+    assert np.all(np.abs(og[used] - o_ref[used]) <= rel * np.abs(o_ref[used]) + 1e-5)
     dead = np.isneginf(l_ref) & used[None, :]
     assert np.all(og.transpose(1, 0, 2)[dead] == 0.0)
 
