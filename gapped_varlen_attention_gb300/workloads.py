@@ -167,7 +167,7 @@ def long_replay(seed: int = 1005) -> Geometry:
 
 def long_replay_small(seed: int = 1006) -> Geometry:
     """A reduced long replay for profiling captures: 2 segments of 8192 query rows and
-    32768 keys with the same seeded used fractions; Hq=32, Hkv=8, d=128 (Q + K + V about
+    32768 keys, used fractions drawn from the same ranges; Hq=32, Hkv=8, d=128 (Q + K + V about
     0.4 GB, above the 129 MB L2)."""
     rng = np.random.default_rng(seed)
     B, cq, ck = 2, 8192, 32768
