@@ -9,8 +9,8 @@ Public API (a thin binding of the C ABI in include/gva.h):
 The library (libgva.so) is built in-tree by ``build()``; nothing here computes on the
 CPU, and calls raise if the library or a supported GPU is missing.
 """
-from ._lib import (GVA_BF16, GVA_FP32, EXPORTS, GvaError, Plan, device_status, forward, load_library,
-                   lse_merge)
+from ._lib import (GVA_BF16, GVA_FP32, EXPORTS, GvaError, Plan, device_status, forward, forward_noalloc,
+                   load_library, lse_merge)
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
@@ -18,5 +18,5 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return _build(force=force, verbose=verbose)
 
 
-__all__ = ["Plan", "forward", "lse_merge", "device_status", "load_library", "build", "GvaError", "EXPORTS",
+__all__ = ["Plan", "forward", "forward_noalloc", "lse_merge", "device_status", "load_library", "build", "GvaError", "EXPORTS",
            "GVA_BF16", "GVA_FP32"]

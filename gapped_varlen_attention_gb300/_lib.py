@@ -21,7 +21,8 @@ GVA_BF16, GVA_FP32 = 0, 1
 
 # Every symbol include/gva.h declares.
 EXPORTS = ("gva_plan", "gva_forward", "gva_lse_merge", "gva_plan_destroy", "gva_plan_get_info",
-           "gva_device_status", "gva_status_string", "gva_last_error")
+           "gva_device_status", "gva_status_string", "gva_last_error", "gva_forward_noalloc")
+NOALLOC_MAX_WORK_ITEMS = 32768  # GVA_NOALLOC_MAX_WORK_ITEMS in include/gva.h
 
 
 class GvaError(RuntimeError):
@@ -63,8 +64,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.gva_status_string.restype = ctypes.c_char_p
     lib.gva_last_error.argtypes = []
     lib.gva_last_error.restype = ctypes.c_char_p
+    lib.gva_forward_noalloc.argtypes = [pi32, pi32, pi32, pi32, i32, i32, i32, i32, vp, vp, vp, vp, i32, vp, f32,
+                                        vp]
     for name in ("gva_plan", "gva_forward", "gva_lse_merge", "gva_plan_destroy", "gva_plan_get_info",
-                 "gva_device_status"):
+                 "gva_device_status", "gva_forward_noalloc"):
         getattr(lib, name).restype = i32
     if path is None:
         _lib = lib
@@ -199,3 +202,38 @@ def lse_merge(plan: Plan, outs: Sequence, lses: Sequence, out, lse, stream=None)
 def device_status(plan: Plan):
     """Synchronise and raise if a kernel of this plan recorded a device-side failure."""
     _check(plan._lib, plan._lib.gva_device_status(plan.handle), "gva_device_status")
+
+
+def forward_noalloc(cu_seqlens_q, seqused_q, cu_seqlens_k, seqused_k, num_heads_q: int, num_heads_kv: int,
+                    q, k, v, out, lse, softmax_scale: float = 0.0, stream=None):
+    """``gva_forward_noalloc``: the forward without a plan, for callers that may not
+    allocate device memory (the work list goes to a fixed scratch array inside the
+    library). Same tensors as ``forward``; the geometry is given as host arrays."""
+    import torch
+    lib = load_library()
+    a = [_i32(x) for x in (cu_seqlens_q, seqused_q, cu_seqlens_k, seqused_k)]
+    n = int(a[1].shape[0])
+    if a[0].shape[0] != n + 1 or a[2].shape[0] != n + 1 or a[3].shape[0] != n:
+        raise ValueError("cu_seqlens must have num_segments + 1 entries and seqused num_segments")
+    d = int(q.shape[-1])
+    total_q, total_k = int(a[0][-1]), int(a[2][-1])
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise TypeError("q, k and v must be bfloat16")
+    if out.dtype not in (torch.bfloat16, torch.float32) or lse.dtype != torch.float32:
+        raise TypeError("out must be bfloat16 or float32 and lse float32")
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("lse", lse)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if tuple(q.shape) != (total_q, num_heads_q, d) or tuple(out.shape) != (total_q, num_heads_q, d):
+        raise ValueError(f"q / out must be [{total_q}, {num_heads_q}, {d}]")
+    if tuple(k.shape) != (total_k, num_heads_kv, d) or tuple(v.shape) != (total_k, num_heads_kv, d):
+        raise ValueError(f"k / v must be [{total_k}, {num_heads_kv}, {d}]")
+    if tuple(lse.shape) != (num_heads_q, total_q):
+        raise ValueError(f"lse must be [{num_heads_q}, {total_q}]")
+    as_p = lambda x: x.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))  # noqa: E731
+    st = lib.gva_forward_noalloc(as_p(a[0]), as_p(a[1]), as_p(a[2]), as_p(a[3]), n, int(num_heads_q),
+                                 int(num_heads_kv), d, _dev_ptr(q), _dev_ptr(k), _dev_ptr(v), _dev_ptr(out),
+                                 GVA_FP32 if out.dtype == torch.float32 else GVA_BF16, _dev_ptr(lse),
+                                 float(softmax_scale), _stream_ptr(stream))
+    _check(lib, st, "gva_forward_noalloc")
+    return out, lse

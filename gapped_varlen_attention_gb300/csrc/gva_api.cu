@@ -104,6 +104,10 @@ void free_plan(struct gva_plan* p) {
 
 }  // namespace
 
+namespace gva {
+void set_last_error(const char* message) { g_last_error = message; }
+}  // namespace gva
+
 extern "C" {
 
 gva_status gva_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, const int32_t* cu_seqlens_k,

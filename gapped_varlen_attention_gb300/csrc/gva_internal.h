@@ -66,5 +66,7 @@ cudaError_t launch_forward(int head_dim, bool out_f32, const FwdParams& p, const
                            const CUtensorMap& map_k, const CUtensorMap& map_v, int grid, cudaStream_t stream);
 cudaError_t launch_merge(bool in_f32, bool out_f32, const MergeParams& p, int grid, cudaStream_t stream);
 int forward_smem_bytes(int head_dim);
+// Set the calling thread's gva_last_error() text (defined in gva_api.cu).
+void set_last_error(const char* message);
 
 }  // namespace gva

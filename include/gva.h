@@ -153,6 +153,38 @@ GVA_API gva_status gva_plan_get_info(gva_plan_t plan, gva_plan_info* info);
  * is not needed on the fast path. */
 GVA_API gva_status gva_device_status(gva_plan_t plan);
 
+/*
+ * gva_forward_noalloc - gva_forward for callers that cannot allocate device memory.
+ *
+ * The paper has no counterpart for this entry point. It exists for callers that may
+ * not call cudaMalloc: a serving runtime that hands out all device memory from its own
+ * pool, code under a fixed memory budget, or a loop that must not take cudaMalloc's
+ * implicit device synchronisation. gva_plan allocates a device work list; this call
+ * instead builds the work list on the host and copies it, on `stream`, into a scratch
+ * array that is part of the library image (GVA_NOALLOC_MAX_WORK_ITEMS items of 32
+ * bytes plus an error word, about 1 MiB, held by every GPU that loads the library until
+ * the process exits). It calls no cudaMalloc, cudaFree or allocating library routine.
+ *
+ * Arguments: the geometry exactly as for gva_plan (HOST arrays, same rules), then the
+ * tensors, scale and stream exactly as for gva_forward (the caller still owns and
+ * passes inputs and outputs). A launch needing more than GVA_NOALLOC_MAX_WORK_ITEMS
+ * work items (items = sum over segments of ceil(seqused_q / (256 / (Hq/Hkv))) * Hkv)
+ * is refused with GVA_ERR_INVALID_ARG before any GPU work.
+ *
+ * The first call on a device resolves the scratch array's address for that device
+ * (cudaGetSymbolAddress, with that device current); make that first call before any
+ * stream capture. Every call overwrites the shared scratch and clears its error word
+ * on `stream`: calls on one stream are ordered, but calls whose kernels may overlap on
+ * the GPU (different streams without ordering) race on the scratch and must not be
+ * made.
+ */
+#define GVA_NOALLOC_MAX_WORK_ITEMS 32768
+GVA_API gva_status gva_forward_noalloc(const int32_t* cu_seqlens_q, const int32_t* seqused_q,
+                                       const int32_t* cu_seqlens_k, const int32_t* seqused_k,
+                                       int32_t num_segments, int32_t num_heads_q, int32_t num_heads_kv,
+                                       int32_t head_dim, const void* q, const void* k, const void* v, void* out,
+                                       gva_dtype out_dtype, float* lse, float softmax_scale, cudaStream_t stream);
+
 /* Static description of a status code. */
 GVA_API const char* gva_status_string(gva_status status);
 
