@@ -367,74 +367,81 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         ++sc;
         tcgen05_fence_after();
-        uint32_t raw[128];
-        tmem_ld128_sync(s_addr, raw);
-        float s[128];
-#pragma unroll
-        for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(raw[i]);
         const int rem = it.k_len - j * kBlockKeys;  // used keys in this block (>= 1)
         if (rem < kBlockKeys) {
-#pragma unroll
-          for (int i = 0; i < 128; ++i) s[i] = (i < rem) ? s[i] : -CUDART_INF_F;
+          // Last, partial block: keys past the used length (gap, padding or another
+          // segment, possibly NaN) leave the softmax. Their score columns are set to
+          // -inf in TMEM before the row is read (the range is uniform over the warp).
+          for (int col = rem; col < kBlockKeys; ++col) tmem_st1(s_addr + col, 0xff800000u);
+          tmem_wait_st();
         }
-        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+        float s[128];
+        {
+          uint32_t raw[128];
+          tmem_ld128_sync(s_addr, raw);
 #pragma unroll
-        for (int i = 4; i < 128; i += 4) {
-          mx0 = fmaxf(mx0, s[i]);
-          mx1 = fmaxf(mx1, s[i + 1]);
-          mx2 = fmaxf(mx2, s[i + 2]);
-          mx3 = fmaxf(mx3, s[i + 3]);
+          for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(raw[i]);
         }
-        const float m_new = fmaxf(m_used, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c);
+        float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
+        float mx2 = fmax3(s[6], s[7], s[8]), mx3 = fmax3(s[9], s[10], s[11]);
+#pragma unroll
+        for (int i = 12; i < 124; i += 8) {
+          mx0 = fmax3(mx0, s[i], s[i + 1]);
+          mx1 = fmax3(mx1, s[i + 2], s[i + 3]);
+          mx2 = fmax3(mx2, s[i + 4], s[i + 5]);
+          mx3 = fmax3(mx3, s[i + 6], s[i + 7]);
+        }
+        const float mx = fmax3(fmax3(mx0, mx1, s[124]), fmax3(mx2, mx3, s[125]), fmaxf(s[126], s[127]));
+        const float m_new = fmaxf(m_used, mx * c);
+        // O is rescaled when the row max grows by more than the threshold; the O update
+        // itself comes after P is stored, when fewer registers are live.
+        float f_resc = 1.0f;
+        bool resc = false;
         if (j == 0) {
           m_used = m_new;
         } else if (__any_sync(0xffffffffu, m_new > m_used + kRescaleThreshold)) {
-          // Rescale this row's O accumulator (complete: the S MMA just waited for was
-          // issued after the previous PV of this tile).
-          const float f = ex2_approx(m_used - m_new);
-          l *= f;
+          resc = true;
+          f_resc = ex2_approx(m_used - m_new);
+          l *= f_resc;
           m_used = m_new;
+        }
+        // P = 2^(s*c - m) as bf16 pairs (column i holds keys 2i, 2i+1), stored to the
+        // first 64 columns of S_t in 16-column pieces as they are ready.
+        const uint64_t c2 = f32x2(c, c);
+        const uint64_t neg_m2 = f32x2(-m_used, -m_used);
+        uint64_t acc0 = f32x2(0.0f, 0.0f), acc1 = acc0;
+#pragma unroll
+        for (int q16 = 0; q16 < 4; ++q16) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int k2 = q16 * 32 + 2 * i;
+            float a, b;
+            f32x2_split(ffma2(f32x2(s[k2], s[k2 + 1]), c2, neg_m2), a, b);
+            a = ex2_approx(a);
+            b = ex2_approx(b);
+            pk[i] = pack_bf16x2(a, b);
+            if (i & 1) acc1 = fadd2(acc1, f32x2(a, b));
+            else acc0 = fadd2(acc0, f32x2(a, b));
+          }
+          tmem_st16(s_addr + q16 * 16, pk);
+        }
+        {
+          float la, lb;
+          f32x2_split(fadd2(acc0, acc1), la, lb);
+          l += la + lb;
+        }
+        if (resc) {
+          // Complete: the S MMA just waited for was issued after this tile's previous PV.
 #pragma unroll
           for (int ch = 0; ch < D / 32; ++ch) {
             uint32_t o[32];
             tmem_ld32_sync(o_addr + ch * 32, o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f_resc);
             tmem_st32(o_addr + ch * 32, o);
           }
         }
-        const float neg_m = -m_used;
-        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
-        uint32_t pk_lo[32], pk_hi[32];  // P as bf16 pairs: column i holds keys 2i, 2i+1
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float p0 = ex2_approx(fmaf(s[2 * i + 0], c, neg_m));
-          const float p1 = ex2_approx(fmaf(s[2 * i + 1], c, neg_m));
-          const float p2 = ex2_approx(fmaf(s[2 * i + 2], c, neg_m));
-          const float p3 = ex2_approx(fmaf(s[2 * i + 3], c, neg_m));
-          l0 += p0;
-          l1 += p1;
-          l2 += p2;
-          l3 += p3;
-          pk_lo[i] = pack_bf16x2(p0, p1);
-          pk_lo[i + 1] = pack_bf16x2(p2, p3);
-        }
-        tmem_st32(s_addr, pk_lo);
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float p0 = ex2_approx(fmaf(s[64 + 2 * i + 0], c, neg_m));
-          const float p1 = ex2_approx(fmaf(s[64 + 2 * i + 1], c, neg_m));
-          const float p2 = ex2_approx(fmaf(s[64 + 2 * i + 2], c, neg_m));
-          const float p3 = ex2_approx(fmaf(s[64 + 2 * i + 3], c, neg_m));
-          l0 += p0;
-          l1 += p1;
-          l2 += p2;
-          l3 += p3;
-          pk_hi[i] = pack_bf16x2(p0, p1);
-          pk_hi[i + 1] = pack_bf16x2(p2, p3);
-        }
-        tmem_st32(s_addr + 32, pk_hi);
-        l += (l0 + l1) + (l2 + l3);
         if (t == 0 && rem < kBlockKeys) {
           // Keys past the used length in this V block (gap, padding or another
           // segment) get P = 0, but 0 * NaN would still poison O: zero those rows of
