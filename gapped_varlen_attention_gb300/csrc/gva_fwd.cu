@@ -55,15 +55,17 @@ struct Cfg {
   static constexpr int kKVBytes = kBlockKeys * D * 2;    // one K or V block
   static constexpr int kQChunkBytes = kTileRows * 128;   // one 64-column chunk of a Q tile
   static constexpr int kKVChunkBytes = kBlockKeys * 128;
-  static constexpr int kStages = D == 64 ? 3 : 2;        // K stages; V has as many
-  static constexpr int kSmem = kTilesPerItem * kQBytes + 2 * kStages * kKVBytes;
+  // One ring of K/V slots, loaded in the order K_0, V_0, K_1, V_1, ... so the producer
+  // runs about two key blocks ahead of the tensor core.
+  static constexpr int kSlots = D == 64 ? 10 : 5;
+  static constexpr int kSmem = kTilesPerItem * kQBytes + kSlots * kKVBytes;
   static constexpr int kSmemAlloc = kSmem + 1024;        // slack for 1024-byte alignment
   static_assert(kSmemAlloc <= 227 * 1024, "shared memory budget");
 };
 
 struct Ctrl {
   uint64_t q_full, q_empty;
-  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t kv_full[10], kv_empty[10];
   uint64_t s_full[2], p_full[2], o_full[2];
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -112,28 +114,29 @@ __device__ __forceinline__ WorkItem load_item(const WorkItem* items, int idx) {
   return it;
 }
 
+// MMA issue. One thread issues every tcgen05.mma, so the issue path must be short:
+// the shared-memory descriptors are built once per operand buffer, and each K step only
+// adds its byte offset (in 16-byte units) to the start-address field (bits 0-13; every
+// address here is below 256 KB, so the field never carries). Building a 64-bit
+// descriptor per MMA instead costs more issue time than a 128x128x16 MMA executes.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t s_col, uint32_t q_smem, uint32_t k_smem) {
+__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint64_t q_desc, uint64_t k_desc) {
   constexpr uint32_t idesc = make_idesc_bf16(kTileRows, kBlockKeys, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off_q = (kk / 4) * Cfg<D>::kQChunkBytes + (kk % 4) * 32;
-    const uint32_t off_k = (kk / 4) * Cfg<D>::kKVChunkBytes + (kk % 4) * 32;
-    umma_bf16_ss(tmem + s_col, make_smem_desc_sw128(q_smem + off_q, 16, 1024),
-                 make_smem_desc_sw128(k_smem + off_k, 16, 1024), idesc, kk > 0);
+    static_assert(Cfg<D>::kQChunkBytes == Cfg<D>::kKVChunkBytes, "Q and K chunks share offsets");
+    const uint32_t off = ((kk / 4) * Cfg<D>::kQChunkBytes + (kk % 4) * 32) >> 4;
+    umma_bf16_ss(tmem_s, q_desc + off, k_desc + off, idesc, kk > 0);
   }
 }
 
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t s_col, uint32_t o_col, uint32_t v_smem,
-                                         bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint64_t v_desc, uint32_t accumulate) {
   constexpr uint32_t idesc = make_idesc_bf16(kTileRows, D, true);
+  umma_bf16_ts(tmem_o, tmem_p, v_desc, idesc, accumulate);
 #pragma unroll
-  for (int kk = 0; kk < kBlockKeys / 16; ++kk) {
-    umma_bf16_ts(tmem + o_col, tmem + s_col + kk * 8,
-                 make_smem_desc_sw128(v_smem + kk * 16 * 128, Cfg<D>::kKVChunkBytes, 1024), idesc,
-                 (accumulate || kk > 0) ? 1u : 0u);
-  }
+  for (int kk = 1; kk < kBlockKeys / 16; ++kk)
+    umma_bf16_ts(tmem_o, tmem_p + kk * 8, v_desc + ((kk * 16 * 128) >> 4), idesc, 1u);
 }
 
 template <typename TOut>
@@ -161,13 +164,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     gva_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                    const __grid_constant__ CUtensorMap map_v, const FwdParams p) {
   using C = Cfg<D>;
-  constexpr int S = C::kStages;
+  constexpr uint32_t NS = C::kSlots;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Ctrl ctrl;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;                                          // 2 tiles
-  uint8_t* sK = sQ + kTilesPerItem * C::kQBytes;               // S stages
-  uint8_t* sV = sK + S * C::kKVBytes;                          // S stages
+  uint8_t* sKV = sQ + kTilesPerItem * C::kQBytes;              // NS slots
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -176,11 +178,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&ctrl.q_full, 1);
     mbar_init(&ctrl.q_empty, 1);
-    for (int i = 0; i < S; ++i) {
-      mbar_init(&ctrl.k_full[i], 1);
-      mbar_init(&ctrl.k_empty[i], 1);
-      mbar_init(&ctrl.v_full[i], 1);
-      mbar_init(&ctrl.v_empty[i], 1);
+    for (uint32_t i = 0; i < NS; ++i) {
+      mbar_init(&ctrl.kv_full[i], 1);
+      mbar_init(&ctrl.kv_empty[i], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&ctrl.s_full[t], 1);
@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&map_q);
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
-      uint32_t q_it = 0, kb = 0, vb = 0;
+      uint32_t q_it = 0, ld = 0;  // ld: loads issued into the K/V ring so far
       for (int round = 0;; ++round) {
         const int idx = item_index(round, blockIdx.x, gridDim.x);
         if (idx >= p.num_items) break;
@@ -226,39 +226,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int j = 0; j < nblk && ok; ++j) {
           const int key0 = it.k_row0 + j * kBlockKeys;
-          const uint32_t ks = kb % S, vs = vb % S;
-          ok = wait_bar(&ctrl.k_empty[ks], ((kb / S) & 1) ^ 1, abort_flag, p.error_flag);
-          if (!ok) break;
-          mbar_arrive_expect_tx(&ctrl.k_full[ks], C::kKVBytes);
 #pragma unroll
-          for (int ch = 0; ch < C::kChunks; ++ch)
-            tma_load_3d(sK + ks * C::kKVBytes + ch * C::kKVChunkBytes, &map_k, &ctrl.k_full[ks], ch * 64, key0,
-                        it.head_kv);
-          ++kb;
-          ok = wait_bar(&ctrl.v_empty[vs], ((vb / S) & 1) ^ 1, abort_flag, p.error_flag);
-          if (!ok) break;
-          mbar_arrive_expect_tx(&ctrl.v_full[vs], C::kKVBytes);
+          for (int kv = 0; kv < 2; ++kv) {  // K_j, then V_j
+            const uint32_t sl = ld % NS;
+            ok = wait_bar(&ctrl.kv_empty[sl], ((ld / NS) & 1) ^ 1, abort_flag, p.error_flag);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&ctrl.kv_full[sl], C::kKVBytes);
+            const CUtensorMap* map = kv == 0 ? &map_k : &map_v;
 #pragma unroll
-          for (int ch = 0; ch < C::kChunks; ++ch)
-            tma_load_3d(sV + vs * C::kKVBytes + ch * C::kKVChunkBytes, &map_v, &ctrl.v_full[vs], ch * 64, key0,
-                        it.head_kv);
-          ++vb;
+            for (int ch = 0; ch < C::kChunks; ++ch)
+              tma_load_3d(sKV + sl * C::kKVBytes + ch * C::kKVChunkBytes, map, &ctrl.kv_full[sl], ch * 64, key0,
+                          it.head_kv);
+            ++ld;
+          }
         }
         if (!ok) break;
       }
       // Drain: every copy this thread issued has landed before the CTA may exit.
       if (q_it > 0) drain_bar(&ctrl.q_full, (q_it - 1) & 1, p.error_flag);
-      for (uint32_t i = (kb > (uint32_t)S ? kb - S : 0); i < kb; ++i) drain_bar(&ctrl.k_full[i % S], (i / S) & 1, p.error_flag);
-      for (uint32_t i = (vb > (uint32_t)S ? vb - S : 0); i < vb; ++i) drain_bar(&ctrl.v_full[i % S], (i / S) & 1, p.error_flag);
+      for (uint32_t i = (ld > NS ? ld - NS : 0); i < ld; ++i) drain_bar(&ctrl.kv_full[i % NS], (i / NS) & 1, p.error_flag);
     }
     __syncwarp();
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t q_base = smem_addr(sQ);
-      const uint32_t k_base = smem_addr(sK);
-      const uint32_t v_base = smem_addr(sV);
-      uint32_t q_it = 0, kb = 0, vb = 0, pc0 = 0, pc1 = 0;
+      // Descriptors of the first buffer of each kind; the others are whole-buffer offsets
+      // of the start-address field. A slot holds K (K-major operand) or V (MN-major).
+      const uint64_t q_desc0 = make_smem_desc_sw128(smem_addr(sQ), 16, 1024);
+      const uint64_t k_desc0 = make_smem_desc_sw128(smem_addr(sKV), 16, 1024);
+      const uint64_t v_desc0 = make_smem_desc_sw128(smem_addr(sKV), C::kKVChunkBytes, 1024);
+      const uint64_t q_desc[2] = {q_desc0, q_desc0 + (C::kQBytes >> 4)};
+      auto k_desc = [&](uint32_t sl) { return k_desc0 + sl * (C::kKVBytes >> 4); };
+      auto v_desc = [&](uint32_t sl) { return v_desc0 + sl * (C::kKVBytes >> 4); };
+      uint32_t q_it = 0, blk = 0, pc0 = 0, pc1 = 0;  // blk: key blocks consumed so far
       bool ok = true;
       for (int round = 0; ok; ++round) {
         const int idx = item_index(round, blockIdx.x, gridDim.x);
@@ -270,33 +270,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = wait_bar(&ctrl.q_full, q_it & 1, abort_flag, p.error_flag);
         if (!ok) break;
         ++q_it;
-        uint32_t ks = kb % S;
-        ok = wait_bar(&ctrl.k_full[ks], (kb / S) & 1, abort_flag, p.error_flag);
+        // K_j has ring sequence number 2 * (blk + j), V_j the next one.
+        uint32_t kseq = 2 * blk;
+        ok = wait_bar(&ctrl.kv_full[kseq % NS], (kseq / NS) & 1, abort_flag, p.error_flag);
         if (!ok) break;
         tcgen05_fence_after();
-        issue_qk<D>(tmem, col_s(0), q_base, k_base + ks * C::kKVBytes);
+        issue_qk<D>(tmem + col_s(0), q_desc[0], k_desc(kseq % NS));
         umma_commit(&ctrl.s_full[0]);
         if (two) {
-          issue_qk<D>(tmem, col_s(1), q_base + C::kQBytes, k_base + ks * C::kKVBytes);
+          issue_qk<D>(tmem + col_s(1), q_desc[1], k_desc(kseq % NS));
           umma_commit(&ctrl.s_full[1]);
         }
-        umma_commit(&ctrl.k_empty[ks]);
-        ++kb;
+        umma_commit(&ctrl.kv_empty[kseq % NS]);
         if (nblk == 1) umma_commit(&ctrl.q_empty);
         for (int j = 0; j < nblk; ++j) {
           const bool more = j + 1 < nblk;
-          const uint32_t vs = vb % S;
-          ks = kb % S;
-          ok = wait_bar(&ctrl.v_full[vs], (vb / S) & 1, abort_flag, p.error_flag);
-          if (ok && more) ok = wait_bar(&ctrl.k_full[ks], (kb / S) & 1, abort_flag, p.error_flag);
+          const uint32_t vseq = 2 * (blk + j) + 1;
+          kseq = vseq + 1;  // K_{j+1}
+          ok = wait_bar(&ctrl.kv_full[vseq % NS], (vseq / NS) & 1, abort_flag, p.error_flag);
           if (ok) ok = wait_bar(&ctrl.p_full[0], pc0 & 1, abort_flag, p.error_flag);
           if (!ok) break;
           ++pc0;
           tcgen05_fence_after();
-          issue_pv<D>(tmem, col_s(0), col_o(0), v_base + vs * C::kKVBytes, j > 0);
+          issue_pv<D>(tmem + col_o(0), tmem + col_s(0), v_desc(vseq % NS), j > 0);
           if (!more) umma_commit(&ctrl.o_full[0]);
           if (more) {
-            issue_qk<D>(tmem, col_s(0), q_base, k_base + ks * C::kKVBytes);
+            ok = wait_bar(&ctrl.kv_full[kseq % NS], (kseq / NS) & 1, abort_flag, p.error_flag);
+            if (!ok) break;
+            tcgen05_fence_after();
+            issue_qk<D>(tmem + col_s(0), q_desc[0], k_desc(kseq % NS));
             umma_commit(&ctrl.s_full[0]);
           }
           if (two) {
@@ -304,21 +306,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             ++pc1;
             tcgen05_fence_after();
-            issue_pv<D>(tmem, col_s(1), col_o(1), v_base + vs * C::kKVBytes, j > 0);
+            issue_pv<D>(tmem + col_o(1), tmem + col_s(1), v_desc(vseq % NS), j > 0);
             if (!more) umma_commit(&ctrl.o_full[1]);
             if (more) {
-              issue_qk<D>(tmem, col_s(1), q_base + C::kQBytes, k_base + ks * C::kKVBytes);
+              issue_qk<D>(tmem + col_s(1), q_desc[1], k_desc(kseq % NS));
               umma_commit(&ctrl.s_full[1]);
             }
           }
-          umma_commit(&ctrl.v_empty[vs]);
-          ++vb;
+          umma_commit(&ctrl.kv_empty[vseq % NS]);
           if (more) {
-            umma_commit(&ctrl.k_empty[ks]);
-            ++kb;
+            umma_commit(&ctrl.kv_empty[kseq % NS]);
             if (j + 2 == nblk) umma_commit(&ctrl.q_empty);
           }
         }
+        blk += nblk;
       }
       // Every MMA issued so far completes before TMEM is released.
       umma_commit(&ctrl.mma_done);
@@ -446,11 +447,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Keys past the used length in this V block (gap, padding or another
           // segment) get P = 0, but 0 * NaN would still poison O: zero those rows of
           // the staged V block before the PV MMA reads it.
-          const uint32_t vblk = vb + j;
+          const uint32_t vseq = 2 * (vb + j) + 1;  // ring sequence number of V_j
           ok = __all_sync(0xffffffffu,
-                          wait_bar(&ctrl.v_full[vblk % S], (vblk / S) & 1, abort_flag, p.error_flag));
+                          wait_bar(&ctrl.kv_full[vseq % NS], (vseq / NS) & 1, abort_flag, p.error_flag));
           if (!ok) break;
-          uint8_t* vbase = sV + (vblk % S) * C::kKVBytes;
+          uint8_t* vbase = sKV + (vseq % NS) * C::kKVBytes;
           const int n16 = (kBlockKeys - rem) * C::kChunks * 8;  // 16-byte pieces to clear
           for (int i = row; i < n16; i += 128) {
             const int r = rem + i / (C::kChunks * 8);
