@@ -162,7 +162,7 @@ def recorded_traffic(workload: str):
         return None
     text = open(TRAFFIC_SUMMARY).read()
     h = re.search(r"kernel source sha256\[:16\]:\s*`?([0-9a-f]{16})", text)
-    t = re.search(r"dram bytes per full launch:\s*`?([0-9.eE+]+)", text)
+    t = re.search(r"dram bytes per full launch\s*[:|]\s*`?([0-9.eE+]+)", text)
     if not h or not t or h.group(1) != fwd_source_hash():
         return None
     return float(t.group(1))
