@@ -48,7 +48,7 @@ from typing import Optional, Sequence
 
 import numpy as np
 
-__all__ = ["attention_forward", "attention_rows", "lse_merge", "used_flops"]
+__all__ = ["attention_forward", "attention_forward_ranges", "attention_rows", "lse_merge", "used_flops"]
 
 DEFAULT_BUDGET_BYTES = 1 << 30
 
@@ -123,6 +123,50 @@ def attention_forward(q, k, v, cu_q, used_q, cu_k, used_k, *, scale: Optional[fl
             qs = q[r0:r0 + nq, hk * g:(hk + 1) * g, :].astype(np.float64).reshape(nq * g, d)
             ks = k[k0:k0 + nk, hk, :].astype(np.float64)
             vs = v[k0:k0 + nk, hk, :].astype(np.float64)
+            ob, lb = _segment_attention(qs, ks, vs, s, budget_bytes)
+            o_out[r0:r0 + nq, hk * g:(hk + 1) * g, :] = ob.reshape(nq, g, -1)
+            l_out[hk * g:(hk + 1) * g, r0:r0 + nq] = lb.reshape(nq, g).T
+    return o_out, l_out
+
+
+def attention_forward_ranges(q, k, v, cu_q, used_q, key_ranges, *, scale: Optional[float] = None, out=None,
+                             lse=None, num_heads_kv: Optional[int] = None,
+                             budget_bytes: int = DEFAULT_BUDGET_BYTES):
+    """The forward when a segment's keys are several row ranges of K/V.
+
+    ``key_ranges[b]`` lists ``(start, length)`` pairs; segment b's keys are the
+    concatenation of K/V rows ``start .. start + length`` over its pairs, in order.
+    This is the single-launch form of the visibility partitions of cosmos-framework
+    PR #312 ("Problem and behavior"), and covers valid keys that are not a prefix
+    (TensorRT-LLM issue #18687, "additional notes": rank-major key order). With one
+    ``(cu_k[b], used_k[b])`` pair per segment it is ``attention_forward``.
+    Rows past a segment's used length keep ``out`` / ``lse``; no keys at all gives
+    0 / -inf. FP64."""
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    total_q, hq, d = q.shape
+    hkv = k.shape[1] if num_heads_kv is None else num_heads_kv
+    if hq % hkv:
+        raise ValueError(f"Hq={hq} is not a multiple of Hkv={hkv}")
+    g = hq // hkv
+    s = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    cu_q = np.asarray(cu_q, np.int64)
+    used_q = np.asarray(used_q, np.int64)
+    o_out = np.zeros((total_q, hq, v.shape[2]), np.float64) if out is None else _as_f64(out).astype(np.float64, copy=True)
+    l_out = np.zeros((hq, total_q), np.float64) if lse is None else _as_f64(lse).astype(np.float64, copy=True)
+    for b in range(len(used_q)):
+        r0, nq = int(cu_q[b]), int(used_q[b])
+        if nq == 0:
+            continue
+        rows = [np.arange(int(st), int(st) + int(n)) for st, n in key_ranges[b] if int(n) > 0]
+        idx = np.concatenate(rows) if rows else np.zeros(0, np.int64)
+        if idx.size == 0:
+            o_out[r0:r0 + nq] = 0.0
+            l_out[:, r0:r0 + nq] = -np.inf
+            continue
+        for hk in range(hkv):
+            qs = q[r0:r0 + nq, hk * g:(hk + 1) * g, :].astype(np.float64).reshape(nq * g, d)
+            ks = k[idx, hk, :].astype(np.float64)
+            vs = v[idx, hk, :].astype(np.float64)
             ob, lb = _segment_attention(qs, ks, vs, s, budget_bytes)
             o_out[r0:r0 + nq, hk * g:(hk + 1) * g, :] = ob.reshape(nq, g, -1)
             l_out[hk * g:(hk + 1) * g, r0:r0 + nq] = lb.reshape(nq, g).T

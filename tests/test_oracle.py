@@ -249,9 +249,48 @@ def pin_rows_match(orc):
     assert np.array_equal(o2, o[rows]) and np.array_equal(l2, l[:, rows])
 
 
+def pin_ranges(orc):
+    """Key ranges: one prefix range per segment is the plain forward (bit for bit);
+    several ranges equal the LSE merge of their separate forwards; an empty range list
+    gives 0 / -inf."""
+    rng = np.random.default_rng(16)
+    g = W.random_geometry(rng, 4, 7, 30, 4, 2, 8, allow_empty=False)
+    q = _rand(rng, g.total_q, 4, 8)
+    k = _rand(rng, g.total_k, 2, 8)
+    v = _rand(rng, g.total_k, 2, 8)
+    prefix = [[(int(g.cu_k[b]), int(g.used_k[b]))] for b in range(g.num_segments)]
+    a = orc.attention_forward(q, k, v, g.cu_q, g.used_q, g.cu_k, g.used_k)
+    b = orc.attention_forward_ranges(q, k, v, g.cu_q, g.used_q, prefix)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    # arbitrary ranges anywhere in K/V (including overlaps across segments and gaps)
+    ranges = []
+    for b_ in range(g.num_segments):
+        rr = []
+        for _ in range(int(rng.integers(1, 4))):
+            st = int(rng.integers(0, g.total_k))
+            rr.append((st, int(rng.integers(0, g.total_k - st + 1))))
+        if sum(n for _, n in rr) == 0:
+            rr.append((0, 1))
+        ranges.append(rr)
+    full = orc.attention_forward_ranges(q, k, v, g.cu_q, g.used_q, ranges)
+    parts = []
+    for i in range(3):
+        sub = [[rr[i]] if i < len(rr) else [] for rr in ranges]
+        parts.append(orc.attention_forward_ranges(q, k, v, g.cu_q, g.used_q, sub))
+    o, l = orc.lse_merge([x[0] for x in parts], [x[1] for x in parts], g.cu_q, g.used_q)
+    used = ~W.gap_rows(g.cu_q, g.used_q)
+    np.testing.assert_allclose(o[used], full[0][used], atol=1e-12)
+    np.testing.assert_allclose(l[:, used], full[1][:, used], atol=1e-12)
+    none = orc.attention_forward_ranges(q, k, v, g.cu_q, g.used_q, [[] for _ in range(g.num_segments)])
+    assert np.all(none[0][used] == 0.0) and np.all(np.isneginf(none[1][:, used]))
+    # the concatenation order of the ranges does not matter
+    rev = orc.attention_forward_ranges(q, k, v, g.cu_q, g.used_q, [list(reversed(rr)) for rr in ranges])
+    np.testing.assert_allclose(rev[0], full[0], atol=1e-12)
+
+
 PINS = [pin_bruteforce, pin_default_scale, pin_dilution_golden, pin_zero_keys_closed_form,
         pin_single_key, pin_keyless_and_gap_rows, pin_pad_invariance, pin_sdpa_equal_lengths,
-        pin_gqa_repeat, pin_key_permutation, pin_merge_union, pin_rows_match]
+        pin_gqa_repeat, pin_key_permutation, pin_merge_union, pin_rows_match, pin_ranges]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -284,6 +323,7 @@ MUTANTS = {
     "transposed_lse": ("lb.reshape(nq, g).T", "lb.reshape(g, nq)"),
     "merge_weight_sign": ("np.exp(ls - safe[None])", "np.exp(safe[None] - ls)"),
     "sqrt_d_scale": ("1.0 / math.sqrt(d) if scale is None", "1.0 / d if scale is None"),
+    "range_end_dropped": ("np.arange(int(st), int(st) + int(n))", "np.arange(int(st), int(st) + int(n) - 1)"),
 }
 
 
