@@ -86,6 +86,13 @@ class Workload:
             self.q, self.k, self.v = W.make_qkv(full, 1003 + seed_offset, device=dev)
             self.parts = full
             self.label = "multiview causal gapped replay: 7 segments, 2 visibility partitions + FP32 LSE merge"
+        elif name == "multiview_fused":
+            full, parts = W.multiview_causal()
+            self.geoms = [full]
+            self.q, self.k, self.v = W.make_qkv(full, 1003 + seed_offset, device=dev)
+            self.parts = None
+            self.ranges = [[(int(p.cu_k[b]), int(p.used_k[b])) for p in parts] for b in range(full.num_segments)]
+            self.label = "multiview causal gapped replay: 7 segments, 2 visibility partitions fused in one launch"
         elif name == "tiny":
             g = W.tiny()
             self.geoms = [g]
@@ -94,7 +101,12 @@ class Workload:
             self.label = "tiny: 3 segments, Hq=4, Hkv=2, d=64"
         else:
             raise SystemExit(f"unknown workload {name}")
-        self.plans = [gva.Plan.from_geometry(g) for g in self.geoms]
+        if getattr(self, "ranges", None) is not None:
+            g = self.geoms[0]
+            self.plans = [gva.Plan.from_ranges(g.cu_q, g.used_q, self.ranges, g.total_k, g.num_heads_q,
+                                               g.num_heads_kv, g.head_dim)]
+        else:
+            self.plans = [gva.Plan.from_geometry(g) for g in self.geoms]
         g0 = self.geoms[0]
         if self.parts is None:
             self.out, self.lse = W.make_outputs(g0, 0.0, device=dev)
@@ -276,7 +288,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gva", "reference"], default="gva")
     ap.add_argument("--workload", default="long_replay",
-                    choices=["long_replay", "long_replay_small", "cfg_text_cross", "multiview_causal", "tiny"])
+                    choices=["long_replay", "long_replay_small", "cfg_text_cross", "multiview_causal",
+                             "multiview_fused", "tiny"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     args = ap.parse_args()
@@ -437,7 +450,7 @@ def run_reference(args, world, rank):
         g = W.cfg_text_cross()
         wl.geoms = [g]
         seed = 1002
-    elif args.workload == "multiview_causal":
+    elif args.workload in ("multiview_causal", "multiview_fused"):
         g, parts = W.multiview_causal()
         wl.geoms = parts
         seed = 1003

@@ -21,7 +21,7 @@ GVA_BF16, GVA_FP32 = 0, 1
 
 # Every symbol include/gva.h declares.
 EXPORTS = ("gva_plan", "gva_forward", "gva_lse_merge", "gva_plan_destroy", "gva_plan_get_info",
-           "gva_device_status", "gva_status_string", "gva_last_error", "gva_forward_noalloc")
+           "gva_device_status", "gva_status_string", "gva_last_error", "gva_forward_noalloc", "gva_plan_ranges")
 NOALLOC_MAX_WORK_ITEMS = 32768  # GVA_NOALLOC_MAX_WORK_ITEMS in include/gva.h
 
 
@@ -66,8 +66,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.gva_last_error.restype = ctypes.c_char_p
     lib.gva_forward_noalloc.argtypes = [pi32, pi32, pi32, pi32, i32, i32, i32, i32, vp, vp, vp, vp, i32, vp, f32,
                                         vp]
+    lib.gva_plan_ranges.argtypes = [pi32, pi32, i32, pi32, pi32, pi32, ctypes.c_int64, i32, i32, i32,
+                                    ctypes.POINTER(vp)]
     for name in ("gva_plan", "gva_forward", "gva_lse_merge", "gva_plan_destroy", "gva_plan_get_info",
-                 "gva_device_status", "gva_forward_noalloc"):
+                 "gva_device_status", "gva_forward_noalloc", "gva_plan_ranges"):
         getattr(lib, name).restype = i32
     if path is None:
         _lib = lib
@@ -108,6 +110,33 @@ class Plan:
     @classmethod
     def from_geometry(cls, g) -> "Plan":
         return cls(g.cu_q, g.used_q, g.cu_k, g.used_k, g.num_heads_q, g.num_heads_kv, g.head_dim)
+
+    @classmethod
+    def from_ranges(cls, cu_seqlens_q, seqused_q, key_ranges, total_k: int, num_heads_q: int, num_heads_kv: int,
+                    head_dim: int) -> "Plan":
+        """``gva_plan_ranges``: segment b attends the concatenation of the K/V row ranges
+        ``key_ranges[b]`` (a list of ``(start, length)`` pairs)."""
+        self = cls.__new__(cls)
+        self._lib = load_library()
+        self.cu_q, self.used_q = _i32(cu_seqlens_q), _i32(seqused_q)
+        n = int(self.used_q.shape[0])
+        if self.cu_q.shape[0] != n + 1 or len(key_ranges) != n:
+            raise ValueError("cu_seqlens_q must have num_segments + 1 entries, seqused_q and key_ranges num_segments")
+        off = _i32(np.concatenate([[0], np.cumsum([len(r) for r in key_ranges])]))
+        flat = [x for r in key_ranges for x in r]
+        starts = _i32([st for st, _ in flat]) if flat else _i32(np.zeros(1))
+        lens = _i32([ln for _, ln in flat]) if flat else _i32(np.zeros(1))
+        ptr = ctypes.c_void_p()
+        as_p = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))  # noqa: E731
+        st = self._lib.gva_plan_ranges(as_p(self.cu_q), as_p(self.used_q), n, as_p(off), as_p(starts), as_p(lens),
+                                       int(total_k), int(num_heads_q), int(num_heads_kv), int(head_dim),
+                                       ctypes.byref(ptr))
+        _check(self._lib, st, "gva_plan_ranges")
+        self._handle = ptr
+        self.num_heads_q, self.num_heads_kv, self.head_dim = int(num_heads_q), int(num_heads_kv), int(head_dim)
+        self.total_q, self.total_k = int(self.cu_q[-1]), int(total_k)
+        self.cu_k = self.used_k = None
+        return self
 
     @property
     def handle(self) -> ctypes.c_void_p:

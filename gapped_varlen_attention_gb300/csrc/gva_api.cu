@@ -21,6 +21,7 @@ struct gva_plan {
   int32_t num_items = 0, num_units = 0, grid = 0, merge_grid = 0;
   double used_flops = 0.0;
   gva::WorkItem* d_items = nullptr;
+  gva::KeyBlock* d_blocks = nullptr;
   gva::MergeUnit* d_units = nullptr;
   int* d_error = nullptr;
 };
@@ -97,44 +98,34 @@ gva_status validate_offsets(const int32_t* cu, const int32_t* used, int32_t n, c
 void free_plan(struct gva_plan* p) {
   if (p == nullptr) return;
   if (p->d_items) cudaFree(p->d_items);
+  if (p->d_blocks) cudaFree(p->d_blocks);
   if (p->d_units) cudaFree(p->d_units);
   if (p->d_error) cudaFree(p->d_error);
   delete p;
 }
 
-}  // namespace
-
-namespace gva {
-void set_last_error(const char* message) { g_last_error = message; }
-}  // namespace gva
-
-extern "C" {
-
-gva_status gva_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, const int32_t* cu_seqlens_k,
-                    const int32_t* seqused_k, int32_t num_segments, int32_t num_heads_q, int32_t num_heads_kv,
-                    int32_t head_dim, gva_plan_t* out_plan) {
-  if (out_plan == nullptr) return fail(GVA_ERR_INVALID_ARG, "out_plan is NULL");
-  *out_plan = nullptr;
-  // ---- host-only validation (no CUDA call before this block passes)
-  if (num_segments < 0) return fail(GVA_ERR_INVALID_ARG, "num_segments = %d < 0", num_segments);
-  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr || (num_segments > 0 && (seqused_q == nullptr || seqused_k == nullptr)))
-    return fail(GVA_ERR_INVALID_ARG, "a geometry array is NULL");
-  if (num_heads_q <= 0 || num_heads_kv <= 0)
-    return fail(GVA_ERR_INVALID_ARG, "head counts must be positive (Hq=%d, Hkv=%d)", num_heads_q, num_heads_kv);
-  if (num_heads_q % num_heads_kv != 0)
-    return fail(GVA_ERR_INVALID_ARG, "num_heads_q=%d is not divisible by num_heads_kv=%d", num_heads_q, num_heads_kv);
+// Shared by gva_plan and gva_plan_ranges once the arguments are validated: segment b's
+// keys are the ranges range_off[b] .. range_off[b+1] of (range_start, range_len).
+gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int32_t num_segments,
+                      const int32_t* range_off, const int32_t* range_start, const int32_t* range_len,
+                      int64_t total_k, int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim,
+                      gva_plan_t* out_plan) {
   const int32_t group = num_heads_q / num_heads_kv;
-  if (gva::kTileRows % group != 0)
-    return fail(GVA_ERR_UNSUPPORTED, "query heads per KV head (%d) must divide %d", group, gva::kTileRows);
-  if (head_dim != 64 && head_dim != 128)
-    return fail(GVA_ERR_UNSUPPORTED, "head_dim=%d is not supported (64 or 128)", head_dim);
-  if (num_heads_q * gva::kMergeRows * gva::kMaxMergeParts * 4 > 200 * 1024)
-    return fail(GVA_ERR_UNSUPPORTED, "num_heads_q=%d is too large", num_heads_q);
-  gva_status s = validate_offsets(cu_seqlens_q, seqused_q, num_segments, "q");
-  if (s != GVA_OK) return s;
-  s = validate_offsets(cu_seqlens_k, seqused_k, num_segments, "k");
-  if (s != GVA_OK) return s;
-
+  // ---- key blocks: each range cut into blocks of at most kBlockKeys keys
+  std::vector<gva::KeyBlock> blocks;
+  std::vector<int32_t> seg_blk0(num_segments), seg_nblk(num_segments), seg_keys(num_segments);
+  for (int32_t b = 0; b < num_segments; ++b) {
+    seg_blk0[b] = static_cast<int32_t>(blocks.size());
+    int64_t keys = 0;
+    for (int32_t r = range_off[b]; r < range_off[b + 1]; ++r) {
+      for (int32_t o = 0; o < range_len[r]; o += gva::kBlockKeys)
+        blocks.push_back({range_start[r] + o, std::min(gva::kBlockKeys, range_len[r] - o)});
+      keys += range_len[r];
+    }
+    if (keys > INT32_MAX) return fail(GVA_ERR_INVALID_ARG, "segment %d has more than 2^31 keys", b);
+    seg_nblk[b] = static_cast<int32_t>(blocks.size()) - seg_blk0[b];
+    seg_keys[b] = static_cast<int32_t>(keys);
+  }
   // ---- work list: (segment, KV head, 2 x 128 folded rows), keyless items epilogue-only
   const int32_t tokens_per_tile = gva::kTileRows / group;
   const int32_t tokens_per_item = tokens_per_tile * gva::kTilesPerItem;
@@ -143,22 +134,22 @@ gva_status gva_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, const
   std::vector<gva::MergeUnit> units;
   double flops = 0.0;
   for (int32_t b = 0; b < num_segments; ++b) {
-    const int32_t uq = seqused_q[b], uk = seqused_k[b];
-    flops += 4.0 * head_dim * num_heads_q * static_cast<double>(uq) * static_cast<double>(uk);
+    const int32_t uq = seqused_q[b];
+    flops += 4.0 * head_dim * num_heads_q * static_cast<double>(uq) * static_cast<double>(seg_keys[b]);
     for (int32_t r0 = 0; r0 < uq; r0 += gva::kMergeRows)
       units.push_back({cu_seqlens_q[b] + r0, std::min(gva::kMergeRows, uq - r0)});
-    const int64_t nblk = (uk + gva::kBlockKeys - 1) / gva::kBlockKeys;
     for (int32_t hk = 0; hk < num_heads_kv; ++hk) {
       for (int32_t t0 = 0; t0 < uq; t0 += tokens_per_item) {
         gva::WorkItem it{};
         it.q_row0 = cu_seqlens_q[b] + t0;
         it.q_rows = std::min(tokens_per_item, uq - t0);
-        it.k_row0 = cu_seqlens_k[b];
-        it.k_len = uk;
+        it.blk0 = seg_blk0[b];
+        it.nblk = seg_nblk[b];
         it.head_kv = hk;
         it.n_tiles = it.q_rows > tokens_per_tile ? 2 : 1;
+        it.k_len = seg_keys[b];
         items.push_back(it);
-        cost.push_back(nblk * it.n_tiles * 4 + it.n_tiles);
+        cost.push_back(static_cast<int64_t>(it.nblk) * it.n_tiles * 4 + it.n_tiles);
       }
     }
   }
@@ -189,7 +180,7 @@ gva_status gva_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, const
   p->head_dim = head_dim;
   p->group = group;
   p->total_q = cu_seqlens_q[num_segments];
-  p->total_k = cu_seqlens_k[num_segments];
+  p->total_k = total_k;
   p->num_items = static_cast<int32_t>(sorted.size());
   p->num_units = static_cast<int32_t>(units.size());
   p->grid = std::min(p->num_items, sms);
@@ -207,6 +198,14 @@ gva_status gva_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, const
       return cuda_fail(e, "uploading the work list");
     }
   }
+  if (!blocks.empty()) {
+    if ((e = cudaMalloc(&p->d_blocks, blocks.size() * sizeof(gva::KeyBlock))) != cudaSuccess ||
+        (e = cudaMemcpy(p->d_blocks, blocks.data(), blocks.size() * sizeof(gva::KeyBlock), cudaMemcpyHostToDevice)) !=
+            cudaSuccess) {
+      free_plan(p);
+      return cuda_fail(e, "uploading the key blocks");
+    }
+  }
   if (!units.empty()) {
     if ((e = cudaMalloc(&p->d_units, units.size() * sizeof(gva::MergeUnit))) != cudaSuccess ||
         (e = cudaMemcpy(p->d_units, units.data(), units.size() * sizeof(gva::MergeUnit), cudaMemcpyHostToDevice)) !=
@@ -217,6 +216,84 @@ gva_status gva_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, const
   }
   *out_plan = p;
   return ok();
+}
+
+// Checks shared by both plan builders (before any CUDA call).
+gva_status validate_common(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int32_t num_segments,
+                           int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim) {
+  if (num_segments < 0) return fail(GVA_ERR_INVALID_ARG, "num_segments = %d < 0", num_segments);
+  if (cu_seqlens_q == nullptr || (num_segments > 0 && seqused_q == nullptr))
+    return fail(GVA_ERR_INVALID_ARG, "a geometry array is NULL");
+  if (num_heads_q <= 0 || num_heads_kv <= 0)
+    return fail(GVA_ERR_INVALID_ARG, "head counts must be positive (Hq=%d, Hkv=%d)", num_heads_q, num_heads_kv);
+  if (num_heads_q % num_heads_kv != 0)
+    return fail(GVA_ERR_INVALID_ARG, "num_heads_q=%d is not divisible by num_heads_kv=%d", num_heads_q, num_heads_kv);
+  const int32_t group = num_heads_q / num_heads_kv;
+  if (gva::kTileRows % group != 0)
+    return fail(GVA_ERR_UNSUPPORTED, "query heads per KV head (%d) must divide %d", group, gva::kTileRows);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(GVA_ERR_UNSUPPORTED, "head_dim=%d is not supported (64 or 128)", head_dim);
+  if (num_heads_q * gva::kMergeRows * gva::kMaxMergeParts * 4 > 200 * 1024)
+    return fail(GVA_ERR_UNSUPPORTED, "num_heads_q=%d is too large", num_heads_q);
+  return validate_offsets(cu_seqlens_q, seqused_q, num_segments, "q");
+}
+
+}  // namespace
+
+namespace gva {
+void set_last_error(const char* message) { g_last_error = message; }
+}  // namespace gva
+
+extern "C" {
+
+gva_status gva_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, const int32_t* cu_seqlens_k,
+                    const int32_t* seqused_k, int32_t num_segments, int32_t num_heads_q, int32_t num_heads_kv,
+                    int32_t head_dim, gva_plan_t* out_plan) {
+  if (out_plan == nullptr) return fail(GVA_ERR_INVALID_ARG, "out_plan is NULL");
+  *out_plan = nullptr;
+  // ---- host-only validation (no CUDA call before it passes)
+  gva_status s = validate_common(cu_seqlens_q, seqused_q, num_segments, num_heads_q, num_heads_kv, head_dim);
+  if (s != GVA_OK) return s;
+  if (cu_seqlens_k == nullptr || (num_segments > 0 && seqused_k == nullptr))
+    return fail(GVA_ERR_INVALID_ARG, "a geometry array is NULL");
+  s = validate_offsets(cu_seqlens_k, seqused_k, num_segments, "k");
+  if (s != GVA_OK) return s;
+  // one key range per segment: its used prefix
+  std::vector<int32_t> off(num_segments + 1), start(num_segments), len(num_segments);
+  for (int32_t b = 0; b <= num_segments; ++b) off[b] = b;
+  for (int32_t b = 0; b < num_segments; ++b) {
+    start[b] = cu_seqlens_k[b];
+    len[b] = seqused_k[b];
+  }
+  return build_plan(cu_seqlens_q, seqused_q, num_segments, off.data(), start.data(), len.data(),
+                    cu_seqlens_k[num_segments], num_heads_q, num_heads_kv, head_dim, out_plan);
+}
+
+gva_status gva_plan_ranges(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int32_t num_segments,
+                           const int32_t* key_range_offsets, const int32_t* key_range_starts,
+                           const int32_t* key_range_lengths, int64_t total_k, int32_t num_heads_q,
+                           int32_t num_heads_kv, int32_t head_dim, gva_plan_t* out_plan) {
+  if (out_plan == nullptr) return fail(GVA_ERR_INVALID_ARG, "out_plan is NULL");
+  *out_plan = nullptr;
+  gva_status s = validate_common(cu_seqlens_q, seqused_q, num_segments, num_heads_q, num_heads_kv, head_dim);
+  if (s != GVA_OK) return s;
+  if (key_range_offsets == nullptr) return fail(GVA_ERR_INVALID_ARG, "key_range_offsets is NULL");
+  if (total_k < 0 || total_k > INT32_MAX) return fail(GVA_ERR_INVALID_ARG, "total_k=%lld is out of range", (long long)total_k);
+  if (key_range_offsets[0] != 0) return fail(GVA_ERR_INVALID_ARG, "key_range_offsets[0] must be 0");
+  for (int32_t b = 0; b < num_segments; ++b)
+    if (key_range_offsets[b + 1] < key_range_offsets[b])
+      return fail(GVA_ERR_INVALID_ARG, "key_range_offsets decreases at segment %d", b);
+  const int32_t num_ranges = key_range_offsets[num_segments];
+  if (num_ranges > 0 && (key_range_starts == nullptr || key_range_lengths == nullptr))
+    return fail(GVA_ERR_INVALID_ARG, "key range arrays are NULL");
+  for (int32_t r = 0; r < num_ranges; ++r) {
+    const int64_t st = key_range_starts[r], n = key_range_lengths[r];
+    if (st < 0 || n < 0 || st + n > total_k)
+      return fail(GVA_ERR_INVALID_ARG, "key range %d = [%lld, %lld) is outside [0, total_k=%lld)", r, (long long)st,
+                  (long long)(st + n), (long long)total_k);
+  }
+  return build_plan(cu_seqlens_q, seqused_q, num_segments, key_range_offsets, key_range_starts, key_range_lengths,
+                    total_k, num_heads_q, num_heads_kv, head_dim, out_plan);
 }
 
 gva_status gva_forward(gva_plan_t plan, const void* q, const void* k, const void* v, void* out, gva_dtype out_dtype,
@@ -249,6 +326,7 @@ gva_status gva_forward(gva_plan_t plan, const void* q, const void* k, const void
   const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(plan->head_dim));
   gva::FwdParams prm{};
   prm.items = plan->d_items;
+  prm.blocks = plan->d_blocks;
   prm.num_items = plan->num_items;
   prm.out = out;
   prm.lse = lse;

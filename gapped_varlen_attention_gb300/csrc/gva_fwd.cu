@@ -109,9 +109,14 @@ __device__ __forceinline__ WorkItem load_item(const WorkItem* items, int idx) {
   const int4* p = reinterpret_cast<const int4*>(items + idx);
   const int4 a = __ldg(p), b = __ldg(p + 1);
   WorkItem it;
-  it.q_row0 = a.x; it.q_rows = a.y; it.k_row0 = a.z; it.k_len = a.w;
-  it.head_kv = b.x; it.n_tiles = b.y; it.pad0 = b.z; it.pad1 = b.w;
+  it.q_row0 = a.x; it.q_rows = a.y; it.blk0 = a.z; it.nblk = a.w;
+  it.head_kv = b.x; it.n_tiles = b.y; it.k_len = b.z; it.pad = b.w;
   return it;
+}
+
+__device__ __forceinline__ KeyBlock load_block(const KeyBlock* blocks, int idx) {
+  const int2 v = __ldg(reinterpret_cast<const int2*>(blocks) + idx);
+  return KeyBlock{v.x, v.y};
 }
 
 // MMA issue. One thread issues every tcgen05.mma, so the issue path must be short:
@@ -213,8 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int idx = item_index(round, blockIdx.x, gridDim.x);
         if (idx >= p.num_items) break;
         const WorkItem it = load_item(p.items, idx);
-        if (it.k_len == 0) continue;
-        const int nblk = (it.k_len + kBlockKeys - 1) / kBlockKeys;
+        if (it.nblk == 0) continue;
+        const int nblk = it.nblk;
         if (!wait_bar(&ctrl.q_empty, (q_it & 1) ^ 1, abort_flag, p.error_flag)) break;
         mbar_arrive_expect_tx(&ctrl.q_full, it.n_tiles * C::kQBytes);
         for (int t = 0; t < it.n_tiles; ++t)
@@ -225,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++q_it;
         bool ok = true;
         for (int j = 0; j < nblk && ok; ++j) {
-          const int key0 = it.k_row0 + j * kBlockKeys;
+          const int key0 = load_block(p.blocks, it.blk0 + j).row0;
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {  // K_j, then V_j
             const uint32_t sl = ld % NS;
@@ -264,8 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int idx = item_index(round, blockIdx.x, gridDim.x);
         if (idx >= p.num_items) break;
         const WorkItem it = load_item(p.items, idx);
-        if (it.k_len == 0) continue;
-        const int nblk = (it.k_len + kBlockKeys - 1) / kBlockKeys;
+        if (it.nblk == 0) continue;
+        const int nblk = it.nblk;
         const bool two = it.n_tiles == 2;
         ok = wait_bar(&ctrl.q_full, q_it & 1, abort_flag, p.error_flag);
         if (!ok) break;
@@ -349,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int head = it.head_kv * G + hl;
       TOut* orow = out + (token * p.num_heads_q + head) * D;
       float* lrow = p.lse + static_cast<int64_t>(head) * p.total_q + token;
-      if (it.k_len == 0) {
+      if (it.nblk == 0) {
         if (valid) {
           float z[32];
 #pragma unroll
@@ -360,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      const int nblk = (it.k_len + kBlockKeys - 1) / kBlockKeys;
+      const int nblk = it.nblk;
       float m_used = -CUDART_INF_F;
       float l = 0.0f;
       for (int j = 0; j < nblk; ++j) {
@@ -368,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         ++sc;
         tcgen05_fence_after();
-        const int rem = it.k_len - j * kBlockKeys;  // used keys in this block (>= 1)
+        const int rem = load_block(p.blocks, it.blk0 + j).valid;  // used keys in this block (>= 1)
         if (rem < kBlockKeys) {
           // Last, partial block: keys past the used length (gap, padding or another
           // segment, possibly NaN) leave the softmax. Their score columns are set to

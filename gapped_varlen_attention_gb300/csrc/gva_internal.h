@@ -16,15 +16,24 @@ constexpr int kMergeRows = 16;
 constexpr int kMaxMergeParts = 8;
 
 // One forward work item: up to 2 x 128 folded rows (tokens x the query heads of one KV
-// head) of one segment, attending the segment's used keys.
+// head) of one segment, attending the segment's used keys. The keys are a list of key
+// blocks (see KeyBlock) shared by every item of the segment.
 struct alignas(16) WorkItem {
   int32_t q_row0;   // global token row of the item's first token
   int32_t q_rows;   // used tokens covered by the item (1 .. 2 * tokens_per_tile)
-  int32_t k_row0;   // global key row of the segment's first key
-  int32_t k_len;    // used keys of the segment (0: keyless, epilogue only)
+  int32_t blk0;     // first key block of the segment in the block table
+  int32_t nblk;     // key blocks (0: keyless, epilogue only)
   int32_t head_kv;  // KV head; query heads head_kv * group .. + group - 1
   int32_t n_tiles;  // 1 or 2 Q tiles with used rows
-  int32_t pad0, pad1;
+  int32_t k_len;    // used keys in all (sum of the blocks' valid counts)
+  int32_t pad;
+};
+
+// Up to kBlockKeys keys: K/V rows row0 .. row0 + valid (a key range is cut into such
+// blocks; only its last block can be partial).
+struct alignas(8) KeyBlock {
+  int32_t row0;
+  int32_t valid;
 };
 
 struct alignas(8) MergeUnit {
@@ -34,6 +43,7 @@ struct alignas(8) MergeUnit {
 
 struct FwdParams {
   const WorkItem* items;
+  const KeyBlock* blocks;
   int32_t num_items;
   void* out;
   float* lse;

@@ -5,9 +5,10 @@
 // error word with cudaMalloc. Some callers cannot do that: a serving runtime that owns
 // all device memory through its own pool, code that runs under a fixed memory budget,
 // or a hot loop that must not hit cudaMalloc's implicit device synchronisation. This
-// entry point keeps the work list and the error word in one file-scope __device__
-// array instead. The array is part of the library image, so every GPU that loads the
-// library holds it (kNoallocScratchBytes, about 1 MiB) until the process exits.
+// entry point keeps the work list, the key-block table and the error word in one
+// file-scope __device__ array instead. The array is part of the library image, so every
+// GPU that loads the library holds it (kNoallocScratchBytes, about 1.5 MiB) until the
+// process exits.
 //
 // Set-up: the first call on a device (with that device current) resolves the array's
 // device address with cudaGetSymbolAddress and caches it; make that first call before
@@ -29,17 +30,21 @@
 namespace {
 
 constexpr int32_t kNoallocMaxItems = GVA_NOALLOC_MAX_WORK_ITEMS;
+constexpr int32_t kNoallocMaxBlocks = GVA_NOALLOC_MAX_KEY_BLOCKS;
 constexpr size_t kNoallocItemBytes = static_cast<size_t>(kNoallocMaxItems) * sizeof(gva::WorkItem);
-constexpr size_t kNoallocScratchBytes = kNoallocItemBytes + 256;  // work list, then the error word
+constexpr size_t kNoallocBlockBytes = static_cast<size_t>(kNoallocMaxBlocks) * sizeof(gva::KeyBlock);
+// work list, key blocks, then the error word
+constexpr size_t kNoallocScratchBytes = kNoallocItemBytes + kNoallocBlockBytes + 256;
 constexpr int kMaxDevices = 64;
 
-// The scratch: [work items | error word]. Host code must not use this name as an
+// The scratch: [work items | key blocks | error word]. Host code must not use this name as an
 // address; it uses the pointer cudaGetSymbolAddress returns for the current device.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 std::mutex g_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
-gva::WorkItem g_staging[kNoallocMaxItems];  // host staging of the work list (under g_mutex)
+gva::WorkItem g_staging[kNoallocMaxItems];       // host staging of the work list (under g_mutex)
+gva::KeyBlock g_staging_blocks[kNoallocMaxBlocks];  // host staging of the key blocks (under g_mutex)
 
 // Errors are reported through gva_last_error(), like every other entry point.
 gva_status fail(gva_status s, const char* fmt, ...) {
@@ -119,6 +124,12 @@ extern "C" GVA_API gva_status gva_forward_noalloc(
     return fail(GVA_ERR_INVALID_ARG,
                 "this launch needs %lld work items; gva_forward_noalloc holds at most %d (use gva_plan + gva_forward)",
                 static_cast<long long>(count), kNoallocMaxItems);
+  int64_t nblocks = 0;
+  for (int32_t b = 0; b < num_segments; ++b) nblocks += (seqused_k[b] + gva::kBlockKeys - 1) / gva::kBlockKeys;
+  if (nblocks > kNoallocMaxBlocks)
+    return fail(GVA_ERR_INVALID_ARG,
+                "this launch needs %lld key blocks; gva_forward_noalloc holds at most %d (use gva_plan + gva_forward)",
+                static_cast<long long>(nblocks), kNoallocMaxBlocks);
   if (count == 0) return GVA_OK;  // no used rows: nothing to write
   const int64_t total_q = cu_seqlens_q[num_segments];
   const int64_t total_k = cu_seqlens_k[num_segments];
@@ -151,12 +162,17 @@ extern "C" GVA_API gva_status gva_forward_noalloc(
   }
   unsigned char* scratch = static_cast<unsigned char*>(g_scratch_ptr[dev]);
   gva::WorkItem* d_items = reinterpret_cast<gva::WorkItem*>(scratch);
-  int* d_error = reinterpret_cast<int*>(scratch + kNoallocItemBytes);
+  gva::KeyBlock* d_blocks = reinterpret_cast<gva::KeyBlock*>(scratch + kNoallocItemBytes);
+  int* d_error = reinterpret_cast<int*>(scratch + kNoallocItemBytes + kNoallocBlockBytes);
 
   // ---- work list in the host staging array: most key blocks first (the persistent
   // kernel hands items out in this order)
-  int32_t n = 0;
+  // key blocks of each segment's used prefix, then the segment's work items
+  int32_t nb = 0, n = 0;
   for (int32_t b = 0; b < num_segments; ++b) {
+    const int32_t blk0 = nb;
+    for (int32_t o = 0; o < seqused_k[b]; o += gva::kBlockKeys)
+      g_staging_blocks[nb++] = gva::KeyBlock{cu_seqlens_k[b] + o, std::min(gva::kBlockKeys, seqused_k[b] - o)};
     const int32_t uq = seqused_q[b];
     for (int32_t hk = 0; hk < num_heads_kv; ++hk) {
       for (int32_t t0 = 0; t0 < uq; t0 += tpi) {
@@ -164,7 +180,8 @@ extern "C" GVA_API gva_status gva_forward_noalloc(
         it = gva::WorkItem{};
         it.q_row0 = cu_seqlens_q[b] + t0;
         it.q_rows = std::min(tpi, uq - t0);
-        it.k_row0 = cu_seqlens_k[b];
+        it.blk0 = blk0;
+        it.nblk = nb - blk0;
         it.k_len = seqused_k[b];
         it.head_kv = hk;
         it.n_tiles = it.q_rows > tpt ? 2 : 1;
@@ -172,15 +189,27 @@ extern "C" GVA_API gva_status gva_forward_noalloc(
     }
   }
   auto cost = [](const gva::WorkItem& it) {
-    return static_cast<int64_t>((it.k_len + gva::kBlockKeys - 1) / gva::kBlockKeys) * it.n_tiles * 4 + it.n_tiles;
+    return static_cast<int64_t>(it.nblk) * it.n_tiles * 4 + it.n_tiles;
   };
-  std::stable_sort(g_staging, g_staging + n,
-                   [&](const gva::WorkItem& a, const gva::WorkItem& c) { return cost(a) > cost(c); });
+  // In place (std::sort allocates nothing); ties are broken by position so the order is
+  // deterministic. The order only affects scheduling: each output row is computed by
+  // exactly one item, with the same arithmetic wherever it runs.
+  std::sort(g_staging, g_staging + n, [&](const gva::WorkItem& a, const gva::WorkItem& c) {
+    const int64_t ca = cost(a), cc = cost(c);
+    if (ca != cc) return ca > cc;
+    if (a.q_row0 != c.q_row0) return a.q_row0 < c.q_row0;
+    return a.head_kv < c.head_kv;
+  });
 
   // Pageable-to-device copy: the staging array is free again once the call returns.
   e = cudaMemcpyAsync(d_items, g_staging, static_cast<size_t>(n) * sizeof(gva::WorkItem), cudaMemcpyHostToDevice,
                       stream);
   if (e != cudaSuccess) return fail(GVA_ERR_CUDA, "copying the work list: %s", cudaGetErrorString(e));
+  if (nb > 0) {
+    e = cudaMemcpyAsync(d_blocks, g_staging_blocks, static_cast<size_t>(nb) * sizeof(gva::KeyBlock),
+                        cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return fail(GVA_ERR_CUDA, "copying the key blocks: %s", cudaGetErrorString(e));
+  }
   e = cudaMemsetAsync(d_error, 0, sizeof(int), stream);
   if (e != cudaSuccess) return fail(GVA_ERR_CUDA, "clearing the error word: %s", cudaGetErrorString(e));
 
@@ -193,6 +222,7 @@ extern "C" GVA_API gva_status gva_forward_noalloc(
   const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
   gva::FwdParams prm{};
   prm.items = d_items;
+  prm.blocks = d_blocks;
   prm.num_items = n;
   prm.out = out;
   prm.lse = lse;

@@ -98,6 +98,31 @@ GVA_API gva_status gva_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_
                     int32_t head_dim, gva_plan_t* out_plan);
 
 /*
+ * gva_plan_ranges - like gva_plan, but each segment's keys are several row ranges of
+ * K/V, attended as one softmax over their concatenation.
+ *
+ * Cites: cosmos-framework PR #312, "Problem and behavior" (visibility partitions of
+ * one launch, normally merged with an FP32 LSE merge: here they run as one launch
+ * with no merge), and TensorRT-LLM issue #18687, "additional notes" (after an
+ * all-to-all the valid keys of a sample are not a prefix: rank-major order).
+ *
+ *   cu_seqlens_q, seqused_q : HOST int32, as for gva_plan
+ *   key_range_offsets       : HOST int32 [num_segments + 1], starts at 0,
+ *                             non-decreasing: segment b owns ranges
+ *                             key_range_offsets[b] .. key_range_offsets[b+1]
+ *   key_range_starts/lengths: HOST int32 [key_range_offsets[num_segments]]: K/V rows
+ *                             start .. start + length, each inside [0, total_k)
+ *   total_k                 : rows of the K and V buffers
+ * A segment whose ranges hold no key is keyless (O = 0, LSE = -inf on used rows).
+ * Ranges may lie anywhere (also overlapping other segments' ranges). gva_forward and
+ * gva_lse_merge take a plan from either builder. Errors as for gva_plan.
+ */
+GVA_API gva_status gva_plan_ranges(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int32_t num_segments,
+                                   const int32_t* key_range_offsets, const int32_t* key_range_starts,
+                                   const int32_t* key_range_lengths, int64_t total_k, int32_t num_heads_q,
+                                   int32_t num_heads_kv, int32_t head_dim, gva_plan_t* out_plan);
+
+/*
  * gva_forward - the gapped varlen attention forward of one launch (one kernel).
  *
  * Cites: PR #302 "What" (used rows attend used keys; rows past the used length left
@@ -161,15 +186,17 @@ GVA_API gva_status gva_device_status(gva_plan_t plan);
  * pool, code under a fixed memory budget, or a loop that must not take cudaMalloc's
  * implicit device synchronisation. gva_plan allocates a device work list; this call
  * instead builds the work list on the host and copies it, on `stream`, into a scratch
- * array that is part of the library image (GVA_NOALLOC_MAX_WORK_ITEMS items of 32
- * bytes plus an error word, about 1 MiB, held by every GPU that loads the library until
- * the process exits). It calls no cudaMalloc, cudaFree or allocating library routine.
+ * array that is part of the library image (GVA_NOALLOC_MAX_WORK_ITEMS work items of 32
+ * bytes, GVA_NOALLOC_MAX_KEY_BLOCKS key blocks of 8 bytes and an error word, about
+ * 1.5 MiB, held by every GPU that loads the library until the process exits). It calls
+ * no cudaMalloc, cudaFree or allocating library routine.
  *
  * Arguments: the geometry exactly as for gva_plan (HOST arrays, same rules), then the
  * tensors, scale and stream exactly as for gva_forward (the caller still owns and
  * passes inputs and outputs). A launch needing more than GVA_NOALLOC_MAX_WORK_ITEMS
  * work items (items = sum over segments of ceil(seqused_q / (256 / (Hq/Hkv))) * Hkv)
- * is refused with GVA_ERR_INVALID_ARG before any GPU work.
+ * or more than GVA_NOALLOC_MAX_KEY_BLOCKS key blocks (sum over segments of
+ * ceil(seqused_k / 128)) is refused with GVA_ERR_INVALID_ARG before any GPU work.
  *
  * The first call on a device resolves the scratch array's address for that device
  * (cudaGetSymbolAddress, with that device current); make that first call before any
@@ -179,6 +206,7 @@ GVA_API gva_status gva_device_status(gva_plan_t plan);
  * made.
  */
 #define GVA_NOALLOC_MAX_WORK_ITEMS 32768
+#define GVA_NOALLOC_MAX_KEY_BLOCKS 65536
 GVA_API gva_status gva_forward_noalloc(const int32_t* cu_seqlens_q, const int32_t* seqused_q,
                                        const int32_t* cu_seqlens_k, const int32_t* seqused_k,
                                        int32_t num_segments, int32_t num_heads_q, int32_t num_heads_kv,

@@ -100,3 +100,31 @@ def test_valid_plan_without_a_gpu_is_refused_cleanly(lib):
 def test_python_binding_fails_loudly_without_the_library(tmp_path):
     with pytest.raises(RuntimeError, match="missing"):
         _lib.load_library(str(tmp_path / "libgva.so"))
+
+
+def _ranges_status(lib, cu_q, uq, off, starts, lens, total_k, hq=4, hkv=2, d=64):
+    a = [np.ascontiguousarray(np.asarray(x, np.int32)) for x in (cu_q, uq, off, starts, lens)]
+    p = lambda x: x.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))  # noqa: E731
+    h = ctypes.c_void_p()
+    st = lib.gva_plan_ranges(p(a[0]), p(a[1]), len(a[1]), p(a[2]), p(a[3]), p(a[4]), total_k, hq, hkv, d,
+                             ctypes.byref(h))
+    if st == 0:
+        lib.gva_plan_destroy(h)
+    return st, lib.gva_last_error().decode()
+
+
+BAD_RANGES = [
+    ("range past total_k", ([0, 8], [8], [0, 1], [90], [20], 100), "outside"),
+    ("negative start", ([0, 8], [8], [0, 1], [-1], [2], 100), "outside"),
+    ("negative length", ([0, 8], [8], [0, 1], [3], [-2], 100), "outside"),
+    ("offsets not from 0", ([0, 8], [8], [1, 1], [3], [2], 100), "key_range_offsets[0]"),
+    ("decreasing offsets", ([0, 4, 8], [4, 4], [0, 2, 1], [3, 5], [2, 2], 100), "decreases"),
+    ("negative total_k", ([0, 8], [8], [0, 0], [0], [0], -1), "total_k"),
+]
+
+
+@pytest.mark.parametrize("name,args,msg", BAD_RANGES, ids=[b[0] for b in BAD_RANGES])
+def test_plan_ranges_rejects_bad_ranges_on_the_host(lib, name, args, msg):
+    st, err = _ranges_status(lib, *args)
+    assert st == 1, (st, err)
+    assert msg in err
