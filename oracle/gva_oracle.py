@@ -34,6 +34,10 @@ sets of the same query rows:
     L = max_p lse_p;   if L = -inf:  O = 0, lse = -inf
     else  w_p = exp(lse_p - L),  lse = L + ln sum_p w_p,  O = sum_p w_p O_p / sum_p w_p
 
+Block-causal masking within a segment (``causal_block``) restricts row i to keys
+j < (floor(pos / B) + 1) * B with pos = i + used_k - used_q: a single launch covers the
+causal replay that the visibility partitions of PR #312 split into maskless launches.
+
 Score blocks are sized from a byte budget rather than a fixed row count (the
 review of PR #302 on the FP32 fallback's score block), so long segments do not
 materialise a huge score matrix.
@@ -48,7 +52,8 @@ from typing import Optional, Sequence
 
 import numpy as np
 
-__all__ = ["attention_forward", "attention_forward_ranges", "attention_rows", "lse_merge", "used_flops"]
+__all__ = ["attention_forward", "attention_forward_ranges", "attention_rows", "causal_limits", "lse_merge",
+           "used_flops"]
 
 DEFAULT_BUDGET_BYTES = 1 << 30
 
@@ -87,14 +92,43 @@ def _segment_attention(qs: np.ndarray, ks: np.ndarray, vs: np.ndarray, scale: fl
     return o, lse
 
 
+def causal_limits(used_q: int, used_k: int, causal_block: int) -> np.ndarray:
+    """Keys visible to each used query row of a segment under block-causal masking.
+
+    Query row i sits at key position i + (used_k - used_q) (the queries are the last
+    used_q positions of the key sequence); it sees keys j < (floor(pos / B) + 1) * B,
+    capped at used_k, with B = ``causal_block`` (1: token-causal)."""
+    pos = np.arange(used_q, dtype=np.int64) + (int(used_k) - int(used_q))
+    lim = (np.floor_divide(pos, int(causal_block)) + 1) * int(causal_block)
+    return np.clip(lim, 0, int(used_k))
+
+
+def _masked_attention(qs: np.ndarray, ks: np.ndarray, vs: np.ndarray, scale: float, limits: np.ndarray):
+    """Softmax attention where row r sees keys ``j < limits[r]``; rows with no key get
+    O = 0 and LSE = -inf. FP64, one row block (causal workloads are small enough)."""
+    x = (qs @ ks.T) * scale
+    mask = np.arange(ks.shape[0])[None, :] < limits[:, None]
+    x = np.where(mask, x, -np.inf)
+    mx = x.max(axis=1)
+    live = np.isfinite(mx)
+    e = np.where(mask, np.exp(x - np.where(live, mx, 0.0)[:, None]), 0.0)
+    l = e.sum(axis=1)
+    o = np.where(live[:, None], (e @ vs) / np.where(live, l, 1.0)[:, None], 0.0)
+    lse = np.where(live, np.where(live, mx, 0.0) + np.log(np.where(live, l, 1.0)), -np.inf)
+    return o, lse
+
+
 def attention_forward(q, k, v, cu_q, used_q, cu_k, used_k, *, scale: Optional[float] = None,
                       out=None, lse=None, num_heads_kv: Optional[int] = None,
-                      budget_bytes: int = DEFAULT_BUDGET_BYTES, segments: Optional[Sequence[int]] = None):
+                      budget_bytes: int = DEFAULT_BUDGET_BYTES, segments: Optional[Sequence[int]] = None,
+                      causal_block: int = 0):
     """Gapped varlen attention forward over packed Q [total_q, Hq, d], K/V [total_k, Hkv, d].
 
     ``out`` ([total_q, Hq, d]) and ``lse`` ([Hq, total_q]) give the buffers' prior
     contents; rows past a segment's used length keep them (default: zeros). Returns
-    FP64 (out, lse). ``segments`` restricts the work to a subset of segments."""
+    FP64 (out, lse). ``segments`` restricts the work to a subset of segments.
+    ``causal_block`` > 0 applies block-causal masking within each segment (see
+    ``causal_limits``); 0 is the maskless forward."""
     q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
     total_q, hq, d = q.shape
     hkv = k.shape[1] if num_heads_kv is None else num_heads_kv
@@ -118,12 +152,16 @@ def attention_forward(q, k, v, cu_q, used_q, cu_k, used_k, *, scale: Optional[fl
             o_out[r0:r0 + nq] = 0.0
             l_out[:, r0:r0 + nq] = -np.inf
             continue
+        lim = np.repeat(causal_limits(nq, nk, causal_block), g) if causal_block > 0 else None
         for hk in range(hkv):
             # the g query heads sharing KV head hk, folded into one row block
             qs = q[r0:r0 + nq, hk * g:(hk + 1) * g, :].astype(np.float64).reshape(nq * g, d)
             ks = k[k0:k0 + nk, hk, :].astype(np.float64)
             vs = v[k0:k0 + nk, hk, :].astype(np.float64)
-            ob, lb = _segment_attention(qs, ks, vs, s, budget_bytes)
+            if lim is None:
+                ob, lb = _segment_attention(qs, ks, vs, s, budget_bytes)
+            else:
+                ob, lb = _masked_attention(qs, ks, vs, s, lim)
             o_out[r0:r0 + nq, hk * g:(hk + 1) * g, :] = ob.reshape(nq, g, -1)
             l_out[hk * g:(hk + 1) * g, r0:r0 + nq] = lb.reshape(nq, g).T
     return o_out, l_out
@@ -175,7 +213,7 @@ def attention_forward_ranges(q, k, v, cu_q, used_q, key_ranges, *, scale: Option
 
 def attention_rows(q, k, v, cu_q, used_q, cu_k, used_k, rows: Sequence[int], *,
                    scale: Optional[float] = None, num_heads_kv: Optional[int] = None,
-                   budget_bytes: int = DEFAULT_BUDGET_BYTES):
+                   budget_bytes: int = DEFAULT_BUDGET_BYTES, causal_block: int = 0):
     """The same definition evaluated for a list of global query rows (all heads).
 
     For spot checks of launches too large to evaluate in full. Every row must be a
@@ -204,11 +242,18 @@ def attention_rows(q, k, v, cu_q, used_q, cu_k, used_k, rows: Sequence[int], *,
             l[:, idx] = -np.inf
             continue
         sel = [rows[i] for i in idx]
+        lim = None
+        if causal_block > 0:
+            seg_lim = causal_limits(int(used_q[b]), nk, causal_block)
+            lim = np.repeat(seg_lim[[r - int(cu_q[b]) for r in sel]], g)
         for hk in range(hkv):
             qs = np.concatenate([_as_f64(q[r, hk * g:(hk + 1) * g, :]) for r in sel]).astype(np.float64)
             ks = _as_f64(k[k0:k0 + nk, hk, :]).astype(np.float64)
             vs = _as_f64(v[k0:k0 + nk, hk, :]).astype(np.float64)
-            ob, lb = _segment_attention(qs, ks, vs, s, budget_bytes)
+            if lim is None:
+                ob, lb = _segment_attention(qs, ks, vs, s, budget_bytes)
+            else:
+                ob, lb = _masked_attention(qs, ks, vs, s, lim)
             o[idx, hk * g:(hk + 1) * g] = ob.reshape(len(sel), g, -1)
             l[hk * g:(hk + 1) * g, idx] = lb.reshape(len(sel), g).T
     return o, l

@@ -288,9 +288,61 @@ def pin_ranges(orc):
     np.testing.assert_allclose(rev[0], full[0], atol=1e-12)
 
 
+def pin_causal(orc):
+    """Block-causal masking within a segment.
+
+    * hand-written limits from the definition (queries are the last positions);
+    * token-causal with equal lengths is float64 SDPA with is_causal;
+    * every row equals the maskless forward over its own visible key prefix;
+    * a block larger than any segment is the maskless forward;
+    * a row that sees no key gets 0 / -inf."""
+    assert list(orc.causal_limits(5, 8, 1)) == [4, 5, 6, 7, 8]
+    assert list(orc.causal_limits(5, 8, 4)) == [4, 8, 8, 8, 8]
+    assert list(orc.causal_limits(6, 4, 2)) == [0, 0, 2, 2, 4, 4]
+    rng = np.random.default_rng(17)
+    # equal lengths, token-causal: SDPA is_causal (row i sees keys 0..i)
+    B, L, hq, hkv, d = 2, 9, 4, 2, 8
+    q = _rand(rng, B * L, hq, d)
+    k = _rand(rng, B * L, hkv, d)
+    v = _rand(rng, B * L, hkv, d)
+    cu = np.arange(B + 1) * L
+    o, _ = orc.attention_forward(q, k, v, cu, [L] * B, cu, [L] * B, scale=0.3, causal_block=1)
+    tq = torch.from_numpy(q).view(B, L, hq, d).transpose(1, 2)
+    tk = torch.from_numpy(k).view(B, L, hkv, d).transpose(1, 2)
+    tv = torch.from_numpy(v).view(B, L, hkv, d).transpose(1, 2)
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=0.3, is_causal=True, enable_gqa=True)
+    np.testing.assert_allclose(o, ref.transpose(1, 2).reshape(B * L, hq, d).numpy(), atol=1e-12)
+    # unequal lengths and blocks: each row equals the maskless forward over its prefix
+    for (uq, uk, blk) in [(7, 10, 3), (6, 4, 2), (5, 5, 1), (4, 9, 100)]:
+        q = _rand(rng, uq, hq, d)
+        k = _rand(rng, uk + 2, hkv, d)
+        v = _rand(rng, uk + 2, hkv, d)
+        o, l = orc.attention_forward(q, k, v, [0, uq], [uq], [0, uk + 2], [uk], causal_block=blk)
+        lim = orc.causal_limits(uq, uk, blk)
+        for i in range(uq):
+            oi, li = orc.attention_forward(q[i:i + 1], k, v, [0, 1], [1], [0, uk + 2], [int(lim[i])])
+            np.testing.assert_allclose(o[i], oi[0], atol=1e-12)
+            assert (np.isneginf(l[:, i]) == np.isneginf(li[:, 0])).all()
+            fin = np.isfinite(li[:, 0])
+            np.testing.assert_allclose(l[fin, i], li[fin, 0], atol=1e-12)
+        if blk >= uq + uk:
+            o2, l2 = orc.attention_forward(q, k, v, [0, uq], [uq], [0, uk + 2], [uk])
+            np.testing.assert_allclose(o, o2, atol=1e-12)
+            np.testing.assert_allclose(l, l2, atol=1e-12)
+    # a row with no visible key
+    q = _rand(rng, 6, 2, 4)
+    k = _rand(rng, 4, 1, 4)
+    o, l = orc.attention_forward(q, k, k, [0, 6], [6], [0, 4], [4], causal_block=2)
+    assert np.all(o[:2] == 0.0) and np.all(np.isneginf(l[:, :2])) and np.all(np.isfinite(l[:, 2:]))
+    # spot rows agree with the full evaluation
+    rows = [0, 3, 5]
+    o3, l3 = orc.attention_rows(q, k, k, [0, 6], [6], [0, 4], [4], rows, causal_block=2)
+    np.testing.assert_array_equal(o3, o[rows])
+
+
 PINS = [pin_bruteforce, pin_default_scale, pin_dilution_golden, pin_zero_keys_closed_form,
         pin_single_key, pin_keyless_and_gap_rows, pin_pad_invariance, pin_sdpa_equal_lengths,
-        pin_gqa_repeat, pin_key_permutation, pin_merge_union, pin_rows_match, pin_ranges]
+        pin_gqa_repeat, pin_key_permutation, pin_merge_union, pin_rows_match, pin_ranges, pin_causal]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -323,6 +375,8 @@ MUTANTS = {
     "transposed_lse": ("lb.reshape(nq, g).T", "lb.reshape(g, nq)"),
     "merge_weight_sign": ("np.exp(ls - safe[None])", "np.exp(safe[None] - ls)"),
     "sqrt_d_scale": ("1.0 / math.sqrt(d) if scale is None", "1.0 / d if scale is None"),
+    "causal_off_by_one": ("(np.floor_divide(pos, int(causal_block)) + 1)", "np.floor_divide(pos, int(causal_block))"),
+    "causal_top_left": ("+ (int(used_k) - int(used_q))", "+ 0"),
     "range_end_dropped": ("np.arange(int(st), int(st) + int(n))", "np.arange(int(st), int(st) + int(n) - 1)"),
 }
 
