@@ -93,6 +93,14 @@ class Workload:
             self.parts = None
             self.ranges = [[(int(p.cu_k[b]), int(p.used_k[b])) for p in parts] for b in range(full.num_segments)]
             self.label = "multiview causal gapped replay: 7 segments, 2 visibility partitions fused in one launch"
+        elif name == "multiview_blockcausal":
+            full, _ = W.multiview_causal()
+            self.geoms = [full]
+            self.q, self.k, self.v = W.make_qkv(full, 1003 + seed_offset, device=dev)
+            self.parts = None
+            self.causal_block = 512
+            self.label = ("multiview causal gapped replay: 7 segments, block-causal masking with 512-token frames "
+                          "in one launch (FLOPs count visible keys only)")
         elif name == "tiny":
             g = W.tiny()
             self.geoms = [g]
@@ -106,7 +114,7 @@ class Workload:
             self.plans = [gva.Plan.from_ranges(g.cu_q, g.used_q, self.ranges, g.total_k, g.num_heads_q,
                                                g.num_heads_kv, g.head_dim)]
         else:
-            self.plans = [gva.Plan.from_geometry(g) for g in self.geoms]
+            self.plans = [gva.Plan.from_geometry(g, getattr(self, "causal_block", 0)) for g in self.geoms]
         g0 = self.geoms[0]
         if self.parts is None:
             self.out, self.lse = W.make_outputs(g0, 0.0, device=dev)
@@ -115,7 +123,7 @@ class Workload:
             self.merge_plan = gva.Plan.from_geometry(self.parts)
             self.out, self.lse = W.make_outputs(self.parts, 0.0, device=dev)
             self.partials = [W.make_outputs(p, 0.0, device=dev, out_dtype=torch.float32) for p in self.geoms]
-        self.flops = float(sum(g.used_flops() for g in self.geoms))
+        self.flops = float(sum(p.info()["used_flops"] for p in self.plans))
         self.launches_per_step = len(self.geoms) + (0 if self.parts is None else 1)
 
     def step(self, q=None, k=None, v=None):
@@ -289,7 +297,7 @@ def main():
     ap.add_argument("--impl", choices=["gva", "reference"], default="gva")
     ap.add_argument("--workload", default="long_replay",
                     choices=["long_replay", "long_replay_small", "cfg_text_cross", "multiview_causal",
-                             "multiview_fused", "tiny"])
+                             "multiview_fused", "multiview_blockcausal", "tiny"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     args = ap.parse_args()
@@ -386,7 +394,7 @@ def main():
     sustained = args.steps * ms_step > 1000.0
     peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
     value = world * wl.flops / (ms_step * 1e-3) / 1e12
-    fwd_flops = wl.geoms[0].used_flops()
+    fwd_flops = wl.plans[0].info()["used_flops"]
     achieved = fwd_flops / (fwd_ms * 1e-3) / 1e12
     traffic = recorded_traffic(args.workload)
     cpu_rate, cpu_desc, _, _ = oracle_sample_rate(wl, args.cpu_budget_s)
@@ -450,7 +458,7 @@ def run_reference(args, world, rank):
         g = W.cfg_text_cross()
         wl.geoms = [g]
         seed = 1002
-    elif args.workload in ("multiview_causal", "multiview_fused"):
+    elif args.workload in ("multiview_causal", "multiview_fused", "multiview_blockcausal"):
         g, parts = W.multiview_causal()
         wl.geoms = parts
         seed = 1003

@@ -21,7 +21,8 @@ GVA_BF16, GVA_FP32 = 0, 1
 
 # Every symbol include/gva.h declares.
 EXPORTS = ("gva_plan", "gva_forward", "gva_lse_merge", "gva_plan_destroy", "gva_plan_get_info",
-           "gva_device_status", "gva_status_string", "gva_last_error", "gva_forward_noalloc", "gva_plan_ranges")
+           "gva_device_status", "gva_status_string", "gva_last_error", "gva_forward_noalloc", "gva_plan_ranges",
+           "gva_plan_causal")
 NOALLOC_MAX_WORK_ITEMS = 32768  # GVA_NOALLOC_MAX_WORK_ITEMS in include/gva.h
 
 
@@ -66,10 +67,12 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.gva_last_error.restype = ctypes.c_char_p
     lib.gva_forward_noalloc.argtypes = [pi32, pi32, pi32, pi32, i32, i32, i32, i32, vp, vp, vp, vp, i32, vp, f32,
                                         vp]
+    lib.gva_plan_causal.argtypes = [pi32, pi32, pi32, pi32, i32, i32, i32, i32, i32, ctypes.POINTER(vp)]
     lib.gva_plan_ranges.argtypes = [pi32, pi32, i32, pi32, pi32, pi32, ctypes.c_int64, i32, i32, i32,
                                     ctypes.POINTER(vp)]
     for name in ("gva_plan", "gva_forward", "gva_lse_merge", "gva_plan_destroy", "gva_plan_get_info",
-                 "gva_device_status", "gva_forward_noalloc", "gva_plan_ranges"):
+                 "gva_device_status", "gva_forward_noalloc", "gva_plan_ranges",
+           "gva_plan_causal"):
         getattr(lib, name).restype = i32
     if path is None:
         _lib = lib
@@ -91,7 +94,8 @@ class Plan:
     """A validated segment geometry with its device work list (``gva_plan``)."""
 
     def __init__(self, cu_seqlens_q, seqused_q, cu_seqlens_k, seqused_k, num_heads_q: int, num_heads_kv: int,
-                 head_dim: int):
+                 head_dim: int, causal_block: int = 0):
+        """``causal_block`` > 0 builds a block-causal plan (``gva_plan_causal``)."""
         self._lib = load_library()
         self.cu_q, self.used_q = _i32(cu_seqlens_q), _i32(seqused_q)
         self.cu_k, self.used_k = _i32(cu_seqlens_k), _i32(seqused_k)
@@ -100,16 +104,23 @@ class Plan:
             raise ValueError("cu_seqlens must have num_segments + 1 entries and seqused num_segments")
         ptr = ctypes.c_void_p()
         as_p = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))  # noqa: E731
-        st = self._lib.gva_plan(as_p(self.cu_q), as_p(self.used_q), as_p(self.cu_k), as_p(self.used_k), n,
-                                int(num_heads_q), int(num_heads_kv), int(head_dim), ctypes.byref(ptr))
-        _check(self._lib, st, "gva_plan")
+        if causal_block:
+            st = self._lib.gva_plan_causal(as_p(self.cu_q), as_p(self.used_q), as_p(self.cu_k), as_p(self.used_k),
+                                           n, int(causal_block), int(num_heads_q), int(num_heads_kv), int(head_dim),
+                                           ctypes.byref(ptr))
+            _check(self._lib, st, "gva_plan_causal")
+        else:
+            st = self._lib.gva_plan(as_p(self.cu_q), as_p(self.used_q), as_p(self.cu_k), as_p(self.used_k), n,
+                                    int(num_heads_q), int(num_heads_kv), int(head_dim), ctypes.byref(ptr))
+            _check(self._lib, st, "gva_plan")
+        self.causal_block = int(causal_block)
         self._handle = ptr
         self.num_heads_q, self.num_heads_kv, self.head_dim = int(num_heads_q), int(num_heads_kv), int(head_dim)
         self.total_q, self.total_k = int(self.cu_q[-1]), int(self.cu_k[-1])
 
     @classmethod
-    def from_geometry(cls, g) -> "Plan":
-        return cls(g.cu_q, g.used_q, g.cu_k, g.used_k, g.num_heads_q, g.num_heads_kv, g.head_dim)
+    def from_geometry(cls, g, causal_block: int = 0) -> "Plan":
+        return cls(g.cu_q, g.used_q, g.cu_k, g.used_k, g.num_heads_q, g.num_heads_kv, g.head_dim, causal_block)
 
     @classmethod
     def from_ranges(cls, cu_seqlens_q, seqused_q, key_ranges, total_k: int, num_heads_q: int, num_heads_kv: int,
@@ -136,6 +147,7 @@ class Plan:
         self.num_heads_q, self.num_heads_kv, self.head_dim = int(num_heads_q), int(num_heads_kv), int(head_dim)
         self.total_q, self.total_k = int(self.cu_q[-1]), int(total_k)
         self.cu_k = self.used_k = None
+        self.causal_block = 0
         return self
 
     @property

@@ -16,7 +16,7 @@
 struct gva_plan {
   int device = -1;
   int sm_count = 0;
-  int32_t num_segments = 0, num_heads_q = 0, num_heads_kv = 0, head_dim = 0, group = 0;
+  int32_t num_segments = 0, num_heads_q = 0, num_heads_kv = 0, head_dim = 0, group = 0, causal_block = 0;
   int64_t total_q = 0, total_k = 0;
   int32_t num_items = 0, num_units = 0, grid = 0, merge_grid = 0;
   double used_flops = 0.0;
@@ -106,10 +106,12 @@ void free_plan(struct gva_plan* p) {
 
 // Shared by gva_plan and gva_plan_ranges once the arguments are validated: segment b's
 // keys are the ranges range_off[b] .. range_off[b+1] of (range_start, range_len).
+// causal_block > 0 (block-causal, one prefix range per segment): each item only gets the
+// key blocks its last row sees, and FLOPs count the visible keys of every row.
 gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int32_t num_segments,
                       const int32_t* range_off, const int32_t* range_start, const int32_t* range_len,
                       int64_t total_k, int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim,
-                      gva_plan_t* out_plan) {
+                      int32_t causal_block, gva_plan_t* out_plan) {
   const int32_t group = num_heads_q / num_heads_kv;
   // ---- key blocks: each range cut into blocks of at most kBlockKeys keys
   std::vector<gva::KeyBlock> blocks;
@@ -133,9 +135,21 @@ gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
   std::vector<int64_t> cost;
   std::vector<gva::MergeUnit> units;
   double flops = 0.0;
+  // keys visible to the row at key position pos (block-causal)
+  auto limit_at = [&](int64_t pos, int32_t keys) -> int32_t {
+    if (pos < 0) return 0;
+    return static_cast<int32_t>(std::min<int64_t>(keys, (pos / causal_block + 1) * causal_block));
+  };
   for (int32_t b = 0; b < num_segments; ++b) {
     const int32_t uq = seqused_q[b];
-    flops += 4.0 * head_dim * num_heads_q * static_cast<double>(uq) * static_cast<double>(seg_keys[b]);
+    const int32_t pos_shift = seg_keys[b] - uq;  // key position of row token 0
+    if (causal_block > 0) {
+      double pairs = 0.0;
+      for (int32_t i = 0; i < uq; ++i) pairs += limit_at(static_cast<int64_t>(i) + pos_shift, seg_keys[b]);
+      flops += 4.0 * head_dim * num_heads_q * pairs;
+    } else {
+      flops += 4.0 * head_dim * num_heads_q * static_cast<double>(uq) * static_cast<double>(seg_keys[b]);
+    }
     for (int32_t r0 = 0; r0 < uq; r0 += gva::kMergeRows)
       units.push_back({cu_seqlens_q[b] + r0, std::min(gva::kMergeRows, uq - r0)});
     for (int32_t hk = 0; hk < num_heads_kv; ++hk) {
@@ -148,6 +162,11 @@ gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
         it.head_kv = hk;
         it.n_tiles = it.q_rows > tokens_per_tile ? 2 : 1;
         it.k_len = seg_keys[b];
+        if (causal_block > 0) {
+          it.q_pos0 = t0 + pos_shift;
+          const int32_t last = limit_at(static_cast<int64_t>(it.q_pos0) + it.q_rows - 1, seg_keys[b]);
+          it.nblk = (last + gva::kBlockKeys - 1) / gva::kBlockKeys;
+        }
         items.push_back(it);
         cost.push_back(static_cast<int64_t>(it.nblk) * it.n_tiles * 4 + it.n_tiles);
       }
@@ -179,6 +198,7 @@ gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
   p->num_heads_kv = num_heads_kv;
   p->head_dim = head_dim;
   p->group = group;
+  p->causal_block = causal_block;
   p->total_q = cu_seqlens_q[num_segments];
   p->total_k = total_k;
   p->num_items = static_cast<int32_t>(sorted.size());
@@ -266,7 +286,29 @@ gva_status gva_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, const
     len[b] = seqused_k[b];
   }
   return build_plan(cu_seqlens_q, seqused_q, num_segments, off.data(), start.data(), len.data(),
-                    cu_seqlens_k[num_segments], num_heads_q, num_heads_kv, head_dim, out_plan);
+                    cu_seqlens_k[num_segments], num_heads_q, num_heads_kv, head_dim, 0, out_plan);
+}
+
+gva_status gva_plan_causal(const int32_t* cu_seqlens_q, const int32_t* seqused_q, const int32_t* cu_seqlens_k,
+                           const int32_t* seqused_k, int32_t num_segments, int32_t causal_block,
+                           int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim, gva_plan_t* out_plan) {
+  if (out_plan == nullptr) return fail(GVA_ERR_INVALID_ARG, "out_plan is NULL");
+  *out_plan = nullptr;
+  if (causal_block < 1) return fail(GVA_ERR_INVALID_ARG, "causal_block=%d must be >= 1", causal_block);
+  gva_status s = validate_common(cu_seqlens_q, seqused_q, num_segments, num_heads_q, num_heads_kv, head_dim);
+  if (s != GVA_OK) return s;
+  if (cu_seqlens_k == nullptr || (num_segments > 0 && seqused_k == nullptr))
+    return fail(GVA_ERR_INVALID_ARG, "a geometry array is NULL");
+  s = validate_offsets(cu_seqlens_k, seqused_k, num_segments, "k");
+  if (s != GVA_OK) return s;
+  std::vector<int32_t> off(num_segments + 1), start(num_segments), len(num_segments);
+  for (int32_t b = 0; b <= num_segments; ++b) off[b] = b;
+  for (int32_t b = 0; b < num_segments; ++b) {
+    start[b] = cu_seqlens_k[b];
+    len[b] = seqused_k[b];
+  }
+  return build_plan(cu_seqlens_q, seqused_q, num_segments, off.data(), start.data(), len.data(),
+                    cu_seqlens_k[num_segments], num_heads_q, num_heads_kv, head_dim, causal_block, out_plan);
 }
 
 gva_status gva_plan_ranges(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int32_t num_segments,
@@ -293,7 +335,7 @@ gva_status gva_plan_ranges(const int32_t* cu_seqlens_q, const int32_t* seqused_q
                   (long long)(st + n), (long long)total_k);
   }
   return build_plan(cu_seqlens_q, seqused_q, num_segments, key_range_offsets, key_range_starts, key_range_lengths,
-                    total_k, num_heads_q, num_heads_kv, head_dim, out_plan);
+                    total_k, num_heads_q, num_heads_kv, head_dim, 0, out_plan);
 }
 
 gva_status gva_forward(gva_plan_t plan, const void* q, const void* k, const void* v, void* out, gva_dtype out_dtype,
@@ -335,6 +377,7 @@ gva_status gva_forward(gva_plan_t plan, const void* q, const void* k, const void
   prm.group = plan->group;
   prm.tokens_per_tile = tokens_per_tile;
   prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.causal_block = plan->causal_block;
   prm.error_flag = plan->d_error;
   e = gva::launch_forward(plan->head_dim, out_dtype == GVA_FP32, prm, mq, mk, mv, plan->grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launching the forward kernel");

@@ -110,7 +110,7 @@ __device__ __forceinline__ WorkItem load_item(const WorkItem* items, int idx) {
   const int4 a = __ldg(p), b = __ldg(p + 1);
   WorkItem it;
   it.q_row0 = a.x; it.q_rows = a.y; it.blk0 = a.z; it.nblk = a.w;
-  it.head_kv = b.x; it.n_tiles = b.y; it.k_len = b.z; it.pad = b.w;
+  it.head_kv = b.x; it.n_tiles = b.y; it.k_len = b.z; it.q_pos0 = b.w;
   return it;
 }
 
@@ -164,7 +164,10 @@ __device__ __forceinline__ void store_row32<float>(float* dst, const float (&x)[
   for (int i = 0; i < 8; ++i) d[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
 }
 
-template <int D, typename TOut>
+// kCausal: block-causal masking within each segment. Row token i of a segment sits at
+// key position pos = i + used_k - used_q and sees keys j < (floor(pos / B) + 1) * B
+// (B = p.causal_block); the plan gives each item only the key blocks its last row sees.
+template <int D, typename TOut, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     gva_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                    const __grid_constant__ CUtensorMap map_v, const FwdParams p) {
@@ -366,6 +369,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       const int nblk = it.nblk;
+      int row_limit = 0;  // block-causal: keys of the segment this row sees
+      if constexpr (kCausal) {
+        const int pos = it.q_pos0 + t * T + tok;
+        const int bc = p.causal_block;
+        row_limit = pos < 0 ? 0 : min(it.k_len, (pos / bc + 1) * bc);
+      }
       float m_used = -CUDART_INF_F;
       float l = 0.0f;
       for (int j = 0; j < nblk; ++j) {
@@ -387,6 +396,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld128_sync(s_addr, raw);
 #pragma unroll
           for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(raw[i]);
+        }
+        if constexpr (kCausal) {
+          // Diagonal blocks: keys at or past the row's limit leave the softmax (the
+          // limit differs per row, so this is done on the registers).
+          const int lim = row_limit - j * kBlockKeys;
+          if (__any_sync(0xffffffffu, lim < kBlockKeys)) {
+#pragma unroll
+            for (int i = 0; i < 128; ++i) s[i] = (i < lim) ? s[i] : -CUDART_INF_F;
+          }
         }
         float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
         float mx2 = fmax3(s[6], s[7], s[8]), mx3 = fmax3(s[9], s[10], s[11]);
@@ -414,7 +432,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P = 2^(s*c - m) as bf16 pairs (column i holds keys 2i, 2i+1), stored to the
         // first 64 columns of S_t in 16-column pieces as they are ready.
         const uint64_t c2 = f32x2(c, c);
-        const uint64_t neg_m2 = f32x2(-m_used, -m_used);
+        // A row that has seen no key yet (block-causal only) has m = -inf and all P = 0.
+        const float m_ref = (kCausal && m_used == -CUDART_INF_F) ? 0.0f : m_used;
+        const uint64_t neg_m2 = f32x2(-m_ref, -m_ref);
         uint64_t acc0 = f32x2(0.0f, 0.0f), acc1 = acc0;
 #pragma unroll
         for (int q16 = 0; q16 < 4; ++q16) {
@@ -476,8 +496,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       ++oc;
       tcgen05_fence_after();
-      const float inv_l = 1.0f / l;
-      const float lse_val = (m_used + log2f(l)) * kLn2;
+      // l > 0 for every row with a key; a block-causal row that sees none gets 0 / -inf.
+      const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+      const float lse_val = l > 0.0f ? (m_used + log2f(l)) * kLn2 : -CUDART_INF_F;
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
         uint32_t o[32];
@@ -500,10 +521,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, typename TOut>
+template <int D, typename TOut, bool kCausal>
 cudaError_t launch_impl(const FwdParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                         int grid, cudaStream_t stream) {
-  auto kern = gva_fwd_kernel<D, TOut>;
+  auto kern = gva_fwd_kernel<D, TOut, kCausal>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemAlloc);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, Cfg<D>::kSmemAlloc, stream>>>(mq, mk, mv, p);
@@ -518,12 +539,19 @@ int forward_smem_bytes(int head_dim) {
 
 cudaError_t launch_forward(int head_dim, bool out_f32, const FwdParams& p, const CUtensorMap& map_q,
                            const CUtensorMap& map_k, const CUtensorMap& map_v, int grid, cudaStream_t stream) {
+  const bool causal = p.causal_block > 0;
   if (head_dim == 128) {
-    return out_f32 ? launch_impl<128, float>(p, map_q, map_k, map_v, grid, stream)
-                   : launch_impl<128, __nv_bfloat16>(p, map_q, map_k, map_v, grid, stream);
+    if (causal)
+      return out_f32 ? launch_impl<128, float, true>(p, map_q, map_k, map_v, grid, stream)
+                     : launch_impl<128, __nv_bfloat16, true>(p, map_q, map_k, map_v, grid, stream);
+    return out_f32 ? launch_impl<128, float, false>(p, map_q, map_k, map_v, grid, stream)
+                   : launch_impl<128, __nv_bfloat16, false>(p, map_q, map_k, map_v, grid, stream);
   }
-  return out_f32 ? launch_impl<64, float>(p, map_q, map_k, map_v, grid, stream)
-                 : launch_impl<64, __nv_bfloat16>(p, map_q, map_k, map_v, grid, stream);
+  if (causal)
+    return out_f32 ? launch_impl<64, float, true>(p, map_q, map_k, map_v, grid, stream)
+                   : launch_impl<64, __nv_bfloat16, true>(p, map_q, map_k, map_v, grid, stream);
+  return out_f32 ? launch_impl<64, float, false>(p, map_q, map_k, map_v, grid, stream)
+                 : launch_impl<64, __nv_bfloat16, false>(p, map_q, map_k, map_v, grid, stream);
 }
 
 }  // namespace gva

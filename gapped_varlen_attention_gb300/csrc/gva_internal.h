@@ -26,7 +26,7 @@ struct alignas(16) WorkItem {
   int32_t head_kv;  // KV head; query heads head_kv * group .. + group - 1
   int32_t n_tiles;  // 1 or 2 Q tiles with used rows
   int32_t k_len;    // used keys in all (sum of the blocks' valid counts)
-  int32_t pad;
+  int32_t q_pos0;   // block-causal plans: key position of the item's first token
 };
 
 // Up to kBlockKeys keys: K/V rows row0 .. row0 + valid (a key range is cut into such
@@ -52,6 +52,7 @@ struct FwdParams {
   int32_t group;            // Hq / Hkv
   int32_t tokens_per_tile;  // kTileRows / group
   float scale_log2;         // softmax scale * log2(e)
+  int32_t causal_block;     // > 0: block-causal masking within each segment
   int* error_flag;
 };
 

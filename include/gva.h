@@ -123,6 +123,27 @@ GVA_API gva_status gva_plan_ranges(const int32_t* cu_seqlens_q, const int32_t* s
                                    int32_t num_heads_kv, int32_t head_dim, gva_plan_t* out_plan);
 
 /*
+ * gva_plan_causal - like gva_plan, with block-causal masking inside each segment.
+ *
+ * Cites: cosmos-framework PR #312, "Problem and behavior" (causal replay split into
+ * maskless visibility partitions merged by an FP32 LSE merge) and PR #302, "What" (the
+ * FA4 varlen forward it stands in for also takes a causal flag): here one launch
+ * applies the mask.
+ *
+ * Row token i of segment b (i < seqused_q[b]) sits at key position
+ * pos = i + seqused_k[b] - seqused_q[b] (the queries are the last positions of the
+ * segment's key sequence) and attends keys j < min(seqused_k[b],
+ * (floor(pos / causal_block) + 1) * causal_block); causal_block = 1 is token-causal. A
+ * row that sees no key gets O = +0 and LSE = -inf. Each work item only loads the key
+ * blocks its last row sees. causal_block >= 1, else GVA_ERR_INVALID_ARG; other
+ * arguments and errors as for gva_plan.
+ */
+GVA_API gva_status gva_plan_causal(const int32_t* cu_seqlens_q, const int32_t* seqused_q,
+                                   const int32_t* cu_seqlens_k, const int32_t* seqused_k, int32_t num_segments,
+                                   int32_t causal_block, int32_t num_heads_q, int32_t num_heads_kv,
+                                   int32_t head_dim, gva_plan_t* out_plan);
+
+/*
  * gva_forward - the gapped varlen attention forward of one launch (one kernel).
  *
  * Cites: PR #302 "What" (used rows attend used keys; rows past the used length left
