@@ -52,8 +52,8 @@ from typing import Optional, Sequence
 
 import numpy as np
 
-__all__ = ["attention_forward", "attention_forward_ranges", "attention_rows", "causal_limits", "lse_merge",
-           "used_flops"]
+__all__ = ["attention_backward", "attention_forward", "attention_forward_ranges", "attention_rows",
+           "causal_limits", "lse_merge", "used_flops"]
 
 DEFAULT_BUDGET_BYTES = 1 << 30
 
@@ -292,3 +292,60 @@ def lse_merge(outs: Sequence, lses: Sequence, cu_q, used_q, *, out=None, lse=Non
         o_out[r0:r1] = acc
         l_out[:, r0:r1] = merged_lse
     return o_out, l_out
+
+
+def attention_backward(q, k, v, d_out, cu_q, used_q, cu_k, used_k, *, scale: Optional[float] = None,
+                       dq=None, dk=None, dv=None, num_heads_kv: Optional[int] = None):
+    """Gradients of the gapped varlen forward with respect to Q, K and V. FP64.
+
+    The backward the pages mark as missing on the non-FA4 paths (cosmos-framework
+    PR #302 review, PR #312 "Problem and behavior": forward only), written from the
+    forward's definition. For each segment, query head h and used row i, with P the
+    softmax over the used keys and dO the output gradient:
+
+        dP_ij = <dO_i, V_j>,   D_i = sum_j P_ij dP_ij,   dS_ij = P_ij (dP_ij - D_i)
+        dQ_i  = s sum_j dS_ij K_j
+        dK_j  = s sum_{i, h in the KV group} dS_ij Q_i
+        dV_j  = sum_{i, h in the KV group} P_ij dO_i
+
+    Only used rows of dQ and used keys of dK / dV are written (others keep ``dq`` /
+    ``dk`` / ``dv``, default zeros); a keyless segment's used rows get dQ = 0. Each
+    segment's used keys must not overlap another segment's. Returns (dq, dk, dv)."""
+    q, k, v, d_out = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(d_out)
+    total_q, hq, d = q.shape
+    hkv = k.shape[1] if num_heads_kv is None else num_heads_kv
+    g = hq // hkv
+    s = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    cu_q = np.asarray(cu_q, np.int64)
+    cu_k = np.asarray(cu_k, np.int64)
+    used_q = np.asarray(used_q, np.int64)
+    used_k = np.asarray(used_k, np.int64)
+    dq_out = np.zeros(q.shape, np.float64) if dq is None else _as_f64(dq).astype(np.float64, copy=True)
+    dk_out = np.zeros(k.shape, np.float64) if dk is None else _as_f64(dk).astype(np.float64, copy=True)
+    dv_out = np.zeros(v.shape, np.float64) if dv is None else _as_f64(dv).astype(np.float64, copy=True)
+    for b in range(len(used_q)):
+        r0, nq = int(cu_q[b]), int(used_q[b])
+        k0, nk = int(cu_k[b]), int(used_k[b])
+        if nq == 0:
+            continue
+        if nk == 0:
+            dq_out[r0:r0 + nq] = 0.0
+            continue
+        dk_out[k0:k0 + nk] = 0.0
+        dv_out[k0:k0 + nk] = 0.0
+        for hk in range(hkv):
+            qs = q[r0:r0 + nq, hk * g:(hk + 1) * g, :].astype(np.float64).reshape(nq * g, d)
+            dos = d_out[r0:r0 + nq, hk * g:(hk + 1) * g, :].astype(np.float64).reshape(nq * g, d)
+            ks = k[k0:k0 + nk, hk, :].astype(np.float64)
+            vs = v[k0:k0 + nk, hk, :].astype(np.float64)
+            x = (qs @ ks.T) * s
+            x -= x.max(axis=1, keepdims=True)
+            p = np.exp(x)
+            p /= p.sum(axis=1, keepdims=True)
+            dp = dos @ vs.T
+            dd = (p * dp).sum(axis=1, keepdims=True)
+            ds = p * (dp - dd)
+            dq_out[r0:r0 + nq, hk * g:(hk + 1) * g, :] = (s * (ds @ ks)).reshape(nq, g, d)
+            dk_out[k0:k0 + nk, hk, :] = s * (ds.T @ qs)
+            dv_out[k0:k0 + nk, hk, :] = p.T @ dos
+    return dq_out, dk_out, dv_out

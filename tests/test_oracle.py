@@ -340,9 +340,58 @@ def pin_causal(orc):
     np.testing.assert_array_equal(o3, o[rows])
 
 
+def pin_backward(orc):
+    """Gradients: central finite differences of sum(dO * O) on a tiny gapped geometry
+    (GQA, keyless segment, gap rows), float64 autograd of SDPA on equal lengths, and
+    untouched gap rows."""
+    rng = np.random.default_rng(18)
+    cu_q, used_q = np.array([0, 4, 7, 9]), np.array([3, 3, 2])
+    cu_k, used_k = np.array([0, 5, 9, 12]), np.array([4, 3, 0])
+    hq, hkv, d, sc = 4, 2, 3, 0.7
+    q = _rand(rng, 9, hq, d)
+    k = _rand(rng, 12, hkv, d)
+    v = _rand(rng, 12, hkv, d)
+    do = _rand(rng, 9, hq, d)
+    dq, dk, dv = orc.attention_backward(q, k, v, do, cu_q, used_q, cu_k, used_k, scale=sc,
+                                        dq=np.full(q.shape, 3.0), dk=np.full(k.shape, 4.0), dv=np.full(v.shape, 5.0))
+
+    def loss(qq, kk, vv):
+        o, _ = orc.attention_forward(qq, kk, vv, cu_q, used_q, cu_k, used_k, scale=sc)
+        return float(np.sum(o * do))
+    eps = 1e-6
+    for name, arr, grad, rows in [("q", q, dq, [0, 2, 4, 7, 8]), ("k", k, dk, [0, 3, 5, 7]), ("v", v, dv, [1, 3, 6])]:
+        for r in rows:
+            for h in range(arr.shape[1]):
+                for t in range(d):
+                    a, b_ = arr.copy(), arr.copy()
+                    a[r, h, t] += eps
+                    b_[r, h, t] -= eps
+                    args_a = {"q": (a, k, v), "k": (q, a, v), "v": (q, k, a)}[name]
+                    args_b = {"q": (b_, k, v), "k": (q, b_, v), "v": (q, k, b_)}[name]
+                    fd = (loss(*args_a) - loss(*args_b)) / (2 * eps)
+                    assert abs(fd - grad[r, h, t]) < 1e-6, (name, r, h, t, fd, grad[r, h, t])
+    # untouched: gap q row 3; keys past used (4, 8) and the keyless segment's keys
+    assert np.all(dq[3] == 3.0) and np.all(dk[[4, 8, 9, 10, 11]] == 4.0) and np.all(dv[[4, 8, 9, 10, 11]] == 5.0)
+    assert np.all(dq[7:9] == 0.0)  # keyless segment: O = 0 does not depend on Q
+    # equal lengths: float64 autograd of SDPA
+    B, L, S = 2, 5, 6
+    q = torch.randn(B, hq, L, d, dtype=torch.float64, requires_grad=True)
+    kt = torch.randn(B, hkv, S, d, dtype=torch.float64, requires_grad=True)
+    vt = torch.randn(B, hkv, S, d, dtype=torch.float64, requires_grad=True)
+    gout = torch.randn(B, hq, L, d, dtype=torch.float64)
+    torch.nn.functional.scaled_dot_product_attention(q, kt, vt, scale=sc, enable_gqa=True).backward(gout)
+    pack = lambda t: t.detach().transpose(1, 2).reshape(-1, t.shape[1], d).numpy()  # noqa: E731
+    dq2, dk2, dv2 = orc.attention_backward(pack(q), pack(kt), pack(vt), pack(gout), np.arange(B + 1) * L, [L] * B,
+                                           np.arange(B + 1) * S, [S] * B, scale=sc)
+    np.testing.assert_allclose(dq2, pack(q.grad), atol=1e-12)
+    np.testing.assert_allclose(dk2, pack(kt.grad), atol=1e-12)
+    np.testing.assert_allclose(dv2, pack(vt.grad), atol=1e-12)
+
+
 PINS = [pin_bruteforce, pin_default_scale, pin_dilution_golden, pin_zero_keys_closed_form,
         pin_single_key, pin_keyless_and_gap_rows, pin_pad_invariance, pin_sdpa_equal_lengths,
-        pin_gqa_repeat, pin_key_permutation, pin_merge_union, pin_rows_match, pin_ranges, pin_causal]
+        pin_gqa_repeat, pin_key_permutation, pin_merge_union, pin_rows_match, pin_ranges, pin_causal,
+        pin_backward]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -377,6 +426,9 @@ MUTANTS = {
     "sqrt_d_scale": ("1.0 / math.sqrt(d) if scale is None", "1.0 / d if scale is None"),
     "causal_off_by_one": ("(np.floor_divide(pos, int(causal_block)) + 1)", "np.floor_divide(pos, int(causal_block))"),
     "causal_top_left": ("+ (int(used_k) - int(used_q))", "+ 0"),
+    "backward_no_D": ("ds = p * (dp - dd)", "ds = p * dp"),
+    "backward_dk_unscaled": ("dk_out[k0:k0 + nk, hk, :] = s * (ds.T @ qs)", "dk_out[k0:k0 + nk, hk, :] = ds.T @ qs"),
+    "backward_dv_uses_ds": ("dv_out[k0:k0 + nk, hk, :] = p.T @ dos", "dv_out[k0:k0 + nk, hk, :] = ds.T @ dos"),
     "range_end_dropped": ("np.arange(int(st), int(st) + int(n))", "np.arange(int(st), int(st) + int(n) - 1)"),
 }
 
