@@ -309,7 +309,8 @@ def attention_backward(q, k, v, d_out, cu_q, used_q, cu_k, used_k, *, scale: Opt
         dV_j  = sum_{i, h in the KV group} P_ij dO_i
 
     Only used rows of dQ and used keys of dK / dV are written (others keep ``dq`` /
-    ``dk`` / ``dv``, default zeros); a keyless segment's used rows get dQ = 0. Each
+    ``dk`` / ``dv``, default zeros); a keyless segment's used rows get dQ = 0 and the
+    used keys of a segment without used rows get dK = dV = 0. Each
     segment's used keys must not overlap another segment's. Returns (dq, dk, dv)."""
     q, k, v, d_out = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(d_out)
     total_q, hq, d = q.shape
@@ -326,13 +327,14 @@ def attention_backward(q, k, v, d_out, cu_q, used_q, cu_k, used_k, *, scale: Opt
     for b in range(len(used_q)):
         r0, nq = int(cu_q[b]), int(used_q[b])
         k0, nk = int(cu_k[b]), int(used_k[b])
+        if nk > 0:  # a used key no used row reads still has a (zero) gradient
+            dk_out[k0:k0 + nk] = 0.0
+            dv_out[k0:k0 + nk] = 0.0
         if nq == 0:
             continue
         if nk == 0:
             dq_out[r0:r0 + nq] = 0.0
             continue
-        dk_out[k0:k0 + nk] = 0.0
-        dv_out[k0:k0 + nk] = 0.0
         for hk in range(hkv):
             qs = q[r0:r0 + nq, hk * g:(hk + 1) * g, :].astype(np.float64).reshape(nq * g, d)
             dos = d_out[r0:r0 + nq, hk * g:(hk + 1) * g, :].astype(np.float64).reshape(nq * g, d)

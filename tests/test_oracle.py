@@ -342,15 +342,15 @@ def pin_causal(orc):
 
 def pin_backward(orc):
     """Gradients: central finite differences of sum(dO * O) on a tiny gapped geometry
-    (GQA, keyless segment, gap rows), float64 autograd of SDPA on equal lengths, and
-    untouched gap rows."""
+    (GQA, a keyless segment, a segment with keys but no rows, gap rows), float64
+    autograd of SDPA on equal lengths, and untouched gap rows."""
     rng = np.random.default_rng(18)
-    cu_q, used_q = np.array([0, 4, 7, 9]), np.array([3, 3, 2])
-    cu_k, used_k = np.array([0, 5, 9, 12]), np.array([4, 3, 0])
+    cu_q, used_q = np.array([0, 4, 7, 9, 9]), np.array([3, 3, 2, 0])
+    cu_k, used_k = np.array([0, 5, 9, 12, 14]), np.array([4, 3, 0, 2])
     hq, hkv, d, sc = 4, 2, 3, 0.7
     q = _rand(rng, 9, hq, d)
-    k = _rand(rng, 12, hkv, d)
-    v = _rand(rng, 12, hkv, d)
+    k = _rand(rng, 14, hkv, d)
+    v = _rand(rng, 14, hkv, d)
     do = _rand(rng, 9, hq, d)
     dq, dk, dv = orc.attention_backward(q, k, v, do, cu_q, used_q, cu_k, used_k, scale=sc,
                                         dq=np.full(q.shape, 3.0), dk=np.full(k.shape, 4.0), dv=np.full(v.shape, 5.0))
@@ -359,7 +359,8 @@ def pin_backward(orc):
         o, _ = orc.attention_forward(qq, kk, vv, cu_q, used_q, cu_k, used_k, scale=sc)
         return float(np.sum(o * do))
     eps = 1e-6
-    for name, arr, grad, rows in [("q", q, dq, [0, 2, 4, 7, 8]), ("k", k, dk, [0, 3, 5, 7]), ("v", v, dv, [1, 3, 6])]:
+    for name, arr, grad, rows in [("q", q, dq, [0, 2, 4, 7, 8]), ("k", k, dk, [0, 3, 5, 7, 12]),
+                                  ("v", v, dv, [1, 3, 6, 13])]:
         for r in rows:
             for h in range(arr.shape[1]):
                 for t in range(d):
@@ -429,6 +430,7 @@ MUTANTS = {
     "backward_no_D": ("ds = p * (dp - dd)", "ds = p * dp"),
     "backward_dk_unscaled": ("dk_out[k0:k0 + nk, hk, :] = s * (ds.T @ qs)", "dk_out[k0:k0 + nk, hk, :] = ds.T @ qs"),
     "backward_dv_uses_ds": ("dv_out[k0:k0 + nk, hk, :] = p.T @ dos", "dv_out[k0:k0 + nk, hk, :] = ds.T @ dos"),
+    "backward_rowless_keys_untouched": ("        if nk > 0:  # a used key", "        if nk > 0 and nq > 0:  # a used key"),
     "range_end_dropped": ("np.arange(int(st), int(st) + int(n))", "np.arange(int(st), int(st) + int(n) - 1)"),
 }
 
