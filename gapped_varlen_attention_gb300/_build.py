@@ -12,7 +12,7 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libgva.so")
-SOURCES = ["gva_api.cu", "gva_fwd.cu", "gva_merge.cu", "gva_noalloc.cu"]
+SOURCES = ["gva_api.cu", "gva_fwd.cu", "gva_bwd.cu", "gva_merge.cu", "gva_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -22,7 +22,7 @@ GVA_BF16, GVA_FP32 = 0, 1
 # Every symbol include/gva.h declares.
 EXPORTS = ("gva_plan", "gva_forward", "gva_lse_merge", "gva_plan_destroy", "gva_plan_get_info",
            "gva_device_status", "gva_status_string", "gva_last_error", "gva_forward_noalloc", "gva_plan_ranges",
-           "gva_plan_causal")
+           "gva_plan_causal", "gva_backward_workspace_size", "gva_backward")
 NOALLOC_MAX_WORK_ITEMS = 32768  # GVA_NOALLOC_MAX_WORK_ITEMS in include/gva.h
 
 
@@ -70,9 +70,11 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.gva_plan_causal.argtypes = [pi32, pi32, pi32, pi32, i32, i32, i32, i32, i32, ctypes.POINTER(vp)]
     lib.gva_plan_ranges.argtypes = [pi32, pi32, i32, pi32, pi32, pi32, ctypes.c_int64, i32, i32, i32,
                                     ctypes.POINTER(vp)]
+    lib.gva_backward_workspace_size.argtypes = [vp, ctypes.POINTER(ctypes.c_size_t)]
+    lib.gva_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, vp, ctypes.c_size_t, f32, vp]
     for name in ("gva_plan", "gva_forward", "gva_lse_merge", "gva_plan_destroy", "gva_plan_get_info",
-                 "gva_device_status", "gva_forward_noalloc", "gva_plan_ranges",
-           "gva_plan_causal"):
+                 "gva_device_status", "gva_forward_noalloc", "gva_plan_ranges", "gva_plan_causal",
+                 "gva_backward_workspace_size", "gva_backward"):
         getattr(lib, name).restype = i32
     if path is None:
         _lib = lib
@@ -238,6 +240,61 @@ def lse_merge(plan: Plan, outs: Sequence, lses: Sequence, out, lse, stream=None)
                            _stream_ptr(stream))
     _check(lib, st, "gva_lse_merge")
     return out, lse
+
+
+def backward_workspace_bytes(plan: Plan) -> int:
+    """``gva_backward_workspace_size``: device scratch bytes ``backward`` needs."""
+    n = ctypes.c_size_t()
+    _check(plan._lib, plan._lib.gva_backward_workspace_size(plan.handle, ctypes.byref(n)),
+           "gva_backward_workspace_size")
+    return int(n.value)
+
+
+def backward(plan: Plan, q, k, v, out, lse, d_out, dq, dk, dv, softmax_scale: float = 0.0, workspace=None,
+             stream=None):
+    """``gva_backward``: dQ, dK, dV of the forward (``out`` / ``lse`` from ``forward`` on
+    the same inputs) for the output gradient ``d_out``.
+
+    q, out, d_out [total_q, Hq, d] bf16; k, v [total_k, Hkv, d] bf16; lse [Hq, total_q]
+    fp32; dq [total_q, Hq, d] and dk / dv [total_k, Hkv, d] bf16 or fp32 (dk and dv the
+    same dtype). ``workspace``: a CUDA uint8 tensor of at least
+    ``backward_workspace_bytes(plan)`` bytes, allocated here if None."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("d_out", d_out)):
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be bfloat16")
+    if lse.dtype != torch.float32:
+        raise TypeError("lse must be float32")
+    if dq.dtype not in (torch.bfloat16, torch.float32) or dk.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("dq / dk / dv must be bfloat16 or float32")
+    if dv.dtype != dk.dtype:
+        raise TypeError("dk and dv must share one dtype")
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("lse", lse), ("d_out", d_out), ("dq", dq),
+                    ("dk", dk), ("dv", dv)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    hq, hkv, d = plan.num_heads_q, plan.num_heads_kv, plan.head_dim
+    for name, t in (("q", q), ("out", out), ("d_out", d_out), ("dq", dq)):
+        if tuple(t.shape) != (plan.total_q, hq, d):
+            raise ValueError(f"{name} must be [{plan.total_q}, {hq}, {d}]")
+    for name, t in (("k", k), ("v", v), ("dk", dk), ("dv", dv)):
+        if tuple(t.shape) != (plan.total_k, hkv, d):
+            raise ValueError(f"{name} must be [{plan.total_k}, {hkv}, {d}]")
+    if tuple(lse.shape) != (hq, plan.total_q):
+        raise ValueError(f"lse must be [{hq}, {plan.total_q}]")
+    need = backward_workspace_bytes(plan)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace must be a CUDA tensor of at least {need} bytes")
+    lib = plan._lib
+    st = lib.gva_backward(plan.handle, _dev_ptr(q), _dev_ptr(k), _dev_ptr(v), _dev_ptr(out), _dev_ptr(d_out),
+                          _dev_ptr(lse), _dev_ptr(dq), GVA_FP32 if dq.dtype == torch.float32 else GVA_BF16,
+                          _dev_ptr(dk), _dev_ptr(dv), GVA_FP32 if dk.dtype == torch.float32 else GVA_BF16,
+                          _dev_ptr(workspace), workspace.numel() * workspace.element_size(), float(softmax_scale),
+                          _stream_ptr(stream))
+    _check(lib, st, "gva_backward")
+    return dq, dk, dv
 
 
 def device_status(plan: Plan):

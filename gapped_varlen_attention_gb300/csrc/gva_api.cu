@@ -24,6 +24,12 @@ struct gva_plan {
   gva::KeyBlock* d_blocks = nullptr;
   gva::MergeUnit* d_units = nullptr;
   int* d_error = nullptr;
+  // backward work (plans from gva_plan only): one Q tile per dQ item, one key block of
+  // one KV head per dK / dV unit
+  bool backward_ok = false;
+  int32_t num_bwd_items = 0, num_kv_units = 0, bwd_grid = 0;
+  gva::WorkItem* d_bwd_items = nullptr;
+  gva::KvUnit* d_kv_units = nullptr;
 };
 
 namespace {
@@ -101,6 +107,8 @@ void free_plan(struct gva_plan* p) {
   if (p->d_blocks) cudaFree(p->d_blocks);
   if (p->d_units) cudaFree(p->d_units);
   if (p->d_error) cudaFree(p->d_error);
+  if (p->d_bwd_items) cudaFree(p->d_bwd_items);
+  if (p->d_kv_units) cudaFree(p->d_kv_units);
   delete p;
 }
 
@@ -108,10 +116,12 @@ void free_plan(struct gva_plan* p) {
 // keys are the ranges range_off[b] .. range_off[b+1] of (range_start, range_len).
 // causal_block > 0 (block-causal, one prefix range per segment): each item only gets the
 // key blocks its last row sees, and FLOPs count the visible keys of every row.
+// backward (maskless, one prefix range per segment, segments' keys disjoint): also build
+// the dQ items and the dK / dV units.
 gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int32_t num_segments,
                       const int32_t* range_off, const int32_t* range_start, const int32_t* range_len,
                       int64_t total_k, int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim,
-                      int32_t causal_block, gva_plan_t* out_plan) {
+                      int32_t causal_block, bool backward, gva_plan_t* out_plan) {
   const int32_t group = num_heads_q / num_heads_kv;
   // ---- key blocks: each range cut into blocks of at most kBlockKeys keys
   std::vector<gva::KeyBlock> blocks;
@@ -178,6 +188,36 @@ gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
   std::vector<gva::WorkItem> sorted(items.size());
   for (size_t i = 0; i < order.size(); ++i) sorted[i] = items[order[i]];
 
+  // ---- backward work lists, longest first
+  std::vector<gva::WorkItem> bwd_items;
+  std::vector<gva::KvUnit> kv_units;
+  if (backward) {
+    for (int32_t b = 0; b < num_segments; ++b) {
+      const int32_t uq = seqused_q[b];
+      for (int32_t hk = 0; hk < num_heads_kv; ++hk) {
+        for (int32_t t0 = 0; t0 < uq; t0 += tokens_per_tile) {
+          gva::WorkItem it{};
+          it.q_row0 = cu_seqlens_q[b] + t0;
+          it.q_rows = std::min(tokens_per_tile, uq - t0);
+          it.blk0 = seg_blk0[b];
+          it.nblk = seg_nblk[b];
+          it.head_kv = hk;
+          it.n_tiles = 1;
+          it.k_len = seg_keys[b];
+          bwd_items.push_back(it);
+        }
+        for (int32_t j = 0; j < seg_nblk[b]; ++j) {
+          const gva::KeyBlock& kb = blocks[seg_blk0[b] + j];
+          kv_units.push_back({kb.row0, kb.valid, cu_seqlens_q[b], uq, hk, 0, 0, 0});
+        }
+      }
+    }
+    std::stable_sort(bwd_items.begin(), bwd_items.end(),
+                     [](const gva::WorkItem& a, const gva::WorkItem& c) { return a.nblk > c.nblk; });
+    std::stable_sort(kv_units.begin(), kv_units.end(),
+                     [](const gva::KvUnit& a, const gva::KvUnit& c) { return a.q_used > c.q_used; });
+  }
+
   // ---- device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -234,6 +274,26 @@ gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
       return cuda_fail(e, "uploading the merge units");
     }
   }
+  p->backward_ok = backward;
+  p->num_bwd_items = static_cast<int32_t>(bwd_items.size());
+  p->num_kv_units = static_cast<int32_t>(kv_units.size());
+  p->bwd_grid = std::min(p->num_bwd_items, sms);
+  if (!bwd_items.empty()) {
+    if ((e = cudaMalloc(&p->d_bwd_items, bwd_items.size() * sizeof(gva::WorkItem))) != cudaSuccess ||
+        (e = cudaMemcpy(p->d_bwd_items, bwd_items.data(), bwd_items.size() * sizeof(gva::WorkItem),
+                        cudaMemcpyHostToDevice)) != cudaSuccess) {
+      free_plan(p);
+      return cuda_fail(e, "uploading the backward work list");
+    }
+  }
+  if (!kv_units.empty()) {
+    if ((e = cudaMalloc(&p->d_kv_units, kv_units.size() * sizeof(gva::KvUnit))) != cudaSuccess ||
+        (e = cudaMemcpy(p->d_kv_units, kv_units.data(), kv_units.size() * sizeof(gva::KvUnit),
+                        cudaMemcpyHostToDevice)) != cudaSuccess) {
+      free_plan(p);
+      return cuda_fail(e, "uploading the dK / dV units");
+    }
+  }
   *out_plan = p;
   return ok();
 }
@@ -286,7 +346,7 @@ gva_status gva_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, const
     len[b] = seqused_k[b];
   }
   return build_plan(cu_seqlens_q, seqused_q, num_segments, off.data(), start.data(), len.data(),
-                    cu_seqlens_k[num_segments], num_heads_q, num_heads_kv, head_dim, 0, out_plan);
+                    cu_seqlens_k[num_segments], num_heads_q, num_heads_kv, head_dim, 0, true, out_plan);
 }
 
 gva_status gva_plan_causal(const int32_t* cu_seqlens_q, const int32_t* seqused_q, const int32_t* cu_seqlens_k,
@@ -308,7 +368,8 @@ gva_status gva_plan_causal(const int32_t* cu_seqlens_q, const int32_t* seqused_q
     len[b] = seqused_k[b];
   }
   return build_plan(cu_seqlens_q, seqused_q, num_segments, off.data(), start.data(), len.data(),
-                    cu_seqlens_k[num_segments], num_heads_q, num_heads_kv, head_dim, causal_block, out_plan);
+                    cu_seqlens_k[num_segments], num_heads_q, num_heads_kv, head_dim, causal_block, false,
+                    out_plan);
 }
 
 gva_status gva_plan_ranges(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int32_t num_segments,
@@ -335,7 +396,7 @@ gva_status gva_plan_ranges(const int32_t* cu_seqlens_q, const int32_t* seqused_q
                   (long long)(st + n), (long long)total_k);
   }
   return build_plan(cu_seqlens_q, seqused_q, num_segments, key_range_offsets, key_range_starts, key_range_lengths,
-                    total_k, num_heads_q, num_heads_kv, head_dim, 0, out_plan);
+                    total_k, num_heads_q, num_heads_kv, head_dim, 0, false, out_plan);
 }
 
 gva_status gva_forward(gva_plan_t plan, const void* q, const void* k, const void* v, void* out, gva_dtype out_dtype,
@@ -419,6 +480,88 @@ gva_status gva_lse_merge(gva_plan_t plan, int32_t num_parts, const void* const* 
   prm.head_dim = plan->head_dim;
   e = gva::launch_merge(in_dtype == GVA_FP32, out_dtype == GVA_FP32, prm, plan->merge_grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launching the LSE merge kernel");
+  return ok();
+}
+
+gva_status gva_backward_workspace_size(gva_plan_t plan, size_t* bytes) {
+  if (plan == nullptr || bytes == nullptr) return fail(GVA_ERR_INVALID_ARG, "plan or bytes is NULL");
+  if (!plan->backward_ok)
+    return fail(GVA_ERR_UNSUPPORTED, "the backward needs a plan from gva_plan (maskless, prefix keys)");
+  *bytes = static_cast<size_t>(plan->num_heads_q) * static_cast<size_t>(plan->total_q) * sizeof(float);
+  return ok();
+}
+
+gva_status gva_backward(gva_plan_t plan, const void* q, const void* k, const void* v, const void* out,
+                        const void* d_out, const float* lse, void* dq, gva_dtype dq_dtype, void* dk, void* dv,
+                        gva_dtype dkv_dtype, void* workspace, size_t workspace_bytes, float softmax_scale,
+                        cudaStream_t stream) {
+  if (plan == nullptr) return fail(GVA_ERR_INVALID_ARG, "plan is NULL");
+  if (!plan->backward_ok)
+    return fail(GVA_ERR_UNSUPPORTED, "the backward needs a plan from gva_plan (maskless, prefix keys)");
+  if ((dq_dtype != GVA_BF16 && dq_dtype != GVA_FP32) || (dkv_dtype != GVA_BF16 && dkv_dtype != GVA_FP32))
+    return fail(GVA_ERR_INVALID_ARG, "bad gradient dtype");
+  if (plan->num_bwd_items == 0 && plan->num_kv_units == 0) return ok();  // no used row and no used key
+  // With no keys (or no rows) at all, the K-side (or Q-side) tensors are never read or
+  // written and may be empty; one of the two sides is non-empty here.
+  const bool has_keys = plan->total_k > 0;
+  const bool has_rows = plan->total_q > 0;
+  if (!has_keys) k = v = dk = dv = const_cast<void*>(q);
+  if (!has_rows) {
+    q = out = d_out = dq = const_cast<void*>(k);
+    lse = static_cast<const float*>(k);
+  }
+  if (q == nullptr || k == nullptr || v == nullptr || dk == nullptr || dv == nullptr || out == nullptr ||
+      d_out == nullptr || lse == nullptr || dq == nullptr)
+    return fail(GVA_ERR_INVALID_ARG, "a tensor pointer is NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(d_out) || !aligned16(lse) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
+    return fail(GVA_ERR_INVALID_ARG, "every tensor and the workspace must be 16-byte aligned");
+  const size_t need = static_cast<size_t>(plan->num_heads_q) * static_cast<size_t>(plan->total_q) * sizeof(float);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(GVA_ERR_INVALID_ARG, "the workspace needs %zu bytes, got %zu", need, workspace_bytes);
+  if (!(softmax_scale == softmax_scale) || std::isinf(softmax_scale))
+    return fail(GVA_ERR_INVALID_ARG, "softmax_scale is not finite");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != plan->device)
+    return fail(GVA_ERR_INVALID_ARG, "the plan was built on device %d, the current device is %d", plan->device, dev);
+  const int32_t tokens_per_tile = gva::kTileRows / plan->group;
+  const int64_t qrows = has_rows ? plan->total_q : 1;  // the maps need one row
+  const int64_t krows = has_keys ? plan->total_k : 1;
+  CUtensorMap mq, mk, mv, mdo;
+  gva_status s;
+  if ((s = make_map(&mq, q, qrows, plan->num_heads_q, plan->head_dim, tokens_per_tile, plan->group, "Q")) != GVA_OK)
+    return s;
+  if ((s = make_map(&mdo, d_out, qrows, plan->num_heads_q, plan->head_dim, tokens_per_tile,
+                    plan->group, "dO")) != GVA_OK)
+    return s;
+  if ((s = make_map(&mk, k, krows, plan->num_heads_kv, plan->head_dim, gva::kBlockKeys, 1, "K")) != GVA_OK) return s;
+  if ((s = make_map(&mv, v, krows, plan->num_heads_kv, plan->head_dim, gva::kBlockKeys, 1, "V")) != GVA_OK) return s;
+  const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(plan->head_dim));
+  gva::BwdParams prm{};
+  prm.items = plan->d_bwd_items;
+  prm.blocks = plan->d_blocks;
+  prm.num_items = plan->num_bwd_items;
+  prm.kv_units = plan->d_kv_units;
+  prm.num_kv_units = plan->num_kv_units;
+  prm.lse = lse;
+  prm.dvec = static_cast<float*>(workspace);
+  prm.dq = dq;
+  prm.dk = dk;
+  prm.dv = dv;
+  prm.total_q = plan->total_q;
+  prm.num_heads_q = plan->num_heads_q;
+  prm.num_heads_kv = plan->num_heads_kv;
+  prm.group = plan->group;
+  prm.tokens_per_tile = tokens_per_tile;
+  prm.scale = scale;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.error_flag = plan->d_error;
+  e = gva::launch_backward(plan->head_dim, dq_dtype == GVA_FP32, dkv_dtype == GVA_FP32, prm, plan->d_units,
+                           plan->num_units, out, d_out, static_cast<float*>(workspace), mq, mk, mv, mdo,
+                           plan->bwd_grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launching the backward kernels");
   return ok();
 }
 

@@ -30,6 +30,7 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include "gva_device_common.cuh"
 #include "gva_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -45,7 +46,6 @@ constexpr uint32_t kTmemCols = 512;
 __host__ __device__ constexpr uint32_t col_s(int t) { return 128u * t; }
 __host__ __device__ constexpr uint32_t col_o(int t) { return 256u + 128u * t; }
 constexpr float kRescaleThreshold = 8.0f;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr float kLn2 = 0.693147180559945309f;
 
 template <int D>
@@ -71,98 +71,6 @@ struct Ctrl {
   uint32_t tmem_base;
   int abort;
 };
-
-// Wait for the phase of `bar` with parity `parity` to complete. Gives up (returning
-// false) when another role has aborted or after kWaitLimitNs, recording the timeout.
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      *abort_flag = 1;
-      atomicOr(err, kErrWaitTimeout);
-      return false;
-    }
-  }
-}
-
-// Same, ignoring the abort flag: used to drain copies and MMAs already in flight.
-__device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, int* err) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      atomicOr(err, kErrWaitTimeout);
-      return;
-    }
-  }
-}
-
-// Persistent schedule: the items are sorted by decreasing cost; CTA c takes item
-// r * grid + c in even rounds and r * grid + (grid - 1 - c) in odd ones.
-__device__ __forceinline__ int item_index(int round, int cta, int grid) {
-  return (round & 1) ? round * grid + (grid - 1 - cta) : round * grid + cta;
-}
-
-__device__ __forceinline__ WorkItem load_item(const WorkItem* items, int idx) {
-  const int4* p = reinterpret_cast<const int4*>(items + idx);
-  const int4 a = __ldg(p), b = __ldg(p + 1);
-  WorkItem it;
-  it.q_row0 = a.x; it.q_rows = a.y; it.blk0 = a.z; it.nblk = a.w;
-  it.head_kv = b.x; it.n_tiles = b.y; it.k_len = b.z; it.q_pos0 = b.w;
-  return it;
-}
-
-__device__ __forceinline__ KeyBlock load_block(const KeyBlock* blocks, int idx) {
-  const int2 v = __ldg(reinterpret_cast<const int2*>(blocks) + idx);
-  return KeyBlock{v.x, v.y};
-}
-
-// MMA issue. One thread issues every tcgen05.mma, so the issue path must be short:
-// the shared-memory descriptors are built once per operand buffer, and each K step only
-// adds its byte offset (in 16-byte units) to the start-address field (bits 0-13; every
-// address here is below 256 KB, so the field never carries). Building a 64-bit
-// descriptor per MMA instead costs more issue time than a 128x128x16 MMA executes.
-template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint64_t q_desc, uint64_t k_desc) {
-  constexpr uint32_t idesc = make_idesc_bf16(kTileRows, kBlockKeys, false);
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    static_assert(Cfg<D>::kQChunkBytes == Cfg<D>::kKVChunkBytes, "Q and K chunks share offsets");
-    const uint32_t off = ((kk / 4) * Cfg<D>::kQChunkBytes + (kk % 4) * 32) >> 4;
-    umma_bf16_ss(tmem_s, q_desc + off, k_desc + off, idesc, kk > 0);
-  }
-}
-
-template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint64_t v_desc, uint32_t accumulate) {
-  constexpr uint32_t idesc = make_idesc_bf16(kTileRows, D, true);
-  umma_bf16_ts(tmem_o, tmem_p, v_desc, idesc, accumulate);
-#pragma unroll
-  for (int kk = 1; kk < kBlockKeys / 16; ++kk)
-    umma_bf16_ts(tmem_o, tmem_p + kk * 8, v_desc + ((kk * 16 * 128) >> 4), idesc, 1u);
-}
-
-template <typename TOut>
-__device__ __forceinline__ void store_row32(TOut* dst, const float (&x)[32]);
-
-template <>
-__device__ __forceinline__ void store_row32<__nv_bfloat16>(__nv_bfloat16* dst, const float (&x)[32]) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    d[i] = make_uint4(pack_bf16x2(x[8 * i + 0], x[8 * i + 1]), pack_bf16x2(x[8 * i + 2], x[8 * i + 3]),
-                      pack_bf16x2(x[8 * i + 4], x[8 * i + 5]), pack_bf16x2(x[8 * i + 6], x[8 * i + 7]));
-  }
-}
-
-template <>
-__device__ __forceinline__ void store_row32<float>(float* dst, const float (&x)[32]) {
-  float4* d = reinterpret_cast<float4*>(dst);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) d[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
-}
 
 // kCausal: block-causal masking within each segment. Row token i of a segment sits at
 // key position pos = i + used_k - used_q and sees keys j < (floor(pos / B) + 1) * B

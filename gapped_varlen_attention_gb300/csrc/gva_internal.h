@@ -36,6 +36,17 @@ struct alignas(8) KeyBlock {
   int32_t valid;
 };
 
+// One unit of the dK / dV kernel: one key block of one segment for one KV head, run
+// against every Q tile of the segment.
+struct alignas(16) KvUnit {
+  int32_t key_row0;  // global K/V row of the block's first key
+  int32_t keys;      // used keys in the block (1 .. kBlockKeys)
+  int32_t q_row0;    // global token row of the segment's first query
+  int32_t q_used;    // used query rows of the segment (0: dK = dV = 0)
+  int32_t head_kv;
+  int32_t pad0, pad1, pad2;
+};
+
 struct alignas(8) MergeUnit {
   int32_t row0;   // global token row of the first row
   int32_t rows;   // used rows in this unit (1 .. kMergeRows)
@@ -69,6 +80,27 @@ struct MergeParams {
   int32_t head_dim;
 };
 
+struct BwdParams {
+  const WorkItem* items;   // dQ work: one Q tile (up to 128 folded rows) per item
+  const KeyBlock* blocks;
+  int32_t num_items;
+  const KvUnit* kv_units;  // dK / dV work
+  int32_t num_kv_units;
+  const float* lse;        // [Hq, total_q] from the forward
+  const float* dvec;       // [Hq, total_q]: rowsum(dO * O)
+  void* dq;                // [total_q, Hq, d]
+  void* dk;                // [total_k, Hkv, d]
+  void* dv;
+  int64_t total_q;
+  int32_t num_heads_q;
+  int32_t num_heads_kv;
+  int32_t group;
+  int32_t tokens_per_tile;
+  float scale;             // softmax scale s
+  float scale_log2;        // s * log2(e)
+  int* error_flag;
+};
+
 // Device error word bits.
 constexpr int kErrWaitTimeout = 1;
 
@@ -77,6 +109,11 @@ cudaError_t launch_forward(int head_dim, bool out_f32, const FwdParams& p, const
                            const CUtensorMap& map_k, const CUtensorMap& map_v, int grid, cudaStream_t stream);
 cudaError_t launch_merge(bool in_f32, bool out_f32, const MergeParams& p, int grid, cudaStream_t stream);
 int forward_smem_bytes(int head_dim);
+// Backward: rowsum(dO * O) over used rows, then dQ, then dK / dV (gva_bwd.cu).
+cudaError_t launch_backward(int head_dim, bool dq_f32, bool dkv_f32, const BwdParams& p, const MergeUnit* units,
+                            int32_t num_units, const void* out, const void* d_out, float* dvec,
+                            const CUtensorMap& map_q, const CUtensorMap& map_k, const CUtensorMap& map_v,
+                            const CUtensorMap& map_do, int dq_grid, cudaStream_t stream);
 // Set the calling thread's gva_last_error() text (defined in gva_api.cu).
 void set_last_error(const char* message);
 

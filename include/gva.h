@@ -38,6 +38,7 @@
 #ifndef GVA_H_
 #define GVA_H_
 
+#include <stddef.h>
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
@@ -185,6 +186,50 @@ GVA_API gva_status gva_forward(gva_plan_t plan, const void* q, const void* k, co
 GVA_API gva_status gva_lse_merge(gva_plan_t plan, int32_t num_parts, const void* const* outs, gva_dtype in_dtype,
                          const float* const* lses, void* out, gva_dtype out_dtype, float* lse,
                          cudaStream_t stream);
+
+/*
+ * gva_backward_workspace_size - bytes of device workspace gva_backward needs.
+ *
+ * Writes Hq * total_q * 4 (one fp32 D value per row and query head) to *bytes. Returns
+ * GVA_ERR_UNSUPPORTED for plans from gva_plan_ranges or gva_plan_causal.
+ */
+GVA_API gva_status gva_backward_workspace_size(gva_plan_t plan, size_t* bytes);
+
+/*
+ * gva_backward - gradients of gva_forward with respect to Q, K and V.
+ *
+ * Cites: cosmos-framework PR #302, review (the FP32 fallback covers the forward only)
+ * and PR #312, "Problem and behavior" (the SM120 path raises on backward): the
+ * gradients the forward's definition implies. For each segment b, query head h (KV
+ * head h_kv = h / (Hq/Hkv)), used row i and used key j, with P the softmax of the
+ * forward recomputed from `lse`:
+ *   dP_ij = <dO_i, V_j>,  D_i = <dO_i, O_i>,  dS_ij = P_ij (dP_ij - D_i)
+ *   dQ_i = s sum_j dS_ij K_j
+ *   dK_j = s sum_{i, h of the KV group} dS_ij Q_i,   dV_j = sum_{i, h} P_ij dO_i
+ * Only for plans from gva_plan (maskless, keys a prefix of each segment's K/V rows).
+ *
+ *   q, k, v   : DEVICE bf16, as given to gva_forward
+ *   out, lse  : DEVICE, the forward's bf16 output [total_q, Hq, d] and fp32 LSE
+ *               [Hq, total_q] (natural log) for the same inputs and scale
+ *   d_out     : DEVICE bf16 [total_q, Hq, d], the gradient of the output
+ *   dq        : DEVICE dq_dtype (GVA_BF16 / GVA_FP32) [total_q, Hq, d]
+ *   dk, dv    : DEVICE dkv_dtype [total_k, Hkv, d]
+ *   workspace : DEVICE, 16-byte aligned, >= gva_backward_workspace_size bytes; scratch
+ *               for the duration of the call (stream order)
+ *   softmax_scale : the forward's s; <= 0 selects 1/sqrt(head_dim)
+ *   stream    : CUDA stream the kernels are enqueued on
+ *
+ * Rows written: dq on used rows (zero on the used rows of a keyless segment); dk / dv
+ * on each segment's used keys (zero where the segment has no used row). Gap rows and
+ * keys past seqused_k are not written; their contents (even NaN) do not affect any
+ * written value. Every pointer 16-byte aligned; inputs must not alias outputs. No
+ * atomics: the result is deterministic. Asynchronous; bounded device waits as for
+ * gva_forward (gva_device_status reports a timeout).
+ */
+GVA_API gva_status gva_backward(gva_plan_t plan, const void* q, const void* k, const void* v, const void* out,
+                                const void* d_out, const float* lse, void* dq, gva_dtype dq_dtype, void* dk,
+                                void* dv, gva_dtype dkv_dtype, void* workspace, size_t workspace_bytes,
+                                float softmax_scale, cudaStream_t stream);
 
 /* Release a plan's device memory. NULL is accepted. Synchronous with respect to the
  * host only through cudaFree. */

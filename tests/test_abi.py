@@ -89,6 +89,10 @@ def test_null_arguments(lib):
     assert lib.gva_lse_merge(None, 1, None, 0, None, None, 0, None, None) == 1
     assert lib.gva_plan_destroy(None) == 0
     assert lib.gva_device_status(None) == 1
+    n = ctypes.c_size_t(7)
+    assert lib.gva_backward_workspace_size(None, ctypes.byref(n)) == 1 and n.value == 7
+    assert lib.gva_backward(None, None, None, None, None, None, None, None, 0, None, None, 0, None, 0, 0.0,
+                            None) == 1
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")

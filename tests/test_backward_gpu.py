@@ -1,0 +1,233 @@
+"""GPU parity of the backward (gva_backward) against the FP64 oracle.
+
+Tolerance, from the arithmetic: the kernels round P and dS to bf16 before the two
+tensor-core products that use them (relative error 2^-9 per term, unbiased), read O
+in bf16 for D = <dO, O>, and accumulate in FP32. For sums of many such terms the error
+stays a small multiple of 2^-9 of the result's scale, so each gradient tensor must
+satisfy max |g - g_ref| <= 2^-6 max |g_ref| (4 x the single rounding of a bf16 store
+of the largest element) and rms(g - g_ref) <= 2^-8 rms(g_ref). Rows the backward must
+not write keep their sentinel bit for bit; keyless rows get dQ = 0 exactly and the
+keys of a segment without rows get dK = dV = 0 exactly."""
+import numpy as np
+import pytest
+import torch
+
+import gapped_varlen_attention_gb300 as gva
+from gapped_varlen_attention_gb300 import workloads as W
+from oracle import gva_oracle
+
+pytestmark = pytest.mark.gpu
+FILL = W.TINY_SENTINEL
+MAX_REL = 2.0 ** -6
+RMS_REL = 2.0 ** -8
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    gva.build()
+
+
+def _make_dout(g, seed, gap_fill=float("nan"), device="cpu"):
+    gen = torch.Generator(device=device).manual_seed(seed + 7)
+    do = torch.randn((g.total_q, g.num_heads_q, g.head_dim), generator=gen, device=device).bfloat16()
+    if gap_fill is not None:
+        do[torch.from_numpy(W.gap_rows(g.cu_q, g.used_q)).to(device)] = gap_fill
+    return do
+
+
+def _masks(g):
+    """Rows of dq and keys of dk / dv the backward writes."""
+    dq_rows = ~W.gap_rows(g.cu_q, g.used_q)
+    dk_rows = np.zeros(g.total_k, bool)
+    for b in range(g.num_segments):
+        dk_rows[g.cu_k[b]:g.cu_k[b] + g.used_k[b]] = True
+    return dq_rows, dk_rows
+
+
+def gpu_backward(g, q, k, v, do, scale=0.0, grad_dtype=torch.bfloat16, plan=None):
+    plan = plan or gva.Plan.from_geometry(g)
+    qc, kc, vc, doc = (t.cuda() for t in (q, k, v, do))
+    o, l = W.make_outputs(g, FILL, device="cuda")
+    gva.forward(plan, qc, kc, vc, o, l, scale)
+    dq = torch.full(qc.shape, FILL, dtype=grad_dtype, device="cuda")
+    dk = torch.full(kc.shape, FILL, dtype=grad_dtype, device="cuda")
+    dv = torch.full(vc.shape, FILL, dtype=grad_dtype, device="cuda")
+    gva.backward(plan, qc, kc, vc, o, l, doc, dq, dk, dv, scale)
+    gva.device_status(plan)
+    return dq, dk, dv
+
+
+def oracle_backward(g, q, k, v, do, scale=None):
+    qn, kn, vn, don = (t.detach().cpu().float().numpy() for t in (q, k, v, do))
+    return gva_oracle.attention_backward(qn, kn, vn, don, g.cu_q, g.used_q, g.cu_k, g.used_k, scale=scale,
+                                         dq=np.full(qn.shape, FILL), dk=np.full(kn.shape, FILL),
+                                         dv=np.full(vn.shape, FILL))
+
+
+def _close(name, got, ref, max_rel=MAX_REL, rms_rel=RMS_REL):
+    if ref.size == 0:
+        return 0.0
+    err = np.abs(got - ref)
+    scale = max(np.abs(ref).max(), 1e-30)
+    assert np.all(np.isfinite(got)), f"{name}: non-finite values"
+    assert err.max() <= max_rel * scale, f"{name}: max err {err.max():.3e} > {max_rel:.1e} x {scale:.3e}"
+    rms_ref = max(np.sqrt(np.mean(ref ** 2)), 1e-30)
+    rms_err = np.sqrt(np.mean(err ** 2))
+    assert rms_err <= rms_rel * rms_ref, f"{name}: rms err {rms_err:.3e} > {rms_rel:.1e} x {rms_ref:.3e}"
+    return float(err.max() / scale)
+
+
+def check_backward(g, got, ref, max_rel=MAX_REL, rms_rel=RMS_REL):
+    dq, dk, dv = (t.float().cpu().numpy().astype(np.float64) for t in got)
+    dq_ref, dk_ref, dv_ref = ref
+    dq_rows, dk_rows = _masks(g)
+    fill32 = np.float64(np.float32(FILL))
+    assert np.all(dq[~dq_rows] == fill32), "a gap row of dQ was written"
+    assert np.all(dk[~dk_rows] == fill32) and np.all(dv[~dk_rows] == fill32), "a key past seqused_k was written"
+    exact = []  # rows whose exact answer is 0: keyless segments' rows, row-less segments' keys
+    for b in range(g.num_segments):
+        r0, nq, k0, nk = int(g.cu_q[b]), int(g.used_q[b]), int(g.cu_k[b]), int(g.used_k[b])
+        if nq and not nk:
+            assert np.all(dq[r0:r0 + nq] == 0.0), "keyless segment: dQ must be 0"
+        if nk and not nq:
+            assert np.all(dk[k0:k0 + nk] == 0.0) and np.all(dv[k0:k0 + nk] == 0.0), "row-less segment: dK/dV must be 0"
+            exact.append(b)
+    errs = (_close("dQ", dq[dq_rows], dq_ref[dq_rows], max_rel, rms_rel),
+            _close("dK", dk[dk_rows], dk_ref[dk_rows], max_rel, rms_rel),
+            _close("dV", dv[dk_rows], dv_ref[dk_rows], max_rel, rms_rel))
+    print(f"max err / max |ref|: dQ {errs[0]:.2e}  dK {errs[1]:.2e}  dV {errs[2]:.2e}")
+    return errs
+
+
+def test_tiny():
+    g = W.tiny()
+    q, k, v = W.make_qkv(g, 1001, gap_fill=float("nan"))
+    do = _make_dout(g, 1001)
+    check_backward(g, gpu_backward(g, q, k, v, do), oracle_backward(g, q, k, v, do))
+
+
+CASES = [  # (Hq, Hkv, d, seed)
+    (8, 2, 128, 201),
+    (16, 16, 128, 202),
+    (32, 8, 64, 203),
+    (4, 4, 64, 204),
+    (16, 1, 128, 205),
+    (128, 1, 64, 206),
+]
+
+
+@pytest.mark.parametrize("hq,hkv,d,seed", CASES)
+def test_random_geometries(hq, hkv, d, seed):
+    """Ragged segments spanning several Q tiles and key blocks, empty segments, NaN in
+    every gap row of Q, K, V and dO."""
+    rng = np.random.default_rng(seed)
+    g = W.random_geometry(rng, 6, 600, 700, hq, hkv, d)
+    q, k, v = W.make_qkv(g, seed, gap_fill=float("nan"))
+    do = _make_dout(g, seed)
+    check_backward(g, gpu_backward(g, q, k, v, do), oracle_backward(g, q, k, v, do))
+
+
+def test_keyless_and_rowless_segments():
+    """A segment with rows but no keys (dQ = 0) and one with keys but no rows (dK = dV = 0)."""
+    cu_q = np.array([0, 100, 230, 230, 300], np.int32)
+    used_q = np.array([90, 130, 0, 61], np.int32)
+    cu_k = np.array([0, 150, 150, 400, 700], np.int32)
+    used_k = np.array([150, 0, 250, 129], np.int32)
+    g = W.Geometry(cu_q, used_q, cu_k, used_k, 8, 4, 128)
+    q, k, v = W.make_qkv(g, 301, gap_fill=float("nan"))
+    do = _make_dout(g, 301)
+    check_backward(g, gpu_backward(g, q, k, v, do), oracle_backward(g, q, k, v, do))
+
+
+def test_fp32_gradients_and_explicit_scale():
+    rng = np.random.default_rng(401)
+    g = W.random_geometry(rng, 4, 500, 500, 16, 4, 128, allow_empty=False)
+    q, k, v = W.make_qkv(g, 401)
+    do = _make_dout(g, 401)
+    got = gpu_backward(g, q, k, v, do, scale=0.05, grad_dtype=torch.float32)
+    # no bf16 store of the result: half the bound
+    check_backward(g, got, oracle_backward(g, q, k, v, do, scale=0.05), max_rel=MAX_REL / 2, rms_rel=RMS_REL / 2)
+
+
+def test_deterministic():
+    rng = np.random.default_rng(501)
+    g = W.random_geometry(rng, 5, 700, 900, 32, 8, 128, allow_empty=False)
+    q, k, v = W.make_qkv(g, 501)
+    do = _make_dout(g, 501)
+    plan = gva.Plan.from_geometry(g)
+    a = gpu_backward(g, q, k, v, do, plan=plan)
+    b = gpu_backward(g, q, k, v, do, plan=plan)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_masked_plans_are_refused():
+    g = W.tiny()
+    plan = gva.Plan.from_geometry(g, causal_block=16)
+    with pytest.raises(gva.GvaError, match="UNSUPPORTED"):
+        gva.backward_workspace_bytes(plan)
+    rplan = gva.Plan.from_ranges(g.cu_q, g.used_q, [[(0, 48)], [(48, 33)], []], g.total_k, 4, 2, 64)
+    with pytest.raises(gva.GvaError, match="UNSUPPORTED"):
+        gva.backward_workspace_bytes(rplan)
+
+
+def test_cfg_text_cross_full():
+    """The CFG text cross-attention workload at full size (8192 rows, 700 / 20 used of
+    1024 padded keys), every gradient element against the oracle."""
+    g = W.cfg_text_cross()
+    q, k, v = W.make_qkv(g, 1002, k_pad_fill=0.0)
+    do = _make_dout(g, 1002)
+    check_backward(g, gpu_backward(g, q, k, v, do), oracle_backward(g, q, k, v, do))
+
+
+def _segment_properties(g, q, k, do, dq, dk, dv, b, s):
+    """Identities of the exact gradients of one segment, per KV head:
+    sum_j dV_j = sum_{i, h in group} dO_i (softmax rows sum to 1), sum_j dK_j = 0 (the
+    rows of dS sum to 0), and sum_i <Q_i, dQ_i> = sum_j <K_j, dK_j> (both equal
+    sum_ij dS_ij x_ij)."""
+    r0, nq, k0, nk = int(g.cu_q[b]), int(g.used_q[b]), int(g.cu_k[b]), int(g.used_k[b])
+    grp = g.num_heads_q // g.num_heads_kv
+    f = lambda t: t.double()  # noqa: E731
+    for hk in range(g.num_heads_kv):
+        heads = slice(hk * grp, (hk + 1) * grp)
+        sdo = f(do[r0:r0 + nq, heads]).sum(dim=(0, 1))
+        sdv = f(dv[k0:k0 + nk, hk]).sum(dim=0)
+        scale_dv = f(dv[k0:k0 + nk, hk]).abs().sum(dim=0).max().item()
+        assert (sdv - sdo).abs().max().item() <= 1e-2 * scale_dv + 1e-3, "sum dV != sum dO"
+        sdk = f(dk[k0:k0 + nk, hk]).sum(dim=0)
+        scale_dk = f(dk[k0:k0 + nk, hk]).abs().sum(dim=0).max().item()
+        assert sdk.abs().max().item() <= 1e-2 * scale_dk, "sum dK != 0"
+        qdq = (f(q[r0:r0 + nq, heads]) * f(dq[r0:r0 + nq, heads])).sum().item()
+        kdk = (f(k[k0:k0 + nk, hk]) * f(dk[k0:k0 + nk, hk])).sum().item()
+        mag = (f(q[r0:r0 + nq, heads]) * f(dq[r0:r0 + nq, heads])).abs().sum().item()
+        assert abs(qdq - kdk) <= 1e-2 * mag, f"<Q,dQ> {qdq:.4e} != <K,dK> {kdk:.4e}"
+
+
+@pytest.mark.slow
+def test_long_replay_full_size_sampled():
+    """The long replay workload at full size (4 segments, up to 32768 rows and 65536
+    keys each): dQ on sampled rows against the oracle (a row's dQ depends on that row
+    only), dK / dV through identities that hold at any size."""
+    g = W.long_replay()
+    q, k, v = W.make_qkv(g, 1005, device="cuda", gap_fill=float("nan"))
+    do = _make_dout(g, 1005, device="cuda")
+    dq, dk, dv = gpu_backward(g, q, k, v, do)
+    dq_rows, dk_rows = _masks(g)
+    assert bool((dq[torch.from_numpy(~dq_rows).cuda()].float() == FILL).all())
+    assert bool((dk[torch.from_numpy(~dk_rows).cuda()].float() == FILL).all())
+    rng = np.random.default_rng(12)
+    s = 1.0 / np.sqrt(g.head_dim)
+    for b in range(g.num_segments):
+        _segment_properties(g, q, k, do, dq, dk, dv, b, s)
+        # sampled rows, each a one-row segment over the segment's keys
+        rows = sorted(set(int(x) for x in rng.integers(0, g.used_q[b], size=3)) | {0, int(g.used_q[b]) - 1})
+        k0, nk = int(g.cu_k[b]), int(g.used_k[b])
+        sel = [int(g.cu_q[b]) + r for r in rows]
+        qs, dos = q[sel].cpu(), do[sel].cpu()
+        n = len(sel)
+        ks, vs = k[k0:k0 + nk].cpu(), v[k0:k0 + nk].cpu()
+        dq_ref, _, _ = gva_oracle.attention_backward(qs, ks, vs, dos, np.arange(n + 1), np.ones(n, np.int64),
+                                                     np.zeros(n + 1, np.int64), np.full(n, nk))
+        got = dq[sel].float().cpu().numpy().astype(np.float64)
+        scale = np.abs(dq_ref).max()
+        assert np.abs(got - dq_ref).max() <= MAX_REL * scale
