@@ -1,7 +1,8 @@
 """Throughput of the gapped varlen attention forward on GB300.
 
 One step = one pass of the whole hot path over one batch of synthetic input: the
-forward launch(es) and, for partitioned workloads, the LSE merge. The default workload
+forward launch(es) and, for partitioned workloads, the LSE merge (for the
+``long_replay_bwd`` workload: the backward, dQ / dK / dV, of the long replay). The default workload
 is the long joint video + LiDAR replay (4 segments x 32768 query rows, 65536 keys each,
 seeded used fractions; Hq=32, Hkv=8, d=128, bf16), the largest single-GPU workload.
 
@@ -101,6 +102,15 @@ class Workload:
             self.causal_block = 512
             self.label = ("multiview causal gapped replay: 7 segments, block-causal masking with 512-token frames "
                           "in one launch (FLOPs count visible keys only)")
+        elif name == "long_replay_bwd":
+            g = W.long_replay()
+            self.geoms = [g]
+            self.q, self.k, self.v = W.make_qkv(g, 1005 + seed_offset, device=dev)
+            self.parts = None
+            self.backward = True
+            self.label = ("backward (dQ, dK, dV) of the long joint video+LiDAR replay: 4 segments x 32768 q rows "
+                          "(used 60-100%) x 65536 keys (used 50-100%), Hq=32, Hkv=8, d=128, bf16; FLOPs = 2.5 x "
+                          "the forward's (five used-row products)")
         elif name == "tiny":
             g = W.tiny()
             self.geoms = [g]
@@ -125,13 +135,33 @@ class Workload:
             self.partials = [W.make_outputs(p, 0.0, device=dev, out_dtype=torch.float32) for p in self.geoms]
         self.flops = float(sum(p.info()["used_flops"] for p in self.plans))
         self.launches_per_step = len(self.geoms) + (0 if self.parts is None else 1)
+        self.metric = METRIC
+        self.kernel = "gva_fwd_kernel"
+        self.inputs = [self.q, self.k, self.v]
+        self.outputs = [self.out, self.lse]
+        if getattr(self, "backward", False):
+            # the forward's O and LSE are inputs of the backward (computed once, untimed)
+            gva.forward(self.plans[0], self.q, self.k, self.v, self.out, self.lse)
+            gen = torch.Generator(device=dev).manual_seed(2005 + seed_offset)
+            self.d_out = torch.randn(self.q.shape, generator=gen, device=dev).bfloat16()
+            self.grads = [torch.empty_like(self.q), torch.empty_like(self.k), torch.empty_like(self.v)]
+            self.ws = torch.empty(max(16, gva.backward_workspace_bytes(self.plans[0])), dtype=torch.uint8,
+                                  device=dev)
+            self.flops *= 2.5
+            self.launches_per_step = 3  # rowsum(dO * O), dQ, dK / dV
+            self.metric = "gapped-varlen attn bwd TFLOP/s (used rows, 2.5 x fwd FLOPs) & % of GB300 BF16 peak"
+            self.kernel = "gva_backward (3 launches: rowsum, dQ, dK/dV)"
+            self.inputs = [self.q, self.k, self.v, self.out, self.lse, self.d_out]
+            self.outputs = list(self.grads)
 
-    def step(self, q=None, k=None, v=None):
+    def step(self, *inputs):
         gva = self.gva
-        q = self.q if q is None else q
-        k = self.k if k is None else k
-        v = self.v if v is None else v
-        if self.partials is None:
+        inputs = inputs or self.inputs
+        q, k, v = inputs[:3]
+        if getattr(self, "backward", False):
+            out, lse, d_out = inputs[3:]
+            gva.backward(self.plans[0], q, k, v, out, lse, d_out, *self.grads, workspace=self.ws)
+        elif self.partials is None:
             gva.forward(self.plans[0], q, k, v, self.out, self.lse)
         else:
             for plan, (o, l) in zip(self.plans, self.partials):
@@ -151,10 +181,10 @@ class Workload:
                 else "L2 flushed between steps (256 MB write)"}
 
     def input_bytes(self):
-        return sum(t.numel() * t.element_size() for t in (self.q, self.k, self.v))
+        return sum(t.numel() * t.element_size() for t in self.inputs)
 
     def output_bytes(self):
-        return self.out.numel() * self.out.element_size() + self.lse.numel() * self.lse.element_size()
+        return sum(t.numel() * t.element_size() for t in self.outputs)
 
 
 # --------------------------------------------------------------------------------------
@@ -269,6 +299,8 @@ def oracle_sample_rate(wl, budget_s: float, seed: int = 0):
     q = wl.q.cpu()
     k = wl.k.cpu()
     v = wl.v.cpu()
+    backward = getattr(wl, "backward", False)
+    d_out = wl.d_out.cpu() if backward else None
     done_flops = 0.0
     rows_done = 0
     t0 = time.perf_counter()
@@ -276,13 +308,21 @@ def oracle_sample_rate(wl, budget_s: float, seed: int = 0):
         for g in geoms:
             b = int(rng.choice(np.flatnonzero(g.used_q > 0)))
             rows = [int(g.cu_q[b]) + int(x) for x in rng.integers(0, int(g.used_q[b]), size=4)]
-            gva_oracle.attention_rows(q, k, v, g.cu_q, g.used_q, g.cu_k, g.used_k, rows)
-            done_flops += 4.0 * g.head_dim * g.num_heads_q * float(g.used_k[b]) * len(rows)
+            if backward:
+                # the sampled rows as one segment over their segment's keys: all five products
+                k0, nk = int(g.cu_k[b]), int(g.used_k[b])
+                gva_oracle.attention_backward(q[rows], k[k0:k0 + nk], v[k0:k0 + nk], d_out[rows], [0, len(rows)],
+                                              [len(rows)], [0, nk], [nk])
+                done_flops += 10.0 * g.head_dim * g.num_heads_q * float(nk) * len(rows)
+            else:
+                gva_oracle.attention_rows(q, k, v, g.cu_q, g.used_q, g.cu_k, g.used_k, rows)
+                done_flops += 4.0 * g.head_dim * g.num_heads_q * float(g.used_k[b]) * len(rows)
             rows_done += len(rows)
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    desc = (f"{rows_done} seeded used rows (all {geoms[0].num_heads_q} heads, every used key of their "
+    what = "backward of " if backward else ""
+    desc = (f"{what}{rows_done} seeded used rows (all {geoms[0].num_heads_q} heads, every used key of their "
             f"segment) of the {wl.name} workload, FP64 NumPy oracle")
     return done_flops / el / 1e12, desc, rows_done, el
 
@@ -297,7 +337,7 @@ def main():
     ap.add_argument("--impl", choices=["gva", "reference"], default="gva")
     ap.add_argument("--workload", default="long_replay",
                     choices=["long_replay", "long_replay_small", "cfg_text_cross", "multiview_causal",
-                             "multiview_fused", "multiview_blockcausal", "tiny"])
+                             "multiview_fused", "multiview_blockcausal", "long_replay_bwd", "tiny"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     args = ap.parse_args()
@@ -355,24 +395,27 @@ def main():
         torch.cuda.nvtx.range_pop()
     barrier()
     ms_step = ms / args.steps
-    # kernel-only time of the dominant launch (the forward) over the same kind of region
-    fwd_only = lambda: wl.gva.forward(wl.plans[0], wl.q, wl.k, wl.v, *(wl.partials[0] if wl.partials else  # noqa
-                                                                       (wl.out, wl.lse)))
+    # kernel-only time of the dominant launch (the forward; for the backward workload the
+    # whole backward call) over the same kind of region
+    if getattr(wl, "backward", False):
+        fwd_only = wl.step
+    else:
+        fwd_only = lambda: wl.gva.forward(wl.plans[0], wl.q, wl.k, wl.v,  # noqa: E731
+                                          *(wl.partials[0] if wl.partials else (wl.out, wl.lse)))
     fwd_ms = time_steps(fwd_only, max(3, args.steps // 2), stream) / max(3, args.steps // 2)
     wl.check()
 
     # end to end through the public API: pinned host inputs -> device, step, result -> host
-    hq = [t.cpu().pin_memory() for t in (wl.q, wl.k, wl.v)]
-    dq = [torch.empty_like(t) for t in (wl.q, wl.k, wl.v)]
-    ho = torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory()
-    hl = torch.empty(wl.lse.shape, dtype=wl.lse.dtype).pin_memory()
+    hq = [t.cpu().pin_memory() for t in wl.inputs]
+    dq = [torch.empty_like(t) for t in wl.inputs]
+    ho = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in wl.outputs]
 
     def e2e_step():
         for d, h in zip(dq, hq):
             d.copy_(h, non_blocking=True)
         wl.step(*dq)
-        ho.copy_(wl.out, non_blocking=True)
-        hl.copy_(wl.lse, non_blocking=True)
+        for h, t in zip(ho, wl.outputs):
+            h.copy_(t, non_blocking=True)
 
     e2e_step()
     torch.cuda.synchronize()
@@ -394,13 +437,13 @@ def main():
     sustained = args.steps * ms_step > 1000.0
     peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
     value = world * wl.flops / (ms_step * 1e-3) / 1e12
-    fwd_flops = wl.plans[0].info()["used_flops"]
+    fwd_flops = wl.flops if getattr(wl, "backward", False) else wl.plans[0].info()["used_flops"]
     achieved = fwd_flops / (fwd_ms * 1e-3) / 1e12
     traffic = recorded_traffic(args.workload)
     cpu_rate, cpu_desc, _, _ = oracle_sample_rate(wl, args.cpu_budget_s)
     e2e_value = world * wl.flops / (e2e_ms * 1e-3) / 1e12
     line = {
-        "metric": METRIC,
+        "metric": wl.metric,
         "value": round(value, 3),
         "unit": UNIT,
         "n_gpus": world,
@@ -421,7 +464,7 @@ def main():
             "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4),
             "traffic": traffic,
-            "kernel": "gva_fwd_kernel",
+            "kernel": wl.kernel,
             "ms_per_launch": round(fwd_ms, 4),
             "peak_source": f"{peak_src} {'sustained' if sustained else 'burst'} dense bf16 (cuBLAS)",
         },
@@ -450,7 +493,7 @@ def run_reference(args, world, rank):
 
     wl = HostWorkload()
     wl.name = args.workload
-    if args.workload == "long_replay":
+    if args.workload in ("long_replay", "long_replay_bwd"):
         g = W.long_replay()
         wl.geoms = [g]
         seed = 1005
@@ -471,6 +514,11 @@ def run_reference(args, world, rank):
         wl.geoms = [g]
         seed = 1001
     wl.q, wl.k, wl.v = W.make_qkv(g, seed)
+    metric = METRIC
+    if args.workload == "long_replay_bwd":
+        wl.backward = True
+        wl.d_out = torch.randn(wl.q.shape, generator=torch.Generator().manual_seed(2005)).bfloat16()
+        metric = "gapped-varlen attn bwd TFLOP/s (used rows, 2.5 x fwd FLOPs) & % of GB300 BF16 peak"
     budget = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     for i in range(args.warmup):
         oracle_sample_rate(wl, budget, seed=i)
@@ -483,7 +531,7 @@ def run_reference(args, world, rank):
     value = float(np.mean(rates))
     line = {
         "impl": "reference",
-        "metric": METRIC,
+        "metric": metric,
         "value": round(value, 6),
         "unit": UNIT,
         "n_gpus": world,
