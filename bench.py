@@ -111,6 +111,13 @@ class Workload:
             self.label = ("backward (dQ, dK, dV) of the long joint video+LiDAR replay: 4 segments x 32768 q rows "
                           "(used 60-100%) x 65536 keys (used 50-100%), Hq=32, Hkv=8, d=128, bf16; FLOPs = 2.5 x "
                           "the forward's (five used-row products)")
+        elif name == "long_replay_small_bwd":
+            g = W.long_replay_small()
+            self.geoms = [g]
+            self.q, self.k, self.v = W.make_qkv(g, 1006 + seed_offset, device=dev)
+            self.parts = None
+            self.backward = True
+            self.label = "backward of the reduced long replay (profiling): 2 segments x 8192 q rows x 32768 keys"
         elif name == "tiny":
             g = W.tiny()
             self.geoms = [g]
@@ -337,7 +344,8 @@ def main():
     ap.add_argument("--impl", choices=["gva", "reference"], default="gva")
     ap.add_argument("--workload", default="long_replay",
                     choices=["long_replay", "long_replay_small", "cfg_text_cross", "multiview_causal",
-                             "multiview_fused", "multiview_blockcausal", "long_replay_bwd", "tiny"])
+                             "multiview_fused", "multiview_blockcausal", "long_replay_bwd", "long_replay_small_bwd",
+                             "tiny"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     args = ap.parse_args()
@@ -505,7 +513,7 @@ def run_reference(args, world, rank):
         g, parts = W.multiview_causal()
         wl.geoms = parts
         seed = 1003
-    elif args.workload == "long_replay_small":
+    elif args.workload in ("long_replay_small", "long_replay_small_bwd"):
         g = W.long_replay_small()
         wl.geoms = [g]
         seed = 1006
@@ -515,7 +523,7 @@ def run_reference(args, world, rank):
         seed = 1001
     wl.q, wl.k, wl.v = W.make_qkv(g, seed)
     metric = METRIC
-    if args.workload == "long_replay_bwd":
+    if args.workload in ("long_replay_bwd", "long_replay_small_bwd"):
         wl.backward = True
         wl.d_out = torch.randn(wl.q.shape, generator=torch.Generator().manual_seed(2005)).bfloat16()
         metric = "gapped-varlen attn bwd TFLOP/s (used rows, 2.5 x fwd FLOPs) & % of GB300 BF16 peak"

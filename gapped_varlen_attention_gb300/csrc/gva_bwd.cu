@@ -12,11 +12,16 @@
 //   1. gva_bwd_dvec_kernel: D = rowsum(dO * O) for every used row and head.
 //   2. gva_bwd_dq_kernel: one 128-row Q tile (folded GQA rows, as in the forward) per
 //      work item, streaming the segment's key blocks: S = Q K^T and dP = dO V^T into
-//      TMEM, P and dS by one thread per row, dQ += dS K with dS read from TMEM.
+//      TMEM, P and dS by the compute threads, dQ += dS K with dS read from TMEM.
 //   3. gva_bwd_dkdv_kernel: one key block of one KV head per unit, streaming the
 //      segment's Q / dO tiles: S^T = K Q^T and dP^T = V dO^T into TMEM, P^T and dS^T by
-//      one thread per key, dV += P^T dO and dK += dS^T Q accumulated in TMEM, then
+//      the compute threads, dV += P^T dO and dK += dS^T Q accumulated in TMEM, then
 //      written once. No atomics anywhere.
+// In both kernels the 128 score columns of a block are two halves of 64, each with its
+// own warpgroup of compute threads (one TMEM lane each) and its own full / ready
+// barriers. The MMA thread runs one half ahead: while one warpgroup turns its half of
+// S and dP into P and dS, the tensor core computes the other half's products, so the
+// exponentials and the matrix products overlap instead of alternating.
 // Operand rows past the used lengths (gaps, padding, possibly NaN) are zeroed in shared
 // memory before an MMA could multiply them by a zero weight.
 #include <cuda_bf16.h>
@@ -29,7 +34,7 @@
 namespace gva {
 namespace {
 
-constexpr int kBwdThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 compute
+constexpr int kBwdThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 compute (two warpgroups)
 constexpr uint32_t kBwdTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -71,12 +76,14 @@ struct BwdCtrl {
   uint64_t a_full, a_empty;            // dQ: Q + dO tiles;   dK/dV: K + V blocks
   uint64_t r_full[4], r_empty[4];      // dQ: K/V ring;       dK/dV: Q/dO slots (2)
   uint64_t zero_bar;                   // partial tiles: the producer's own copy wait
-  uint64_t s_full, p_full, acc_full, mma_done;
+  uint64_t s_full[2], p_full[2];       // dQ: per S buffer;   dK/dV: per column half
+  uint64_t dp_full, dp_consumed;       // dQ: dP ready / read into registers
+  uint64_t acc_full, mma_done;
   uint32_t tmem_base;
   int abort;
 };
 
-__device__ __forceinline__ void init_ctrl(BwdCtrl& c, int ring) {
+__device__ __forceinline__ void init_ctrl(BwdCtrl& c, int ring, uint32_t p_count) {
   mbar_init(&c.a_full, 1);
   mbar_init(&c.a_empty, 1);
   for (int i = 0; i < ring; ++i) {
@@ -84,8 +91,12 @@ __device__ __forceinline__ void init_ctrl(BwdCtrl& c, int ring) {
     mbar_init(&c.r_empty[i], 1);
   }
   mbar_init(&c.zero_bar, 1);
-  mbar_init(&c.s_full, 1);
-  mbar_init(&c.p_full, 128);
+  for (int h = 0; h < 2; ++h) {
+    mbar_init(&c.s_full[h], 1);
+    mbar_init(&c.p_full[h], p_count);
+  }
+  mbar_init(&c.dp_full, 1);
+  mbar_init(&c.dp_consumed, 2 * kTileRows);
   mbar_init(&c.acc_full, 1);
   mbar_init(&c.mma_done, 1);
   c.abort = 0;
@@ -135,6 +146,40 @@ __global__ void __launch_bounds__(256) gva_bwd_dvec_kernel(const MergeUnit* unit
   }
 }
 
+// Half-block products (N = 64 of the 128 rows of the B tile).
+// D[128 x 64] = A[128 x D] B[rows 64h .. 64h + 63]^T, both K-major.
+template <int D>
+__device__ __forceinline__ void issue_qk_half(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc, int h) {
+  constexpr uint32_t idesc = make_idesc_bf16(kTileRows, 64, false);
+  const uint64_t b = b_desc + static_cast<uint64_t>(h) * ((64 * 128) >> 4);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = ((kk / 4) * kChunkBytes + (kk % 4) * 32) >> 4;
+    umma_bf16_ss(tmem_d, a_desc + off, b + off, idesc, kk > 0);
+  }
+}
+
+// D[128 x D] (+)= A[128 x 64] B[rows 64h .. 64h + 63] with A (bf16 pairs, 32 columns)
+// in TMEM and B MN-major in shared memory.
+template <int D>
+__device__ __forceinline__ void issue_pv_half(uint32_t tmem_d, uint32_t tmem_a, uint64_t b_desc, int h,
+                                              uint32_t accumulate) {
+  constexpr uint32_t idesc = make_idesc_bf16(kTileRows, D, true);
+  const uint64_t b = b_desc + static_cast<uint64_t>(h) * ((64 * 128) >> 4);
+  umma_bf16_ts(tmem_d, tmem_a, b, idesc, accumulate);
+#pragma unroll
+  for (int kk = 1; kk < 4; ++kk) umma_bf16_ts(tmem_d, tmem_a + kk * 8, b + ((kk * 16 * 128) >> 4), idesc, 1u);
+}
+
+template <typename TOut, int N>
+__device__ __forceinline__ void store_zero_cols(TOut* row) {
+  float z[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) z[i] = 0.0f;
+#pragma unroll
+  for (int c = 0; c < N / 32; ++c) store_row32<TOut>(row + c * 32, z);
+}
+
 // ---------------------------------------------------------------------------------
 // 2. dQ
 // ---------------------------------------------------------------------------------
@@ -153,7 +198,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sKV = sDO + C::kTileBytes;  // NS slots: K_0, V_0, K_1, V_1, ...
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = &ctrl.abort;
-  if (threadIdx.x == 0) init_ctrl(ctrl, NS);
+  if (threadIdx.x == 0) init_ctrl(ctrl, NS, 2 * kTileRows);
   if (warp == 1) {
     tmem_alloc(&ctrl.tmem_base, kBwdTmemCols);
     tmem_relinquish_alloc_permit();
@@ -164,8 +209,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = ctrl.tmem_base;
   const int T = p.tokens_per_tile;
   const int G = p.group;
-  // TMEM: S [0,128) (dS as bf16 pairs overwrites [0,64)), dP [128,256), dQ [256,256+D)
-  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+  // TMEM: two S buffers [0,128) and [128,256) (block m uses buffer m & 1), dP
+  // [256,384), dQ [384,384+D). The dS of key half h (bf16 pairs) overwrites columns
+  // [64h, 64h+32) of its block's S buffer. With S double-buffered, the products of
+  // block m+1 run on the tensor core while the compute threads turn block m into dS;
+  // dP has one buffer, released as soon as the compute threads hold it in registers.
+  constexpr uint32_t kColS = 0, kColDP = 256, kColDQ = 384;
 
   if (warp == 0) {
     // The whole warp walks the work list; lane 0 issues the copies, and all lanes
@@ -233,58 +282,88 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
+      // Per block m: S(m+1) into the other S buffer, dP(m+1) once the compute threads
+      // hold dP(m), then dQ += dS(m) K(m) once dS(m) is in TMEM.
       const uint64_t q_desc = make_smem_desc_sw128(smem_addr(sQ), 16, 1024);
       const uint64_t do_desc = make_smem_desc_sw128(smem_addr(sDO), 16, 1024);
       const uint64_t kv_desc0 = make_smem_desc_sw128(smem_addr(sKV), 16, 1024);            // K-major (K, V)
       const uint64_t kmn_desc0 = make_smem_desc_sw128(smem_addr(sKV), kChunkBytes, 1024);  // K as MN-major B
-      auto slot_off = [](uint32_t sl) { return static_cast<uint64_t>(sl) * (C::kTileBytes >> 4); };
-      uint32_t q_it = 0, blk = 0, pc = 0;
+      auto slot_off = [](uint32_t seq) { return static_cast<uint64_t>(seq % NS) * (C::kTileBytes >> 4); };
+      uint32_t q_it = 0, n = 0;  // n: blocks of this CTA so far (global block counter)
       bool ok = true;
+      auto wait_kv = [&](uint32_t m) {
+        const uint32_t ks = 2 * m, vs = ks + 1;
+        bool r = wait_bar(&ctrl.r_full[ks % NS], (ks / NS) & 1, abort_flag, p.error_flag);
+        if (r) r = wait_bar(&ctrl.r_full[vs % NS], (vs / NS) & 1, abort_flag, p.error_flag);
+        if (r) tcgen05_fence_after();
+        return r;
+      };
+      auto issue_s = [&](uint32_t m) {  // complete before dP(m), which is issued after it
+        issue_qk<D>(tmem + kColS + 128 * (m & 1), q_desc, kv_desc0 + slot_off(2 * m));
+      };
+      auto issue_dp = [&](uint32_t m) {  // after the compute threads released dP(m - 1)
+        if (m > 0) {
+          if (!wait_bar(&ctrl.dp_consumed, (m - 1) & 1, abort_flag, p.error_flag)) return false;
+          tcgen05_fence_after();
+        }
+        issue_qk<D>(tmem + kColDP, do_desc, kv_desc0 + slot_off(2 * m + 1));
+        umma_commit(&ctrl.dp_full);
+        umma_commit(&ctrl.r_empty[(2 * m + 1) % NS]);  // V(m) read
+        return true;
+      };
       for (int round = 0; ok; ++round) {
         const int idx = item_index(round, blockIdx.x, gridDim.x);
         if (idx >= p.num_items) break;
         const WorkItem it = load_item(p.items, idx);
         if (it.nblk == 0) continue;
         ok = wait_bar(&ctrl.a_full, q_it & 1, abort_flag, p.error_flag);
+        if (ok) ok = wait_kv(n);
         if (!ok) break;
         ++q_it;
+        issue_s(n);
+        ok = issue_dp(n);
+        if (!ok) break;
+        if (it.nblk == 1) umma_commit(&ctrl.a_empty);  // Q, dO read
         for (int j = 0; j < it.nblk; ++j) {
-          const uint32_t kseq = 2 * (blk + j), vseq = kseq + 1;
-          ok = wait_bar(&ctrl.r_full[kseq % NS], (kseq / NS) & 1, abort_flag, p.error_flag);
-          if (ok) ok = wait_bar(&ctrl.r_full[vseq % NS], (vseq / NS) & 1, abort_flag, p.error_flag);
+          const uint32_t m = n + j;
+          if (j + 1 < it.nblk) {
+            ok = wait_kv(m + 1);
+            if (!ok) break;
+            issue_s(m + 1);
+            ok = issue_dp(m + 1);
+            if (!ok) break;
+            if (j + 2 == it.nblk) umma_commit(&ctrl.a_empty);
+          }
+          // dS(m) is in TMEM (both warpgroups; for the first block of an item they
+          // arrive only after reading out the previous item's dQ)
+          ok = wait_bar(&ctrl.p_full[m & 1], (m >> 1) & 1, abort_flag, p.error_flag);
           if (!ok) break;
           tcgen05_fence_after();
-          issue_qk<D>(tmem + kColS, q_desc, kv_desc0 + slot_off(kseq % NS));    // S = Q K^T
-          issue_qk<D>(tmem + kColDP, do_desc, kv_desc0 + slot_off(vseq % NS));  // dP = dO V^T
-          umma_commit(&ctrl.s_full);
-          umma_commit(&ctrl.r_empty[vseq % NS]);
-          if (j + 1 == it.nblk) umma_commit(&ctrl.a_empty);
-          ok = wait_bar(&ctrl.p_full, pc & 1, abort_flag, p.error_flag);
-          if (!ok) break;
-          ++pc;
-          tcgen05_fence_after();
-          issue_pv<D>(tmem + kColDQ, tmem + kColS, kmn_desc0 + slot_off(kseq % NS), j > 0);  // dQ += dS K
-          umma_commit(&ctrl.r_empty[kseq % NS]);
-          if (j + 1 == it.nblk) umma_commit(&ctrl.acc_full);
+          const uint32_t sb = tmem + kColS + 128 * (m & 1);
+          issue_pv_half<D>(tmem + kColDQ, sb, kmn_desc0 + slot_off(2 * m), 0, j > 0);
+          issue_pv_half<D>(tmem + kColDQ, sb + 64, kmn_desc0 + slot_off(2 * m), 1, 1u);
+          umma_commit(&ctrl.r_empty[(2 * m) % NS]);  // K(m) read
         }
-        blk += it.nblk;
+        if (!ok) break;
+        umma_commit(&ctrl.acc_full);
+        n += it.nblk;
       }
       umma_commit(&ctrl.mma_done);
       drain_bar(&ctrl.mma_done, 0, p.error_flag);
     }
     __syncwarp();
   } else {
+    const int wg = (warp - 2) >> 2;  // key half of each block this thread turns into dS
     const int lane_base = (warp & 3) * 32;
     const int row = lane_base + lane;
     const int hl = row / T;
     const int tok = row - hl * T;
-    const uint32_t s_addr = tmem_addr(tmem, lane_base, kColS);
-    const uint32_t dp_addr = tmem_addr(tmem, lane_base, kColDP);
-    const uint32_t dq_addr = tmem_addr(tmem, lane_base, kColDQ);
+    const uint32_t dp_addr = tmem_addr(tmem, lane_base, kColDP + 64 * wg);
+    const uint32_t dq_addr = tmem_addr(tmem, lane_base, kColDQ + (D / 2) * wg);
     const float c = p.scale_log2;
     const uint64_t c2 = f32x2(c, c);
     TOut* dq = reinterpret_cast<TOut*>(p.dq);
-    uint32_t sc = 0, ac = 0;
+    uint32_t n = 0, ac = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
       const int idx = item_index(round, blockIdx.x, gridDim.x);
@@ -293,53 +372,50 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const bool valid = tok < it.q_rows;
       const int64_t token = static_cast<int64_t>(it.q_row0) + tok;
       const int head = it.head_kv * G + hl;
-      TOut* qrow = dq + (token * p.num_heads_q + head) * D;
+      TOut* qrow = dq + (token * p.num_heads_q + head) * D + (D / 2) * wg;
       if (it.nblk == 0) {  // keyless segment: O = 0 does not depend on Q
-        if (valid) {
-          float z[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) z[i] = 0.0f;
-#pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch) store_row32<TOut>(qrow + ch * 32, z);
-        }
+        if (valid) store_zero_cols<TOut, D / 2>(qrow);
         continue;
       }
       const int64_t li = static_cast<int64_t>(head) * p.total_q + token;
       const float lse2 = valid ? p.lse[li] * kLog2e : 0.0f;
       const float drow = valid ? p.dvec[li] : 0.0f;
       const uint64_t neg_l2 = f32x2(-lse2, -lse2);
-      for (int j = 0; j < it.nblk; ++j) {
-        ok = __all_sync(0xffffffffu, wait_bar(&ctrl.s_full, sc & 1, abort_flag, p.error_flag));
+      for (int j = 0; j < it.nblk; ++j, ++n) {
+        // dP(n) complete implies S(n) complete (issued before it by the same thread)
+        ok = __all_sync(0xffffffffu, wait_bar(&ctrl.dp_full, n & 1, abort_flag, p.error_flag));
         if (!ok) break;
-        ++sc;
         tcgen05_fence_after();
-        const int rem = load_block(p.blocks, it.blk0 + j).valid;
-        if (rem < kBlockKeys) {  // keys past the used length: P = 0 (range uniform over the warp)
-          for (int col = rem; col < kBlockKeys; ++col) tmem_st1(s_addr + col, 0xff800000u);
-          tmem_wait_st();
+        const uint32_t s_addr = tmem_addr(tmem, lane_base, kColS + 128 * (n & 1) + 64 * wg);
+        uint32_t sraw[64], dpr[64];
+        tmem_ld64x2_sync(s_addr, sraw, dp_addr, dpr);
+        tcgen05_fence_before();
+        mbar_arrive(&ctrl.dp_consumed);  // the tensor core may overwrite dP now
+        // used keys of this half: only a segment's last block is partial (one prefix range)
+        const int rem = min(kBlockKeys, it.k_len - j * kBlockKeys) - 64 * wg;
+        if (rem < 64) {  // keys past the used length: P = 0 (uniform over the warp)
+#pragma unroll
+          for (int i = 0; i < 64; ++i) sraw[i] = i < rem ? sraw[i] : 0xff800000u;
         }
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t sraw[64], draw[64];
-          tmem_ld64_sync(s_addr + half * 64, sraw);
-          tmem_ld64_sync(dp_addr + half * 64, draw);
-          uint32_t pk[32];
+        for (int part = 0; part < 2; ++part) {
+          uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
+          for (int i = 0; i < 16; ++i) {
             float a, b;
-            f32x2_split(ffma2(f32x2(__uint_as_float(sraw[2 * i]), __uint_as_float(sraw[2 * i + 1])), c2, neg_l2),
+            f32x2_split(ffma2(f32x2(__uint_as_float(sraw[32 * part + 2 * i]), __uint_as_float(sraw[32 * part + 2 * i + 1])),
+                              c2, neg_l2),
                         a, b);
             a = ex2_approx(a);
             b = ex2_approx(b);
-            const float da = a * (__uint_as_float(draw[2 * i]) - drow);
-            const float db = b * (__uint_as_float(draw[2 * i + 1]) - drow);
-            pk[i] = pack_bf16x2(da, db);
+            pk[i] = pack_bf16x2(a * (__uint_as_float(dpr[32 * part + 2 * i]) - drow),
+                                b * (__uint_as_float(dpr[32 * part + 2 * i + 1]) - drow));
           }
-          tmem_st32(s_addr + half * 32, pk);  // dS pairs: columns [32 half, 32 half + 32)
+          tmem_st16(s_addr + part * 16, pk);  // dS pairs: columns [16 part, 16 part + 16) of the half
         }
         tmem_wait_st();
         tcgen05_fence_before();
-        mbar_arrive(&ctrl.p_full);
+        mbar_arrive(&ctrl.p_full[n & 1]);
       }
       if (!ok) break;
       ok = __all_sync(0xffffffffu, wait_bar(&ctrl.acc_full, ac & 1, abort_flag, p.error_flag));
@@ -347,7 +423,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ++ac;
       tcgen05_fence_after();
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
+      for (int ch = 0; ch < D / 64; ++ch) {
         uint32_t o[32];
         tmem_ld32_sync(dq_addr + ch * 32, o);
         float x[32];
@@ -356,7 +432,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (valid) store_row32<TOut>(qrow + ch * 32, x);
       }
     }
-    tmem_wait_st();
   }
   tcgen05_fence_before();
   __syncthreads();
@@ -383,7 +458,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sSlots = sV + C::kTileBytes;  // 2 slots of {Q tile, dO tile}
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = &ctrl.abort;
-  if (threadIdx.x == 0) init_ctrl(ctrl, 2);
+  if (threadIdx.x == 0) init_ctrl(ctrl, 2, kTileRows);
   if (warp == 1) {
     tmem_alloc(&ctrl.tmem_base, kBwdTmemCols);
     tmem_relinquish_alloc_permit();
@@ -394,8 +469,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = ctrl.tmem_base;
   const int T = p.tokens_per_tile;
   const int G = p.group;
-  // TMEM: S^T [0,128) (P^T pairs overwrite [0,64)), dP^T [128,256) (dS^T pairs overwrite
-  // [128,192)), dV [256,256+D), dK [384,384+D)
+  // TMEM: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [384,384+D). Column half h
+  // (Q-tile rows 64h .. 64h+63) of S^T / dP^T is [64h, +64) / [128+64h, +64); its P^T
+  // and dS^T (bf16 pairs) overwrite [64h, +32) and [128+64h, +32).
   constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
   auto n_tiles = [&](const KvUnit& u) { return (u.q_used + T - 1) / T; };
 
@@ -487,13 +563,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
+      // Per Q tile i: S^T / dP^T of half 0 and half 1, then dV, dK of half 0, the next
+      // tile's half-0 products, dV, dK of half 1, the next tile's half-1 products.
       const uint64_t k_desc = make_smem_desc_sw128(smem_addr(sK), 16, 1024);
       const uint64_t v_desc = make_smem_desc_sw128(smem_addr(sV), 16, 1024);
       const uint64_t slot_k0 = make_smem_desc_sw128(smem_addr(sSlots), 16, 1024);            // K-major
       const uint64_t slot_mn0 = make_smem_desc_sw128(smem_addr(sSlots), kChunkBytes, 1024);  // MN-major B
       constexpr uint64_t kTileUnits = C::kTileBytes >> 4;
-      uint32_t kv_it = 0, qi = 0, pc = 0;
+      uint32_t kv_it = 0, qi = 0;
+      uint32_t pc[2] = {0, 0};
       bool ok = true;
+      auto wait_tile = [&](uint32_t t) {
+        const bool r = wait_bar(&ctrl.r_full[t & 1], (t >> 1) & 1, abort_flag, p.error_flag);
+        if (r) tcgen05_fence_after();
+        return r;
+      };
+      auto products = [&](uint32_t t, int h) {  // S^T and dP^T of half h of tile t
+        const uint64_t qk = slot_k0 + (t & 1) * 2 * kTileUnits;
+        issue_qk_half<D>(tmem + kColS + 64 * h, k_desc, qk, h);
+        issue_qk_half<D>(tmem + kColDP + 64 * h, v_desc, qk + kTileUnits, h);
+        umma_commit(&ctrl.s_full[h]);
+      };
       for (int round = 0; ok; ++round) {
         const int idx = item_index(round, blockIdx.x, gridDim.x);
         if (idx >= p.num_kv_units) break;
@@ -501,29 +591,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int nqt = n_tiles(u);
         if (nqt == 0) continue;
         ok = wait_bar(&ctrl.a_full, kv_it & 1, abort_flag, p.error_flag);
+        if (ok) ok = wait_tile(qi);
         if (!ok) break;
         ++kv_it;
+        products(qi, 0);
+        products(qi, 1);
+        if (nqt == 1) umma_commit(&ctrl.a_empty);  // K, V read
         for (int i = 0; i < nqt; ++i) {
-          const uint32_t sl = qi & 1;
-          ok = wait_bar(&ctrl.r_full[sl], (qi >> 1) & 1, abort_flag, p.error_flag);
+          const uint32_t t = qi + i;
+          const bool more = i + 1 < nqt;
+          const uint64_t qmn = slot_mn0 + (t & 1) * 2 * kTileUnits, domn = qmn + kTileUnits;
+          ok = wait_bar(&ctrl.p_full[0], pc[0] & 1, abort_flag, p.error_flag);
+          // the first products overwrite dV / dK: both warpgroups must have finished
+          // reading the previous unit's accumulators (they arrive after their epilogue)
+          if (ok && i == 0) ok = wait_bar(&ctrl.p_full[1], pc[1] & 1, abort_flag, p.error_flag);
           if (!ok) break;
+          ++pc[0];
           tcgen05_fence_after();
-          const uint64_t qk = slot_k0 + sl * 2 * kTileUnits, dok = qk + kTileUnits;
-          const uint64_t qmn = slot_mn0 + sl * 2 * kTileUnits, domn = qmn + kTileUnits;
-          issue_qk<D>(tmem + kColS, k_desc, qk);    // S^T = K Q^T
-          issue_qk<D>(tmem + kColDP, v_desc, dok);  // dP^T = V dO^T
-          umma_commit(&ctrl.s_full);
-          ok = wait_bar(&ctrl.p_full, pc & 1, abort_flag, p.error_flag);
+          issue_pv_half<D>(tmem + kColDV, tmem + kColS, domn, 0, i > 0);   // dV += P^T dO
+          issue_pv_half<D>(tmem + kColDK, tmem + kColDP, qmn, 0, i > 0);   // dK += dS^T Q
+          if (more) {
+            ok = wait_tile(t + 1);
+            if (!ok) break;
+            products(t + 1, 0);
+          }
+          if (i > 0) ok = wait_bar(&ctrl.p_full[1], pc[1] & 1, abort_flag, p.error_flag);
           if (!ok) break;
-          ++pc;
+          ++pc[1];
           tcgen05_fence_after();
-          issue_pv<D>(tmem + kColDV, tmem + kColS, domn, i > 0);  // dV += P^T dO
-          issue_pv<D>(tmem + kColDK, tmem + kColDP, qmn, i > 0);  // dK += dS^T Q
-          umma_commit(&ctrl.r_empty[sl]);
-          ++qi;
+          issue_pv_half<D>(tmem + kColDV, tmem + kColS + 64, domn, 1, 1u);
+          issue_pv_half<D>(tmem + kColDK, tmem + kColDP + 64, qmn, 1, 1u);
+          umma_commit(&ctrl.r_empty[t & 1]);
+          if (more) {
+            products(t + 1, 1);
+            if (i + 2 == nqt) umma_commit(&ctrl.a_empty);
+          }
         }
         if (!ok) break;
-        umma_commit(&ctrl.a_empty);
+        qi += nqt;
         umma_commit(&ctrl.acc_full);
       }
       umma_commit(&ctrl.mma_done);
@@ -531,12 +636,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     __syncwarp();
   } else {
+    const int wg = (warp - 2) >> 2;        // column half: Q-tile rows 64 wg .. 64 wg + 63
+    const int tid = threadIdx.x - 64 - 128 * wg;  // 0 .. 127 within the warpgroup
     const int lane_base = (warp & 3) * 32;
     const int key = lane_base + lane;  // S^T row = TMEM lane = key within the block
-    const int rhl = key / T;           // as a loader: the Q-tile row this thread fetches
-    const int rtok = key - rhl * T;
-    const uint32_t s_addr = tmem_addr(tmem, lane_base, kColS);
-    const uint32_t dp_addr = tmem_addr(tmem, lane_base, kColDP);
+    const int lrow = 64 * wg + (tid & 63);  // as a loader (tid < 64): the Q-tile row it fetches
+    const int rhl = lrow / T;
+    const int rtok = lrow - rhl * T;
+    const uint32_t s_addr = tmem_addr(tmem, lane_base, kColS + 64 * wg);
+    const uint32_t dp_addr = tmem_addr(tmem, lane_base, kColDP + 64 * wg);
     const float c = p.scale_log2;
     TOut* dk = reinterpret_cast<TOut*>(p.dk);
     TOut* dv = reinterpret_cast<TOut*>(p.dv);
@@ -549,83 +657,86 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int nqt = n_tiles(u);
       const bool key_valid = key < u.keys;
       const int64_t krow = static_cast<int64_t>(u.key_row0) + key;
-      TOut* dkrow = dk + (krow * p.num_heads_kv + u.head_kv) * D;
-      TOut* dvrow = dv + (krow * p.num_heads_kv + u.head_kv) * D;
+      TOut* dkrow = dk + (krow * p.num_heads_kv + u.head_kv) * D + (D / 2) * wg;
+      TOut* dvrow = dv + (krow * p.num_heads_kv + u.head_kv) * D + (D / 2) * wg;
       if (nqt == 0) {  // no query attends these keys
         if (key_valid) {
-          float z[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) z[i] = 0.0f;
-#pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch) {
-            store_row32<TOut>(dkrow + ch * 32, z);
-            store_row32<TOut>(dvrow + ch * 32, z);
-          }
+          store_zero_cols<TOut, D / 2>(dkrow);
+          store_zero_cols<TOut, D / 2>(dvrow);
         }
         continue;
       }
+      // log2-LSE and D of this half's Q-tile rows (loader threads tid < 64), fetched one
+      // tile ahead; +inf LSE (P = 0) and D = 0 past the used rows
+      const int64_t lrow0 = static_cast<int64_t>(u.head_kv * G + rhl) * p.total_q + u.q_row0 + rtok;
+      auto fetch = [&](int i, float& xl_v, float& xd_v) {
+        const bool rvalid = i * T + rtok < u.q_used;
+        xl_v = rvalid ? __ldg(p.lse + lrow0 + i * T) * kLog2e : CUDART_INF_F;
+        xd_v = rvalid ? __ldg(p.dvec + lrow0 + i * T) : 0.0f;
+      };
+      float nxl = 0.0f, nxd = 0.0f;
+      if (tid < 64) fetch(0, nxl, nxd);
       for (int i = 0; i < nqt; ++i) {
         const int par = tiles & 1;
         ++tiles;
-        // this thread fetches the log2-LSE and D of Q-tile row `key`; +inf LSE (P = 0)
-        // for rows past the used queries
-        const bool rvalid = i * T + rtok < u.q_used;
-        const int64_t li = static_cast<int64_t>(u.head_kv * G + rhl) * p.total_q + u.q_row0 + i * T + rtok;
-        ctrl.xl[par][key] = rvalid ? p.lse[li] * kLog2e : CUDART_INF_F;
-        ctrl.xd[par][key] = rvalid ? p.dvec[li] : 0.0f;
-        bool fine = __all_sync(0xffffffffu, wait_bar(&ctrl.s_full, sc & 1, abort_flag, p.error_flag));
+        if (tid < 64) {
+          ctrl.xl[par][lrow] = nxl;
+          ctrl.xd[par][lrow] = nxd;
+          if (i + 1 < nqt) fetch(i + 1, nxl, nxd);
+        }
+        const bool fine = __all_sync(0xffffffffu, wait_bar(&ctrl.s_full[wg], sc & 1, abort_flag, p.error_flag));
         ++sc;
-        if (named_barrier_or(1, 128, !fine)) {
+        if (named_barrier_or(1 + wg, 128, !fine)) {
           ok = false;
           break;
         }
         tcgen05_fence_after();
+        const float* xl = &ctrl.xl[par][64 * wg];
+        const float* xd = &ctrl.xd[par][64 * wg];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t sraw[64], draw[64];
-          tmem_ld64_sync(s_addr + half * 64, sraw);
-          tmem_ld64_sync(dp_addr + half * 64, draw);
-          uint32_t pp[32], pd[32];
+        for (int part = 0; part < 2; ++part) {
+          uint32_t sraw[32], draw[32];
+          tmem_ld32x2_sync(s_addr + part * 32, sraw, dp_addr + part * 32, draw);
+          uint32_t pp[16], pd[16];
 #pragma unroll
-          for (int i2 = 0; i2 < 32; ++i2) {
-            const int col = half * 64 + 2 * i2;
-            float a = ex2_approx(fmaf(__uint_as_float(sraw[2 * i2]), c, -ctrl.xl[par][col]));
-            float b = ex2_approx(fmaf(__uint_as_float(sraw[2 * i2 + 1]), c, -ctrl.xl[par][col + 1]));
-            float da = a * (__uint_as_float(draw[2 * i2]) - ctrl.xd[par][col]);
-            float db = b * (__uint_as_float(draw[2 * i2 + 1]) - ctrl.xd[par][col + 1]);
+          for (int i2 = 0; i2 < 16; ++i2) {
+            const int col = part * 32 + 2 * i2;
+            float a = ex2_approx(fmaf(__uint_as_float(sraw[2 * i2]), c, -xl[col]));
+            float b = ex2_approx(fmaf(__uint_as_float(sraw[2 * i2 + 1]), c, -xl[col + 1]));
+            float da = a * (__uint_as_float(draw[2 * i2]) - xd[col]);
+            float db = b * (__uint_as_float(draw[2 * i2 + 1]) - xd[col + 1]);
             if (!key_valid) a = b = da = db = 0.0f;
             pp[i2] = pack_bf16x2(a, b);
             pd[i2] = pack_bf16x2(da, db);
           }
-          tmem_st32(s_addr + half * 32, pp);   // P^T pairs
-          tmem_st32(dp_addr + half * 32, pd);  // dS^T pairs
+          tmem_st16(s_addr + part * 16, pp);   // P^T pairs
+          tmem_st16(dp_addr + part * 16, pd);  // dS^T pairs
         }
         tmem_wait_st();
         tcgen05_fence_before();
-        mbar_arrive(&ctrl.p_full);
+        mbar_arrive(&ctrl.p_full[wg]);
       }
       if (!ok) break;
-      {  // all four warps take the same decision (the next unit's barrier needs all 128)
+      {  // the warpgroup takes one decision (its next barrier needs all 128 threads)
         const bool fine = __all_sync(0xffffffffu, wait_bar(&ctrl.acc_full, ac & 1, abort_flag, p.error_flag));
-        if (named_barrier_or(1, 128, !fine)) break;
+        if (named_barrier_or(1 + wg, 128, !fine)) break;
       }
       ++ac;
       tcgen05_fence_after();
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
+      for (int ch = 0; ch < D / 64; ++ch) {
         uint32_t o[32];
         float x[32];
-        tmem_ld32_sync(tmem_addr(tmem, lane_base, kColDV + ch * 32), o);
+        tmem_ld32_sync(tmem_addr(tmem, lane_base, kColDV + (D / 2) * wg + ch * 32), o);
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(o[i]);
         if (key_valid) store_row32<TOut>(dvrow + ch * 32, x);
-        tmem_ld32_sync(tmem_addr(tmem, lane_base, kColDK + ch * 32), o);
+        tmem_ld32_sync(tmem_addr(tmem, lane_base, kColDK + (D / 2) * wg + ch * 32), o);
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(o[i]) * p.scale;
         if (key_valid) store_row32<TOut>(dkrow + ch * 32, x);
       }
     }
-    tmem_wait_st();
   }
   tcgen05_fence_before();
   __syncthreads();

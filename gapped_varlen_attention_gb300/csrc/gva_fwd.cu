@@ -285,12 +285,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float m_used = -CUDART_INF_F;
       float l = 0.0f;
+      // used keys of each block (>= 1), fetched one block ahead so the load's latency
+      // hides behind the wait for the scores
+      int rem_next = load_block(p.blocks, it.blk0).valid;
       for (int j = 0; j < nblk; ++j) {
+        const int rem = rem_next;
+        if (j + 1 < nblk) rem_next = load_block(p.blocks, it.blk0 + j + 1).valid;
         ok = __all_sync(0xffffffffu, wait_bar(&ctrl.s_full[t], sc & 1, abort_flag, p.error_flag));
         if (!ok) break;
         ++sc;
         tcgen05_fence_after();
-        const int rem = load_block(p.blocks, it.blk0 + j).valid;  // used keys in this block (>= 1)
         if (rem < kBlockKeys) {
           // Last, partial block: keys past the used length (gap, padding or another
           // segment, possibly NaN) leave the softmax. Their score columns are set to

@@ -158,6 +158,39 @@ __device__ __forceinline__ void tmem_ld128_sync(uint32_t taddr, uint32_t (&r)[12
       : "memory");
 }
 
+#define GVA_RA8(a, i) "=r"(a[i + 0]), "=r"(a[i + 1]), "=r"(a[i + 2]), "=r"(a[i + 3]), "=r"(a[i + 4]), \
+                      "=r"(a[i + 5]), "=r"(a[i + 6]), "=r"(a[i + 7])
+
+// Two loads of 32 columns each (two column ranges of the thread's lane) and one wait:
+// both latencies overlap.
+__device__ __forceinline__ void tmem_ld32x2_sync(uint32_t taddr0, uint32_t (&r0)[32], uint32_t taddr1,
+                                                 uint32_t (&r1)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : GVA_RA8(r0, 0), GVA_RA8(r0, 8), GVA_RA8(r0, 16), GVA_RA8(r0, 24),
+        GVA_RA8(r1, 0), GVA_RA8(r1, 8), GVA_RA8(r1, 16), GVA_RA8(r1, 24)
+      : "r"(taddr0), "r"(taddr1)
+      : "memory");
+}
+
+// Two loads of 64 columns each and one wait.
+__device__ __forceinline__ void tmem_ld64x2_sync(uint32_t taddr0, uint32_t (&r0)[64], uint32_t taddr1,
+                                                 uint32_t (&r1)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%128];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%129];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : GVA_RA8(r0, 0), GVA_RA8(r0, 8), GVA_RA8(r0, 16), GVA_RA8(r0, 24), GVA_RA8(r0, 32), GVA_RA8(r0, 40),
+        GVA_RA8(r0, 48), GVA_RA8(r0, 56), GVA_RA8(r1, 0), GVA_RA8(r1, 8), GVA_RA8(r1, 16), GVA_RA8(r1, 24),
+        GVA_RA8(r1, 32), GVA_RA8(r1, 40), GVA_RA8(r1, 48), GVA_RA8(r1, 56)
+      : "r"(taddr0), "r"(taddr1)
+      : "memory");
+}
+
+#undef GVA_RA8
+
 // Same for 16 columns.
 __device__ __forceinline__ void tmem_ld16_sync(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
