@@ -42,8 +42,10 @@ template <int D>
 struct BCfg {
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = kTileRows * D * 2;  // a Q, dO, K or V tile of 128 rows
-  static constexpr int kSlots = 4;                      // dQ kernel K/V ring
-  static constexpr int kSmemDq = 2 * kTileBytes + kSlots * kTileBytes + 1024;
+  // dQ kernel: K lives from S(m) to dQ(m), which comes two products later, V only
+  // until dP(m); three K slots and two V slots keep the next block's loads ahead.
+  static constexpr int kKSlots = 3, kVSlots = 2;
+  static constexpr int kSmemDq = (2 + kKSlots + kVSlots) * kTileBytes + 1024;
   static constexpr int kSmemDkv = 2 * kTileBytes + 2 * 2 * kTileBytes + 1024;
   static_assert(kSmemDq <= 227 * 1024 && kSmemDkv <= 227 * 1024, "shared memory budget");
 };
@@ -70,33 +72,62 @@ __device__ __forceinline__ KvUnit load_unit(const KvUnit* units, int idx) {
   return u;
 }
 
+// dK / dV kernel control block.
 struct BwdCtrl {
-  float xl[2][kTileRows];  // dK / dV kernel: per-column log2-LSE of the current Q tile
-  float xd[2][kTileRows];  //                 per-column D
-  uint64_t a_full, a_empty;            // dQ: Q + dO tiles;   dK/dV: K + V blocks
-  uint64_t r_full[4], r_empty[4];      // dQ: K/V ring;       dK/dV: Q/dO slots (2)
+  float xl[2][kTileRows];  // per-column log2-LSE of the current Q tile (two tiles in flight)
+  float xd[2][kTileRows];  // per-column D
+  uint64_t a_full, a_empty;            // K + V blocks
+  uint64_t r_full[2], r_empty[2];      // Q / dO slots
   uint64_t zero_bar;                   // partial tiles: the producer's own copy wait
-  uint64_t s_full[2], p_full[2];       // dQ: per S buffer;   dK/dV: per column half
-  uint64_t dp_full, dp_consumed;       // dQ: dP ready / read into registers
+  uint64_t s_full[2], p_full[2];       // per column half: products ready / P, dS ready
   uint64_t acc_full, mma_done;
   uint32_t tmem_base;
   int abort;
 };
 
-__device__ __forceinline__ void init_ctrl(BwdCtrl& c, int ring, uint32_t p_count) {
+// dQ kernel control block (no per-column staging; K and V in separate rings).
+struct DqCtrl {
+  uint64_t a_full, a_empty;  // Q + dO tiles
+  uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];
+  uint64_t zero_bar;         // partial blocks: the producer's own copy wait
+  uint64_t p_full[2];        // per S buffer: dS in TMEM (256 compute threads)
+  uint64_t dp_full, dp_consumed;
+  uint64_t acc_full, mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ void init_dq_ctrl(DqCtrl& c) {
   mbar_init(&c.a_full, 1);
   mbar_init(&c.a_empty, 1);
-  for (int i = 0; i < ring; ++i) {
-    mbar_init(&c.r_full[i], 1);
-    mbar_init(&c.r_empty[i], 1);
+  for (int i = 0; i < 3; ++i) {
+    mbar_init(&c.k_full[i], 1);
+    mbar_init(&c.k_empty[i], 1);
+  }
+  for (int i = 0; i < 2; ++i) {
+    mbar_init(&c.v_full[i], 1);
+    mbar_init(&c.v_empty[i], 1);
+    mbar_init(&c.p_full[i], 2 * kTileRows);
   }
   mbar_init(&c.zero_bar, 1);
-  for (int h = 0; h < 2; ++h) {
-    mbar_init(&c.s_full[h], 1);
-    mbar_init(&c.p_full[h], p_count);
-  }
   mbar_init(&c.dp_full, 1);
   mbar_init(&c.dp_consumed, 2 * kTileRows);
+  mbar_init(&c.acc_full, 1);
+  mbar_init(&c.mma_done, 1);
+  c.abort = 0;
+  fence_barrier_init();
+}
+
+__device__ __forceinline__ void init_ctrl(BwdCtrl& c) {
+  mbar_init(&c.a_full, 1);
+  mbar_init(&c.a_empty, 1);
+  for (int i = 0; i < 2; ++i) {
+    mbar_init(&c.r_full[i], 1);
+    mbar_init(&c.r_empty[i], 1);
+    mbar_init(&c.s_full[i], 1);
+    mbar_init(&c.p_full[i], kTileRows);
+  }
+  mbar_init(&c.zero_bar, 1);
   mbar_init(&c.acc_full, 1);
   mbar_init(&c.mma_done, 1);
   c.abort = 0;
@@ -189,16 +220,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                       const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                       const BwdParams p) {
   using C = BCfg<D>;
-  constexpr uint32_t NS = C::kSlots;
+  constexpr uint32_t NK = C::kKSlots, NV = C::kVSlots;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ BwdCtrl ctrl;
+  __shared__ DqCtrl ctrl;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sDO = sQ + C::kTileBytes;
-  uint8_t* sKV = sDO + C::kTileBytes;  // NS slots: K_0, V_0, K_1, V_1, ...
+  uint8_t* sK = sDO + C::kTileBytes;      // NK slots; block m in slot m % NK
+  uint8_t* sV = sK + NK * C::kTileBytes;  // NV slots; block m in slot m % NV
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = &ctrl.abort;
-  if (threadIdx.x == 0) init_ctrl(ctrl, NS, 2 * kTileRows);
+  if (threadIdx.x == 0) init_dq_ctrl(ctrl);
   if (warp == 1) {
     tmem_alloc(&ctrl.tmem_base, kBwdTmemCols);
     tmem_relinquish_alloc_permit();
@@ -227,7 +259,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_desc(&map_v);
       tma_prefetch_desc(&map_do);
     }
-    uint32_t q_it = 0, ld = 0, zph = 0;
+    uint32_t q_it = 0, m = 0, zph = 0;  // m: blocks of this CTA so far
     bool ok = true;
     for (int round = 0; ok; ++round) {
       const int idx = item_index(round, blockIdx.x, gridDim.x);
@@ -245,16 +277,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       ++q_it;
-      for (int j = 0; j < it.nblk && ok; ++j) {
+      for (int j = 0; j < it.nblk && ok; ++j, ++m) {
         const KeyBlock blk = load_block(p.blocks, it.blk0 + j);
         for (int kv = 0; kv < 2; ++kv) {
-          const uint32_t sl = ld % NS;
-          if (leader) ok = wait_bar(&ctrl.r_empty[sl], ((ld / NS) & 1) ^ 1, abort_flag, p.error_flag);
+          const uint32_t nslots = kv == 0 ? NK : NV;
+          const uint32_t sl = m % nslots;
+          uint64_t* empty = kv == 0 ? &ctrl.k_empty[sl] : &ctrl.v_empty[sl];
+          uint64_t* full = kv == 0 ? &ctrl.k_full[sl] : &ctrl.v_full[sl];
+          if (leader) ok = wait_bar(empty, ((m / nslots) & 1) ^ 1, abort_flag, p.error_flag);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
-          uint8_t* dst = sKV + sl * C::kTileBytes;
+          uint8_t* dst = (kv == 0 ? sK : sV) + sl * C::kTileBytes;
           const CUtensorMap* map = kv == 0 ? &map_k : &map_v;
-          uint64_t* bar = blk.valid == kBlockKeys ? &ctrl.r_full[sl] : &ctrl.zero_bar;
+          uint64_t* bar = blk.valid == kBlockKeys ? full : &ctrl.zero_bar;
           if (leader) {
             mbar_arrive_expect_tx(bar, C::kTileBytes);
 #pragma unroll
@@ -269,15 +304,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int r = blk.valid + lane; r < kBlockKeys; r += 32) zero_tile_row<D>(dst, r);
             fence_proxy_async_smem();
             __syncwarp();
-            if (leader) mbar_arrive(&ctrl.r_full[sl]);
+            if (leader) mbar_arrive(full);
           }
-          ++ld;
         }
       }
     }
     if (leader) {
+      // after an abort the drains below may wait on a load that was never issued;
+      // each wait is bounded and the error is already recorded
       if (q_it > 0) drain_bar(&ctrl.a_full, (q_it - 1) & 1, p.error_flag);
-      for (uint32_t i = (ld > NS ? ld - NS : 0); i < ld; ++i) drain_bar(&ctrl.r_full[i % NS], (i / NS) & 1, p.error_flag);
+      for (uint32_t i = (m > NK ? m - NK : 0); i < m; ++i) drain_bar(&ctrl.k_full[i % NK], (i / NK) & 1, p.error_flag);
+      for (uint32_t i = (m > NV ? m - NV : 0); i < m; ++i) drain_bar(&ctrl.v_full[i % NV], (i / NV) & 1, p.error_flag);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -286,29 +323,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // hold dP(m), then dQ += dS(m) K(m) once dS(m) is in TMEM.
       const uint64_t q_desc = make_smem_desc_sw128(smem_addr(sQ), 16, 1024);
       const uint64_t do_desc = make_smem_desc_sw128(smem_addr(sDO), 16, 1024);
-      const uint64_t kv_desc0 = make_smem_desc_sw128(smem_addr(sKV), 16, 1024);            // K-major (K, V)
-      const uint64_t kmn_desc0 = make_smem_desc_sw128(smem_addr(sKV), kChunkBytes, 1024);  // K as MN-major B
-      auto slot_off = [](uint32_t seq) { return static_cast<uint64_t>(seq % NS) * (C::kTileBytes >> 4); };
+      const uint64_t k_desc0 = make_smem_desc_sw128(smem_addr(sK), 16, 1024);             // K-major
+      const uint64_t v_desc0 = make_smem_desc_sw128(smem_addr(sV), 16, 1024);             // K-major
+      const uint64_t kmn_desc0 = make_smem_desc_sw128(smem_addr(sK), kChunkBytes, 1024);  // K as MN-major B
+      constexpr uint64_t kTileUnits = C::kTileBytes >> 4;
       uint32_t q_it = 0, n = 0;  // n: blocks of this CTA so far (global block counter)
       bool ok = true;
       auto wait_kv = [&](uint32_t m) {
-        const uint32_t ks = 2 * m, vs = ks + 1;
-        bool r = wait_bar(&ctrl.r_full[ks % NS], (ks / NS) & 1, abort_flag, p.error_flag);
-        if (r) r = wait_bar(&ctrl.r_full[vs % NS], (vs / NS) & 1, abort_flag, p.error_flag);
+        bool r = wait_bar(&ctrl.k_full[m % NK], (m / NK) & 1, abort_flag, p.error_flag);
+        if (r) r = wait_bar(&ctrl.v_full[m % NV], (m / NV) & 1, abort_flag, p.error_flag);
         if (r) tcgen05_fence_after();
         return r;
       };
       auto issue_s = [&](uint32_t m) {  // complete before dP(m), which is issued after it
-        issue_qk<D>(tmem + kColS + 128 * (m & 1), q_desc, kv_desc0 + slot_off(2 * m));
+        issue_qk<D>(tmem + kColS + 128 * (m & 1), q_desc, k_desc0 + (m % NK) * kTileUnits);
       };
       auto issue_dp = [&](uint32_t m) {  // after the compute threads released dP(m - 1)
         if (m > 0) {
           if (!wait_bar(&ctrl.dp_consumed, (m - 1) & 1, abort_flag, p.error_flag)) return false;
           tcgen05_fence_after();
         }
-        issue_qk<D>(tmem + kColDP, do_desc, kv_desc0 + slot_off(2 * m + 1));
+        issue_qk<D>(tmem + kColDP, do_desc, v_desc0 + (m % NV) * kTileUnits);
         umma_commit(&ctrl.dp_full);
-        umma_commit(&ctrl.r_empty[(2 * m + 1) % NS]);  // V(m) read
+        umma_commit(&ctrl.v_empty[m % NV]);  // V(m) read
         return true;
       };
       for (int round = 0; ok; ++round) {
@@ -340,9 +377,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!ok) break;
           tcgen05_fence_after();
           const uint32_t sb = tmem + kColS + 128 * (m & 1);
-          issue_pv_half<D>(tmem + kColDQ, sb, kmn_desc0 + slot_off(2 * m), 0, j > 0);
-          issue_pv_half<D>(tmem + kColDQ, sb + 64, kmn_desc0 + slot_off(2 * m), 1, 1u);
-          umma_commit(&ctrl.r_empty[(2 * m) % NS]);  // K(m) read
+          issue_pv_half<D>(tmem + kColDQ, sb, kmn_desc0 + (m % NK) * kTileUnits, 0, j > 0);
+          issue_pv_half<D>(tmem + kColDQ, sb + 64, kmn_desc0 + (m % NK) * kTileUnits, 1, 1u);
+          umma_commit(&ctrl.k_empty[m % NK]);  // K(m) read
         }
         if (!ok) break;
         umma_commit(&ctrl.acc_full);
@@ -458,7 +495,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sSlots = sV + C::kTileBytes;  // 2 slots of {Q tile, dO tile}
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = &ctrl.abort;
-  if (threadIdx.x == 0) init_ctrl(ctrl, 2, kTileRows);
+  if (threadIdx.x == 0) init_ctrl(ctrl);
   if (warp == 1) {
     tmem_alloc(&ctrl.tmem_base, kBwdTmemCols);
     tmem_relinquish_alloc_permit();
@@ -639,12 +676,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int wg = (warp - 2) >> 2;        // column half: Q-tile rows 64 wg .. 64 wg + 63
     const int tid = threadIdx.x - 64 - 128 * wg;  // 0 .. 127 within the warpgroup
     const int lane_base = (warp & 3) * 32;
-    const int key = lane_base + lane;  // S^T row = TMEM lane = key within the block
+    const int key = lane_base + lane;  // epilogue: S^T row = TMEM lane = key within the block
+    const int g = lane >> 2, c4 = lane & 3;  // 16-lane shapes: lane offset and column pair of this thread
     const int lrow = 64 * wg + (tid & 63);  // as a loader (tid < 64): the Q-tile row it fetches
     const int rhl = lrow / T;
     const int rtok = lrow - rhl * T;
-    const uint32_t s_addr = tmem_addr(tmem, lane_base, kColS + 64 * wg);
-    const uint32_t dp_addr = tmem_addr(tmem, lane_base, kColDP + 64 * wg);
     const float c = p.scale_log2;
     TOut* dk = reinterpret_cast<TOut*>(p.dk);
     TOut* dv = reinterpret_cast<TOut*>(p.dv);
@@ -691,26 +727,47 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           break;
         }
         tcgen05_fence_after();
+        // 16-lane TMEM shapes: each thread handles 4 keys (lanes) x 8 columns per part,
+        // so it needs the LSE / D of only 8 columns (two per 8-column group).
         const float* xl = &ctrl.xl[par][64 * wg];
         const float* xd = &ctrl.xd[par][64 * wg];
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
-          uint32_t sraw[32], draw[32];
-          tmem_ld32x2_sync(s_addr + part * 32, sraw, dp_addr + part * 32, draw);
-          uint32_t pp[16], pd[16];
+          float2 l2[4], d2[4];
 #pragma unroll
-          for (int i2 = 0; i2 < 16; ++i2) {
-            const int col = part * 32 + 2 * i2;
-            float a = ex2_approx(fmaf(__uint_as_float(sraw[2 * i2]), c, -xl[col]));
-            float b = ex2_approx(fmaf(__uint_as_float(sraw[2 * i2 + 1]), c, -xl[col + 1]));
-            float da = a * (__uint_as_float(draw[2 * i2]) - xd[col]);
-            float db = b * (__uint_as_float(draw[2 * i2 + 1]) - xd[col + 1]);
-            if (!key_valid) a = b = da = db = 0.0f;
-            pp[i2] = pack_bf16x2(a, b);
-            pd[i2] = pack_bf16x2(da, db);
+          for (int k = 0; k < 4; ++k) {
+            l2[k] = *reinterpret_cast<const float2*>(xl + 32 * part + 8 * k + 2 * c4);
+            d2[k] = *reinterpret_cast<const float2*>(xd + 32 * part + 8 * k + 2 * c4);
           }
-          tmem_st16(s_addr + part * 16, pp);   // P^T pairs
-          tmem_st16(dp_addr + part * 16, pd);  // dS^T pairs
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int lane0 = lane_base + 16 * h;
+            uint32_t sr[16], dr[16];
+            tmem_ld16x256b_x4_pair_sync(tmem_addr(tmem, lane0, kColS + 64 * wg + 32 * part), sr,
+                                        tmem_addr(tmem, lane0, kColDP + 64 * wg + 32 * part), dr);
+            const bool va = lane0 + g < u.keys;      // key of registers 4k, 4k+1
+            const bool vb = lane0 + g + 8 < u.keys;  // key of registers 4k+2, 4k+3
+            uint32_t pp[8], pd[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              float p0 = ex2_approx(fmaf(__uint_as_float(sr[4 * k + 0]), c, -l2[k].x));
+              float p1 = ex2_approx(fmaf(__uint_as_float(sr[4 * k + 1]), c, -l2[k].y));
+              float p2 = ex2_approx(fmaf(__uint_as_float(sr[4 * k + 2]), c, -l2[k].x));
+              float p3 = ex2_approx(fmaf(__uint_as_float(sr[4 * k + 3]), c, -l2[k].y));
+              float s0 = p0 * (__uint_as_float(dr[4 * k + 0]) - d2[k].x);
+              float s1 = p1 * (__uint_as_float(dr[4 * k + 1]) - d2[k].y);
+              float s2 = p2 * (__uint_as_float(dr[4 * k + 2]) - d2[k].x);
+              float s3 = p3 * (__uint_as_float(dr[4 * k + 3]) - d2[k].y);
+              if (!va) p0 = p1 = s0 = s1 = 0.0f;
+              if (!vb) p2 = p3 = s2 = s3 = 0.0f;
+              pp[2 * k] = pack_bf16x2(p0, p1);
+              pp[2 * k + 1] = pack_bf16x2(p2, p3);
+              pd[2 * k] = pack_bf16x2(s0, s1);
+              pd[2 * k + 1] = pack_bf16x2(s2, s3);
+            }
+            tmem_st16x128b_x4(tmem_addr(tmem, lane0, kColS + 64 * wg + 16 * part), pp);   // P^T pairs
+            tmem_st16x128b_x4(tmem_addr(tmem, lane0, kColDP + 64 * wg + 16 * part), pd);  // dS^T pairs
+          }
         }
         tmem_wait_st();
         tcgen05_fence_before();

@@ -191,6 +191,34 @@ __device__ __forceinline__ void tmem_ld64x2_sync(uint32_t taddr0, uint32_t (&r0)
 
 #undef GVA_RA8
 
+// 16-lane shapes. For a warp whose address names lane L and column C:
+//   .16x256b.x4 load: thread t gets, for repeat k = 0..3, registers 4k..4k+3 =
+//     (lane L + t/4, columns C + 8k + 2(t%4) and +1), then (lane L + 8 + t/4, same columns);
+//   .16x128b.x4 store: thread t writes, for repeat k, registers 2k, 2k+1 to
+//     (lane L + t/4, column C + 4k + t%4) and (lane L + 8 + t/4, same column).
+// So a thread that packs its two adjacent 32-bit values of a loaded pair into one
+// register stores them exactly where a 2:1 packed copy of the loaded columns belongs.
+// Two such loads (16 registers each) and one wait.
+__device__ __forceinline__ void tmem_ld16x256b_x4_pair_sync(uint32_t taddr0, uint32_t (&a)[16], uint32_t taddr1,
+                                                            uint32_t (&b)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
+        "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]),
+        "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]),
+        "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15])
+      : "r"(taddr0), "r"(taddr1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16x128b_x4(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.16x128b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 // Same for 16 columns.
 __device__ __forceinline__ void tmem_ld16_sync(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
