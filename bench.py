@@ -37,8 +37,12 @@ import torch  # noqa: E402
 
 METRIC = "gapped-varlen attn fwd TFLOP/s (used rows) & % of GB300 BF16 peak; ms/launch"
 UNIT = "TFLOP/s"
-FWD_SOURCE = os.path.join(ROOT, "gapped_varlen_attention_gb300", "csrc", "gva_fwd.cu")
-TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "gva_fwd_kernel_long_replay.md")
+CSRC = os.path.join(ROOT, "gapped_varlen_attention_gb300", "csrc")
+# workload -> (ncu summary holding its DRAM bytes per launch, kernel source it was taken on)
+TRAFFIC_SUMMARIES = {
+    "long_replay": (os.path.join(ROOT, "profiles", "gva_fwd_kernel_long_replay.md"), os.path.join(CSRC, "gva_fwd.cu")),
+    "long_replay_bwd": (os.path.join(ROOT, "profiles", "gva_backward_long_replay.md"), os.path.join(CSRC, "gva_bwd.cu")),
+}
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
 
@@ -207,20 +211,23 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def fwd_source_hash():
-    with open(FWD_SOURCE, "rb") as f:
+def source_hash(path: str) -> str:
+    with open(path, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current forward kernel source; else None."""
-    if workload != "long_replay" or not os.path.exists(TRAFFIC_SUMMARY):
+    """DRAM bytes per launch (per step for the backward's three launches) from the
+    committed ncu summary, if it was taken on the current kernel source; else None."""
+    if workload not in TRAFFIC_SUMMARIES:
         return None
-    text = open(TRAFFIC_SUMMARY).read()
-    h = re.search(r"kernel source sha256\[:16\]:\s*`?([0-9a-f]{16})", text)
-    t = re.search(r"dram bytes per full launch\s*[:|]\s*`?([0-9.eE+]+)", text)
-    if not h or not t or h.group(1) != fwd_source_hash():
+    summary, source = TRAFFIC_SUMMARIES[workload]
+    if not os.path.exists(summary):
+        return None
+    text = open(summary).read()
+    h = re.search(r"kernel source sha256\[:16\][^:]*:\s*`?([0-9a-f]{16})", text)
+    t = re.search(r"dram bytes per full (?:launch|step)\s*[:|]\s*`?([0-9.eE+]+)", text)
+    if not h or not t or h.group(1) != source_hash(source):
         return None
     return float(t.group(1))
 
