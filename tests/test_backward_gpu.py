@@ -139,6 +139,26 @@ def test_keyless_and_rowless_segments():
     check_backward(g, gpu_backward(g, q, k, v, do), oracle_backward(g, q, k, v, do))
 
 
+def test_no_keys_at_all():
+    """Every segment keyless: K / V are empty, dQ is zero on used rows only."""
+    cu_q = np.array([0, 50, 50, 170], np.int32)
+    g = W.Geometry(cu_q, np.array([31, 0, 100], np.int32), np.zeros(4, np.int32), np.zeros(3, np.int32), 16, 4, 128)
+    q, k, v = W.make_qkv(g, 311, gap_fill=float("nan"))
+    assert k.shape[0] == 0
+    do = _make_dout(g, 311)
+    check_backward(g, gpu_backward(g, q, k, v, do), oracle_backward(g, q, k, v, do))
+
+
+def test_no_rows_at_all():
+    """No used query row anywhere: the used keys get dK = dV = 0, nothing else is written."""
+    g = W.Geometry(np.zeros(3, np.int32), np.zeros(2, np.int32), np.array([0, 130, 300], np.int32),
+                   np.array([129, 77], np.int32), 8, 8, 64)
+    q, k, v = W.make_qkv(g, 312, gap_fill=float("nan"))
+    assert q.shape[0] == 0
+    do = _make_dout(g, 312)
+    check_backward(g, gpu_backward(g, q, k, v, do), oracle_backward(g, q, k, v, do))
+
+
 def test_fp32_gradients_and_explicit_scale():
     rng = np.random.default_rng(401)
     g = W.random_geometry(rng, 4, 500, 500, 16, 4, 128, allow_empty=False)
