@@ -295,7 +295,7 @@ def lse_merge(outs: Sequence, lses: Sequence, cu_q, used_q, *, out=None, lse=Non
 
 
 def attention_backward(q, k, v, d_out, cu_q, used_q, cu_k, used_k, *, scale: Optional[float] = None,
-                       dq=None, dk=None, dv=None, num_heads_kv: Optional[int] = None):
+                       dq=None, dk=None, dv=None, num_heads_kv: Optional[int] = None, causal_block: int = 0):
     """Gradients of the gapped varlen forward with respect to Q, K and V. FP64.
 
     The backward the pages mark as missing on the non-FA4 paths (cosmos-framework
@@ -311,7 +311,10 @@ def attention_backward(q, k, v, d_out, cu_q, used_q, cu_k, used_k, *, scale: Opt
     Only used rows of dQ and used keys of dK / dV are written (others keep ``dq`` /
     ``dk`` / ``dv``, default zeros); a keyless segment's used rows get dQ = 0 and the
     used keys of a segment without used rows get dK = dV = 0. Each
-    segment's used keys must not overlap another segment's. Returns (dq, dk, dv)."""
+    segment's used keys must not overlap another segment's. ``causal_block`` > 0 takes
+    the gradients of the block-causal forward (``causal_limits``): a row's P is zero
+    past its limit, and a row that sees no key has P = 0 and so dQ = 0. Returns
+    (dq, dk, dv)."""
     q, k, v, d_out = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(d_out)
     total_q, hq, d = q.shape
     hkv = k.shape[1] if num_heads_kv is None else num_heads_kv
@@ -335,15 +338,24 @@ def attention_backward(q, k, v, d_out, cu_q, used_q, cu_k, used_k, *, scale: Opt
         if nk == 0:
             dq_out[r0:r0 + nq] = 0.0
             continue
+        lim = np.repeat(causal_limits(nq, nk, causal_block), g) if causal_block > 0 else None
         for hk in range(hkv):
             qs = q[r0:r0 + nq, hk * g:(hk + 1) * g, :].astype(np.float64).reshape(nq * g, d)
             dos = d_out[r0:r0 + nq, hk * g:(hk + 1) * g, :].astype(np.float64).reshape(nq * g, d)
             ks = k[k0:k0 + nk, hk, :].astype(np.float64)
             vs = v[k0:k0 + nk, hk, :].astype(np.float64)
             x = (qs @ ks.T) * s
-            x -= x.max(axis=1, keepdims=True)
-            p = np.exp(x)
-            p /= p.sum(axis=1, keepdims=True)
+            if lim is None:
+                x -= x.max(axis=1, keepdims=True)
+                p = np.exp(x)
+                p /= p.sum(axis=1, keepdims=True)
+            else:  # keys past a row's limit leave its softmax; a row with none has P = 0
+                vis = np.arange(nk)[None, :] < lim[:, None]
+                live = vis.any(axis=1)
+                x = np.where(vis, x, -np.inf)
+                mx = np.where(live, x.max(axis=1), 0.0)
+                p = np.exp(x - mx[:, None])
+                p /= np.where(live, p.sum(axis=1), 1.0)[:, None]
             dp = dos @ vs.T
             dd = (p * dp).sum(axis=1, keepdims=True)
             ds = p * (dp - dd)

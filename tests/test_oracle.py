@@ -389,10 +389,56 @@ def pin_backward(orc):
     np.testing.assert_allclose(dv2, pack(vt.grad), atol=1e-12)
 
 
+def pin_backward_causal(orc):
+    """Block-causal gradients: central finite differences of sum(dO * O) through the
+    oracle's block-causal forward (rows with no visible key included), and float64
+    autograd of SDPA with is_causal on equal lengths (token-causal)."""
+    rng = np.random.default_rng(19)
+    cu_q, used_q = np.array([0, 6, 9]), np.array([6, 3])
+    cu_k, used_k = np.array([0, 4, 10]), np.array([4, 6])  # segment 0: two rows before the first key
+    hq, hkv, d, sc = 4, 2, 3, 0.8
+    q = _rand(rng, 9, hq, d)
+    k = _rand(rng, 10, hkv, d)
+    v = _rand(rng, 10, hkv, d)
+    do = _rand(rng, 9, hq, d)
+    for blk in (1, 2, 3):
+        dq, dk, dv = orc.attention_backward(q, k, v, do, cu_q, used_q, cu_k, used_k, scale=sc, causal_block=blk)
+
+        def loss(qq, kk, vv):
+            o, _ = orc.attention_forward(qq, kk, vv, cu_q, used_q, cu_k, used_k, scale=sc, causal_block=blk)
+            return float(np.sum(o * do))
+        eps = 1e-6
+        for name, arr, grad, rows in [("q", q, dq, [0, 2, 5, 6, 8]), ("k", k, dk, [0, 3, 4, 9]),
+                                      ("v", v, dv, [1, 3, 5, 8])]:
+            for r in rows:
+                for h in range(arr.shape[1]):
+                    for t in range(d):
+                        a, b_ = arr.copy(), arr.copy()
+                        a[r, h, t] += eps
+                        b_[r, h, t] -= eps
+                        args_a = {"q": (a, k, v), "k": (q, a, v), "v": (q, k, a)}[name]
+                        args_b = {"q": (b_, k, v), "k": (q, b_, v), "v": (q, k, b_)}[name]
+                        fd = (loss(*args_a) - loss(*args_b)) / (2 * eps)
+                        assert abs(fd - grad[r, h, t]) < 1e-6, (blk, name, r, h, t, fd, grad[r, h, t])
+        assert np.all(dq[0:2] == 0.0)  # rows 0, 1 sit before the segment's first key
+    B, L = 2, 6
+    qt = torch.randn(B, hq, L, d, dtype=torch.float64, requires_grad=True)
+    kt = torch.randn(B, hkv, L, d, dtype=torch.float64, requires_grad=True)
+    vt = torch.randn(B, hkv, L, d, dtype=torch.float64, requires_grad=True)
+    gout = torch.randn(B, hq, L, d, dtype=torch.float64)
+    torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=sc, is_causal=True,
+                                                     enable_gqa=True).backward(gout)
+    pack = lambda t: t.detach().transpose(1, 2).reshape(-1, t.shape[1], d).numpy()  # noqa: E731
+    got = orc.attention_backward(pack(qt), pack(kt), pack(vt), pack(gout), np.arange(B + 1) * L, [L] * B,
+                                 np.arange(B + 1) * L, [L] * B, scale=sc, causal_block=1)
+    for g_, ref in zip(got, (qt.grad, kt.grad, vt.grad)):
+        np.testing.assert_allclose(g_, pack(ref), atol=1e-12)
+
+
 PINS = [pin_bruteforce, pin_default_scale, pin_dilution_golden, pin_zero_keys_closed_form,
         pin_single_key, pin_keyless_and_gap_rows, pin_pad_invariance, pin_sdpa_equal_lengths,
         pin_gqa_repeat, pin_key_permutation, pin_merge_union, pin_rows_match, pin_ranges, pin_causal,
-        pin_backward]
+        pin_backward, pin_backward_causal]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -431,6 +477,8 @@ MUTANTS = {
     "backward_dk_unscaled": ("dk_out[k0:k0 + nk, hk, :] = s * (ds.T @ qs)", "dk_out[k0:k0 + nk, hk, :] = ds.T @ qs"),
     "backward_dv_uses_ds": ("dv_out[k0:k0 + nk, hk, :] = p.T @ dos", "dv_out[k0:k0 + nk, hk, :] = ds.T @ dos"),
     "backward_rowless_keys_untouched": ("        if nk > 0:  # a used key", "        if nk > 0 and nq > 0:  # a used key"),
+    "backward_causal_mask_dropped": ("                x = np.where(vis, x, -np.inf)\n                mx = np.where(live",
+                                     "                x = x\n                mx = np.where(live"),
     "range_end_dropped": ("np.arange(int(st), int(st) + int(n))", "np.arange(int(st), int(st) + int(n) - 1)"),
 }
 
