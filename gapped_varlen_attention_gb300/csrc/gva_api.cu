@@ -116,8 +116,8 @@ void free_plan(struct gva_plan* p) {
 // keys are the ranges range_off[b] .. range_off[b+1] of (range_start, range_len).
 // causal_block > 0 (block-causal, one prefix range per segment): each item only gets the
 // key blocks its last row sees, and FLOPs count the visible keys of every row.
-// backward (maskless, one prefix range per segment, segments' keys disjoint): also build
-// the dQ items and the dK / dV units.
+// backward (one prefix range per segment, so segments' keys are disjoint; maskless or
+// block-causal): also build the dQ items and the dK / dV units.
 gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int32_t num_segments,
                       const int32_t* range_off, const int32_t* range_start, const int32_t* range_len,
                       int64_t total_k, int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim,
@@ -194,6 +194,8 @@ gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
   if (backward) {
     for (int32_t b = 0; b < num_segments; ++b) {
       const int32_t uq = seqused_q[b];
+      const int32_t pos_shift = seg_keys[b] - uq;  // block-causal: key position of row 0
+      const int32_t n_q_tiles = (uq + tokens_per_tile - 1) / tokens_per_tile;
       for (int32_t hk = 0; hk < num_heads_kv; ++hk) {
         for (int32_t t0 = 0; t0 < uq; t0 += tokens_per_tile) {
           gva::WorkItem it{};
@@ -204,18 +206,34 @@ gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
           it.head_kv = hk;
           it.n_tiles = 1;
           it.k_len = seg_keys[b];
+          if (causal_block > 0) {  // the key blocks the tile's last row sees
+            it.q_pos0 = t0 + pos_shift;
+            const int32_t last = limit_at(static_cast<int64_t>(it.q_pos0) + it.q_rows - 1, seg_keys[b]);
+            it.nblk = (last + gva::kBlockKeys - 1) / gva::kBlockKeys;
+          }
           bwd_items.push_back(it);
         }
         for (int32_t j = 0; j < seg_nblk[b]; ++j) {
           const gva::KeyBlock& kb = blocks[seg_blk0[b] + j];
-          kv_units.push_back({kb.row0, kb.valid, cu_seqlens_q[b], uq, hk, 0, 0, 0});
+          gva::KvUnit u{kb.row0, kb.valid, cu_seqlens_q[b], uq, hk, 0, j * gva::kBlockKeys, pos_shift};
+          if (causal_block > 0) {
+            // rows at key positions >= the start of the frame holding the block's first
+            // key see it; tiles before the first such row never do
+            const int64_t pos_min = (static_cast<int64_t>(u.key_pos0) / causal_block) * causal_block;
+            const int64_t row_min = std::max<int64_t>(0, pos_min - pos_shift);
+            u.tile0 = static_cast<int32_t>(std::min<int64_t>(row_min / tokens_per_tile, n_q_tiles));
+          }
+          kv_units.push_back(u);
         }
       }
     }
     std::stable_sort(bwd_items.begin(), bwd_items.end(),
                      [](const gva::WorkItem& a, const gva::WorkItem& c) { return a.nblk > c.nblk; });
+    auto unit_tiles = [&](const gva::KvUnit& u) {
+      return (u.q_used + tokens_per_tile - 1) / tokens_per_tile - u.tile0;
+    };
     std::stable_sort(kv_units.begin(), kv_units.end(),
-                     [](const gva::KvUnit& a, const gva::KvUnit& c) { return a.q_used > c.q_used; });
+                     [&](const gva::KvUnit& a, const gva::KvUnit& c) { return unit_tiles(a) > unit_tiles(c); });
   }
 
   // ---- device
@@ -368,7 +386,7 @@ gva_status gva_plan_causal(const int32_t* cu_seqlens_q, const int32_t* seqused_q
     len[b] = seqused_k[b];
   }
   return build_plan(cu_seqlens_q, seqused_q, num_segments, off.data(), start.data(), len.data(),
-                    cu_seqlens_k[num_segments], num_heads_q, num_heads_kv, head_dim, causal_block, false,
+                    cu_seqlens_k[num_segments], num_heads_q, num_heads_kv, head_dim, causal_block, true,
                     out_plan);
 }
 
@@ -486,7 +504,7 @@ gva_status gva_lse_merge(gva_plan_t plan, int32_t num_parts, const void* const* 
 gva_status gva_backward_workspace_size(gva_plan_t plan, size_t* bytes) {
   if (plan == nullptr || bytes == nullptr) return fail(GVA_ERR_INVALID_ARG, "plan or bytes is NULL");
   if (!plan->backward_ok)
-    return fail(GVA_ERR_UNSUPPORTED, "the backward needs a plan from gva_plan (maskless, prefix keys)");
+    return fail(GVA_ERR_UNSUPPORTED, "the backward needs a plan from gva_plan or gva_plan_causal (prefix keys)");
   *bytes = static_cast<size_t>(plan->num_heads_q) * static_cast<size_t>(plan->total_q) * sizeof(float);
   return ok();
 }
@@ -497,7 +515,7 @@ gva_status gva_backward(gva_plan_t plan, const void* q, const void* k, const voi
                         cudaStream_t stream) {
   if (plan == nullptr) return fail(GVA_ERR_INVALID_ARG, "plan is NULL");
   if (!plan->backward_ok)
-    return fail(GVA_ERR_UNSUPPORTED, "the backward needs a plan from gva_plan (maskless, prefix keys)");
+    return fail(GVA_ERR_UNSUPPORTED, "the backward needs a plan from gva_plan or gva_plan_causal (prefix keys)");
   if ((dq_dtype != GVA_BF16 && dq_dtype != GVA_FP32) || (dkv_dtype != GVA_BF16 && dkv_dtype != GVA_FP32))
     return fail(GVA_ERR_INVALID_ARG, "bad gradient dtype");
   if (plan->num_bwd_items == 0 && plan->num_kv_units == 0) return ok();  // no used row and no used key
@@ -557,6 +575,7 @@ gva_status gva_backward(gva_plan_t plan, const void* q, const void* k, const voi
   prm.tokens_per_tile = tokens_per_tile;
   prm.scale = scale;
   prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.causal_block = plan->causal_block;
   prm.error_flag = plan->d_error;
   e = gva::launch_backward(plan->head_dim, dq_dtype == GVA_FP32, dkv_dtype == GVA_FP32, prm, plan->d_units,
                            plan->num_units, out, d_out, static_cast<float*>(workspace), mq, mk, mv, mdo,

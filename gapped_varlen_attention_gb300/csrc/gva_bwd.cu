@@ -64,11 +64,10 @@ __device__ __forceinline__ void zero_tile_row(uint8_t* tile, int row) {
 
 __device__ __forceinline__ KvUnit load_unit(const KvUnit* units, int idx) {
   const int4* p = reinterpret_cast<const int4*>(units + idx);
-  const int4 a = __ldg(p);
+  const int4 a = __ldg(p), b = __ldg(p + 1);
   KvUnit u;
   u.key_row0 = a.x; u.keys = a.y; u.q_row0 = a.z; u.q_used = a.w;
-  u.head_kv = __ldg(reinterpret_cast<const int*>(p + 1));
-  u.pad0 = u.pad1 = u.pad2 = 0;
+  u.head_kv = b.x; u.tile0 = b.y; u.key_pos0 = b.z; u.pos_shift = b.w;
   return u;
 }
 
@@ -76,6 +75,7 @@ __device__ __forceinline__ KvUnit load_unit(const KvUnit* units, int idx) {
 struct BwdCtrl {
   float xl[2][kTileRows];  // per-column log2-LSE of the current Q tile (two tiles in flight)
   float xd[2][kTileRows];  // per-column D
+  int xlim[2][kTileRows];  // block-causal: per-column key limit
   uint64_t a_full, a_empty;            // K + V blocks
   uint64_t r_full[2], r_empty[2];      // Q / dO slots
   uint64_t zero_bar;                   // partial tiles: the producer's own copy wait
@@ -214,7 +214,7 @@ __device__ __forceinline__ void store_zero_cols(TOut* row) {
 // ---------------------------------------------------------------------------------
 // 2. dQ
 // ---------------------------------------------------------------------------------
-template <int D, typename TOut>
+template <int D, typename TOut, bool kCausal>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     gva_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                       const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
@@ -415,7 +415,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         continue;
       }
       const int64_t li = static_cast<int64_t>(head) * p.total_q + token;
-      const float lse2 = valid ? p.lse[li] * kLog2e : 0.0f;
+      int row_limit = it.k_len;  // keys of the segment this row sees
+      if constexpr (kCausal) {
+        const int pos = it.q_pos0 + tok;
+        row_limit = pos < 0 ? 0 : min(it.k_len, (pos / p.causal_block + 1) * p.causal_block);
+      }
+      // a row that sees no key (its LSE is -inf) takes +inf here, so its P is 0
+      const float lse2 = valid && row_limit > 0 ? p.lse[li] * kLog2e : CUDART_INF_F;
       const float drow = valid ? p.dvec[li] : 0.0f;
       const uint64_t neg_l2 = f32x2(-lse2, -lse2);
       for (int j = 0; j < it.nblk; ++j, ++n) {
@@ -428,8 +434,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_ld64x2_sync(s_addr, sraw, dp_addr, dpr);
         tcgen05_fence_before();
         mbar_arrive(&ctrl.dp_consumed);  // the tensor core may overwrite dP now
-        // used keys of this half: only a segment's last block is partial (one prefix range)
-        const int rem = min(kBlockKeys, it.k_len - j * kBlockKeys) - 64 * wg;
+        // keys of this half the row sees: the used keys (only a segment's last block is
+        // partial, one prefix range), capped by the row's block-causal limit
+        const int rem = min(kBlockKeys, row_limit - j * kBlockKeys) - 64 * wg;
         if (rem < 64) {  // keys past the used length: P = 0 (uniform over the warp)
 #pragma unroll
           for (int i = 0; i < 64; ++i) sraw[i] = i < rem ? sraw[i] : 0xff800000u;
@@ -481,7 +488,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // ---------------------------------------------------------------------------------
 // 3. dK, dV
 // ---------------------------------------------------------------------------------
-template <int D, typename TOut>
+template <int D, typename TOut, bool kCausal>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     gva_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                         const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
@@ -510,7 +517,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // (Q-tile rows 64h .. 64h+63) of S^T / dP^T is [64h, +64) / [128+64h, +64); its P^T
   // and dS^T (bf16 pairs) overwrite [64h, +32) and [128+64h, +32).
   constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
-  auto n_tiles = [&](const KvUnit& u) { return (u.q_used + T - 1) / T; };
+  // Q tiles of the unit: from the first one that sees the block (block-causal) to the end
+  auto n_tiles = [&](const KvUnit& u) { return (u.q_used + T - 1) / T - u.tile0; };
 
   if (warp == 0) {
     // As in the dQ kernel: lane 0 copies, the warp clears rows past the used keys of a
@@ -564,8 +572,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!ok) break;
         uint8_t* tq = sSlots + sl * 2 * C::kTileBytes;
         uint8_t* tdo = tq + C::kTileBytes;
-        const int t0 = u.q_row0 + i * T;
-        const int vt = min(T, u.q_used - i * T);  // used tokens of this tile
+        const int t0 = u.q_row0 + (u.tile0 + i) * T;
+        const int vt = min(T, u.q_used - (u.tile0 + i) * T);  // used tokens of this tile
         uint64_t* bar = vt == T ? &ctrl.r_full[sl] : &ctrl.zero_bar;
         if (leader) {
           mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
@@ -705,20 +713,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // log2-LSE and D of this half's Q-tile rows (loader threads tid < 64), fetched one
       // tile ahead; +inf LSE (P = 0) and D = 0 past the used rows
       const int64_t lrow0 = static_cast<int64_t>(u.head_kv * G + rhl) * p.total_q + u.q_row0 + rtok;
-      auto fetch = [&](int i, float& xl_v, float& xd_v) {
-        const bool rvalid = i * T + rtok < u.q_used;
-        xl_v = rvalid ? __ldg(p.lse + lrow0 + i * T) * kLog2e : CUDART_INF_F;
-        xd_v = rvalid ? __ldg(p.dvec + lrow0 + i * T) : 0.0f;
+      auto fetch = [&](int i, float& xl_v, float& xd_v, int& lim_v) {
+        const int r = (u.tile0 + i) * T + rtok;  // row within the segment
+        const bool rvalid = r < u.q_used;
+        lim_v = 0x7fffffff;
+        if constexpr (kCausal) {
+          const int pos = r + u.pos_shift;
+          lim_v = pos < 0 ? 0 : (pos / p.causal_block + 1) * p.causal_block;
+        }
+        const float l = rvalid && lim_v > 0 ? __ldg(p.lse + lrow0 + (r - rtok)) : -CUDART_INF_F;
+        xl_v = l > -CUDART_INF_F ? l * kLog2e : CUDART_INF_F;  // +inf: P = 0
+        xd_v = rvalid ? __ldg(p.dvec + lrow0 + (r - rtok)) : 0.0f;
       };
       float nxl = 0.0f, nxd = 0.0f;
-      if (tid < 64) fetch(0, nxl, nxd);
+      int nlim = 0;
+      if (tid < 64) fetch(0, nxl, nxd, nlim);
       for (int i = 0; i < nqt; ++i) {
         const int par = tiles & 1;
         ++tiles;
         if (tid < 64) {
           ctrl.xl[par][lrow] = nxl;
           ctrl.xd[par][lrow] = nxd;
-          if (i + 1 < nqt) fetch(i + 1, nxl, nxd);
+          if constexpr (kCausal) ctrl.xlim[par][lrow] = nlim;
+          if (i + 1 < nqt) fetch(i + 1, nxl, nxd, nlim);
         }
         const bool fine = __all_sync(0xffffffffu, wait_bar(&ctrl.s_full[wg], sc & 1, abort_flag, p.error_flag));
         ++sc;
@@ -734,10 +751,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
           float2 l2[4], d2[4];
+          int2 m2[4];  // block-causal: the columns' key limits
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             l2[k] = *reinterpret_cast<const float2*>(xl + 32 * part + 8 * k + 2 * c4);
             d2[k] = *reinterpret_cast<const float2*>(xd + 32 * part + 8 * k + 2 * c4);
+            if constexpr (kCausal)
+              m2[k] = *reinterpret_cast<const int2*>(&ctrl.xlim[par][64 * wg + 32 * part + 8 * k + 2 * c4]);
           }
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -760,6 +780,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               float s3 = p3 * (__uint_as_float(dr[4 * k + 3]) - d2[k].y);
               if (!va) p0 = p1 = s0 = s1 = 0.0f;
               if (!vb) p2 = p3 = s2 = s3 = 0.0f;
+              if constexpr (kCausal) {  // keys at or past a row's limit: P = dS = 0
+                const int ka = u.key_pos0 + lane0 + g, kb = ka + 8;
+                if (ka >= m2[k].x) p0 = s0 = 0.0f;
+                if (ka >= m2[k].y) p1 = s1 = 0.0f;
+                if (kb >= m2[k].x) p2 = s2 = 0.0f;
+                if (kb >= m2[k].y) p3 = s3 = 0.0f;
+              }
               pp[2 * k] = pack_bf16x2(p0, p1);
               pp[2 * k + 1] = pack_bf16x2(p2, p3);
               pd[2 * k] = pack_bf16x2(s0, s1);
@@ -803,7 +830,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-template <int D, typename TQ, typename TKV>
+template <int D, typename TQ, typename TKV, bool kCausal>
 cudaError_t launch_bwd_impl(const BwdParams& p, const MergeUnit* units, int32_t num_units, const void* out,
                             const void* d_out, float* dvec, const CUtensorMap& mq, const CUtensorMap& mk,
                             const CUtensorMap& mv, const CUtensorMap& mdo, int dq_grid, int sms,
@@ -816,20 +843,37 @@ cudaError_t launch_bwd_impl(const BwdParams& p, const MergeUnit* units, int32_t 
     if (e != cudaSuccess) return e;
   }
   if (p.num_items > 0) {
-    auto kq = gva_bwd_dq_kernel<D, TQ>;
+    auto kq = gva_bwd_dq_kernel<D, TQ, kCausal>;
     cudaError_t e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, BCfg<D>::kSmemDq);
     if (e != cudaSuccess) return e;
     kq<<<dq_grid, kBwdThreads, BCfg<D>::kSmemDq, stream>>>(mq, mk, mv, mdo, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (p.num_kv_units > 0) {
-    auto kkv = gva_bwd_dkdv_kernel<D, TKV>;
+    auto kkv = gva_bwd_dkdv_kernel<D, TKV, kCausal>;
     cudaError_t e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, BCfg<D>::kSmemDkv);
     if (e != cudaSuccess) return e;
     kkv<<<min(p.num_kv_units, sms), kBwdThreads, BCfg<D>::kSmemDkv, stream>>>(mq, mk, mv, mdo, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+template <int D, bool kCausal>
+cudaError_t launch_bwd_dc(bool dq_f32, bool dkv_f32, const BwdParams& p, const MergeUnit* units, int32_t num_units,
+                          const void* out, const void* d_out, float* dvec, const CUtensorMap& mq,
+                          const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo, int dq_grid,
+                          int sms, cudaStream_t stream) {
+  if (dq_f32) {
+    return dkv_f32 ? launch_bwd_impl<D, float, float, kCausal>(p, units, num_units, out, d_out, dvec, mq, mk, mv, mdo,
+                                                               dq_grid, sms, stream)
+                   : launch_bwd_impl<D, float, __nv_bfloat16, kCausal>(p, units, num_units, out, d_out, dvec, mq, mk,
+                                                                       mv, mdo, dq_grid, sms, stream);
+  }
+  return dkv_f32 ? launch_bwd_impl<D, __nv_bfloat16, float, kCausal>(p, units, num_units, out, d_out, dvec, mq, mk,
+                                                                     mv, mdo, dq_grid, sms, stream)
+                 : launch_bwd_impl<D, __nv_bfloat16, __nv_bfloat16, kCausal>(p, units, num_units, out, d_out, dvec,
+                                                                             mq, mk, mv, mdo, dq_grid, sms, stream);
 }
 
 template <int D>
@@ -840,16 +884,11 @@ cudaError_t launch_bwd_d(bool dq_f32, bool dkv_f32, const BwdParams& p, const Me
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (dq_f32) {
-    return dkv_f32 ? launch_bwd_impl<D, float, float>(p, units, num_units, out, d_out, dvec, mq, mk, mv, mdo, dq_grid,
-                                                      sms, stream)
-                   : launch_bwd_impl<D, float, __nv_bfloat16>(p, units, num_units, out, d_out, dvec, mq, mk, mv,
-                                                              mdo, dq_grid, sms, stream);
-  }
-  return dkv_f32 ? launch_bwd_impl<D, __nv_bfloat16, float>(p, units, num_units, out, d_out, dvec, mq, mk, mv, mdo,
-                                                            dq_grid, sms, stream)
-                 : launch_bwd_impl<D, __nv_bfloat16, __nv_bfloat16>(p, units, num_units, out, d_out, dvec, mq, mk,
-                                                                    mv, mdo, dq_grid, sms, stream);
+  if (p.causal_block > 0)
+    return launch_bwd_dc<D, true>(dq_f32, dkv_f32, p, units, num_units, out, d_out, dvec, mq, mk, mv, mdo, dq_grid,
+                                  sms, stream);
+  return launch_bwd_dc<D, false>(dq_f32, dkv_f32, p, units, num_units, out, d_out, dvec, mq, mk, mv, mdo, dq_grid,
+                                 sms, stream);
 }
 
 }  // namespace

@@ -44,7 +44,9 @@ struct alignas(16) KvUnit {
   int32_t q_row0;    // global token row of the segment's first query
   int32_t q_used;    // used query rows of the segment (0: dK = dV = 0)
   int32_t head_kv;
-  int32_t pad0, pad1, pad2;
+  int32_t tile0;     // first Q tile of the segment that sees the block (block-causal; else 0)
+  int32_t key_pos0;  // block-causal: index of the block's first key within the segment
+  int32_t pos_shift; // block-causal: key position of the segment's query row 0 (used_k - used_q)
 };
 
 struct alignas(8) MergeUnit {
@@ -98,6 +100,7 @@ struct BwdParams {
   int32_t tokens_per_tile;
   float scale;             // softmax scale s
   float scale_log2;        // s * log2(e)
+  int32_t causal_block;    // > 0: gradients of the block-causal forward
   int* error_flag;
 };
 
@@ -110,6 +113,7 @@ cudaError_t launch_forward(int head_dim, bool out_f32, const FwdParams& p, const
 cudaError_t launch_merge(bool in_f32, bool out_f32, const MergeParams& p, int grid, cudaStream_t stream);
 int forward_smem_bytes(int head_dim);
 // Backward: rowsum(dO * O) over used rows, then dQ, then dK / dV (gva_bwd.cu).
+// Backward kernels take the block-causal variant when p.causal_block > 0.
 cudaError_t launch_backward(int head_dim, bool dq_f32, bool dkv_f32, const BwdParams& p, const MergeUnit* units,
                             int32_t num_units, const void* out, const void* d_out, float* dvec,
                             const CUtensorMap& map_q, const CUtensorMap& map_k, const CUtensorMap& map_v,

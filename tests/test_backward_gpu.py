@@ -44,8 +44,8 @@ def _masks(g):
     return dq_rows, dk_rows
 
 
-def gpu_backward(g, q, k, v, do, scale=0.0, grad_dtype=torch.bfloat16, plan=None):
-    plan = plan or gva.Plan.from_geometry(g)
+def gpu_backward(g, q, k, v, do, scale=0.0, grad_dtype=torch.bfloat16, plan=None, causal_block=0):
+    plan = plan or gva.Plan.from_geometry(g, causal_block=causal_block)
     qc, kc, vc, doc = (t.cuda() for t in (q, k, v, do))
     o, l = W.make_outputs(g, FILL, device="cuda")
     gva.forward(plan, qc, kc, vc, o, l, scale)
@@ -57,11 +57,11 @@ def gpu_backward(g, q, k, v, do, scale=0.0, grad_dtype=torch.bfloat16, plan=None
     return dq, dk, dv
 
 
-def oracle_backward(g, q, k, v, do, scale=None):
+def oracle_backward(g, q, k, v, do, scale=None, causal_block=0):
     qn, kn, vn, don = (t.detach().cpu().float().numpy() for t in (q, k, v, do))
     return gva_oracle.attention_backward(qn, kn, vn, don, g.cu_q, g.used_q, g.cu_k, g.used_k, scale=scale,
                                          dq=np.full(qn.shape, FILL), dk=np.full(kn.shape, FILL),
-                                         dv=np.full(vn.shape, FILL))
+                                         dv=np.full(vn.shape, FILL), causal_block=causal_block)
 
 
 def _close(name, got, ref, max_rel=MAX_REL, rms_rel=RMS_REL):
@@ -181,14 +181,47 @@ def test_deterministic():
         assert torch.equal(x, y)
 
 
-def test_masked_plans_are_refused():
+def test_range_plans_are_refused():
     g = W.tiny()
-    plan = gva.Plan.from_geometry(g, causal_block=16)
-    with pytest.raises(gva.GvaError, match="UNSUPPORTED"):
-        gva.backward_workspace_bytes(plan)
     rplan = gva.Plan.from_ranges(g.cu_q, g.used_q, [[(0, 48)], [(48, 33)], []], g.total_k, 4, 2, 64)
     with pytest.raises(gva.GvaError, match="UNSUPPORTED"):
         gva.backward_workspace_bytes(rplan)
+
+
+CAUSAL_CASES = [  # (Hq, Hkv, d, causal block, seed)
+    (8, 2, 128, 1, 601),
+    (16, 4, 128, 3, 602),
+    (32, 8, 128, 64, 603),
+    (8, 8, 64, 200, 604),
+    (16, 1, 64, 128, 605),
+    (4, 1, 128, 129, 606),
+]
+
+
+@pytest.mark.parametrize("hq,hkv,d,block,seed", CAUSAL_CASES)
+def test_block_causal_random_geometries(hq, hkv, d, block, seed):
+    """Gradients of the block-causal forward: random gapped geometries where used_q may
+    exceed used_k (early rows see no key: dQ = 0 there), NaN in every gap row."""
+    rng = np.random.default_rng(seed)
+    g = W.random_geometry(rng, 6, 600, 700, hq, hkv, d)
+    q, k, v = W.make_qkv(g, seed, gap_fill=float("nan"))
+    do = _make_dout(g, seed)
+    check_backward(g, gpu_backward(g, q, k, v, do, causal_block=block),
+                   oracle_backward(g, q, k, v, do, causal_block=block))
+
+
+def test_block_causal_huge_block_is_the_maskless_backward():
+    """With used_q <= used_k every row sits at a non-negative key position, so a block
+    longer than any segment masks nothing: bit-identical to the maskless backward."""
+    rng = np.random.default_rng(607)
+    g = W.random_geometry(rng, 5, 500, 800, 16, 4, 128)
+    g.used_q = np.minimum(g.used_q, g.used_k).astype(np.int32)
+    q, k, v = W.make_qkv(g, 607)
+    do = _make_dout(g, 607)
+    a = gpu_backward(g, q, k, v, do, causal_block=1 << 20)
+    b = gpu_backward(g, q, k, v, do)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
 
 
 def test_cfg_text_cross_full():
@@ -251,3 +284,32 @@ def test_long_replay_full_size_sampled():
         got = dq[sel].float().cpu().numpy().astype(np.float64)
         scale = np.abs(dq_ref).max()
         assert np.abs(got - dq_ref).max() <= MAX_REL * scale
+
+
+@pytest.mark.slow
+def test_multiview_block_causal_full_size_sampled():
+    """The multiview workload (7 segments, 512-token frames) at full size: dQ on sampled
+    rows against the oracle (each sampled row attends exactly its visible keys), dK / dV
+    through the identities (every row sees at least its own frame here: used_q < used_k)."""
+    full, _ = W.multiview_causal()
+    blk = 512
+    q, k, v = W.make_qkv(full, 1003, device="cuda", gap_fill=float("nan"))
+    do = _make_dout(full, 1003, device="cuda")
+    dq, dk, dv = gpu_backward(full, q, k, v, do, causal_block=blk)
+    dq_rows, dk_rows = _masks(full)
+    assert bool((dq[torch.from_numpy(~dq_rows).cuda()].float() == FILL).all())
+    assert bool((dk[torch.from_numpy(~dk_rows).cuda()].float() == FILL).all())
+    rng = np.random.default_rng(14)
+    for b in range(full.num_segments):
+        nq, nk = int(full.used_q[b]), int(full.used_k[b])
+        lim = gva_oracle.causal_limits(nq, nk, blk)
+        _segment_properties(full, q, k, do, dq, dk, dv, b, 1.0 / np.sqrt(full.head_dim))
+        rows = sorted(set(int(x) for x in rng.integers(0, nq, size=3)) | {0, nq - 1})
+        k0 = int(full.cu_k[b])
+        for r in rows:
+            sel = [int(full.cu_q[b]) + r]
+            n = int(lim[r])
+            dq_ref, _, _ = gva_oracle.attention_backward(q[sel].cpu(), k[k0:k0 + n].cpu(), v[k0:k0 + n].cpu(),
+                                                         do[sel].cpu(), [0, 1], [1], [0, n], [n])
+            got = dq[sel].float().cpu().numpy().astype(np.float64)
+            assert np.abs(got - dq_ref).max() <= MAX_REL * max(np.abs(dq_ref).max(), 1e-30)
