@@ -115,6 +115,15 @@ class Workload:
             self.label = ("backward (dQ, dK, dV) of the long joint video+LiDAR replay: 4 segments x 32768 q rows "
                           "(used 60-100%) x 65536 keys (used 50-100%), Hq=32, Hkv=8, d=128, bf16; FLOPs = 2.5 x "
                           "the forward's (five used-row products)")
+        elif name == "multiview_blockcausal_bwd":
+            full, _ = W.multiview_causal()
+            self.geoms = [full]
+            self.q, self.k, self.v = W.make_qkv(full, 1003 + seed_offset, device=dev)
+            self.parts = None
+            self.causal_block = 512
+            self.backward = True
+            self.label = ("backward of the multiview causal gapped replay with 512-token block-causal masking "
+                          "(FLOPs: 2.5 x the visible-key forward FLOPs)")
         elif name == "long_replay_small_bwd":
             g = W.long_replay_small()
             self.geoms = [g]
@@ -397,6 +406,7 @@ def oracle_sample_rate(wl, budget_s: float, seed: int = 0):
     k = wl.k.cpu()
     v = wl.v.cpu()
     backward = getattr(wl, "backward", False)
+    cb = getattr(wl, "causal_block", 0)
     d_out = wl.d_out.cpu() if backward else None
     done_flops = 0.0
     rows_done = 0
@@ -404,23 +414,34 @@ def oracle_sample_rate(wl, budget_s: float, seed: int = 0):
     while True:
         for g in geoms:
             b = int(rng.choice(np.flatnonzero(g.used_q > 0)))
-            rows = [int(g.cu_q[b]) + int(x) for x in rng.integers(0, int(g.used_q[b]), size=4)]
-            if backward:
+            local = [int(x) for x in rng.integers(0, int(g.used_q[b]), size=4)]
+            rows = [int(g.cu_q[b]) + r for r in local]
+            k0, nk = int(g.cu_k[b]), int(g.used_k[b])
+            # keys each sampled row sees (all used keys, or its block-causal prefix)
+            vis = (gva_oracle.causal_limits(int(g.used_q[b]), nk, cb)[local] if cb > 0
+                   else np.full(len(local), nk))
+            if backward and cb == 0:
                 # the sampled rows as one segment over their segment's keys: all five products
-                k0, nk = int(g.cu_k[b]), int(g.used_k[b])
                 gva_oracle.attention_backward(q[rows], k[k0:k0 + nk], v[k0:k0 + nk], d_out[rows], [0, len(rows)],
                                               [len(rows)], [0, nk], [nk])
-                done_flops += 10.0 * g.head_dim * g.num_heads_q * float(nk) * len(rows)
+                done_flops += 10.0 * g.head_dim * g.num_heads_q * float(np.sum(vis))
+            elif backward:
+                # block-causal: each sampled row as its own segment over the keys it sees
+                for r, n in zip(rows, vis):
+                    gva_oracle.attention_backward(q[[r]], k[k0:k0 + int(n)], v[k0:k0 + int(n)], d_out[[r]],
+                                                  [0, 1], [1], [0, int(n)], [int(n)])
+                done_flops += 10.0 * g.head_dim * g.num_heads_q * float(np.sum(vis))
             else:
-                gva_oracle.attention_rows(q, k, v, g.cu_q, g.used_q, g.cu_k, g.used_k, rows)
-                done_flops += 4.0 * g.head_dim * g.num_heads_q * float(g.used_k[b]) * len(rows)
+                gva_oracle.attention_rows(q, k, v, g.cu_q, g.used_q, g.cu_k, g.used_k, rows, causal_block=cb)
+                done_flops += 4.0 * g.head_dim * g.num_heads_q * float(np.sum(vis))
             rows_done += len(rows)
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
     what = "backward of " if backward else ""
-    desc = (f"{what}{rows_done} seeded used rows (all {geoms[0].num_heads_q} heads, every used key of their "
-            f"segment) of the {wl.name} workload, FP64 NumPy oracle")
+    keys = "every key each row sees" if cb > 0 else "every used key of their segment"
+    desc = (f"{what}{rows_done} seeded used rows (all {geoms[0].num_heads_q} heads, {keys}) of the {wl.name} "
+            f"workload, FP64 NumPy oracle")
     return done_flops / el / 1e12, desc, rows_done, el
 
 
@@ -435,7 +456,7 @@ def main():
     ap.add_argument("--workload", default="long_replay",
                     choices=["long_replay", "long_replay_small", "cfg_text_cross", "multiview_causal",
                              "multiview_fused", "multiview_blockcausal", "long_replay_bwd", "long_replay_small_bwd",
-                             "tiny"])
+                             "multiview_blockcausal_bwd", "tiny"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     args = ap.parse_args()
@@ -585,9 +606,14 @@ def run_reference(args, world, rank):
         g = W.cfg_text_cross()
         wl.geoms = [g]
         seed = 1002
-    elif args.workload in ("multiview_causal", "multiview_fused", "multiview_blockcausal"):
+    elif args.workload in ("multiview_causal", "multiview_fused"):
         g, parts = W.multiview_causal()
         wl.geoms = parts
+        seed = 1003
+    elif args.workload in ("multiview_blockcausal", "multiview_blockcausal_bwd"):
+        g, _ = W.multiview_causal()
+        wl.geoms = [g]
+        wl.causal_block = 512
         seed = 1003
     elif args.workload in ("long_replay_small", "long_replay_small_bwd"):
         g = W.long_replay_small()
@@ -599,7 +625,7 @@ def run_reference(args, world, rank):
         seed = 1001
     wl.q, wl.k, wl.v = W.make_qkv(g, seed)
     metric = METRIC
-    if args.workload in ("long_replay_bwd", "long_replay_small_bwd"):
+    if args.workload in ("long_replay_bwd", "long_replay_small_bwd", "multiview_blockcausal_bwd"):
         wl.backward = True
         wl.d_out = torch.randn(wl.q.shape, generator=torch.Generator().manual_seed(2005)).bfloat16()
         metric = "gapped-varlen attn bwd TFLOP/s (used rows, 2.5 x fwd FLOPs) & % of GB300 BF16 peak"
