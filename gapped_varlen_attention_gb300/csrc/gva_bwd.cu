@@ -844,14 +844,14 @@ cudaError_t launch_bwd_impl(const BwdParams& p, const MergeUnit* units, int32_t 
   }
   if (p.num_items > 0) {
     auto kq = gva_bwd_dq_kernel<D, TQ, kCausal>;
-    cudaError_t e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, BCfg<D>::kSmemDq);
+    cudaError_t e = ensure_smem_limit<gva_bwd_dq_kernel<D, TQ, kCausal>>(BCfg<D>::kSmemDq);
     if (e != cudaSuccess) return e;
     kq<<<dq_grid, kBwdThreads, BCfg<D>::kSmemDq, stream>>>(mq, mk, mv, mdo, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (p.num_kv_units > 0) {
     auto kkv = gva_bwd_dkdv_kernel<D, TKV, kCausal>;
-    cudaError_t e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, BCfg<D>::kSmemDkv);
+    cudaError_t e = ensure_smem_limit<gva_bwd_dkdv_kernel<D, TKV, kCausal>>(BCfg<D>::kSmemDkv);
     if (e != cudaSuccess) return e;
     kkv<<<min(p.num_kv_units, sms), kBwdThreads, BCfg<D>::kSmemDkv, stream>>>(mq, mk, mv, mdo, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -437,7 +437,7 @@ template <int D, typename TOut, bool kCausal>
 cudaError_t launch_impl(const FwdParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                         int grid, cudaStream_t stream) {
   auto kern = gva_fwd_kernel<D, TOut, kCausal>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemAlloc);
+  cudaError_t e = ensure_smem_limit<gva_fwd_kernel<D, TOut, kCausal>>(Cfg<D>::kSmemAlloc);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, Cfg<D>::kSmemAlloc, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();

@@ -1,6 +1,7 @@
 // Internal types shared by the host API and the kernels.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -118,6 +119,22 @@ cudaError_t launch_backward(int head_dim, bool dq_f32, bool dkv_f32, const BwdPa
                             int32_t num_units, const void* out, const void* d_out, float* dvec,
                             const CUtensorMap& map_q, const CUtensorMap& map_k, const CUtensorMap& map_v,
                             const CUtensorMap& map_do, int dq_grid, cudaStream_t stream);
+// Raise kernel K's dynamic shared-memory limit to `bytes`, once per device: the
+// attribute persists, and setting it on every launch is redundant work inside a CUDA
+// graph capture. One flag word per kernel instantiation (bit d: device d < 64).
+template <auto K>
+inline cudaError_t ensure_smem_limit(int bytes) {
+  static std::atomic<uint64_t> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
+
 // Set the calling thread's gva_last_error() text (defined in gva_api.cu).
 void set_last_error(const char* message);
 

@@ -125,7 +125,8 @@ template <typename TIn, typename TOut>
 cudaError_t launch_merge_impl(const MergeParams& p, int grid, cudaStream_t stream) {
   const int smem = p.num_parts * p.num_heads_q * kMergeRows * static_cast<int>(sizeof(float));
   auto kern = gva_lse_merge_kernel<TIn, TOut>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // the plan validation caps the weights at 200 KB; raise the limit to that once
+  cudaError_t e = ensure_smem_limit<gva_lse_merge_kernel<TIn, TOut>>(200 * 1024);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
