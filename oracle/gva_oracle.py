@@ -52,8 +52,8 @@ from typing import Optional, Sequence
 
 import numpy as np
 
-__all__ = ["attention_backward", "attention_forward", "attention_forward_ranges", "attention_rows",
-           "causal_limits", "lse_merge", "used_flops"]
+__all__ = ["attention_backward", "attention_backward_ranges", "attention_forward", "attention_forward_ranges",
+           "attention_rows", "causal_limits", "lse_merge", "used_flops"]
 
 DEFAULT_BUDGET_BYTES = 1 << 30
 
@@ -362,4 +362,54 @@ def attention_backward(q, k, v, d_out, cu_q, used_q, cu_k, used_k, *, scale: Opt
             dq_out[r0:r0 + nq, hk * g:(hk + 1) * g, :] = (s * (ds @ ks)).reshape(nq, g, d)
             dk_out[k0:k0 + nk, hk, :] = s * (ds.T @ qs)
             dv_out[k0:k0 + nk, hk, :] = p.T @ dos
+    return dq_out, dk_out, dv_out
+
+
+def attention_backward_ranges(q, k, v, d_out, cu_q, used_q, key_ranges, *, scale: Optional[float] = None,
+                              dq=None, dk=None, dv=None, num_heads_kv: Optional[int] = None):
+    """Gradients of ``attention_forward_ranges``: segment b's keys are the concatenation
+    of the K/V row ranges ``key_ranges[b]``. The same formulas as ``attention_backward``
+    per (segment, KV head); a K/V row that several ranges cover (of one segment or of
+    several) receives the sum of its contributions. Rows no range covers keep ``dk`` /
+    ``dv`` (default zeros); covered rows of a segment without used rows get 0; the used
+    rows of a segment without keys get dQ = 0. FP64. Returns (dq, dk, dv)."""
+    q, k, v, d_out = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(d_out)
+    total_q, hq, d = q.shape
+    hkv = k.shape[1] if num_heads_kv is None else num_heads_kv
+    g = hq // hkv
+    s = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    cu_q = np.asarray(cu_q, np.int64)
+    used_q = np.asarray(used_q, np.int64)
+    dq_out = np.zeros(q.shape, np.float64) if dq is None else _as_f64(dq).astype(np.float64, copy=True)
+    dk_out = np.zeros(k.shape, np.float64) if dk is None else _as_f64(dk).astype(np.float64, copy=True)
+    dv_out = np.zeros(v.shape, np.float64) if dv is None else _as_f64(dv).astype(np.float64, copy=True)
+    seg_rows = []
+    for b in range(len(used_q)):
+        rows = [np.arange(int(st), int(st) + int(n)) for st, n in key_ranges[b] if int(n) > 0]
+        seg_rows.append(np.concatenate(rows) if rows else np.zeros(0, np.int64))
+    for idx in seg_rows:  # every covered row starts from zero, then sums its contributions
+        dk_out[idx] = 0.0
+        dv_out[idx] = 0.0
+    for b in range(len(used_q)):
+        r0, nq = int(cu_q[b]), int(used_q[b])
+        idx = seg_rows[b]
+        if nq == 0:
+            continue
+        if idx.size == 0:
+            dq_out[r0:r0 + nq] = 0.0
+            continue
+        for hk in range(hkv):
+            qs = q[r0:r0 + nq, hk * g:(hk + 1) * g, :].astype(np.float64).reshape(nq * g, d)
+            dos = d_out[r0:r0 + nq, hk * g:(hk + 1) * g, :].astype(np.float64).reshape(nq * g, d)
+            ks = k[idx, hk, :].astype(np.float64)
+            vs = v[idx, hk, :].astype(np.float64)
+            x = (qs @ ks.T) * s
+            x -= x.max(axis=1, keepdims=True)
+            p = np.exp(x)
+            p /= p.sum(axis=1, keepdims=True)
+            dp = dos @ vs.T
+            ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+            dq_out[r0:r0 + nq, hk * g:(hk + 1) * g, :] = (s * (ds @ ks)).reshape(nq, g, d)
+            np.add.at(dk_out, (idx, hk), s * (ds.T @ qs))
+            np.add.at(dv_out, (idx, hk), p.T @ dos)
     return dq_out, dk_out, dv_out

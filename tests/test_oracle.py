@@ -435,10 +435,53 @@ def pin_backward_causal(orc):
         np.testing.assert_allclose(g_, pack(ref), atol=1e-12)
 
 
+def pin_backward_ranges(orc):
+    """Range gradients: one prefix range per segment is attention_backward bit for bit;
+    overlapping ranges (shared by two segments and repeated inside one) match central
+    finite differences through attention_forward_ranges, so a covered row sums its
+    contributions."""
+    rng = np.random.default_rng(20)
+    g = W.random_geometry(rng, 3, 6, 9, 4, 2, 3, allow_empty=False)
+    q = _rand(rng, g.total_q, 4, 3)
+    k = _rand(rng, g.total_k, 2, 3)
+    v = _rand(rng, g.total_k, 2, 3)
+    do = _rand(rng, g.total_q, 4, 3)
+    prefix = [[(int(g.cu_k[b]), int(g.used_k[b]))] for b in range(g.num_segments)]
+    a = orc.attention_backward(q, k, v, do, g.cu_q, g.used_q, g.cu_k, g.used_k)
+    b = orc.attention_backward_ranges(q, k, v, do, g.cu_q, g.used_q, prefix)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    total_k = 12
+    k = _rand(rng, total_k, 2, 3)
+    v = _rand(rng, total_k, 2, 3)
+    ranges = [[(0, 4), (2, 3)], [(3, 5)], [(9, 2)]]  # rows 2, 3 twice in segment 0; 3..4 shared
+    sc = 0.9
+    dq, dk, dv = orc.attention_backward_ranges(q, k, v, do, g.cu_q, g.used_q, ranges, scale=sc,
+                                               dk=np.full(k.shape, 4.0), dv=np.full(v.shape, 5.0))
+
+    def loss(qq, kk, vv):
+        o, _ = orc.attention_forward_ranges(qq, kk, vv, g.cu_q, g.used_q, ranges, scale=sc)
+        return float(np.sum(o * do))
+    eps = 1e-6
+    for name, arr, grad, rows in [("q", q, dq, [0, int(g.cu_q[1]), int(g.cu_q[2])]), ("k", k, dk, [0, 2, 3, 4, 9]),
+                                  ("v", v, dv, [2, 3, 7, 10])]:
+        for r in rows:
+            for h in range(arr.shape[1]):
+                for t in range(3):
+                    a_, b_ = arr.copy(), arr.copy()
+                    a_[r, h, t] += eps
+                    b_[r, h, t] -= eps
+                    args_a = {"q": (a_, k, v), "k": (q, a_, v), "v": (q, k, a_)}[name]
+                    args_b = {"q": (b_, k, v), "k": (q, b_, v), "v": (q, k, b_)}[name]
+                    fd = (loss(*args_a) - loss(*args_b)) / (2 * eps)
+                    assert abs(fd - grad[r, h, t]) < 1e-6, (name, r, h, t, fd, grad[r, h, t])
+    assert np.all(dk[[8, 11]] == 4.0) and np.all(dv[[8, 11]] == 5.0)  # rows no range covers
+
+
 PINS = [pin_bruteforce, pin_default_scale, pin_dilution_golden, pin_zero_keys_closed_form,
         pin_single_key, pin_keyless_and_gap_rows, pin_pad_invariance, pin_sdpa_equal_lengths,
         pin_gqa_repeat, pin_key_permutation, pin_merge_union, pin_rows_match, pin_ranges, pin_causal,
-        pin_backward, pin_backward_causal]
+        pin_backward, pin_backward_causal, pin_backward_ranges]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -479,6 +522,8 @@ MUTANTS = {
     "backward_rowless_keys_untouched": ("        if nk > 0:  # a used key", "        if nk > 0 and nq > 0:  # a used key"),
     "backward_causal_mask_dropped": ("                x = np.where(vis, x, -np.inf)\n                mx = np.where(live",
                                      "                x = x\n                mx = np.where(live"),
+    "backward_ranges_overwrite": ("np.add.at(dk_out, (idx, hk), s * (ds.T @ qs))",
+                                  "dk_out[idx, hk] = s * (ds.T @ qs)"),
     "range_end_dropped": ("np.arange(int(st), int(st) + int(n))", "np.arange(int(st), int(st) + int(n) - 1)"),
 }
 
