@@ -116,8 +116,8 @@ void free_plan(struct gva_plan* p) {
 // keys are the ranges range_off[b] .. range_off[b+1] of (range_start, range_len).
 // causal_block > 0 (block-causal, one prefix range per segment): each item only gets the
 // key blocks its last row sees, and FLOPs count the visible keys of every row.
-// backward (one prefix range per segment, so segments' keys are disjoint; maskless or
-// block-causal): also build the dQ items and the dK / dV units.
+// backward (every K/V row in at most one range, so each dK / dV row has one writer;
+// maskless, block-causal or ranges): also build the dQ items and the dK / dV units.
 gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int32_t num_segments,
                       const int32_t* range_off, const int32_t* range_start, const int32_t* range_len,
                       int64_t total_k, int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim,
@@ -413,8 +413,17 @@ gva_status gva_plan_ranges(const int32_t* cu_seqlens_q, const int32_t* seqused_q
       return fail(GVA_ERR_INVALID_ARG, "key range %d = [%lld, %lld) is outside [0, total_k=%lld)", r, (long long)st,
                   (long long)(st + n), (long long)total_k);
   }
+  // The backward needs every K/V row to belong to at most one range (a shared row would
+  // need its dK / dV summed across units): check that the non-empty ranges are disjoint.
+  std::vector<std::pair<int32_t, int32_t>> spans;
+  for (int32_t r = 0; r < num_ranges; ++r)
+    if (key_range_lengths[r] > 0) spans.push_back({key_range_starts[r], key_range_lengths[r]});
+  std::sort(spans.begin(), spans.end());
+  bool disjoint = true;
+  for (size_t i = 1; i < spans.size(); ++i)
+    if (static_cast<int64_t>(spans[i - 1].first) + spans[i - 1].second > spans[i].first) disjoint = false;
   return build_plan(cu_seqlens_q, seqused_q, num_segments, key_range_offsets, key_range_starts, key_range_lengths,
-                    total_k, num_heads_q, num_heads_kv, head_dim, 0, false, out_plan);
+                    total_k, num_heads_q, num_heads_kv, head_dim, 0, disjoint, out_plan);
 }
 
 gva_status gva_forward(gva_plan_t plan, const void* q, const void* k, const void* v, void* out, gva_dtype out_dtype,
@@ -504,7 +513,7 @@ gva_status gva_lse_merge(gva_plan_t plan, int32_t num_parts, const void* const* 
 gva_status gva_backward_workspace_size(gva_plan_t plan, size_t* bytes) {
   if (plan == nullptr || bytes == nullptr) return fail(GVA_ERR_INVALID_ARG, "plan or bytes is NULL");
   if (!plan->backward_ok)
-    return fail(GVA_ERR_UNSUPPORTED, "the backward needs a plan from gva_plan or gva_plan_causal (prefix keys)");
+    return fail(GVA_ERR_UNSUPPORTED, "the backward needs each K/V row in at most one key range of the plan");
   *bytes = static_cast<size_t>(plan->num_heads_q) * static_cast<size_t>(plan->total_q) * sizeof(float);
   return ok();
 }
@@ -515,7 +524,7 @@ gva_status gva_backward(gva_plan_t plan, const void* q, const void* k, const voi
                         cudaStream_t stream) {
   if (plan == nullptr) return fail(GVA_ERR_INVALID_ARG, "plan is NULL");
   if (!plan->backward_ok)
-    return fail(GVA_ERR_UNSUPPORTED, "the backward needs a plan from gva_plan or gva_plan_causal (prefix keys)");
+    return fail(GVA_ERR_UNSUPPORTED, "the backward needs each K/V row in at most one key range of the plan");
   if ((dq_dtype != GVA_BF16 && dq_dtype != GVA_FP32) || (dkv_dtype != GVA_BF16 && dkv_dtype != GVA_FP32))
     return fail(GVA_ERR_INVALID_ARG, "bad gradient dtype");
   if (plan->num_bwd_items == 0 && plan->num_kv_units == 0) return ok();  // no used row and no used key

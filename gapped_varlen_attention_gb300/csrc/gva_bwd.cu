@@ -415,7 +415,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         continue;
       }
       const int64_t li = static_cast<int64_t>(head) * p.total_q + token;
-      int row_limit = it.k_len;  // keys of the segment this row sees
+      // block-causal: keys of the segment this row sees (one prefix range, so block j
+      // holds keys 128 j ..); otherwise every used key of every block
+      int row_limit = 1;
       if constexpr (kCausal) {
         const int pos = it.q_pos0 + tok;
         row_limit = pos < 0 ? 0 : min(it.k_len, (pos / p.causal_block + 1) * p.causal_block);
@@ -424,7 +426,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float lse2 = valid && row_limit > 0 ? p.lse[li] * kLog2e : CUDART_INF_F;
       const float drow = valid ? p.dvec[li] : 0.0f;
       const uint64_t neg_l2 = f32x2(-lse2, -lse2);
+      // used keys of each block, fetched one block ahead (any block of a key range can
+      // be partial)
+      int valid_next = load_block(p.blocks, it.blk0).valid;
       for (int j = 0; j < it.nblk; ++j, ++n) {
+        const int valid_keys = valid_next;
+        if (j + 1 < it.nblk) valid_next = load_block(p.blocks, it.blk0 + j + 1).valid;
         // dP(n) complete implies S(n) complete (issued before it by the same thread)
         ok = __all_sync(0xffffffffu, wait_bar(&ctrl.dp_full, n & 1, abort_flag, p.error_flag));
         if (!ok) break;
@@ -434,9 +441,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_ld64x2_sync(s_addr, sraw, dp_addr, dpr);
         tcgen05_fence_before();
         mbar_arrive(&ctrl.dp_consumed);  // the tensor core may overwrite dP now
-        // keys of this half the row sees: the used keys (only a segment's last block is
-        // partial, one prefix range), capped by the row's block-causal limit
-        const int rem = min(kBlockKeys, row_limit - j * kBlockKeys) - 64 * wg;
+        // keys of this half the row sees: the block's used keys, capped by the row's
+        // block-causal limit (block-causal plans have one prefix range)
+        const int rem = (kCausal ? min(valid_keys, row_limit - j * kBlockKeys) : valid_keys) - 64 * wg;
         if (rem < 64) {  // keys past the used length: P = 0 (uniform over the warp)
 #pragma unroll
           for (int i = 0; i < 64; ++i) sraw[i] = i < rem ? sraw[i] : 0xff800000u;

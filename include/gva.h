@@ -191,7 +191,7 @@ GVA_API gva_status gva_lse_merge(gva_plan_t plan, int32_t num_parts, const void*
  * gva_backward_workspace_size - bytes of device workspace gva_backward needs.
  *
  * Writes Hq * total_q * 4 (one fp32 D value per row and query head) to *bytes. Returns
- * GVA_ERR_UNSUPPORTED for plans from gva_plan_ranges.
+ * GVA_ERR_UNSUPPORTED for a range plan whose ranges overlap (see gva_backward).
  */
 GVA_API gva_status gva_backward_workspace_size(gva_plan_t plan, size_t* bytes);
 
@@ -206,10 +206,11 @@ GVA_API gva_status gva_backward_workspace_size(gva_plan_t plan, size_t* bytes);
  *   dP_ij = <dO_i, V_j>,  D_i = <dO_i, O_i>,  dS_ij = P_ij (dP_ij - D_i)
  *   dQ_i = s sum_j dS_ij K_j
  *   dK_j = s sum_{i, h of the KV group} dS_ij Q_i,   dV_j = sum_{i, h} P_ij dO_i
- * For plans from gva_plan (maskless) and gva_plan_causal (the gradients of the
- * block-causal forward: P is zero past each row's key limit, and a row that sees no key
- * gets dQ = 0); keys must be a prefix of each segment's K/V rows, so plans from
- * gva_plan_ranges are refused with GVA_ERR_UNSUPPORTED.
+ * For plans from gva_plan (maskless), gva_plan_causal (the gradients of the block-causal
+ * forward: P is zero past each row's key limit, and a row that sees no key gets dQ = 0)
+ * and gva_plan_ranges (segment b's keys are its ranges, as in the forward). Every K/V
+ * row must belong to at most one key range of the plan (one writer per dK / dV row): a
+ * range plan whose non-empty ranges overlap is refused with GVA_ERR_UNSUPPORTED.
  *
  *   q, k, v   : DEVICE bf16, as given to gva_forward
  *   out, lse  : DEVICE, the forward's bf16 output [total_q, Hq, d] and fp32 LSE
@@ -224,7 +225,7 @@ GVA_API gva_status gva_backward_workspace_size(gva_plan_t plan, size_t* bytes);
  *
  * Rows written: dq on used rows (zero on the used rows of a keyless segment); dk / dv
  * on each segment's used keys (zero where the segment has no used row). Gap rows and
- * keys past seqused_k are not written; their contents (even NaN) do not affect any
+ * K/V rows outside every segment's keys are not written; their contents (even NaN) do not affect any
  * written value. Every pointer 16-byte aligned; inputs must not alias outputs. No
  * atomics: the result is deterministic. Asynchronous; bounded device waits as for
  * gva_forward (gva_device_status reports a timeout).

@@ -181,11 +181,96 @@ def test_deterministic():
         assert torch.equal(x, y)
 
 
-def test_range_plans_are_refused():
+def test_overlapping_range_plans_are_refused():
+    """A K/V row in two ranges would need its dK / dV summed across units."""
     g = W.tiny()
-    rplan = gva.Plan.from_ranges(g.cu_q, g.used_q, [[(0, 48)], [(48, 33)], []], g.total_k, 4, 2, 64)
+    rplan = gva.Plan.from_ranges(g.cu_q, g.used_q, [[(0, 48)], [(40, 33)], []], g.total_k, 4, 2, 64)
     with pytest.raises(gva.GvaError, match="UNSUPPORTED"):
         gva.backward_workspace_bytes(rplan)
+    ok = gva.Plan.from_ranges(g.cu_q, g.used_q, [[(0, 40)], [(40, 33)], []], g.total_k, 4, 2, 64)
+    assert gva.backward_workspace_bytes(ok) == 4 * g.total_q * 4
+
+
+def _ranges_backward(g, ranges, total_k, q, k, v, do):
+    plan = gva.Plan.from_ranges(g.cu_q, g.used_q, ranges, total_k, g.num_heads_q, g.num_heads_kv, g.head_dim)
+    return gpu_backward(g, q, k, v, do, plan=plan)
+
+
+def _check_ranges(g, ranges, got, q, k, v, do):
+    qn, kn, vn, don = (t.detach().cpu().float().numpy() for t in (q, k, v, do))
+    ref = gva_oracle.attention_backward_ranges(qn, kn, vn, don, g.cu_q, g.used_q, ranges,
+                                               dq=np.full(qn.shape, FILL), dk=np.full(kn.shape, FILL),
+                                               dv=np.full(vn.shape, FILL))
+    dq, dk, dv = (t.float().cpu().numpy().astype(np.float64) for t in got)
+    dq_rows = ~W.gap_rows(g.cu_q, g.used_q)
+    covered = np.zeros(kn.shape[0], bool)
+    for rr in ranges:
+        for st, n in rr:
+            covered[st:st + n] = True
+    fill32 = np.float64(np.float32(FILL))
+    assert np.all(dq[~dq_rows] == fill32) and np.all(dk[~covered] == fill32) and np.all(dv[~covered] == fill32)
+    for b, rr in enumerate(ranges):  # exact zeros: keyless segments' rows, row-less segments' keys
+        if g.used_q[b] and not sum(n for _, n in rr):
+            assert np.all(dq[g.cu_q[b]:g.cu_q[b] + g.used_q[b]] == 0.0)
+        if not g.used_q[b]:
+            for st, n in rr:
+                assert np.all(dk[st:st + n] == 0.0) and np.all(dv[st:st + n] == 0.0)
+    _close("dQ", dq[dq_rows], ref[0][dq_rows])
+    _close("dK", dk[covered], ref[1][covered])
+    _close("dV", dv[covered], ref[2][covered])
+
+
+@pytest.mark.parametrize("hq,hkv,d,seed", [(8, 2, 128, 801), (16, 16, 64, 802), (32, 8, 128, 803)])
+def test_disjoint_key_ranges(hq, hkv, d, seed):
+    """Up to four disjoint ranges per segment anywhere in K/V (ragged lengths, empty
+    ranges, partial blocks in the middle of a segment's keys); rows no range covers are
+    NaN and must stay untouched."""
+    rng = np.random.default_rng(seed)
+    g = W.random_geometry(rng, 5, 500, 10, hq, hkv, d)
+    total_k = 3000
+    cuts = np.sort(rng.choice(np.arange(1, total_k), size=2 * 4 * g.num_segments, replace=False))
+    pieces = [(int(cuts[2 * i]), int(cuts[2 * i + 1] - cuts[2 * i])) for i in range(len(cuts) // 2)]
+    rng.shuffle(pieces)
+    ranges = []
+    for b in range(g.num_segments):
+        take = int(rng.integers(0, 5))
+        ranges.append([(st, min(n, 400)) for st, n in pieces[:take]])
+        pieces = pieces[take:]
+    ranges[0] = []  # one keyless segment
+    gen = torch.Generator().manual_seed(seed)
+    q = torch.randn(g.total_q, hq, d, generator=gen).bfloat16()
+    k = torch.randn(total_k, hkv, d, generator=gen).bfloat16()
+    v = torch.randn(total_k, hkv, d, generator=gen).bfloat16()
+    do = _make_dout(g, seed)
+    covered = np.zeros(total_k, bool)
+    for rr in ranges:
+        for st, n in rr:
+            covered[st:st + n] = True
+    k[torch.from_numpy(~covered)] = float("nan")
+    v[torch.from_numpy(~covered)] = float("nan")
+    _check_ranges(g, ranges, _ranges_backward(g, ranges, total_k, q, k, v, do), q, k, v, do)
+
+
+def test_rank_major_keys_backward():
+    """Keys in the rank-major order an all-to-all leaves (per rank: a text chunk, then a
+    video chunk): each sample attends its text length of every text chunk plus all video
+    keys; the zero pads of the text chunks are in no range and stay untouched."""
+    ranks, text_cap, video = 4, 64, 384
+    text_len = [[37, 64, 5, 0], [64, 64, 64, 12]]
+    hq, hkv, d = 16, 8, 128
+    cu_q = np.array([0, 1000, 2000], np.int32)
+    g = W.Geometry(cu_q, np.array([1000, 777], np.int32), np.array([0, 0, 0], np.int32), np.array([0, 0], np.int32),
+                   hq, hkv, d)
+    chunk = text_cap + video
+    total_k = 2 * ranks * chunk
+    ranges = [[x for r in range(ranks) for x in (((b * ranks + r) * chunk, text_len[b][r]),
+                                                 ((b * ranks + r) * chunk + text_cap, video))] for b in range(2)]
+    gen = torch.Generator().manual_seed(811)
+    q = torch.randn(g.total_q, hq, d, generator=gen).bfloat16()
+    k = torch.randn(total_k, hkv, d, generator=gen).bfloat16()
+    v = torch.randn(total_k, hkv, d, generator=gen).bfloat16()
+    do = _make_dout(g, 811)
+    _check_ranges(g, ranges, _ranges_backward(g, ranges, total_k, q, k, v, do), q, k, v, do)
 
 
 CAUSAL_CASES = [  # (Hq, Hkv, d, causal block, seed)
