@@ -115,6 +115,15 @@ class Workload:
             self.label = ("backward (dQ, dK, dV) of the long joint video+LiDAR replay: 4 segments x 32768 q rows "
                           "(used 60-100%) x 65536 keys (used 50-100%), Hq=32, Hkv=8, d=128, bf16; FLOPs = 2.5 x "
                           "the forward's (five used-row products)")
+        elif name == "multiview_fused_bwd":
+            full, parts = W.multiview_causal()
+            self.geoms = [full]
+            self.q, self.k, self.v = W.make_qkv(full, 1003 + seed_offset, device=dev)
+            self.parts = None
+            self.ranges = [[(int(p.cu_k[b]), int(p.used_k[b])) for p in parts] for b in range(full.num_segments)]
+            self.backward = True
+            self.label = ("backward of the multiview causal gapped replay with its 2 visibility partitions as two "
+                          "key ranges per segment of one plan")
         elif name == "multiview_blockcausal_bwd":
             full, _ = W.multiview_causal()
             self.geoms = [full]
@@ -456,7 +465,7 @@ def main():
     ap.add_argument("--workload", default="long_replay",
                     choices=["long_replay", "long_replay_small", "cfg_text_cross", "multiview_causal",
                              "multiview_fused", "multiview_blockcausal", "long_replay_bwd", "long_replay_small_bwd",
-                             "multiview_blockcausal_bwd", "tiny"])
+                             "multiview_blockcausal_bwd", "multiview_fused_bwd", "tiny"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     args = ap.parse_args()
@@ -606,7 +615,7 @@ def run_reference(args, world, rank):
         g = W.cfg_text_cross()
         wl.geoms = [g]
         seed = 1002
-    elif args.workload in ("multiview_causal", "multiview_fused"):
+    elif args.workload in ("multiview_causal", "multiview_fused", "multiview_fused_bwd"):
         g, parts = W.multiview_causal()
         wl.geoms = parts
         seed = 1003
@@ -625,7 +634,8 @@ def run_reference(args, world, rank):
         seed = 1001
     wl.q, wl.k, wl.v = W.make_qkv(g, seed)
     metric = METRIC
-    if args.workload in ("long_replay_bwd", "long_replay_small_bwd", "multiview_blockcausal_bwd"):
+    if args.workload in ("long_replay_bwd", "long_replay_small_bwd", "multiview_blockcausal_bwd",
+                         "multiview_fused_bwd"):
         wl.backward = True
         wl.d_out = torch.randn(wl.q.shape, generator=torch.Generator().manual_seed(2005)).bfloat16()
         metric = "gapped-varlen attn bwd TFLOP/s (used rows, 2.5 x fwd FLOPs) & % of GB300 BF16 peak"
