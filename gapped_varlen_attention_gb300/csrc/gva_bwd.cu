@@ -17,13 +17,14 @@
 //      segment's Q / dO tiles: S^T = K Q^T and dP^T = V dO^T into TMEM, P^T and dS^T by
 //      the compute threads, dV += P^T dO and dK += dS^T Q accumulated in TMEM, then
 //      written once. No atomics anywhere.
-// In both kernels the 128 score columns of a block are two halves of 64, each with its
-// own warpgroup of compute threads (one TMEM lane each) and its own full / ready
-// barriers. The MMA thread runs one half ahead: while one warpgroup turns its half of
-// S and dP into P and dS, the tensor core computes the other half's products, so the
-// exponentials and the matrix products overlap instead of alternating.
-// Operand rows past the used lengths (gaps, padding, possibly NaN) are zeroed in shared
-// memory before an MMA could multiply them by a zero weight.
+// Both kernels run two warpgroups of compute threads (one TMEM lane each), each on one
+// 64-column half of a block's scores, and keep the tensor core busy while they work:
+// the dQ kernel double-buffers S in TMEM and hands dP back as soon as it sits in
+// registers, so block m+1's products run during block m's exponentials; the dK/dV
+// kernel, whose TMEM is full (S^T, dP^T and both accumulators), issues the products per
+// half and runs one half ahead. Operand rows past the used lengths (gaps, padding,
+// possibly NaN) are zeroed in shared memory before an MMA could multiply them by a zero
+// weight. Block-causal plans take separate kCausal instantiations.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -50,8 +51,8 @@ struct BCfg {
   static_assert(kSmemDq <= 227 * 1024 && kSmemDkv <= 227 * 1024, "shared memory budget");
 };
 
-// Zero the 128-byte rows `rows` of a 128-row tile (all column chunks); the swizzle only
-// permutes 16-byte pieces within a row, so whole rows are cleared position-free.
+// Zero row `row` of a 128-row tile (its 128-byte piece in every column chunk); the
+// swizzle only permutes 16-byte pieces within a row, so a whole row clears in place.
 template <int D>
 __device__ __forceinline__ void zero_tile_row(uint8_t* tile, int row) {
 #pragma unroll
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(256) gva_bwd_dvec_kernel(const MergeUnit* unit
   }
 }
 
-// Half-block products (N = 64 of the 128 rows of the B tile).
+// Half-block products of the dK/dV kernel (N = 64 of the 128 rows of the B tile).
 // D[128 x 64] = A[128 x D] B[rows 64h .. 64h + 63]^T, both K-major.
 template <int D>
 __device__ __forceinline__ void issue_qk_half(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc, int h) {
