@@ -80,7 +80,9 @@ struct BwdCtrl {
   uint64_t a_full, a_empty;            // K + V blocks
   uint64_t r_full[2], r_empty[2];      // Q / dO slots
   uint64_t zero_bar;                   // partial tiles: the producer's own copy wait
-  uint64_t s_full[2], p_full[2];       // per column half: products ready / P, dS ready
+  uint64_t s_full, s_consumed;         // S^T ready; S^T read into registers (256 threads)
+  uint64_t dp_full;                    // dP^T ready
+  uint64_t p_full[2];                  // per column half: P^T, dS^T in TMEM
   uint64_t acc_full, mma_done;
   uint32_t tmem_base;
   int abort;
@@ -125,9 +127,11 @@ __device__ __forceinline__ void init_ctrl(BwdCtrl& c) {
   for (int i = 0; i < 2; ++i) {
     mbar_init(&c.r_full[i], 1);
     mbar_init(&c.r_empty[i], 1);
-    mbar_init(&c.s_full[i], 1);
     mbar_init(&c.p_full[i], kTileRows);
   }
+  mbar_init(&c.s_full, 1);
+  mbar_init(&c.s_consumed, 2 * kTileRows);
+  mbar_init(&c.dp_full, 1);
   mbar_init(&c.zero_bar, 1);
   mbar_init(&c.acc_full, 1);
   mbar_init(&c.mma_done, 1);
@@ -175,19 +179,6 @@ __global__ void __launch_bounds__(256) gva_bwd_dvec_kernel(const MergeUnit* unit
       acc += __shfl_xor_sync(0xffffffffu, acc, 4);
       if (live && sub == 0) dvec[static_cast<int64_t>(h) * total_q + row] = acc;
     }
-  }
-}
-
-// Half-block products of the dK/dV kernel (N = 64 of the 128 rows of the B tile).
-// D[128 x 64] = A[128 x D] B[rows 64h .. 64h + 63]^T, both K-major.
-template <int D>
-__device__ __forceinline__ void issue_qk_half(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc, int h) {
-  constexpr uint32_t idesc = make_idesc_bf16(kTileRows, 64, false);
-  const uint64_t b = b_desc + static_cast<uint64_t>(h) * ((64 * 128) >> 4);
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = ((kk / 4) * kChunkBytes + (kk % 4) * 32) >> 4;
-    umma_bf16_ss(tmem_d, a_desc + off, b + off, idesc, kk > 0);
   }
 }
 
@@ -522,8 +513,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int T = p.tokens_per_tile;
   const int G = p.group;
   // TMEM: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [384,384+D). Column half h
-  // (Q-tile rows 64h .. 64h+63) of S^T / dP^T is [64h, +64) / [128+64h, +64); its P^T
-  // and dS^T (bf16 pairs) overwrite [64h, +32) and [128+64h, +32).
+  // (Q-tile rows 64h .. 64h+63) of S^T / dP^T is [64h, +64) / [128+64h, +64). Its P^T
+  // and dS^T (bf16 pairs) go to [128+64h, +32) and [160+64h, +32), columns of dP^T that
+  // only warpgroup h reads, so S^T is free as soon as it sits in registers and the next
+  // tile's S^T runs while this tile is exponentiated.
   constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
   // Q tiles of the unit: from the first one that sees the block (block-causal) to the end
   auto n_tiles = [&](const KvUnit& u) { return (u.q_used + T - 1) / T - u.tile0; };
@@ -616,14 +609,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      // Per Q tile i: S^T / dP^T of half 0 and half 1, then dV, dK of half 0, the next
-      // tile's half-0 products, dV, dK of half 1, the next tile's half-1 products.
+      // Pipe order per tile t: dP^T(t), S^T(t+1) (once the compute threads hold S^T(t)),
+      // dV += P^T dO and dK += dS^T Q for tile t per column half, dP^T(t+1), ... so the
+      // products of the next tile run while this one is exponentiated.
       const uint64_t k_desc = make_smem_desc_sw128(smem_addr(sK), 16, 1024);
       const uint64_t v_desc = make_smem_desc_sw128(smem_addr(sV), 16, 1024);
       const uint64_t slot_k0 = make_smem_desc_sw128(smem_addr(sSlots), 16, 1024);            // K-major
       const uint64_t slot_mn0 = make_smem_desc_sw128(smem_addr(sSlots), kChunkBytes, 1024);  // MN-major B
       constexpr uint64_t kTileUnits = C::kTileBytes >> 4;
-      uint32_t kv_it = 0, qi = 0;
+      uint32_t kv_it = 0, qi = 0;  // qi: Q tiles so far (global tile counter t)
       uint32_t pc[2] = {0, 0};
       bool ok = true;
       auto wait_tile = [&](uint32_t t) {
@@ -631,11 +625,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (r) tcgen05_fence_after();
         return r;
       };
-      auto products = [&](uint32_t t, int h) {  // S^T and dP^T of half h of tile t
-        const uint64_t qk = slot_k0 + (t & 1) * 2 * kTileUnits;
-        issue_qk_half<D>(tmem + kColS + 64 * h, k_desc, qk, h);
-        issue_qk_half<D>(tmem + kColDP + 64 * h, v_desc, qk + kTileUnits, h);
-        umma_commit(&ctrl.s_full[h]);
+      auto issue_s = [&](uint32_t t) {  // S^T(t) = K Q_t^T
+        issue_qk<D>(tmem + kColS, k_desc, slot_k0 + (t & 1) * 2 * kTileUnits);
+        umma_commit(&ctrl.s_full);
+      };
+      auto issue_dp = [&](uint32_t t) {  // dP^T(t) = V dO_t^T (after tile t-1's dV / dK read dP^T)
+        issue_qk<D>(tmem + kColDP, v_desc, slot_k0 + (t & 1) * 2 * kTileUnits + kTileUnits);
+        umma_commit(&ctrl.dp_full);
       };
       for (int round = 0; ok; ++round) {
         const int idx = item_index(round, blockIdx.x, gridDim.x);
@@ -647,36 +643,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (ok) ok = wait_tile(qi);
         if (!ok) break;
         ++kv_it;
-        products(qi, 0);
-        products(qi, 1);
+        issue_s(qi);  // S^T is free: every tile's S^T was read before its P^T / dS^T existed
+        issue_dp(qi);
         if (nqt == 1) umma_commit(&ctrl.a_empty);  // K, V read
         for (int i = 0; i < nqt; ++i) {
           const uint32_t t = qi + i;
           const bool more = i + 1 < nqt;
-          const uint64_t qmn = slot_mn0 + (t & 1) * 2 * kTileUnits, domn = qmn + kTileUnits;
-          ok = wait_bar(&ctrl.p_full[0], pc[0] & 1, abort_flag, p.error_flag);
-          // the first products overwrite dV / dK: both warpgroups must have finished
-          // reading the previous unit's accumulators (they arrive after their epilogue)
-          if (ok && i == 0) ok = wait_bar(&ctrl.p_full[1], pc[1] & 1, abort_flag, p.error_flag);
-          if (!ok) break;
-          ++pc[0];
-          tcgen05_fence_after();
-          issue_pv_half<D>(tmem + kColDV, tmem + kColS, domn, 0, i > 0);   // dV += P^T dO
-          issue_pv_half<D>(tmem + kColDK, tmem + kColDP, qmn, 0, i > 0);   // dK += dS^T Q
-          if (more) {
+          ok = wait_bar(&ctrl.s_consumed, t & 1, abort_flag, p.error_flag);  // S^T(t) in registers
+          if (ok && more) {
             ok = wait_tile(t + 1);
-            if (!ok) break;
-            products(t + 1, 0);
+            if (ok) issue_s(t + 1);
           }
-          if (i > 0) ok = wait_bar(&ctrl.p_full[1], pc[1] & 1, abort_flag, p.error_flag);
           if (!ok) break;
-          ++pc[1];
-          tcgen05_fence_after();
-          issue_pv_half<D>(tmem + kColDV, tmem + kColS + 64, domn, 1, 1u);
-          issue_pv_half<D>(tmem + kColDK, tmem + kColDP + 64, qmn, 1, 1u);
+          const uint64_t qmn = slot_mn0 + (t & 1) * 2 * kTileUnits, domn = qmn + kTileUnits;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            // the unit's first products overwrite dV / dK: both warpgroups must be done
+            // reading the previous unit's accumulators (they arrive after their epilogue)
+            ok = wait_bar(&ctrl.p_full[h], pc[h] & 1, abort_flag, p.error_flag);
+            if (ok && i == 0 && h == 0) ok = wait_bar(&ctrl.p_full[1], pc[1] & 1, abort_flag, p.error_flag);
+            if (!ok) break;
+            ++pc[h];
+            tcgen05_fence_after();
+            const uint32_t acc = (i > 0 || h > 0) ? 1u : 0u;
+            issue_pv_half<D>(tmem + kColDV, tmem + kColDP + 64 * h, domn, h, acc);       // dV += P^T dO
+            issue_pv_half<D>(tmem + kColDK, tmem + kColDP + 64 * h + 32, qmn, h, acc);  // dK += dS^T Q
+          }
+          if (!ok) break;
           umma_commit(&ctrl.r_empty[t & 1]);
           if (more) {
-            products(t + 1, 1);
+            issue_dp(t + 1);
             if (i + 2 == nqt) umma_commit(&ctrl.a_empty);
           }
         }
@@ -745,65 +741,98 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if constexpr (kCausal) ctrl.xlim[par][lrow] = nlim;
           if (i + 1 < nqt) fetch(i + 1, nxl, nxd, nlim);
         }
-        const bool fine = __all_sync(0xffffffffu, wait_bar(&ctrl.s_full[wg], sc & 1, abort_flag, p.error_flag));
-        ++sc;
+        const bool fine = __all_sync(0xffffffffu, wait_bar(&ctrl.s_full, sc & 1, abort_flag, p.error_flag));
         if (named_barrier_or(1 + wg, 128, !fine)) {
           ok = false;
           break;
         }
         tcgen05_fence_after();
-        // 16-lane TMEM shapes: each thread handles 4 keys (lanes) x 8 columns per part,
-        // so it needs the LSE / D of only 8 columns (two per 8-column group).
+        // 16-lane TMEM shapes: each thread handles 4 keys (lanes) x 16 columns of its
+        // half (8 per part), so it needs the LSE / D / limit of only 16 Q rows.
         const float* xl = &ctrl.xl[par][64 * wg];
         const float* xd = &ctrl.xd[par][64 * wg];
+        const uint64_t c2 = f32x2(c, c);
+        uint32_t sr[2][2][16];  // [part][lane half][register]
+        {
+          const uint32_t col = kColS + 64 * wg;
+          tmem_ld16x256b_x4_quad_sync(tmem_addr(tmem, lane_base, col), sr[0][0], tmem_addr(tmem, lane_base + 16, col),
+                                      sr[0][1], tmem_addr(tmem, lane_base, col + 32), sr[1][0],
+                                      tmem_addr(tmem, lane_base + 16, col + 32), sr[1][1]);
+        }
+        tcgen05_fence_before();
+        mbar_arrive(&ctrl.s_consumed);  // the tensor core may write the next S^T
+        // P^T = 2^(S^T c - lse2), kept as fp32 pairs in the same registers
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-          float2 l2[4], d2[4];
-          int2 m2[4];  // block-causal: the columns' key limits
+        for (int part = 0; part < 2; ++part)
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            l2[k] = *reinterpret_cast<const float2*>(xl + 32 * part + 8 * k + 2 * c4);
-            d2[k] = *reinterpret_cast<const float2*>(xd + 32 * part + 8 * k + 2 * c4);
-            if constexpr (kCausal)
-              m2[k] = *reinterpret_cast<const int2*>(&ctrl.xlim[par][64 * wg + 32 * part + 8 * k + 2 * c4]);
-          }
+        for (int k = 0; k < 4; ++k) {
+          const float2 l2 = *reinterpret_cast<const float2*>(xl + 32 * part + 8 * k + 2 * c4);
+          const uint64_t nl2 = f32x2(-l2.x, -l2.y);
+          int2 m2 = make_int2(0x7fffffff, 0x7fffffff);
+          if constexpr (kCausal)
+            m2 = *reinterpret_cast<const int2*>(&ctrl.xlim[par][64 * wg + 32 * part + 8 * k + 2 * c4]);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const int lane0 = lane_base + 16 * h;
-            uint32_t sr[16], dr[16];
-            tmem_ld16x256b_x4_pair_sync(tmem_addr(tmem, lane0, kColS + 64 * wg + 32 * part), sr,
-                                        tmem_addr(tmem, lane0, kColDP + 64 * wg + 32 * part), dr);
-            const bool va = lane0 + g < u.keys;      // key of registers 4k, 4k+1
-            const bool vb = lane0 + g + 8 < u.keys;  // key of registers 4k+2, 4k+3
-            uint32_t pp[8], pd[8];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              float p0 = ex2_approx(fmaf(__uint_as_float(sr[4 * k + 0]), c, -l2[k].x));
-              float p1 = ex2_approx(fmaf(__uint_as_float(sr[4 * k + 1]), c, -l2[k].y));
-              float p2 = ex2_approx(fmaf(__uint_as_float(sr[4 * k + 2]), c, -l2[k].x));
-              float p3 = ex2_approx(fmaf(__uint_as_float(sr[4 * k + 3]), c, -l2[k].y));
-              float s0 = p0 * (__uint_as_float(dr[4 * k + 0]) - d2[k].x);
-              float s1 = p1 * (__uint_as_float(dr[4 * k + 1]) - d2[k].y);
-              float s2 = p2 * (__uint_as_float(dr[4 * k + 2]) - d2[k].x);
-              float s3 = p3 * (__uint_as_float(dr[4 * k + 3]) - d2[k].y);
-              if (!va) p0 = p1 = s0 = s1 = 0.0f;
-              if (!vb) p2 = p3 = s2 = s3 = 0.0f;
-              if constexpr (kCausal) {  // keys at or past a row's limit: P = dS = 0
-                const int ka = u.key_pos0 + lane0 + g, kb = ka + 8;
-                if (ka >= m2[k].x) p0 = s0 = 0.0f;
-                if (ka >= m2[k].y) p1 = s1 = 0.0f;
-                if (kb >= m2[k].x) p2 = s2 = 0.0f;
-                if (kb >= m2[k].y) p3 = s3 = 0.0f;
-              }
-              pp[2 * k] = pack_bf16x2(p0, p1);
-              pp[2 * k + 1] = pack_bf16x2(p2, p3);
-              pd[2 * k] = pack_bf16x2(s0, s1);
-              pd[2 * k + 1] = pack_bf16x2(s2, s3);
-            }
-            tmem_st16x128b_x4(tmem_addr(tmem, lane0, kColS + 64 * wg + 16 * part), pp);   // P^T pairs
-            tmem_st16x128b_x4(tmem_addr(tmem, lane0, kColDP + 64 * wg + 16 * part), pd);  // dS^T pairs
+            const int ka = lane_base + 16 * h + g, kb = ka + 8;  // keys of registers 4k,4k+1 / 4k+2,4k+3
+            const bool va = ka < u.keys, vb = kb < u.keys;
+            const int pa = kCausal ? u.key_pos0 + ka : 0, pb = kCausal ? u.key_pos0 + kb : 0;
+            uint32_t* sv = &sr[part][h][4 * k];
+            float x0, x1, x2, x3;
+            f32x2_split(ffma2(f32x2(__uint_as_float(sv[0]), __uint_as_float(sv[1])), c2, nl2), x0, x1);
+            f32x2_split(ffma2(f32x2(__uint_as_float(sv[2]), __uint_as_float(sv[3])), c2, nl2), x2, x3);
+            sv[0] = __float_as_uint(va && pa < m2.x ? ex2_approx(x0) : 0.0f);
+            sv[1] = __float_as_uint(va && pa < m2.y ? ex2_approx(x1) : 0.0f);
+            sv[2] = __float_as_uint(vb && pb < m2.x ? ex2_approx(x2) : 0.0f);
+            sv[3] = __float_as_uint(vb && pb < m2.y ? ex2_approx(x3) : 0.0f);
           }
         }
+        ok = __all_sync(0xffffffffu, wait_bar(&ctrl.dp_full, sc & 1, abort_flag, p.error_flag));
+        ++sc;
+        if (named_barrier_or(1 + wg, 128, !ok)) {
+          ok = false;
+          break;
+        }
+        tcgen05_fence_after();
+        // dS^T = P^T (dP^T - D). P^T pairs go to [128+64wg, +32), over part 0's dP^T
+        // columns (each piece after that part is read); dS^T pairs go to [160+64wg, +32),
+        // over part 1's, so they are stored once both parts are read.
+        uint32_t pd[2][2][8];  // [part][lane half][register]
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          uint32_t dr[2][16];  // [lane half][register] of this part
+          const uint32_t col = kColDP + 64 * wg + 32 * part;
+          tmem_ld16x256b_x4_pair_sync(tmem_addr(tmem, lane_base, col), dr[0], tmem_addr(tmem, lane_base + 16, col),
+                                      dr[1]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pp[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float2 d2 = *reinterpret_cast<const float2*>(xd + 32 * part + 8 * k + 2 * c4);
+              const uint64_t nd2 = f32x2(-d2.x, -d2.y);
+              const uint32_t* pv = &sr[part][h][4 * k];
+              const uint32_t* dv4 = &dr[h][4 * k];
+              const uint64_t p01 = f32x2(__uint_as_float(pv[0]), __uint_as_float(pv[1]));
+              const uint64_t p23 = f32x2(__uint_as_float(pv[2]), __uint_as_float(pv[3]));
+              float s0, s1, s2, s3;
+              f32x2_split(ffma2(p01, fadd2(f32x2(__uint_as_float(dv4[0]), __uint_as_float(dv4[1])), nd2), 0ull),
+                          s0, s1);
+              f32x2_split(ffma2(p23, fadd2(f32x2(__uint_as_float(dv4[2]), __uint_as_float(dv4[3])), nd2), 0ull),
+                          s2, s3);
+              pp[2 * k] = pack_bf16x2(__uint_as_float(pv[0]), __uint_as_float(pv[1]));
+              pp[2 * k + 1] = pack_bf16x2(__uint_as_float(pv[2]), __uint_as_float(pv[3]));
+              pd[part][h][2 * k] = pack_bf16x2(s0, s1);
+              pd[part][h][2 * k + 1] = pack_bf16x2(s2, s3);
+            }
+            tmem_st16x128b_x4(tmem_addr(tmem, lane_base + 16 * h, kColDP + 64 * wg + 16 * part), pp);  // P^T
+          }
+        }
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            tmem_st16x128b_x4(tmem_addr(tmem, lane_base + 16 * h, kColDP + 64 * wg + 32 + 16 * part),
+                              pd[part][h]);  // dS^T
         tmem_wait_st();
         tcgen05_fence_before();
         mbar_arrive(&ctrl.p_full[wg]);
