@@ -80,9 +80,8 @@ struct BwdCtrl {
   uint64_t a_full, a_empty;            // K + V blocks
   uint64_t r_full[2], r_empty[2];      // Q / dO slots
   uint64_t zero_bar;                   // partial tiles: the producer's own copy wait
-  uint64_t s_full, s_consumed;         // S^T ready; S^T read into registers (256 threads)
-  uint64_t dp_full;                    // dP^T ready
-  uint64_t p_full[2];                  // per column half: P^T, dS^T in TMEM
+  uint64_t s_full, dp_full;            // S^T ready; dP^T ready
+  uint64_t p_full[2], ds_full[2];      // per column half: P^T in TMEM; dS^T in TMEM
   uint64_t acc_full, mma_done;
   uint32_t tmem_base;
   int abort;
@@ -128,9 +127,9 @@ __device__ __forceinline__ void init_ctrl(BwdCtrl& c) {
     mbar_init(&c.r_full[i], 1);
     mbar_init(&c.r_empty[i], 1);
     mbar_init(&c.p_full[i], kTileRows);
+    mbar_init(&c.ds_full[i], kTileRows);
   }
   mbar_init(&c.s_full, 1);
-  mbar_init(&c.s_consumed, 2 * kTileRows);
   mbar_init(&c.dp_full, 1);
   mbar_init(&c.zero_bar, 1);
   mbar_init(&c.acc_full, 1);
@@ -513,10 +512,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int T = p.tokens_per_tile;
   const int G = p.group;
   // TMEM: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [384,384+D). Column half h
-  // (Q-tile rows 64h .. 64h+63) of S^T / dP^T is [64h, +64) / [128+64h, +64). Its P^T
-  // and dS^T (bf16 pairs) go to [128+64h, +32) and [160+64h, +32), columns of dP^T that
-  // only warpgroup h reads, so S^T is free as soon as it sits in registers and the next
-  // tile's S^T runs while this tile is exponentiated.
+  // (Q-tile rows 64h .. 64h+63) of S^T / dP^T is [64h, +64) / [128+64h, +64); its P^T
+  // (bf16 pairs) overwrites [64h, +32) and its dS^T [128+64h, +32). P^T is ready before
+  // dS^T, so dV += P^T dO runs while the compute threads still form dS^T; the next S^T
+  // follows the dV products and the next dP^T the dK products.
   constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
   // Q tiles of the unit: from the first one that sees the block (block-causal) to the end
   auto n_tiles = [&](const KvUnit& u) { return (u.q_used + T - 1) / T - u.tile0; };
@@ -609,27 +608,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      // Pipe order per tile t: dP^T(t), S^T(t+1) (once the compute threads hold S^T(t)),
-      // dV += P^T dO and dK += dS^T Q for tile t per column half, dP^T(t+1), ... so the
-      // products of the next tile run while this one is exponentiated.
+      // Pipe order per tile t: dV(t) per half as its P^T lands, S^T(t+1), dK(t) per half
+      // as its dS^T lands, dP^T(t+1); the exponentials of tile t+1 and the dS^T of tile t
+      // overlap these products.
       const uint64_t k_desc = make_smem_desc_sw128(smem_addr(sK), 16, 1024);
       const uint64_t v_desc = make_smem_desc_sw128(smem_addr(sV), 16, 1024);
       const uint64_t slot_k0 = make_smem_desc_sw128(smem_addr(sSlots), 16, 1024);            // K-major
       const uint64_t slot_mn0 = make_smem_desc_sw128(smem_addr(sSlots), kChunkBytes, 1024);  // MN-major B
       constexpr uint64_t kTileUnits = C::kTileBytes >> 4;
       uint32_t kv_it = 0, qi = 0;  // qi: Q tiles so far (global tile counter t)
-      uint32_t pc[2] = {0, 0};
+      uint32_t pc[2] = {0, 0}, dc[2] = {0, 0};
       bool ok = true;
       auto wait_tile = [&](uint32_t t) {
         const bool r = wait_bar(&ctrl.r_full[t & 1], (t >> 1) & 1, abort_flag, p.error_flag);
         if (r) tcgen05_fence_after();
         return r;
       };
-      auto issue_s = [&](uint32_t t) {  // S^T(t) = K Q_t^T
+      auto issue_s = [&](uint32_t t) {  // S^T(t) = K Q_t^T (after tile t-1's dV read P^T)
         issue_qk<D>(tmem + kColS, k_desc, slot_k0 + (t & 1) * 2 * kTileUnits);
         umma_commit(&ctrl.s_full);
       };
-      auto issue_dp = [&](uint32_t t) {  // dP^T(t) = V dO_t^T (after tile t-1's dV / dK read dP^T)
+      auto issue_dp = [&](uint32_t t) {  // dP^T(t) = V dO_t^T (after tile t-1's dK read dS^T)
         issue_qk<D>(tmem + kColDP, v_desc, slot_k0 + (t & 1) * 2 * kTileUnits + kTileUnits);
         umma_commit(&ctrl.dp_full);
       };
@@ -643,21 +642,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (ok) ok = wait_tile(qi);
         if (!ok) break;
         ++kv_it;
-        issue_s(qi);  // S^T is free: every tile's S^T was read before its P^T / dS^T existed
+        issue_s(qi);
         issue_dp(qi);
         if (nqt == 1) umma_commit(&ctrl.a_empty);  // K, V read
         for (int i = 0; i < nqt; ++i) {
           const uint32_t t = qi + i;
           const bool more = i + 1 < nqt;
-          ok = wait_bar(&ctrl.s_consumed, t & 1, abort_flag, p.error_flag);  // S^T(t) in registers
-          if (ok && more) {
-            ok = wait_tile(t + 1);
-            if (ok) issue_s(t + 1);
-          }
-          if (!ok) break;
           const uint64_t qmn = slot_mn0 + (t & 1) * 2 * kTileUnits, domn = qmn + kTileUnits;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+          for (int h = 0; h < 2; ++h) {  // dV += P^T dO
             // the unit's first products overwrite dV / dK: both warpgroups must be done
             // reading the previous unit's accumulators (they arrive after their epilogue)
             ok = wait_bar(&ctrl.p_full[h], pc[h] & 1, abort_flag, p.error_flag);
@@ -665,9 +658,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (!ok) break;
             ++pc[h];
             tcgen05_fence_after();
-            const uint32_t acc = (i > 0 || h > 0) ? 1u : 0u;
-            issue_pv_half<D>(tmem + kColDV, tmem + kColDP + 64 * h, domn, h, acc);       // dV += P^T dO
-            issue_pv_half<D>(tmem + kColDK, tmem + kColDP + 64 * h + 32, qmn, h, acc);  // dK += dS^T Q
+            issue_pv_half<D>(tmem + kColDV, tmem + kColS + 64 * h, domn, h, (i > 0 || h > 0) ? 1u : 0u);
+          }
+          if (ok && more) {
+            ok = wait_tile(t + 1);
+            if (ok) issue_s(t + 1);
+          }
+          if (!ok) break;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {  // dK += dS^T Q
+            ok = wait_bar(&ctrl.ds_full[h], dc[h] & 1, abort_flag, p.error_flag);
+            if (!ok) break;
+            ++dc[h];
+            tcgen05_fence_after();
+            issue_pv_half<D>(tmem + kColDK, tmem + kColDP + 64 * h, qmn, h, (i > 0 || h > 0) ? 1u : 0u);
           }
           if (!ok) break;
           umma_commit(&ctrl.r_empty[t & 1]);
@@ -759,8 +763,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                       sr[0][1], tmem_addr(tmem, lane_base, col + 32), sr[1][0],
                                       tmem_addr(tmem, lane_base + 16, col + 32), sr[1][1]);
         }
-        tcgen05_fence_before();
-        mbar_arrive(&ctrl.s_consumed);  // the tensor core may write the next S^T
         // P^T = 2^(S^T c - lse2), kept as fp32 pairs in the same registers
 #pragma unroll
         for (int part = 0; part < 2; ++part)
@@ -786,6 +788,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             sv[3] = __float_as_uint(vb && pb < m2.y ? ex2_approx(x3) : 0.0f);
           }
         }
+        // P^T pairs over this half's first 32 columns of S^T (already read)
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pp[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t* pv = &sr[part][h][4 * k];
+              pp[2 * k] = pack_bf16x2(__uint_as_float(pv[0]), __uint_as_float(pv[1]));
+              pp[2 * k + 1] = pack_bf16x2(__uint_as_float(pv[2]), __uint_as_float(pv[3]));
+            }
+            tmem_st16x128b_x4(tmem_addr(tmem, lane_base + 16 * h, kColS + 64 * wg + 16 * part), pp);
+          }
+        tmem_wait_st();
+        tcgen05_fence_before();
+        mbar_arrive(&ctrl.p_full[wg]);  // dV += P^T dO may start
         ok = __all_sync(0xffffffffu, wait_bar(&ctrl.dp_full, sc & 1, abort_flag, p.error_flag));
         ++sc;
         if (named_barrier_or(1 + wg, 128, !ok)) {
@@ -793,10 +812,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           break;
         }
         tcgen05_fence_after();
-        // dS^T = P^T (dP^T - D). P^T pairs go to [128+64wg, +32), over part 0's dP^T
-        // columns (each piece after that part is read); dS^T pairs go to [160+64wg, +32),
-        // over part 1's, so they are stored once both parts are read.
-        uint32_t pd[2][2][8];  // [part][lane half][register]
+        // dS^T = P^T (dP^T - D), as bf16 pairs over this half's first 32 columns of dP^T:
+        // part p's pairs land on columns part 0 covers, each after part 0 is read
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
           uint32_t dr[2][16];  // [lane half][register] of this part
@@ -805,7 +822,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                       dr[1]);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            uint32_t pp[8];
+            uint32_t pd[8];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const float2 d2 = *reinterpret_cast<const float2*>(xd + 32 * part + 8 * k + 2 * c4);
@@ -819,23 +836,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                           s0, s1);
               f32x2_split(ffma2(p23, fadd2(f32x2(__uint_as_float(dv4[2]), __uint_as_float(dv4[3])), nd2), 0ull),
                           s2, s3);
-              pp[2 * k] = pack_bf16x2(__uint_as_float(pv[0]), __uint_as_float(pv[1]));
-              pp[2 * k + 1] = pack_bf16x2(__uint_as_float(pv[2]), __uint_as_float(pv[3]));
-              pd[part][h][2 * k] = pack_bf16x2(s0, s1);
-              pd[part][h][2 * k + 1] = pack_bf16x2(s2, s3);
+              pd[2 * k] = pack_bf16x2(s0, s1);
+              pd[2 * k + 1] = pack_bf16x2(s2, s3);
             }
-            tmem_st16x128b_x4(tmem_addr(tmem, lane_base + 16 * h, kColDP + 64 * wg + 16 * part), pp);  // P^T
+            tmem_st16x128b_x4(tmem_addr(tmem, lane_base + 16 * h, kColDP + 64 * wg + 16 * part), pd);  // dS^T
           }
         }
-#pragma unroll
-        for (int part = 0; part < 2; ++part)
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-            tmem_st16x128b_x4(tmem_addr(tmem, lane_base + 16 * h, kColDP + 64 * wg + 32 + 16 * part),
-                              pd[part][h]);  // dS^T
         tmem_wait_st();
         tcgen05_fence_before();
-        mbar_arrive(&ctrl.p_full[wg]);
+        mbar_arrive(&ctrl.ds_full[wg]);  // dK += dS^T Q may start
       }
       if (!ok) break;
       {  // the warpgroup takes one decision (its next barrier needs all 128 threads)
