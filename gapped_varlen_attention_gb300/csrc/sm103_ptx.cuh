@@ -124,21 +124,6 @@ __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]
       : "memory");
 }
 
-// 64 consecutive 32-bit columns of the thread's lane, then wait for completion.
-__device__ __forceinline__ void tmem_ld64_sync(uint32_t taddr, uint32_t (&r)[64]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {"
-      "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15," 
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31," 
-      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47," 
-      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63" 
-      "}, [%64];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : GVA_R8(0), GVA_R8(8), GVA_R8(16), GVA_R8(24), GVA_R8(32), GVA_R8(40), GVA_R8(48), GVA_R8(56)
-      : "r"(taddr)
-      : "memory");
-}
-
 // 128 consecutive 32-bit columns of the thread's lane, then wait for completion.
 __device__ __forceinline__ void tmem_ld128_sync(uint32_t taddr, uint32_t (&r)[128]) {
   asm volatile(
@@ -160,20 +145,6 @@ __device__ __forceinline__ void tmem_ld128_sync(uint32_t taddr, uint32_t (&r)[12
 
 #define GVA_RA8(a, i) "=r"(a[i + 0]), "=r"(a[i + 1]), "=r"(a[i + 2]), "=r"(a[i + 3]), "=r"(a[i + 4]), \
                       "=r"(a[i + 5]), "=r"(a[i + 6]), "=r"(a[i + 7])
-
-// Two loads of 32 columns each (two column ranges of the thread's lane) and one wait:
-// both latencies overlap.
-__device__ __forceinline__ void tmem_ld32x2_sync(uint32_t taddr0, uint32_t (&r0)[32], uint32_t taddr1,
-                                                 uint32_t (&r1)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : GVA_RA8(r0, 0), GVA_RA8(r0, 8), GVA_RA8(r0, 16), GVA_RA8(r0, 24),
-        GVA_RA8(r1, 0), GVA_RA8(r1, 8), GVA_RA8(r1, 16), GVA_RA8(r1, 24)
-      : "r"(taddr0), "r"(taddr1)
-      : "memory");
-}
 
 // Two loads of 64 columns each and one wait.
 __device__ __forceinline__ void tmem_ld64x2_sync(uint32_t taddr0, uint32_t (&r0)[64], uint32_t taddr1,
@@ -235,17 +206,6 @@ __device__ __forceinline__ void tmem_st16x128b_x4(uint32_t taddr, const uint32_t
   asm volatile("tcgen05.st.sync.aligned.16x128b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
                "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
                : "memory");
-}
-
-// Same for 16 columns.
-__device__ __forceinline__ void tmem_ld16_sync(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : GVA_R8(0), GVA_R8(8)
-      : "r"(taddr)
-      : "memory");
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
@@ -338,19 +298,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_addr(bar))
                : "memory");
-}
-
-// ----------------------------------------------------------------------------------
-// Per-warpgroup register reallocation (all four warps of a warpgroup execute the same
-// call). The registers a block may hand out are those it was launched with.
-// ----------------------------------------------------------------------------------
-template <uint32_t N>
-__device__ __forceinline__ void warpgroup_reg_dealloc() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void warpgroup_reg_alloc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ----------------------------------------------------------------------------------
