@@ -11,7 +11,7 @@ The library (libgva.so) is built in-tree by ``build()``; nothing here computes o
 CPU, and calls raise if the library or a supported GPU is missing.
 """
 from ._lib import (GVA_BF16, GVA_FP32, EXPORTS, GvaError, Plan, backward, backward_workspace_bytes, device_status,
-                   forward, forward_noalloc, load_library, lse_merge)
+                   forward, forward_noalloc, inspect_plan, load_library, lse_merge)
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
@@ -20,5 +20,5 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
 
 __all__ = ["Plan", "forward", "forward_noalloc", "lse_merge", "backward", "backward_workspace_bytes", "device_status",
-           "load_library", "build", "GvaError", "EXPORTS",
+           "inspect_plan", "load_library", "build", "GvaError", "EXPORTS",
            "GVA_BF16", "GVA_FP32"]

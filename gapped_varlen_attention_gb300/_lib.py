@@ -22,7 +22,7 @@ GVA_BF16, GVA_FP32 = 0, 1
 # Every symbol include/gva.h declares.
 EXPORTS = ("gva_plan", "gva_forward", "gva_lse_merge", "gva_plan_destroy", "gva_plan_get_info",
            "gva_device_status", "gva_status_string", "gva_last_error", "gva_forward_noalloc", "gva_plan_ranges",
-           "gva_plan_causal", "gva_backward_workspace_size", "gva_backward")
+           "gva_plan_causal", "gva_backward_workspace_size", "gva_backward", "gva_plan_inspect")
 NOALLOC_MAX_WORK_ITEMS = 32768  # GVA_NOALLOC_MAX_WORK_ITEMS in include/gva.h
 
 
@@ -39,6 +39,12 @@ class PlanInfo(ctypes.Structure):
                 ("num_work_items", ctypes.c_int32), ("num_merge_units", ctypes.c_int32),
                 ("grid_ctas", ctypes.c_int32), ("sm_count", ctypes.c_int32),
                 ("used_flops", ctypes.c_double)]
+
+
+class WorkSummary(ctypes.Structure):
+    _fields_ = [("num_work_items", ctypes.c_int32), ("num_key_blocks", ctypes.c_int32),
+                ("num_merge_units", ctypes.c_int32), ("num_bwd_items", ctypes.c_int32),
+                ("num_kv_units", ctypes.c_int32), ("reserved", ctypes.c_int32), ("used_flops", ctypes.c_double)]
 
 
 _lib = None
@@ -72,9 +78,11 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
                                     ctypes.POINTER(vp)]
     lib.gva_backward_workspace_size.argtypes = [vp, ctypes.POINTER(ctypes.c_size_t)]
     lib.gva_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, vp, ctypes.c_size_t, f32, vp]
+    lib.gva_plan_inspect.argtypes = [pi32, pi32, pi32, pi32, i32, i32, i32, i32, i32, ctypes.POINTER(WorkSummary),
+                                     pi32, i32, pi32, i32, pi32, i32]
     for name in ("gva_plan", "gva_forward", "gva_lse_merge", "gva_plan_destroy", "gva_plan_get_info",
                  "gva_device_status", "gva_forward_noalloc", "gva_plan_ranges", "gva_plan_causal",
-                 "gva_backward_workspace_size", "gva_backward"):
+                 "gva_backward_workspace_size", "gva_backward", "gva_plan_inspect"):
         getattr(lib, name).restype = i32
     if path is None:
         _lib = lib
@@ -90,6 +98,36 @@ def _check(lib, status: int, what: str):
 
 def _i32(a) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+WORK_ITEM_FIELDS = ("q_row0", "q_rows", "blk0", "nblk", "head_kv", "n_tiles", "k_len", "q_pos0")
+KV_UNIT_FIELDS = ("key_row0", "keys", "q_row0", "q_used", "head_kv", "tile0", "key_pos0", "pos_shift")
+
+
+def inspect_plan(cu_seqlens_q, seqused_q, cu_seqlens_k, seqused_k, num_heads_q: int, num_heads_kv: int,
+                 head_dim: int, causal_block: int = 0) -> dict:
+    """``gva_plan_inspect``: the work lists a plan of this geometry holds, built on the
+    host (no CUDA call). Returns the counts, ``used_flops`` and three int32 arrays of 8
+    columns in the kernels' order: ``items`` (forward, fields ``WORK_ITEM_FIELDS``),
+    ``bwd_items`` (dQ, same fields) and ``kv_units`` (dK / dV, ``KV_UNIT_FIELDS``)."""
+    lib = load_library()
+    a = [_i32(x) for x in (cu_seqlens_q, seqused_q, cu_seqlens_k, seqused_k)]
+    n = int(a[1].shape[0])
+    p = lambda x: x.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))  # noqa: E731
+    summ = WorkSummary()
+    args = [p(a[0]), p(a[1]), p(a[2]), p(a[3]), n, int(causal_block), int(num_heads_q), int(num_heads_kv),
+            int(head_dim), ctypes.byref(summ)]
+    _check(lib, lib.gva_plan_inspect(*args, None, 0, None, 0, None, 0), "gva_plan_inspect")
+    items = np.zeros((max(summ.num_work_items, 1), 8), np.int32)
+    bwd = np.zeros((max(summ.num_bwd_items, 1), 8), np.int32)
+    kvu = np.zeros((max(summ.num_kv_units, 1), 8), np.int32)
+    _check(lib, lib.gva_plan_inspect(*args, p(items), summ.num_work_items, p(bwd), summ.num_bwd_items, p(kvu),
+                                     summ.num_kv_units), "gva_plan_inspect")
+    return {"num_work_items": summ.num_work_items, "num_key_blocks": summ.num_key_blocks,
+            "num_merge_units": summ.num_merge_units, "num_bwd_items": summ.num_bwd_items,
+            "num_kv_units": summ.num_kv_units, "used_flops": summ.used_flops,
+            "items": items[:summ.num_work_items], "bwd_items": bwd[:summ.num_bwd_items],
+            "kv_units": kvu[:summ.num_kv_units]}
 
 
 class Plan:

@@ -118,13 +118,22 @@ void free_plan(struct gva_plan* p) {
 // key blocks its last row sees, and FLOPs count the visible keys of every row.
 // backward (every K/V row in at most one range, so each dK / dV row has one writer;
 // maskless, block-causal or ranges): also build the dQ items and the dK / dV units.
-gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int32_t num_segments,
+struct HostWork {
+  std::vector<gva::KeyBlock> blocks;
+  std::vector<gva::WorkItem> items;  // forward, sorted longest first
+  std::vector<gva::MergeUnit> units;
+  std::vector<gva::WorkItem> bwd_items;
+  std::vector<gva::KvUnit> kv_units;
+  double flops = 0.0;
+};
+
+gva_status build_work(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int32_t num_segments,
                       const int32_t* range_off, const int32_t* range_start, const int32_t* range_len,
-                      int64_t total_k, int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim,
-                      int32_t causal_block, bool backward, gva_plan_t* out_plan) {
+                      int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim, int32_t causal_block,
+                      bool backward, HostWork& w) {
   const int32_t group = num_heads_q / num_heads_kv;
   // ---- key blocks: each range cut into blocks of at most kBlockKeys keys
-  std::vector<gva::KeyBlock> blocks;
+  std::vector<gva::KeyBlock>& blocks = w.blocks;
   std::vector<int32_t> seg_blk0(num_segments), seg_nblk(num_segments), seg_keys(num_segments);
   for (int32_t b = 0; b < num_segments; ++b) {
     seg_blk0[b] = static_cast<int32_t>(blocks.size());
@@ -143,8 +152,8 @@ gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
   const int32_t tokens_per_item = tokens_per_tile * gva::kTilesPerItem;
   std::vector<gva::WorkItem> items;
   std::vector<int64_t> cost;
-  std::vector<gva::MergeUnit> units;
-  double flops = 0.0;
+  std::vector<gva::MergeUnit>& units = w.units;
+  double& flops = w.flops;
   // keys visible to the row at key position pos (block-causal)
   auto limit_at = [&](int64_t pos, int32_t keys) -> int32_t {
     if (pos < 0) return 0;
@@ -185,12 +194,13 @@ gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
   std::vector<int32_t> order(items.size());
   for (size_t i = 0; i < order.size(); ++i) order[i] = static_cast<int32_t>(i);
   std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t c) { return cost[a] > cost[c]; });
-  std::vector<gva::WorkItem> sorted(items.size());
+  std::vector<gva::WorkItem>& sorted = w.items;
+  sorted.resize(items.size());
   for (size_t i = 0; i < order.size(); ++i) sorted[i] = items[order[i]];
 
   // ---- backward work lists, longest first
-  std::vector<gva::WorkItem> bwd_items;
-  std::vector<gva::KvUnit> kv_units;
+  std::vector<gva::WorkItem>& bwd_items = w.bwd_items;
+  std::vector<gva::KvUnit>& kv_units = w.kv_units;
   if (backward) {
     for (int32_t b = 0; b < num_segments; ++b) {
       const int32_t uq = seqused_q[b];
@@ -235,6 +245,24 @@ gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
     std::stable_sort(kv_units.begin(), kv_units.end(),
                      [&](const gva::KvUnit& a, const gva::KvUnit& c) { return unit_tiles(a) > unit_tiles(c); });
   }
+  return GVA_OK;
+}
+
+gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int32_t num_segments,
+                      const int32_t* range_off, const int32_t* range_start, const int32_t* range_len,
+                      int64_t total_k, int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim,
+                      int32_t causal_block, bool backward, gva_plan_t* out_plan) {
+  HostWork w;
+  gva_status st = build_work(cu_seqlens_q, seqused_q, num_segments, range_off, range_start, range_len,
+                             num_heads_q, num_heads_kv, head_dim, causal_block, backward, w);
+  if (st != GVA_OK) return st;
+  const int32_t group = num_heads_q / num_heads_kv;
+  const std::vector<gva::KeyBlock>& blocks = w.blocks;
+  const std::vector<gva::WorkItem>& sorted = w.items;
+  const std::vector<gva::MergeUnit>& units = w.units;
+  const std::vector<gva::WorkItem>& bwd_items = w.bwd_items;
+  const std::vector<gva::KvUnit>& kv_units = w.kv_units;
+  const double flops = w.flops;
 
   // ---- device
   int dev = 0;
@@ -424,6 +452,46 @@ gva_status gva_plan_ranges(const int32_t* cu_seqlens_q, const int32_t* seqused_q
     if (static_cast<int64_t>(spans[i - 1].first) + spans[i - 1].second > spans[i].first) disjoint = false;
   return build_plan(cu_seqlens_q, seqused_q, num_segments, key_range_offsets, key_range_starts, key_range_lengths,
                     total_k, num_heads_q, num_heads_kv, head_dim, 0, disjoint, out_plan);
+}
+
+gva_status gva_plan_inspect(const int32_t* cu_seqlens_q, const int32_t* seqused_q, const int32_t* cu_seqlens_k,
+                            const int32_t* seqused_k, int32_t num_segments, int32_t causal_block, int32_t num_heads_q,
+                            int32_t num_heads_kv, int32_t head_dim, gva_work_summary* summary, int32_t* items,
+                            int32_t items_capacity, int32_t* bwd_items, int32_t bwd_items_capacity,
+                            int32_t* kv_units, int32_t kv_units_capacity) {
+  if (summary == nullptr) return fail(GVA_ERR_INVALID_ARG, "summary is NULL");
+  if (causal_block < 0) return fail(GVA_ERR_INVALID_ARG, "causal_block=%d must be >= 0", causal_block);
+  gva_status s = validate_common(cu_seqlens_q, seqused_q, num_segments, num_heads_q, num_heads_kv, head_dim);
+  if (s != GVA_OK) return s;
+  if (cu_seqlens_k == nullptr || (num_segments > 0 && seqused_k == nullptr))
+    return fail(GVA_ERR_INVALID_ARG, "a geometry array is NULL");
+  s = validate_offsets(cu_seqlens_k, seqused_k, num_segments, "k");
+  if (s != GVA_OK) return s;
+  std::vector<int32_t> off(num_segments + 1), start(num_segments), len(num_segments);
+  for (int32_t b = 0; b <= num_segments; ++b) off[b] = b;
+  for (int32_t b = 0; b < num_segments; ++b) {
+    start[b] = cu_seqlens_k[b];
+    len[b] = seqused_k[b];
+  }
+  HostWork w;
+  s = build_work(cu_seqlens_q, seqused_q, num_segments, off.data(), start.data(), len.data(), num_heads_q,
+                 num_heads_kv, head_dim, causal_block, true, w);
+  if (s != GVA_OK) return s;
+  summary->num_work_items = static_cast<int32_t>(w.items.size());
+  summary->num_key_blocks = static_cast<int32_t>(w.blocks.size());
+  summary->num_merge_units = static_cast<int32_t>(w.units.size());
+  summary->num_bwd_items = static_cast<int32_t>(w.bwd_items.size());
+  summary->num_kv_units = static_cast<int32_t>(w.kv_units.size());
+  summary->used_flops = w.flops;
+  static_assert(sizeof(gva::WorkItem) == 8 * sizeof(int32_t) && sizeof(gva::KvUnit) == 8 * sizeof(int32_t),
+                "8 int32 per exported record");
+  auto copy_out = [](int32_t* dst, int32_t cap, const void* src, size_t n) {
+    if (dst != nullptr && cap > 0) std::memcpy(dst, src, std::min<size_t>(n, cap) * 8 * sizeof(int32_t));
+  };
+  copy_out(items, items_capacity, w.items.data(), w.items.size());
+  copy_out(bwd_items, bwd_items_capacity, w.bwd_items.data(), w.bwd_items.size());
+  copy_out(kv_units, kv_units_capacity, w.kv_units.data(), w.kv_units.size());
+  return ok();
 }
 
 gva_status gva_forward(gva_plan_t plan, const void* q, const void* k, const void* v, void* out, gva_dtype out_dtype,

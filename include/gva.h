@@ -235,6 +235,30 @@ GVA_API gva_status gva_backward(gva_plan_t plan, const void* q, const void* k, c
                                 void* dv, gva_dtype dkv_dtype, void* workspace, size_t workspace_bytes,
                                 float softmax_scale, cudaStream_t stream);
 
+/*
+ * gva_plan_inspect - the work lists a plan would hold, built on the host only.
+ *
+ * For tests and tuning: no CUDA call is made and no plan is created. Takes the
+ * geometry of gva_plan (HOST arrays, same validation) plus causal_block (0: maskless,
+ * > 0: as gva_plan_causal), fills *summary, and copies at most *_capacity records of 8
+ * int32 each into each non-NULL array, in the order the kernels take them:
+ *   items     : forward work items {q_row0, q_rows, blk0, nblk, head_kv, n_tiles, k_len,
+ *               q_pos0}, longest first;
+ *   bwd_items : backward dQ items, same layout, one Q tile each;
+ *   kv_units  : backward dK / dV units {key_row0, keys, q_row0, q_used, head_kv, tile0,
+ *               key_pos0, pos_shift}.
+ */
+typedef struct {
+  int32_t num_work_items, num_key_blocks, num_merge_units, num_bwd_items, num_kv_units, reserved;
+  double used_flops;
+} gva_work_summary;
+GVA_API gva_status gva_plan_inspect(const int32_t* cu_seqlens_q, const int32_t* seqused_q,
+                                    const int32_t* cu_seqlens_k, const int32_t* seqused_k, int32_t num_segments,
+                                    int32_t causal_block, int32_t num_heads_q, int32_t num_heads_kv,
+                                    int32_t head_dim, gva_work_summary* summary, int32_t* items,
+                                    int32_t items_capacity, int32_t* bwd_items, int32_t bwd_items_capacity,
+                                    int32_t* kv_units, int32_t kv_units_capacity);
+
 /* Release a plan's device memory. NULL is accepted. Synchronous with respect to the
  * host only through cudaFree. */
 GVA_API gva_status gva_plan_destroy(gva_plan_t plan);

@@ -1,0 +1,206 @@
+"""The plan builder's work lists, checked on the host (no GPU): ``gva_plan_inspect``
+returns the forward items, the backward dQ items and the dK / dV units a plan holds,
+and each list is re-derived here from the segment geometry and compared.
+
+What the lists must satisfy follows from the method: every used query row of every
+(segment, KV head) is covered exactly once; an item's key blocks are the used keys of
+its segment (block-causal: only those its last row can see, by the visibility rule of
+"Problem and behavior" in the multiview causal replay); FLOPs count the score pairs
+that are computed; and the kernels take the longest work first."""
+import numpy as np
+import pytest
+
+from gapped_varlen_attention_gb300 import _lib, workloads as W
+from oracle import gva_oracle as oracle
+
+TILE_ROWS, BLOCK_KEYS, TILES_PER_ITEM, MERGE_ROWS = 128, 128, 2, 16
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import gapped_varlen_attention_gb300 as gva
+    gva.build()
+
+
+def inspect(g, causal_block=0):
+    return _lib.inspect_plan(g.cu_q, g.used_q, g.cu_k, g.used_k, g.num_heads_q, g.num_heads_kv, g.head_dim,
+                             causal_block)
+
+
+def rec(a, fields):
+    return [dict(zip(fields, map(int, r))) for r in a]
+
+
+def limits(uq, uk, B):
+    """Keys visible to each used row: all of them without masking, else the oracle's rule."""
+    if B == 0:
+        return np.full(uq, uk, np.int64)
+    return oracle.causal_limits(uq, uk, B).astype(np.int64)
+
+
+def check_work(g, B=0):
+    w = inspect(g, B)
+    group = g.num_heads_q // g.num_heads_kv
+    tpt = TILE_ROWS // group
+    nseg = g.num_segments
+    cu_q, uq = g.cu_q.astype(np.int64), g.used_q.astype(np.int64)
+    cu_k, uk = g.cu_k.astype(np.int64), g.used_k.astype(np.int64)
+    seg_of_row = {}
+    for b in range(nseg):
+        for r in range(int(cu_q[b]), int(cu_q[b] + uq[b])):
+            seg_of_row[r] = b
+
+    # ---- counts
+    assert w["num_key_blocks"] == sum(-(-int(k) // BLOCK_KEYS) for k in uk)
+    assert w["num_merge_units"] == sum(-(-int(q) // MERGE_ROWS) for q in uq)
+    pairs = sum(float(limits(int(uq[b]), int(uk[b]), B).sum()) for b in range(nseg))
+    want = 4.0 * g.head_dim * g.num_heads_q * pairs
+    assert w["used_flops"] == pytest.approx(want, rel=1e-12)
+    if B == 0:
+        assert w["used_flops"] == pytest.approx(oracle.used_flops(uq, uk, g.num_heads_q, g.head_dim), rel=1e-12)
+
+    blk0 = np.concatenate([[0], np.cumsum([-(-int(k) // BLOCK_KEYS) for k in uk])]).astype(np.int64)
+
+    def check_items(items, rows_per_item, tiles_per_item):
+        cover = {}
+        for it in items:
+            b = seg_of_row.get(it["q_row0"])
+            assert b is not None, it
+            t0 = it["q_row0"] - int(cu_q[b])
+            assert t0 % rows_per_item == 0
+            assert it["q_rows"] == min(rows_per_item, int(uq[b]) - t0)
+            assert it["n_tiles"] == min(tiles_per_item, -(-it["q_rows"] // tpt))
+            assert it["blk0"] == blk0[b] and it["k_len"] == uk[b]
+            assert 0 <= it["head_kv"] < g.num_heads_kv
+            lim = limits(int(uq[b]), int(uk[b]), B)
+            assert it["nblk"] == -(-int(lim[t0 + it["q_rows"] - 1]) // BLOCK_KEYS)
+            if B > 0:
+                assert it["q_pos0"] == t0 + int(uk[b]) - int(uq[b])
+            for r in range(it["q_row0"], it["q_row0"] + it["q_rows"]):
+                key = (r, it["head_kv"])
+                assert key not in cover, f"row {r} head {it['head_kv']} covered twice"
+                cover[key] = True
+        assert len(cover) == int(uq.sum()) * g.num_heads_kv
+
+    # ---- forward items: up to two Q tiles each, every used row once per KV head
+    items = rec(w["items"], _lib.WORK_ITEM_FIELDS)
+    assert len(items) == w["num_work_items"]
+    check_items(items, tpt * TILES_PER_ITEM, TILES_PER_ITEM)
+    cost = [it["nblk"] * it["n_tiles"] * 4 + it["n_tiles"] for it in items]
+    assert cost == sorted(cost, reverse=True), "forward items not longest first"
+
+    # ---- dQ items: one Q tile each, sorted by key blocks
+    bwd = rec(w["bwd_items"], _lib.WORK_ITEM_FIELDS)
+    check_items(bwd, tpt, 1)
+    nb = [it["nblk"] for it in bwd]
+    assert nb == sorted(nb, reverse=True), "dQ items not longest first"
+
+    # ---- dK / dV units: one per (segment, KV head, key block), every used key once
+    units = rec(w["kv_units"], _lib.KV_UNIT_FIELDS)
+    want_units = []
+    for b in range(nseg):
+        n_tiles = -(-int(uq[b]) // tpt)
+        lim = limits(int(uq[b]), int(uk[b]), B)
+        for hk in range(g.num_heads_kv):
+            for j in range(-(-int(uk[b]) // BLOCK_KEYS)):
+                kp = j * BLOCK_KEYS
+                sees = np.nonzero(lim > kp)[0]  # rows that see the block's first key
+                if B == 0:
+                    tile0 = 0
+                else:
+                    tile0 = int(sees[0]) // tpt if sees.size else None
+                u = dict(key_row0=int(cu_k[b]) + kp, keys=min(BLOCK_KEYS, int(uk[b]) - kp), q_row0=int(cu_q[b]),
+                         q_used=int(uq[b]), head_kv=hk, key_pos0=kp, pos_shift=int(uk[b]) - int(uq[b]))
+                want_units.append((u, tile0, n_tiles, lim))
+    assert len(units) == len(want_units)
+    by_key = {(u["key_row0"], u["head_kv"]): u for u in units}
+    assert len(by_key) == len(units), "a (key block, KV head) unit appears twice"
+    for u, tile0, n_tiles, lim in want_units:
+        got = by_key[(u["key_row0"], u["head_kv"])]
+        assert {k: got[k] for k in u} == u
+        if tile0 is not None:
+            assert got["tile0"] == tile0
+        else:  # no row sees the block: the unit may skip every tile, and skips no row that would
+            assert got["tile0"] <= n_tiles
+            assert not np.any(lim[:got["tile0"] * tpt] > u["key_pos0"])
+        # whatever the start tile, the rows it skips see no key of the block
+        assert not np.any(lim[:min(got["tile0"] * tpt, len(lim))] > u["key_pos0"])
+    tiles = [-(-u["q_used"] // tpt) - u["tile0"] for u in units]
+    assert tiles == sorted(tiles, reverse=True), "dK / dV units not longest first"
+    return w
+
+
+def test_tiny():
+    w = check_work(W.tiny())
+    assert w["num_work_items"] == 3 * 2  # one item per segment and KV head
+
+
+def test_cfg_text_cross():
+    check_work(W.cfg_text_cross())
+
+
+def test_multiview_causal_and_partitions():
+    full, parts = W.multiview_causal()
+    check_work(full)
+    check_work(full, 64)
+    for p in parts:
+        check_work(p)
+
+
+def test_long_replay_counts():
+    g = W.long_replay()
+    w = check_work(g)
+    tpi = (TILE_ROWS // (g.num_heads_q // g.num_heads_kv)) * TILES_PER_ITEM
+    assert w["num_work_items"] == g.num_heads_kv * sum(-(-int(q) // tpi) for q in g.used_q)
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("B", [0, 1, 7, 64, 128, 300])
+def test_random_geometries(seed, B):
+    rng = np.random.default_rng(7100 + seed)
+    hkv = int(rng.choice([1, 2, 4]))
+    group = int(rng.choice([1, 2, 4, 8]))
+    g = W.random_geometry(rng, int(rng.integers(1, 7)), 700, 900, hkv * group, hkv, int(rng.choice([64, 128])))
+    check_work(g, B)
+
+
+def test_more_queries_than_keys_causal():
+    """Rows whose key position is negative see nothing: they cost no key block."""
+    cu = np.array([0, 300], np.int32)
+    g = W._geom(cu, [300], np.array([0, 100], np.int32), [100], 8, 2, 64)
+    w = check_work(g, 16)
+    bwd = rec(w["bwd_items"], _lib.WORK_ITEM_FIELDS)
+    assert min(it["nblk"] for it in bwd) == 0
+
+
+def test_empty_geometry():
+    z = np.zeros(1, np.int32)
+    w = _lib.inspect_plan(z, np.zeros(0, np.int32), z, np.zeros(0, np.int32), 4, 2, 64)
+    assert w["num_work_items"] == w["num_bwd_items"] == w["num_kv_units"] == 0
+    assert w["used_flops"] == 0.0
+
+
+def test_capacity_truncates_and_errors():
+    import ctypes
+    g = W.random_geometry(np.random.default_rng(3), 4, 600, 600, 8, 2, 128, allow_empty=False)
+    full = inspect(g)
+    lib = _lib.load_library()
+    a = [np.ascontiguousarray(x, np.int32) for x in (g.cu_q, g.used_q, g.cu_k, g.used_k)]
+    p = lambda x: x.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))  # noqa: E731
+    s = _lib.WorkSummary()
+    one = np.full((2, 8), -5, np.int32)
+    st = lib.gva_plan_inspect(p(a[0]), p(a[1]), p(a[2]), p(a[3]), 4, 0, 8, 2, 128, ctypes.byref(s), p(one), 1,
+                              None, 0, None, 0)
+    assert st == 0 and s.num_work_items == full["num_work_items"]
+    assert np.array_equal(one[0], full["items"][0]) and np.all(one[1] == -5)
+    # NULL summary, negative block, bad geometry
+    assert lib.gva_plan_inspect(p(a[0]), p(a[1]), p(a[2]), p(a[3]), 4, 0, 8, 2, 128, None, None, 0, None, 0,
+                                None, 0) == 1
+    assert lib.gva_plan_inspect(p(a[0]), p(a[1]), p(a[2]), p(a[3]), 4, -1, 8, 2, 128, ctypes.byref(s), None, 0,
+                                None, 0, None, 0) == 1
+    bad = a[3].copy()
+    bad[0] = a[2][1] - a[2][0] + 1  # used keys above the capacity
+    assert lib.gva_plan_inspect(p(a[0]), p(a[1]), p(a[2]), p(bad), 4, 0, 8, 2, 128, ctypes.byref(s), None, 0,
+                                None, 0, None, 0) == 1
+    assert lib.gva_plan_inspect(p(a[0]), p(a[1]), p(a[2]), p(a[3]), 4, 0, 8, 2, 96, ctypes.byref(s), None, 0,
+                                None, 0, None, 0) == 2
