@@ -140,6 +140,25 @@ class Workload:
             self.parts = None
             self.backward = True
             self.label = "backward of the reduced long replay (profiling): 2 segments x 8192 q rows x 32768 keys"
+        elif name == "lse_merge_union":
+            text, video, union, _ = W.lse_merge_union()
+            self.geoms = [text, video]
+            self.q, kt, vt = W.make_qkv(text, 1004 + seed_offset, device=dev)
+            kvid, vvid = W.make_qkv(video, 2004 + seed_offset, device=dev)[1:]
+            self.part_kv = [(kt, vt), (kvid, vvid)]
+            self.parts = union
+            self.label = ("text + video LSE merge: 8192 q rows in 10 segments, each attending its own 1024 text and "
+                          "16384 video keys as 2 launches (FP32 partials) + FP32 LSE merge, one segment's text "
+                          "partition empty; Hq=Hkv=24, d=128")
+        elif name == "lse_merge":
+            text, video, union, _ = W.lse_merge_union()
+            self.geoms = [union]
+            self.parts = union
+            self.merge_only = True
+            self.used_k_parts = [text.used_k, video.used_k]
+            self.label = ("the FP32 LSE merge alone on the text + video workload's partials: 8192 q rows in 10 "
+                          "segments, 2 FP32 partitions (one segment's text partition keyless), bf16 output, "
+                          "Hq=24, d=128")
         elif name == "tiny":
             g = W.tiny()
             self.geoms = [g]
@@ -148,14 +167,22 @@ class Workload:
             self.label = "tiny: 3 segments, Hq=4, Hkv=2, d=64"
         else:
             raise SystemExit(f"unknown workload {name}")
-        if getattr(self, "ranges", None) is not None:
+        self.merge_only = getattr(self, "merge_only", False)
+        if self.merge_only:
+            self.plans = []
+        elif getattr(self, "ranges", None) is not None:
             g = self.geoms[0]
             self.plans = [gva.Plan.from_ranges(g.cu_q, g.used_q, self.ranges, g.total_k, g.num_heads_q,
                                                g.num_heads_kv, g.head_dim)]
         else:
             self.plans = [gva.Plan.from_geometry(g, getattr(self, "causal_block", 0)) for g in self.geoms]
         g0 = self.geoms[0]
-        if self.parts is None:
+        if self.merge_only:
+            self.merge_plan = gva.Plan.from_geometry(self.parts)
+            self.out, self.lse = W.make_outputs(self.parts, 0.0, device=dev)
+            outs, lses = W.make_partials(self.parts, self.used_k_parts, 3004 + seed_offset, device=dev)
+            self.partials = list(zip(outs, lses))
+        elif self.parts is None:
             self.out, self.lse = W.make_outputs(g0, 0.0, device=dev)
             self.partials = None
         else:
@@ -164,10 +191,22 @@ class Workload:
             self.partials = [W.make_outputs(p, 0.0, device=dev, out_dtype=torch.float32) for p in self.geoms]
         self.flops = float(sum(p.info()["used_flops"] for p in self.plans))
         self.launches_per_step = len(self.geoms) + (0 if self.parts is None else 1)
-        self.metric = METRIC
+        self.metric, self.unit, self.scale, self.bound = METRIC, UNIT, 1e12, "tensor"
         self.kernel = "gva_fwd_kernel"
-        self.inputs = [self.q, self.k, self.v]
+        # the forward launch that dominates the step (most FLOPs)
+        self.dominant = int(np.argmax([p.info()["used_flops"] for p in self.plans])) if self.plans else 0
+        if getattr(self, "part_kv", None) is not None:
+            self.inputs = [self.q] + [t for kv in self.part_kv for t in kv]
+        elif not self.merge_only:
+            self.inputs = [self.q, self.k, self.v]
         self.outputs = [self.out, self.lse]
+        if self.merge_only:
+            self.inputs = [t for o_l in self.partials for t in o_l]
+            self.launches_per_step = 1
+            self.flops = 0.0
+            self.metric = "gapped-varlen FP32 LSE merge GB/s (algorithmic bytes: live partials, LSEs, output)"
+            self.unit, self.scale, self.bound = "GB/s", 1e9, "hbm"
+            self.kernel = "gva_lse_merge_kernel<float, bf16>"
         if getattr(self, "backward", False):
             # the forward's O and LSE are inputs of the backward (computed once, untimed)
             gva.forward(self.plans[0], self.q, self.k, self.v, self.out, self.lse)
@@ -182,6 +221,8 @@ class Workload:
             self.kernel = "gva_backward (3 launches: rowsum, dQ, dK/dV)"
             self.inputs = [self.q, self.k, self.v, self.out, self.lse, self.d_out]
             self.outputs = list(self.grads)
+        self.work = merge_bytes(self.parts, self.used_k_parts, self.out.element_size()) if self.merge_only \
+            else self.flops  # the metric's numerator per step (FLOPs, or bytes for the merge)
 
     def step(self, inputs=None, outputs=None):
         """One pass of the path on the current stream: `inputs` / `outputs` default to the
@@ -189,6 +230,10 @@ class Workload:
         gva = self.gva
         inputs = inputs or self.inputs
         outputs = outputs or self.outputs
+        if self.merge_only:
+            n = len(self.partials)
+            gva.lse_merge(self.merge_plan, inputs[0:2 * n:2], inputs[1:2 * n:2], *outputs)
+            return
         q, k, v = inputs[:3]
         if getattr(self, "backward", False):
             out, lse, d_out = inputs[3:]
@@ -196,27 +241,52 @@ class Workload:
         elif self.partials is None:
             gva.forward(self.plans[0], q, k, v, *outputs)
         else:
-            for plan, (o, l) in zip(self.plans, self.partials):
-                gva.forward(plan, q, k, v, o, l)
+            for i, (plan, (o, l)) in enumerate(zip(self.plans, self.partials)):
+                ki, vi = self.kv_of(i, inputs)
+                gva.forward(plan, q, ki, vi, o, l)
             gva.lse_merge(self.merge_plan, [p[0] for p in self.partials], [p[1] for p in self.partials],
                           *outputs)
 
+    def kv_of(self, i, inputs=None):
+        """K and V of forward launch i (each partition has its own buffers, or all share one)."""
+        inputs = inputs or self.inputs
+        if getattr(self, "part_kv", None) is not None:
+            return inputs[1 + 2 * i], inputs[2 + 2 * i]
+        return inputs[1], inputs[2]
+
     def check(self):
-        for p in self.plans:
+        for p in self.plans + ([self.merge_plan] if self.parts is not None else []):
             self.gva.device_status(p)
 
     def config(self):
         geom = self.parts if self.parts is not None else self.geoms[0]
-        return {"workload": self.name, "description": self.label, **_describe(geom),
-                "useful_flops_per_step": self.flops,
+        per_step = {"algorithmic_bytes_per_step": self.work} if self.merge_only else \
+            {"useful_flops_per_step": self.flops}
+        return {"workload": self.name, "description": self.label, **_describe(geom), **per_step,
                 "l2": "inputs larger than L2 (no flush needed)" if self.input_bytes() > 2 * 129e6
-                else "L2 flushed before every step (256 MB write, outside the timed events)"}
+                else "L2 flushed before every step (256 MB write, then a 256 MB read so that the write's dirty "
+                     "lines are written back before the step; outside the timed events)"}
 
     def input_bytes(self):
         return sum(t.numel() * t.element_size() for t in self.inputs)
 
     def output_bytes(self):
         return sum(t.numel() * t.element_size() for t in self.outputs)
+
+
+def merge_bytes(g, used_k_parts, out_bytes: int, rows=None) -> float:
+    """Algorithmic bytes of one FP32 LSE merge over g's used rows (or the listed rows):
+    every partition's LSE read and the merged LSE written (4 bytes each per row and
+    head), each live partition's FP32 output read (a keyless one, LSE = -inf, is
+    skipped), and the merged output written."""
+    hq, d = g.num_heads_q, g.head_dim
+    total = 0.0
+    for b in range(g.num_segments):
+        n = int(g.used_q[b]) if rows is None else int(np.sum(
+            (np.asarray(rows) >= int(g.cu_q[b])) & (np.asarray(rows) < int(g.cu_q[b]) + int(g.used_q[b]))))
+        live = sum(1 for uk in used_k_parts if int(uk[b]) > 0)
+        total += n * hq * (4.0 * (len(used_k_parts) + 1) + d * (4.0 * live + out_bytes))
+    return total
 
 
 # --------------------------------------------------------------------------------------
@@ -280,6 +350,18 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def wait_samples(self, n: int, timeout_s: float, work=None) -> None:
+        """Wait until `n` samples have arrived (at most `timeout_s`), calling `work`
+        meanwhile if given (to keep the GPU under the same load)."""
+        if self.proc is None:
+            return
+        t_end = time.monotonic() + timeout_s
+        while len(self.lines) < n and time.monotonic() < t_end:
+            if work is None:
+                time.sleep(0.02)
+            else:
+                work()
+
     def __exit__(self, *exc):
         if self.proc is not None:
             self.proc.terminate()
@@ -309,10 +391,25 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+class L2Flush:
+    """Leaves L2 cold before a timed step: writes a 256 MB buffer (twice the 129 MB L2),
+    then reads another 256 MB, so that L2 holds only clean lines of neither input nor
+    output and the write-back of the written lines is not charged to the step."""
+
+    def __init__(self):
+        self.dirty = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        self.clean = torch.ones(64 << 20, dtype=torch.float32, device="cuda")
+        self.acc = torch.empty((), dtype=torch.float32, device="cuda")
+
+    def __call__(self):
+        self.dirty.fill_(1)
+        torch.sum(self.clean, dim=0, out=self.acc)
+
+
 def time_steps(fn, steps: int, stream, flush=None) -> float:
     """Device milliseconds for `steps` calls of fn, CUDA events on `stream`. With a
-    flush buffer (inputs smaller than L2), the buffer is rewritten before every step,
-    outside the events, so each step starts with a cold L2 and only the step is timed."""
+    flush (an L2Flush, for inputs smaller than L2), it runs before every step, outside
+    the events, so each step starts with a cold L2 and only the step is timed."""
     if flush is None:
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
@@ -324,7 +421,7 @@ def time_steps(fn, steps: int, stream, flush=None) -> float:
         return start.elapsed_time(end)
     pairs = []
     for _ in range(steps):
-        flush.fill_(1)
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         fn()
@@ -395,10 +492,15 @@ def max_over_ranks(values, dist, device):
     return [float(x) for x in t.tolist()]
 
 
-def job_tflops(world: int, flops_per_rank: float, ms: float) -> float:
+def job_rate(world: int, work_per_rank: float, ms: float, scale: float = 1e12) -> float:
     """Whole-job throughput: every rank runs its own copy of the workload (weak scaling),
-    so the job does world x the per-rank FLOPs in the slowest rank's time."""
-    return world * flops_per_rank / (ms * 1e-3) / 1e12
+    so the job does world x the per-rank work (FLOPs or bytes) in the slowest rank's
+    time; ``scale`` 1e12 gives TFLOP/s, 1e9 GB/s."""
+    return world * work_per_rank / (ms * 1e-3) / scale
+
+
+def job_tflops(world: int, flops_per_rank: float, ms: float) -> float:
+    return job_rate(world, flops_per_rank, ms, 1e12)
 
 
 # --------------------------------------------------------------------------------------
@@ -411,9 +513,14 @@ def oracle_sample_rate(wl, budget_s: float, seed: int = 0):
     from oracle import gva_oracle
     geoms = wl.geoms
     rng = np.random.default_rng(seed)
+    if getattr(wl, "merge_only", False):
+        return oracle_merge_rate(wl, budget_s, rng)
     q = wl.q.cpu()
-    k = wl.k.cpu()
-    v = wl.v.cpu()
+    part_kv = getattr(wl, "part_kv", None)
+    if part_kv is not None:
+        kvs = [(k_.cpu(), v_.cpu()) for k_, v_ in part_kv]
+    else:
+        kvs = [(wl.k.cpu(), wl.v.cpu())] * len(geoms)
     backward = getattr(wl, "backward", False)
     cb = getattr(wl, "causal_block", 0)
     d_out = wl.d_out.cpu() if backward else None
@@ -421,7 +528,7 @@ def oracle_sample_rate(wl, budget_s: float, seed: int = 0):
     rows_done = 0
     t0 = time.perf_counter()
     while True:
-        for g in geoms:
+        for g, (k, v) in zip(geoms, kvs):
             b = int(rng.choice(np.flatnonzero(g.used_q > 0)))
             local = [int(x) for x in rng.integers(0, int(g.used_q[b]), size=4)]
             rows = [int(g.cu_q[b]) + r for r in local]
@@ -454,6 +561,30 @@ def oracle_sample_rate(wl, budget_s: float, seed: int = 0):
     return done_flops / el / 1e12, desc, rows_done, el
 
 
+def oracle_merge_rate(wl, budget_s: float, rng):
+    """The FP64 oracle merge on seeded samples of 64 used rows of the merge workload for
+    about `budget_s` seconds; return (GB/s of algorithmic bytes, description, rows, seconds)."""
+    from oracle import gva_oracle
+    g = wl.parts
+    outs = [o.cpu().numpy() for o, _ in wl.partials]
+    lses = [l_.cpu().numpy() for _, l_ in wl.partials]
+    used_rows = np.concatenate([np.arange(int(g.cu_q[b]), int(g.cu_q[b]) + int(g.used_q[b]))
+                                for b in range(g.num_segments)])
+    done, rows_done = 0.0, 0
+    t0 = time.perf_counter()
+    while True:
+        rows = np.sort(rng.choice(used_rows, size=64, replace=False))
+        gva_oracle.lse_merge([o[rows] for o in outs], [x[:, rows] for x in lses], [0, len(rows)], [len(rows)])
+        done += merge_bytes(g, wl.used_k_parts, 2, rows=rows)
+        rows_done += len(rows)
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    desc = (f"{rows_done} seeded used rows (all {g.num_heads_q} heads, {len(outs)} FP32 partitions) of the "
+            f"{wl.name} workload, FP64 NumPy oracle merge")
+    return done / el / 1e9, desc, rows_done, el
+
+
 # --------------------------------------------------------------------------------------
 
 def main():
@@ -465,7 +596,8 @@ def main():
     ap.add_argument("--workload", default="long_replay",
                     choices=["long_replay", "long_replay_small", "cfg_text_cross", "multiview_causal",
                              "multiview_fused", "multiview_blockcausal", "long_replay_bwd", "long_replay_small_bwd",
-                             "multiview_blockcausal_bwd", "multiview_fused_bwd", "tiny"])
+                             "multiview_blockcausal_bwd", "multiview_fused_bwd", "lse_merge_union", "lse_merge",
+                             "tiny"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     args = ap.parse_args()
@@ -507,26 +639,50 @@ def main():
 
     flush = None
     if wl.input_bytes() <= 2 * 129e6:
-        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        flush = L2Flush()
 
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clocks:
+        clocks.wait_samples(1, 5.0)  # nvidia-smi is up before the timed region starts
+        n_before = len(clocks.lines)
         torch.cuda.nvtx.range_push("timed")  # lets a profiler keep only the timed launches
         ms = time_steps(wl.step, args.steps, stream, flush)
         torch.cuda.synchronize()
         torch.cuda.nvtx.range_pop()
+        clock_window = "timed region"
+        if len(clocks.lines) - n_before < 3:
+            # a timed region shorter than the 200 ms sampling period: sample the same
+            # steps, untimed, right after it
+            def more():
+                for _ in range(4):
+                    wl.step()
+                torch.cuda.synchronize()
+            clocks.wait_samples(n_before + 3, 3.0, work=more)
+            clock_window = ("timed region plus the same steps, untimed, right after it (the region is shorter "
+                            "than the sampling period)")
     barrier()
     ms_step = ms / args.steps
-    # kernel-only time of the dominant launch (the forward; for the backward workload the
-    # whole backward call) over the same kind of region
-    if getattr(wl, "backward", False):
+    # kernel-only time of the dominant launch (the forward with the most FLOPs; for the
+    # backward workload the whole backward call, for the merge workload the merge) over
+    # the same kind of region
+    if getattr(wl, "backward", False) or wl.merge_only:
         fwd_only = wl.step
     else:
-        fwd_only = lambda: wl.gva.forward(wl.plans[0], wl.q, wl.k, wl.v,  # noqa: E731
-                                          *(wl.partials[0] if wl.partials else (wl.out, wl.lse)))
+        i = wl.dominant
+        fwd_only = lambda: wl.gva.forward(wl.plans[i], wl.q, *wl.kv_of(i),  # noqa: E731
+                                          *(wl.partials[i] if wl.partials else (wl.out, wl.lse)))
     fwd_ms = time_steps(fwd_only, max(3, args.steps // 2), stream, flush) / max(3, args.steps // 2)
     wl.check()
+    copy_gbs = None
+    if wl.bound == "hbm":
+        # context for an HBM-bound kernel of this size: a device copy moving the same
+        # bytes (half read, half written), timed the same way
+        src = torch.empty(int(wl.work // 2), dtype=torch.uint8, device="cuda")
+        dst = torch.empty_like(src)
+        copy_ms = time_steps(lambda: dst.copy_(src), 10, stream, flush) / 10
+        copy_gbs = wl.work / (copy_ms * 1e-3) / 1e9
+        del src, dst
 
     # end to end through the public API: every step copies its inputs from pinned host
     # memory and its results back, inside the timed region (pipelined over two buffers)
@@ -546,17 +702,25 @@ def main():
 
     peaks, peak_src = load_peaks()
     sustained = args.steps * ms_step > 1000.0
-    peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
-    value = job_tflops(world, wl.flops, ms_step)
-    fwd_flops = wl.flops if getattr(wl, "backward", False) else wl.plans[0].info()["used_flops"]
-    achieved = fwd_flops / (fwd_ms * 1e-3) / 1e12
+    if wl.bound == "hbm":
+        peak = peaks["hbm_gbs"]
+        peak_desc = f"{peak_src} HBM copy bandwidth (STREAM-style, read + write bytes)"
+    else:
+        peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+        peak_desc = f"{peak_src} {'sustained' if sustained else 'burst'} dense bf16 (cuBLAS)"
+    value = job_rate(world, wl.work, ms_step, wl.scale)
+    if getattr(wl, "backward", False) or wl.merge_only:
+        dom_work = wl.work
+    else:
+        dom_work = wl.plans[wl.dominant].info()["used_flops"]
+    achieved = dom_work / (fwd_ms * 1e-3) / wl.scale
     traffic = recorded_traffic(args.workload)
     cpu_rate, cpu_desc, _, _ = oracle_sample_rate(wl, args.cpu_budget_s)
-    e2e_value = job_tflops(world, wl.flops, e2e_ms)
+    e2e_value = job_rate(world, wl.work, e2e_ms, wl.scale)
     line = {
         "metric": wl.metric,
         "value": round(value, 3),
-        "unit": UNIT,
+        "unit": wl.unit,
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
@@ -567,27 +731,28 @@ def main():
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16, the pages' segment shapes)",
         "config": {**wl.config(), "parallelism": f"replicas x{world} (independent problems per GPU)"},
-        "pct_of_bf16_peak": round(100.0 * value / world / peak, 2),
+        ("pct_of_hbm_peak" if wl.bound == "hbm" else "pct_of_bf16_peak"): round(100.0 * value / world / peak, 2),
         "roofline": {
-            "bound": "tensor",
+            "bound": wl.bound,
             "achieved": round(achieved, 2),
             "peak": peak,
-            "unit": "TFLOP/s",
+            "unit": wl.unit,
             "frac": round(achieved / peak, 4),
             "traffic": traffic,
             "kernel": wl.kernel,
             "ms_per_launch": round(fwd_ms, 4),
-            "peak_source": f"{peak_src} {'sustained' if sustained else 'burst'} dense bf16 (cuBLAS)",
+            "peak_source": peak_desc,
+            **({"same_size_copy_gbs": round(copy_gbs, 1)} if copy_gbs is not None else {}),
         },
-        "e2e": {"value": round(e2e_value, 3), "unit": UNIT,
+        "e2e": {"value": round(e2e_value, 3), "unit": wl.unit,
                 "h2d_bytes_per_step": int(wl.input_bytes()), "d2h_bytes_per_step": int(wl.output_bytes()),
                 "ms_per_step": round(e2e_ms, 4),
                 "copies": "pinned host buffers; every step copies its inputs in and its results out; two device "
                           "buffer sets and two copy streams overlap step i+1's input copy and step i-1's result "
                           "copy with step i"},
         "gpu_launches": args.steps * wl.launches_per_step,
-        "clocks": clocks.summary(),
-        "cpu_baseline": {"value": round(cpu_rate, 6), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+        "clocks": {**clocks.summary(), "window": clock_window},
+        "cpu_baseline": {"value": round(cpu_rate, 6), "unit": wl.unit, "cores": os.cpu_count(), "kind": "oracle",
                          "sample": cpu_desc},
     }
     print(json.dumps(line))
@@ -628,12 +793,24 @@ def run_reference(args, world, rank):
         g = W.long_replay_small()
         wl.geoms = [g]
         seed = 1006
+    elif args.workload in ("lse_merge_union", "lse_merge"):
+        text, video, g, _ = W.lse_merge_union()
+        wl.geoms = [text, video]
+        seed = 1004
     else:
         g = W.tiny()
         wl.geoms = [g]
         seed = 1001
-    wl.q, wl.k, wl.v = W.make_qkv(g, seed)
-    metric = METRIC
+    metric, unit = METRIC, UNIT
+    if args.workload == "lse_merge_union":
+        wl.q, kt, vt = W.make_qkv(text, seed)
+        wl.part_kv = [(kt, vt), W.make_qkv(video, 2004)[1:]]
+    elif args.workload == "lse_merge":
+        wl.merge_only, wl.parts, wl.used_k_parts = True, g, [text.used_k, video.used_k]
+        wl.partials = list(zip(*W.make_partials(g, wl.used_k_parts, 3004)))
+        metric, unit = "gapped-varlen FP32 LSE merge GB/s (algorithmic bytes: live partials, LSEs, output)", "GB/s"
+    else:
+        wl.q, wl.k, wl.v = W.make_qkv(g, seed)
     if args.workload in ("long_replay_bwd", "long_replay_small_bwd", "multiview_blockcausal_bwd",
                          "multiview_fused_bwd"):
         wl.backward = True
@@ -653,7 +830,7 @@ def run_reference(args, world, rank):
         "impl": "reference",
         "metric": metric,
         "value": round(value, 6),
-        "unit": UNIT,
+        "unit": unit,
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
@@ -664,9 +841,9 @@ def run_reference(args, world, rank):
         "dtype": "f64",
         "data": "synthetic (seeded N(0,1) bf16 widened to f64)",
         "config": {"workload": args.workload},
-        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
                          "sample": descs[-1] + f"; {budget:.1f} s per step"},
-        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
 

@@ -290,7 +290,7 @@ gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
   p->num_items = static_cast<int32_t>(sorted.size());
   p->num_units = static_cast<int32_t>(units.size());
   p->grid = std::min(p->num_items, sms);
-  p->merge_grid = std::min(p->num_units, sms * 8);
+  p->merge_grid = sms * 8;  // the merge launch's cap: 8 resident CTAs per SM
   p->used_flops = flops;
   if ((e = cudaMalloc(&p->d_error, sizeof(int))) != cudaSuccess || (e = cudaMemset(p->d_error, 0, sizeof(int))) != cudaSuccess) {
     free_plan(p);

@@ -111,7 +111,7 @@ constexpr int kErrWaitTimeout = 1;
 // Launchers (defined in gva_fwd.cu / gva_merge.cu). They return the launch error.
 cudaError_t launch_forward(int head_dim, bool out_f32, const FwdParams& p, const CUtensorMap& map_q,
                            const CUtensorMap& map_k, const CUtensorMap& map_v, int grid, cudaStream_t stream);
-cudaError_t launch_merge(bool in_f32, bool out_f32, const MergeParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_merge(bool in_f32, bool out_f32, const MergeParams& p, int max_grid, cudaStream_t stream);
 int forward_smem_bytes(int head_dim);
 // Backward: rowsum(dO * O) over used rows, then dQ, then dK / dV (gva_bwd.cu).
 // Backward kernels take the block-causal variant when p.causal_block > 0.

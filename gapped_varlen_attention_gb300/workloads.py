@@ -230,6 +230,29 @@ def make_qkv(g: Geometry, seed: int, device: str = "cpu", dtype=None,
     return q, k, v
 
 
+def make_partials(g: Geometry, used_k_parts, seed: int, device: str = "cpu", dtype=None):
+    """Partial results of ``len(used_k_parts)`` key partitions of ``g``'s rows, as the
+    forward leaves them: O ~ N(0, 1) ``[total_q, Hq, d]`` (fp32 by default) and LSE ~
+    N(0, 3^2) ``[Hq, total_q]``, except that the used rows of a segment whose partition
+    has no keys (``used_k_parts[p][b] == 0``) hold O = 0 and LSE = -inf."""
+    assert torch is not None
+    dtype = dtype or torch.float32
+    gen = torch.Generator(device=device).manual_seed(seed)
+    outs, lses = [], []
+    for uk in used_k_parts:
+        o = torch.randn((g.total_q, g.num_heads_q, g.head_dim), generator=gen, device=device,
+                        dtype=torch.float32).to(dtype)
+        lse = 3.0 * torch.randn((g.num_heads_q, g.total_q), generator=gen, device=device, dtype=torch.float32)
+        for b in range(g.num_segments):
+            if int(uk[b]) == 0:
+                r0, r1 = int(g.cu_q[b]), int(g.cu_q[b]) + int(g.used_q[b])
+                o[r0:r1] = 0.0
+                lse[:, r0:r1] = -float("inf")
+        outs.append(o)
+        lses.append(lse)
+    return outs, lses
+
+
 def make_outputs(g: Geometry, fill: float, device: str = "cpu", out_dtype=None):
     """O ``[total_q, Hq, d]`` and LSE ``[Hq, total_q]`` prefilled with a sentinel."""
     assert torch is not None

@@ -89,3 +89,46 @@ def test_merge_rejects_bad_counts():
         gva.lse_merge(plan, [], [], o, l)
     with pytest.raises(gva.GvaError, match="num_parts"):
         gva.lse_merge(plan, [o] * 9, [l] * 9, o, l)
+
+
+@pytest.mark.parametrize("parts,in_dtype", [(2, torch.float32), (3, torch.bfloat16), (5, torch.float32)])
+def test_merge_skips_keyless_partitions(parts, in_dtype):
+    """A partition whose LSE is -inf for a row has no keys there: its output is never
+    read (NaN there must not leak), and the merge is the other partitions' result."""
+    g = W.random_geometry(np.random.default_rng(11 + parts), 6, 120, 10, 8, 8, 128, allow_empty=False)
+    gen = torch.Generator().manual_seed(12)
+    outs, lses = _partials(g, parts, gen, in_dtype, dead_frac=0.3)
+    for o, l in zip(outs, lses):
+        o.permute(1, 0, 2)[torch.isneginf(l)] = float("nan")
+    o_ref, l_ref = gva_oracle.lse_merge([x.float().numpy() for x in outs], [x.numpy() for x in lses], g.cu_q,
+                                        g.used_q, out=np.zeros((g.total_q, 8, 128)), lse=np.zeros((8, g.total_q)))
+    plan = gva.Plan.from_geometry(g)
+    o, l = W.make_outputs(g, 0.0, device="cuda", out_dtype=torch.float32)
+    gva.lse_merge(plan, [x.cuda() for x in outs], [x.cuda() for x in lses], o, l)
+    gva.device_status(plan)
+    og = o.cpu().numpy()
+    used = ~W.gap_rows(g.cu_q, g.used_q)
+    assert not np.isnan(og[used]).any()
+    assert np.all(np.abs(og[used] - o_ref[used]) <= 1e-5 * np.abs(o_ref[used]) + 1e-5)
+    dead = np.isneginf(l_ref) & used[None, :]
+    assert np.all(og.transpose(1, 0, 2)[dead] == 0.0)
+
+
+def test_merge_in_place_output_only():
+    """out aliases the first partition while the merged LSE goes to its own buffer (the
+    merge may then share a unit among several CTAs)."""
+    g = W.random_geometry(np.random.default_rng(8), 6, 100, 10, 16, 16, 64, allow_empty=False)
+    gen = torch.Generator().manual_seed(9)
+    outs, lses = _partials(g, 3, gen, torch.float32)
+    o_ref, l_ref = gva_oracle.lse_merge([x.numpy() for x in outs], [x.numpy() for x in lses], g.cu_q, g.used_q,
+                                        out=outs[0].numpy(), lse=np.zeros((16, g.total_q)))
+    plan = gva.Plan.from_geometry(g)
+    o0 = outs[0].cuda()
+    lse = torch.zeros(16, g.total_q, device="cuda")
+    gva.lse_merge(plan, [o0] + [x.cuda() for x in outs[1:]], [x.cuda() for x in lses], o0, lse)
+    gva.device_status(plan)
+    assert np.abs(o0.cpu().numpy() - o_ref).max() <= 1e-5
+    lg = lse.cpu().numpy()
+    assert np.array_equal(np.isneginf(lg), np.isneginf(l_ref))
+    fin = np.isfinite(l_ref)
+    assert np.abs(lg[fin] - l_ref[fin]).max() <= 1e-5
