@@ -42,6 +42,8 @@ CSRC = os.path.join(ROOT, "gapped_varlen_attention_gb300", "csrc")
 TRAFFIC_SUMMARIES = {
     "long_replay": (os.path.join(ROOT, "profiles", "gva_fwd_kernel_long_replay.md"), os.path.join(CSRC, "gva_fwd.cu")),
     "long_replay_bwd": (os.path.join(ROOT, "profiles", "gva_backward_long_replay.md"), os.path.join(CSRC, "gva_bwd.cu")),
+    "lse_merge": (os.path.join(ROOT, "profiles", "gva_lse_merge_kernel_text_video.md"),
+                  os.path.join(CSRC, "gva_merge.cu")),
 }
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 

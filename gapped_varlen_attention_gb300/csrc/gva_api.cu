@@ -18,7 +18,7 @@ struct gva_plan {
   int sm_count = 0;
   int32_t num_segments = 0, num_heads_q = 0, num_heads_kv = 0, head_dim = 0, group = 0, causal_block = 0;
   int64_t total_q = 0, total_k = 0;
-  int32_t num_items = 0, num_units = 0, grid = 0, merge_grid = 0;
+  int32_t num_items = 0, num_units = 0, grid = 0;
   double used_flops = 0.0;
   gva::WorkItem* d_items = nullptr;
   gva::KeyBlock* d_blocks = nullptr;
@@ -290,7 +290,6 @@ gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
   p->num_items = static_cast<int32_t>(sorted.size());
   p->num_units = static_cast<int32_t>(units.size());
   p->grid = std::min(p->num_items, sms);
-  p->merge_grid = sms * 8;  // the merge launch's cap: 8 resident CTAs per SM
   p->used_flops = flops;
   if ((e = cudaMalloc(&p->d_error, sizeof(int))) != cudaSuccess || (e = cudaMemset(p->d_error, 0, sizeof(int))) != cudaSuccess) {
     free_plan(p);
@@ -359,8 +358,7 @@ gva_status validate_common(const int32_t* cu_seqlens_q, const int32_t* seqused_q
     return fail(GVA_ERR_UNSUPPORTED, "query heads per KV head (%d) must divide %d", group, gva::kTileRows);
   if (head_dim != 64 && head_dim != 128)
     return fail(GVA_ERR_UNSUPPORTED, "head_dim=%d is not supported (64 or 128)", head_dim);
-  if (num_heads_q * gva::kMergeRows * gva::kMaxMergeParts * 4 > 200 * 1024)
-    return fail(GVA_ERR_UNSUPPORTED, "num_heads_q=%d is too large", num_heads_q);
+  if (num_heads_q > 256) return fail(GVA_ERR_UNSUPPORTED, "num_heads_q=%d is too large (at most 256)", num_heads_q);
   return validate_offsets(cu_seqlens_q, seqused_q, num_segments, "q");
 }
 
@@ -573,7 +571,12 @@ gva_status gva_lse_merge(gva_plan_t plan, int32_t num_parts, const void* const* 
   prm.total_q = plan->total_q;
   prm.num_heads_q = plan->num_heads_q;
   prm.head_dim = plan->head_dim;
-  e = gva::launch_merge(in_dtype == GVA_FP32, out_dtype == GVA_FP32, prm, plan->merge_grid, stream);
+  prm.error_flag = plan->d_error;
+  int ring_slots = 0;
+  if (gva::merge_smem_bytes(in_dtype == GVA_FP32, num_parts, plan->num_heads_q, &ring_slots) < 0)
+    return fail(GVA_ERR_UNSUPPORTED, "%d partitions of %d query heads do not fit the merge's shared memory",
+                num_parts, plan->num_heads_q);
+  e = gva::launch_merge(in_dtype == GVA_FP32, out_dtype == GVA_FP32, prm, plan->sm_count, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launching the LSE merge kernel");
   return ok();
 }

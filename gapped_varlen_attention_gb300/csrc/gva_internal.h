@@ -81,6 +81,7 @@ struct MergeParams {
   int64_t total_q;
   int32_t num_heads_q;
   int32_t head_dim;
+  int* error_flag;
 };
 
 struct BwdParams {
@@ -111,7 +112,11 @@ constexpr int kErrWaitTimeout = 1;
 // Launchers (defined in gva_fwd.cu / gva_merge.cu). They return the launch error.
 cudaError_t launch_forward(int head_dim, bool out_f32, const FwdParams& p, const CUtensorMap& map_q,
                            const CUtensorMap& map_k, const CUtensorMap& map_v, int grid, cudaStream_t stream);
-cudaError_t launch_merge(bool in_f32, bool out_f32, const MergeParams& p, int max_grid, cudaStream_t stream);
+// The merge runs one persistent CTA per resident slot (as many as fit per SM x sm_count).
+cudaError_t launch_merge(bool in_f32, bool out_f32, const MergeParams& p, int sm_count, cudaStream_t stream);
+// Dynamic shared memory of the merge launch (and its chunk ring slots), or -1 when the
+// partitions' weights leave no room for one chunk of every partition.
+int merge_smem_bytes(bool in_f32, int num_parts, int num_heads_q, int* ring_slots);
 int forward_smem_bytes(int head_dim);
 // Backward: rowsum(dO * O) over used rows, then dQ, then dK / dV (gva_bwd.cu).
 // Backward kernels take the block-causal variant when p.causal_block > 0.

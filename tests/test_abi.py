@@ -71,6 +71,7 @@ BAD = [
     ("zero heads", ([0, 8], [8], [0, 8], [8], 0, 1, 64), 1, "positive"),
     ("head_dim 96", ([0, 8], [8], [0, 8], [8], 4, 2, 96), 2, "head_dim"),
     ("group 3 does not divide 128", ([0, 8], [8], [0, 8], [8], 24, 8, 128), 2, "divide"),
+    ("more than 256 query heads", ([0, 8], [8], [0, 8], [8], 512, 256, 64), 2, "too large"),
 ]
 
 
