@@ -411,7 +411,8 @@ class L2Flush:
 def time_steps(fn, steps: int, stream, flush=None) -> float:
     """Device milliseconds for `steps` calls of fn, CUDA events on `stream`. With a
     flush (an L2Flush, for inputs smaller than L2), it runs before every step, outside
-    the events, so each step starts with a cold L2 and only the step is timed."""
+    the events, so each step starts with a cold L2 and only the step is timed; a short
+    device-side sleep after it covers the host's time to issue the step."""
     if flush is None:
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
@@ -424,6 +425,9 @@ def time_steps(fn, steps: int, stream, flush=None) -> float:
     pairs = []
     for _ in range(steps):
         flush()
+        # keep the device busy (outside the events) while the host issues the step, so
+        # that a short step is timed from its first launch, not from the host's call
+        torch.cuda._sleep(100000)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         fn()

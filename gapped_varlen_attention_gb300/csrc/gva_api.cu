@@ -525,6 +525,7 @@ gva_status gva_forward(gva_plan_t plan, const void* q, const void* k, const void
   prm.blocks = plan->d_blocks;
   prm.num_items = plan->num_items;
   prm.out = out;
+  prm.out_wide = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
   prm.lse = lse;
   prm.total_q = plan->total_q;
   prm.num_heads_q = plan->num_heads_q;

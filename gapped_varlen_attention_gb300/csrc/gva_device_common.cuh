@@ -44,6 +44,10 @@ __device__ __forceinline__ int item_index(int round, int cta, int grid) {
   return (round & 1) ? round * grid + (grid - 1 - cta) : round * grid + cta;
 }
 
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ WorkItem load_item(const WorkItem* items, int idx) {
   const int4* p = reinterpret_cast<const int4*>(items + idx);
   const int4 a = __ldg(p), b = __ldg(p + 1);
@@ -76,6 +80,42 @@ __device__ __forceinline__ void store_row32<float>(float* dst, const float (&x)[
   float4* d = reinterpret_cast<float4*>(dst);
 #pragma unroll
   for (int i = 0; i < 8; ++i) d[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+}
+
+// The same rows with 32-byte stores (st.global.v8.b32, sm_100 and later): half the
+// store instructions. A warp's 32 rows are 32 different rows of the output, so every
+// store instruction touches 32 lines and the epilogue is bound by the number of store
+// instructions. `dst` must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* dst, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t a4, uint32_t a5, uint32_t a6, uint32_t a7) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a0), "r"(a1), "r"(a2),
+               "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+               : "memory");
+}
+
+template <typename TOut>
+__device__ __forceinline__ void store_row32_wide(TOut* dst, const float (&x)[32]);
+
+template <>
+__device__ __forceinline__ void store_row32_wide<__nv_bfloat16>(__nv_bfloat16* dst, const float (&x)[32]) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float* y = x + 16 * i;
+    st_global_v8(dst + 16 * i, pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                 pack_bf16x2(y[6], y[7]), pack_bf16x2(y[8], y[9]), pack_bf16x2(y[10], y[11]),
+                 pack_bf16x2(y[12], y[13]), pack_bf16x2(y[14], y[15]));
+  }
+}
+
+template <>
+__device__ __forceinline__ void store_row32_wide<float>(float* dst, const float (&x)[32]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float* y = x + 8 * i;
+    st_global_v8(dst + 8 * i, __float_as_uint(y[0]), __float_as_uint(y[1]), __float_as_uint(y[2]),
+                 __float_as_uint(y[3]), __float_as_uint(y[4]), __float_as_uint(y[5]), __float_as_uint(y[6]),
+                 __float_as_uint(y[7]));
+  }
 }
 
 // MMA issue. One thread issues every tcgen05.mma, so the issue path must be short:

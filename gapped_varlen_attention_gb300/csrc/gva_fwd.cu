@@ -259,6 +259,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int idx = item_index(round, blockIdx.x, gridDim.x);
       if (idx >= p.num_items) break;
       const WorkItem it = load_item(p.items, idx);
+      // the next round's item is pulled into L1 now, so its load does not sit between
+      // this item's epilogue and the next item's softmax
+      const int idx_next = item_index(round + 1, blockIdx.x, gridDim.x);
+      if (idx_next < p.num_items) prefetch_l1(p.items + idx_next);
       if (it.n_tiles <= t) continue;
       const bool valid = tok < it.q_rows - t * T;
       const int64_t token = static_cast<int64_t>(it.q_row0) + t * T + tok;
@@ -271,7 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) z[i] = 0.0f;
 #pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch) store_row32<TOut>(orow + ch * 32, z);
+          for (int ch = 0; ch < D / 32; ++ch) {
+            if (p.out_wide) store_row32_wide<TOut>(orow + ch * 32, z);
+            else store_row32<TOut>(orow + ch * 32, z);
+          }
           *lrow = -CUDART_INF_F;
         }
         continue;
@@ -418,7 +425,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         float x[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(o[i]) * inv_l;
-        if (valid) store_row32<TOut>(orow + ch * 32, x);
+        if (valid) {
+          if (p.out_wide) store_row32_wide<TOut>(orow + ch * 32, x);
+          else store_row32<TOut>(orow + ch * 32, x);
+        }
       }
       if (valid) *lrow = lse_val;
     }

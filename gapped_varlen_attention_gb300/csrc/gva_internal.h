@@ -67,6 +67,7 @@ struct FwdParams {
   int32_t tokens_per_tile;  // kTileRows / group
   float scale_log2;         // softmax scale * log2(e)
   int32_t causal_block;     // > 0: block-causal masking within each segment
+  int32_t out_wide;         // out is 32-byte aligned: rows are stored with 32-byte stores
   int* error_flag;
 };
 

@@ -225,6 +225,7 @@ extern "C" GVA_API gva_status gva_forward_noalloc(
   prm.blocks = d_blocks;
   prm.num_items = n;
   prm.out = out;
+  prm.out_wide = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
   prm.lse = lse;
   prm.total_q = total_q;
   prm.num_heads_q = num_heads_q;
