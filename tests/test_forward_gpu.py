@@ -38,6 +38,27 @@ def test_tiny_workload_fp32_output():
     check_full(g, o, l, o_ref, l_ref, W.TINY_SENTINEL)
 
 
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_output_only_16_byte_aligned(out_dtype):
+    """An output that is 16- but not 32-byte aligned takes the 16-byte store path; the
+    result is the same as through an aligned buffer, and the elements just before and
+    after the output stay untouched."""
+    g = W.random_geometry(np.random.default_rng(77), 4, 300, 500, 8, 2, 128)
+    q, k, v = W.make_qkv(g, 77)
+    o_ref, l_ref = gpu_forward(g, q, k, v, out_dtype=out_dtype)
+    pad = 16 // torch.tensor([], dtype=out_dtype).element_size()
+    n = g.total_q * g.num_heads_q * g.head_dim
+    buf = torch.full((n + 2 * pad,), W.TINY_SENTINEL, dtype=out_dtype, device="cuda")
+    o = buf[pad:pad + n].view(g.total_q, g.num_heads_q, g.head_dim)
+    assert o.data_ptr() % 32 == 16
+    l = torch.full((g.num_heads_q, g.total_q), W.TINY_SENTINEL, device="cuda")
+    plan = gva.Plan.from_geometry(g)
+    gva.forward(plan, q.cuda(), k.cuda(), v.cuda(), o, l)
+    gva.device_status(plan)
+    assert torch.equal(o, o_ref) and torch.equal(l, l_ref)
+    assert torch.all(buf[:pad] == W.TINY_SENTINEL) and torch.all(buf[pad + n:] == W.TINY_SENTINEL)
+
+
 def test_cfg_text_cross_attention():
     """CFG B=2: 4096 query rows per sample, text keys padded to 1024 with exact-zero pads,
     real lengths 700 and 20. Full comparison."""
