@@ -604,7 +604,7 @@ def main():
                              "multiview_fused", "multiview_blockcausal", "long_replay_bwd", "long_replay_small_bwd",
                              "multiview_blockcausal_bwd", "multiview_fused_bwd", "lse_merge_union", "lse_merge",
                              "tiny"])
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     args = ap.parse_args()
 
