@@ -233,11 +233,12 @@ cudaError_t launch_merge_impl(const MergeParams& p, int sm_count, cudaStream_t s
 int merge_smem_bytes(bool in_f32, int num_parts, int num_heads_q, int* ring_slots) {
   const int chunk = kChunkElems * (in_f32 ? 4 : 2);
   const int fixed = num_parts * num_heads_q * kMergeRows * 4 + (kMaxMergeParts + 1) * 4;
-  // slots: a whole number of chunk groups (one chunk of every partition), within the
-  // ring budget and the shared-memory cap, at least one group
-  int slots = std::min(kRingBytes / chunk, (kMergeSmemCap - fixed) / (chunk + 8));
-  slots = slots / num_parts * num_parts;
-  if (slots < num_parts) return -1;
+  // slots: a whole number of chunk groups (one chunk of every partition), as many as
+  // the ring budget holds but at least one, within the shared-memory cap
+  const int cap_groups = (kMergeSmemCap - fixed) / ((chunk + 8) * num_parts);
+  const int groups = std::min(std::max(kRingBytes / (chunk * num_parts), 1), cap_groups);
+  if (groups < 1) return -1;
+  const int slots = groups * num_parts;
   *ring_slots = slots;
   return slots * (chunk + 8) + fixed;
 }

@@ -36,10 +36,12 @@ def _partials(g, parts, rng, in_dtype, dead_frac=0.15):
     (3, torch.float32, torch.float32, 16, 128),
     (8, torch.bfloat16, torch.float32, 4, 64),
     (1, torch.float32, torch.float32, 32, 128),
+    (8, torch.float32, torch.bfloat16, 256, 64),   # most weights: 8 x 256 heads, one chunk group
+    (7, torch.float32, torch.float32, 48, 128),
 ])
 def test_merge_matches_oracle(parts, in_dtype, out_dtype, hq, d):
     rng_np = np.random.default_rng(parts * 100 + hq)
-    g = W.random_geometry(rng_np, 7, 90, 10, hq, hq, d)
+    g = W.random_geometry(rng_np, 7 if hq <= 64 else 3, 90 if hq <= 64 else 40, 10, hq, hq, d)
     gen = torch.Generator().manual_seed(5)
     outs, lses = _partials(g, parts, gen, in_dtype)
     plan = gva.Plan.from_geometry(g)
