@@ -179,9 +179,13 @@ GVA_API gva_status gva_forward(gva_plan_t plan, const void* q, const void* k, co
  *   outs      : HOST array of num_parts DEVICE pointers, in_dtype, [total_q, Hq, d]
  *   lses      : HOST array of num_parts DEVICE fp32 pointers, [Hq, total_q]
  *   out, lse  : DEVICE outputs (out_dtype / fp32); out may alias outs[0] and lse may
- *               alias lses[0] (each element is read before it is written by the same
- *               thread); rows past the used length are not written.
- * Computed in FP32. Asynchronous on `stream`.
+ *               alias lses[0] (every element is read before it is written); rows past
+ *               the used length are not written.
+ * outs and out must be 16-byte aligned, lses and lse 4-byte aligned. Computed in FP32.
+ * Asynchronous on `stream`; no allocation.
+ * Errors: GVA_ERR_INVALID_ARG for a NULL plan or pointer, num_parts outside 1 .. 8, a bad
+ * dtype, a misaligned pointer or a plan built on another device; GVA_ERR_CUDA if the
+ * launch fails.
  */
 GVA_API gva_status gva_lse_merge(gva_plan_t plan, int32_t num_parts, const void* const* outs, gva_dtype in_dtype,
                          const float* const* lses, void* out, gva_dtype out_dtype, float* lse,
