@@ -275,6 +275,48 @@ class Workload:
     def output_bytes(self):
         return sum(t.numel() * t.element_size() for t in self.outputs)
 
+    def row_ranges(self):
+        """(inputs, outputs): per tensor, the row ranges along dim 0 that hold data (the
+        used rows of every segment), or None for a tensor that is copied whole (LSE and
+        D, laid out [heads, rows]). Gap rows are neither inputs nor results."""
+        def used(cu, n):
+            out = []
+            for b in range(len(n)):
+                r0, k = int(cu[b]), int(n[b])
+                if k == 0:
+                    continue
+                if out and out[-1][0] + out[-1][1] == r0:
+                    out[-1] = (out[-1][0], out[-1][1] + k)
+                else:
+                    out.append((r0, k))
+            return out
+        qg = self.parts if self.parts is not None else self.geoms[0]
+        q = used(qg.cu_q, qg.used_q)
+        if self.merge_only:
+            return [q, None] * len(self.partials), [q, None]
+        if getattr(self, "part_kv", None) is not None:
+            ks = [used(g.cu_k, g.used_k) for g in self.geoms]
+            return [q] + [r for k in ks for r in (k, k)], [q, None]
+        kg = self.parts if self.parts is not None else self.geoms[0]
+        if getattr(self, "ranges", None) is not None:
+            k = sorted((st, n) for rs in self.ranges for st, n in rs if n > 0)
+        else:
+            k = used(kg.cu_k, kg.used_k)
+        if getattr(self, "backward", False):
+            return [q, k, k, q, None, q], [q, k, k]
+        return [q, k, k], [q, None]
+
+    def copy_bytes(self):
+        """Bytes the end-to-end steps copy in and out per step (the row ranges above)."""
+        def nbytes(ts, rs):
+            tot = 0
+            for t, r in zip(ts, rs):
+                row = t[0].numel() * t.element_size() if t.shape[0] else 0
+                tot += t.numel() * t.element_size() if r is None else sum(n for _, n in r) * row
+            return tot
+        ri, ro = self.row_ranges()
+        return nbytes(self.inputs, ri), nbytes(self.outputs, ro)
+
 
 def merge_bytes(g, used_k_parts, out_bytes: int, rows=None) -> float:
     """Algorithmic bytes of one FP32 LSE merge over g's used rows (or the listed rows):
@@ -437,6 +479,15 @@ def time_steps(fn, steps: int, stream, flush=None) -> float:
     return sum(a.elapsed_time(b) for a, b in pairs)
 
 
+def copy_rows(dst, src, ranges):
+    """Asynchronous copy of the listed row ranges (dim 0), or of the whole tensor."""
+    if ranges is None:
+        dst.copy_(src, non_blocking=True)
+        return
+    for r0, n in ranges:
+        dst[r0:r0 + n].copy_(src[r0:r0 + n], non_blocking=True)
+
+
 class E2EPipeline:
     """Steps through the public API with host buffers: for every step, the host->device
     copy of its inputs (pinned host memory), the step, and the device->host copy of its
@@ -446,6 +497,7 @@ class E2EPipeline:
 
     def __init__(self, wl, stream):
         self.wl, self.stream = wl, stream
+        self.r_in, self.r_out = wl.row_ranges()
         self.h_in = [t.cpu().pin_memory() for t in wl.inputs]
         self.d_in = [[torch.empty_like(t) for t in wl.inputs] for _ in range(2)]
         self.d_out = [[torch.empty_like(t) for t in wl.outputs] for _ in range(2)]
@@ -466,8 +518,8 @@ class E2EPipeline:
             with torch.cuda.stream(self.s_in):
                 if computed[b] is not None:
                     self.s_in.wait_event(computed[b])
-                for d, h in zip(self.d_in[b], self.h_in):
-                    d.copy_(h, non_blocking=True)
+                for d, h, r in zip(self.d_in[b], self.h_in, self.r_in):
+                    copy_rows(d, h, r)
                 loaded = torch.cuda.Event()
                 loaded.record(self.s_in)
             st.wait_event(loaded)
@@ -478,8 +530,8 @@ class E2EPipeline:
             computed[b].record(st)
             with torch.cuda.stream(self.s_out):
                 self.s_out.wait_event(computed[b])
-                for h, d in zip(self.h_out[b], self.d_out[b]):
-                    h.copy_(d, non_blocking=True)
+                for h, d, r in zip(self.h_out[b], self.d_out[b], self.r_out):
+                    copy_rows(h, d, r)
                 copied[b] = torch.cuda.Event()
                 copied[b].record(self.s_out)
         st.wait_stream(self.s_in)
@@ -751,11 +803,12 @@ def main():
             **({"same_size_copy_gbs": round(copy_gbs, 1)} if copy_gbs is not None else {}),
         },
         "e2e": {"value": round(e2e_value, 3), "unit": wl.unit,
-                "h2d_bytes_per_step": int(wl.input_bytes()), "d2h_bytes_per_step": int(wl.output_bytes()),
+                "h2d_bytes_per_step": int(wl.copy_bytes()[0]), "d2h_bytes_per_step": int(wl.copy_bytes()[1]),
                 "ms_per_step": round(e2e_ms, 4),
-                "copies": "pinned host buffers; every step copies its inputs in and its results out; two device "
-                          "buffer sets and two copy streams overlap step i+1's input copy and step i-1's result "
-                          "copy with step i"},
+                "copies": "pinned host buffers; every step copies its inputs in and its results out: the used "
+                          "rows of each [rows, heads, d] tensor (gap rows are neither inputs nor results) and whole "
+                          "LSE-shaped tensors; two device buffer sets and two copy streams overlap step i+1's input "
+                          "copy and step i-1's result copy with step i"},
         "gpu_launches": args.steps * wl.launches_per_step,
         "clocks": {**clocks.summary(), "window": clock_window},
         "cpu_baseline": {"value": round(cpu_rate, 6), "unit": wl.unit, "cores": os.cpu_count(), "kind": "oracle",
