@@ -64,20 +64,20 @@ def oracle_backward(g, q, k, v, do, scale=None, causal_block=0):
                                          dv=np.full(vn.shape, FILL), causal_block=causal_block)
 
 
-def _close(name, got, ref, max_rel=MAX_REL, rms_rel=RMS_REL):
+def _close(name, got, ref, max_rel=MAX_REL, rms_rel=RMS_REL, atol=0.0):
     if ref.size == 0:
         return 0.0
     err = np.abs(got - ref)
     scale = max(np.abs(ref).max(), 1e-30)
     assert np.all(np.isfinite(got)), f"{name}: non-finite values"
-    assert err.max() <= max_rel * scale, f"{name}: max err {err.max():.3e} > {max_rel:.1e} x {scale:.3e}"
+    assert err.max() <= max_rel * scale + atol, f"{name}: max err {err.max():.3e} > {max_rel:.1e} x {scale:.3e}"
     rms_ref = max(np.sqrt(np.mean(ref ** 2)), 1e-30)
     rms_err = np.sqrt(np.mean(err ** 2))
-    assert rms_err <= rms_rel * rms_ref, f"{name}: rms err {rms_err:.3e} > {rms_rel:.1e} x {rms_ref:.3e}"
+    assert rms_err <= rms_rel * rms_ref + atol, f"{name}: rms err {rms_err:.3e} > {rms_rel:.1e} x {rms_ref:.3e}"
     return float(err.max() / scale)
 
 
-def check_backward(g, got, ref, max_rel=MAX_REL, rms_rel=RMS_REL):
+def check_backward(g, got, ref, max_rel=MAX_REL, rms_rel=RMS_REL, atol=0.0):
     dq, dk, dv = (t.float().cpu().numpy().astype(np.float64) for t in got)
     dq_ref, dk_ref, dv_ref = ref
     dq_rows, dk_rows = _masks(g)
@@ -92,9 +92,9 @@ def check_backward(g, got, ref, max_rel=MAX_REL, rms_rel=RMS_REL):
         if nk and not nq:
             assert np.all(dk[k0:k0 + nk] == 0.0) and np.all(dv[k0:k0 + nk] == 0.0), "row-less segment: dK/dV must be 0"
             exact.append(b)
-    errs = (_close("dQ", dq[dq_rows], dq_ref[dq_rows], max_rel, rms_rel),
-            _close("dK", dk[dk_rows], dk_ref[dk_rows], max_rel, rms_rel),
-            _close("dV", dv[dk_rows], dv_ref[dk_rows], max_rel, rms_rel))
+    errs = (_close("dQ", dq[dq_rows], dq_ref[dq_rows], max_rel, rms_rel, atol),
+            _close("dK", dk[dk_rows], dk_ref[dk_rows], max_rel, rms_rel, atol),
+            _close("dV", dv[dk_rows], dv_ref[dk_rows], max_rel, rms_rel, atol))
     print(f"max err / max |ref|: dQ {errs[0]:.2e}  dK {errs[1]:.2e}  dV {errs[2]:.2e}")
     return errs
 

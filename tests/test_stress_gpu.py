@@ -1,0 +1,88 @@
+"""Randomised parity sweep of the forward and the backward against the FP64 oracle.
+
+Each case draws a gapped geometry (empty segments, ragged tails, NaN in every gap row),
+a head layout (GQA group 1 to 16, d = 64 or 128), a mask (none, or block-causal with a
+random frame length) and an output dtype, and compares every used element. The
+feature tests pin each case family on its own; this sweep covers their combinations."""
+import numpy as np
+import pytest
+import torch
+
+import gapped_varlen_attention_gb300 as gva
+from gapped_varlen_attention_gb300 import workloads as W
+from helpers_gpu import LSE_TOL, O_TOL
+from oracle import gva_oracle
+from test_backward_gpu import MAX_REL, RMS_REL, _make_dout, check_backward, gpu_backward, oracle_backward
+
+pytestmark = pytest.mark.gpu
+FILL = W.TINY_SENTINEL
+SEEDS = range(5000, 5300)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    gva.build()
+
+
+def _case(seed):
+    rng = np.random.default_rng(seed)
+    hkv = int(rng.choice([1, 2, 3]))
+    group = int(rng.choice([1, 2, 4, 8, 16]))
+    d = int(rng.choice([64, 128]))
+    g = W.random_geometry(rng, int(rng.integers(1, 6)), 400, 600, hkv * group, hkv, d)
+    block = 0 if rng.random() < 0.5 else int(rng.integers(1, 300))
+    out_dtype = torch.float32 if rng.random() < 0.3 else torch.bfloat16
+    return g, block, out_dtype
+
+
+def _check_forward(g, o, l, o_ref, l_ref):
+    """O within O_TOL of the oracle, plus, for a bf16 output, that format's own rounding
+    of the exact value (half an ulp, at most 2^-9 relative): few-key rows average a
+    handful of N(0, 1) values, so |O| reaches 2-4, where half a bf16 ulp alone is 4-8e-3."""
+    rel = 2.0 ** -9 if o.dtype == torch.bfloat16 else 0.0
+    o = o.float().cpu().numpy().astype(np.float64)
+    l = l.cpu().numpy().astype(np.float64)
+    gap = W.gap_rows(g.cu_q, g.used_q)
+    fill32 = np.float64(np.float32(FILL))
+    assert np.all(o[gap] == fill32) and np.all(l[:, gap] == fill32), "a gap row was written"
+    used = ~gap
+    dead = np.isneginf(l_ref) & used[None, :]
+    assert np.array_equal(np.isneginf(l) & used[None, :], dead), "rows without keys differ"
+    assert np.all(o.transpose(1, 0, 2)[dead] == 0.0)
+    live = np.isfinite(l_ref) & used[None, :]
+    if live.any():
+        assert np.abs(l[live] - l_ref[live]).max() <= LSE_TOL
+        o_live = o.transpose(1, 0, 2)[live]
+        ref_live = o_ref.transpose(1, 0, 2)[live]
+        assert np.all(np.isfinite(o_live))
+        assert np.all(np.abs(o_live - ref_live) <= O_TOL + rel * np.abs(ref_live))
+
+
+@pytest.mark.parametrize("seed", SEEDS)
+def test_random_forward(seed):
+    g, block, out_dtype = _case(seed)
+    q, k, v = W.make_qkv(g, seed, gap_fill=float("nan"))
+    plan = gva.Plan.from_geometry(g, causal_block=block)
+    o, l = W.make_outputs(g, FILL, device="cuda", out_dtype=out_dtype)
+    gva.forward(plan, q.cuda(), k.cuda(), v.cuda(), o, l)
+    gva.device_status(plan)
+    qn, kn, vn = (t.float().numpy() for t in (q, k, v))
+    o_ref, l_ref = gva_oracle.attention_forward(qn, kn, vn, g.cu_q, g.used_q, g.cu_k, g.used_k,
+                                                out=np.full(qn.shape, FILL),
+                                                lse=np.full((g.num_heads_q, g.total_q), FILL), causal_block=block)
+    _check_forward(g, o, l, o_ref, l_ref)
+
+
+@pytest.mark.parametrize("seed", SEEDS[::2])
+def test_random_backward(seed):
+    """The backward bound of the feature tests, with two allowances for the degenerate
+    segments a random draw makes. With one to three keys the sums behind dQ have too few
+    terms to average the bf16 roundings of P and dS, and sum_j dS_ij = 0 makes dS a
+    near-cancellation, so the rms bound is doubled (2^-7). With a single visible key,
+    P = 1 and the exact dQ is 0, while the kernel's D and dP round differently, so the
+    relative bounds get an absolute allowance of 1e-5."""
+    g, block, _ = _case(seed)
+    q, k, v = W.make_qkv(g, seed, gap_fill=float("nan"))
+    do = _make_dout(g, seed)
+    check_backward(g, gpu_backward(g, q, k, v, do, causal_block=block),
+                   oracle_backward(g, q, k, v, do, causal_block=block), MAX_REL, 2 * RMS_REL, 1e-5)
