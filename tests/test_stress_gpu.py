@@ -86,3 +86,83 @@ def test_random_backward(seed):
     do = _make_dout(g, seed)
     check_backward(g, gpu_backward(g, q, k, v, do, causal_block=block),
                    oracle_backward(g, q, k, v, do, causal_block=block), MAX_REL, 2 * RMS_REL, 1e-5)
+
+
+def _random_ranges(rng, g, total_k, disjoint):
+    """Up to four K/V row ranges per segment. Disjoint ones are cut from one shuffled
+    partition of [0, total_k), with each range at most 400 keys. Free ones start and end
+    anywhere and may overlap those of other segments."""
+    ranges = []
+    if disjoint:
+        cuts = np.sort(rng.choice(np.arange(1, total_k), size=2 * 4 * g.num_segments, replace=False))
+        pieces = [(int(cuts[2 * i]), int(cuts[2 * i + 1] - cuts[2 * i])) for i in range(len(cuts) // 2)]
+        rng.shuffle(pieces)
+        for _ in range(g.num_segments):
+            take = int(rng.integers(0, 5))
+            ranges.append([(st, min(n, 400)) for st, n in pieces[:take]])
+            pieces = pieces[take:]
+    else:
+        for _ in range(g.num_segments):
+            rr = []
+            for _ in range(int(rng.integers(0, 5))):
+                st = int(rng.integers(0, total_k))
+                rr.append((st, int(rng.integers(0, min(700, total_k - st) + 1))))
+            ranges.append(rr)
+    return ranges
+
+
+def _range_inputs(rng, g, seed, disjoint):
+    total_k = int(rng.integers(200, 3000))
+    ranges = _random_ranges(rng, g, total_k, disjoint)
+    gen = torch.Generator().manual_seed(seed)
+    q = torch.randn(g.total_q, g.num_heads_q, g.head_dim, generator=gen).bfloat16()
+    k = torch.randn(total_k, g.num_heads_kv, g.head_dim, generator=gen).bfloat16()
+    v = torch.randn(total_k, g.num_heads_kv, g.head_dim, generator=gen).bfloat16()
+    q[torch.from_numpy(W.gap_rows(g.cu_q, g.used_q))] = float("nan")
+    covered = np.zeros(total_k, bool)
+    for rr in ranges:
+        for st, n in rr:
+            covered[st:st + n] = True
+    k[torch.from_numpy(~covered)] = float("nan")
+    v[torch.from_numpy(~covered)] = float("nan")
+    return ranges, total_k, covered, q, k, v
+
+
+@pytest.mark.parametrize("seed", SEEDS[::3])
+def test_random_key_ranges_forward(seed):
+    """Several key ranges per segment, overlapping freely, in one launch."""
+    g, _, out_dtype = _case(seed)
+    rng = np.random.default_rng(seed + 1)
+    ranges, total_k, _, q, k, v = _range_inputs(rng, g, seed, disjoint=False)
+    plan = gva.Plan.from_ranges(g.cu_q, g.used_q, ranges, total_k, g.num_heads_q, g.num_heads_kv, g.head_dim)
+    o, l = W.make_outputs(g, FILL, device="cuda", out_dtype=out_dtype)
+    gva.forward(plan, q.cuda(), k.cuda(), v.cuda(), o, l)
+    gva.device_status(plan)
+    qn, kn, vn = (t.float().numpy() for t in (q, k, v))
+    o_ref, l_ref = gva_oracle.attention_forward_ranges(qn, kn, vn, g.cu_q, g.used_q, ranges,
+                                                       out=np.full(qn.shape, FILL),
+                                                       lse=np.full((g.num_heads_q, g.total_q), FILL))
+    _check_forward(g, o, l, o_ref, l_ref)
+
+
+@pytest.mark.parametrize("seed", SEEDS[1::3])
+def test_random_key_ranges_backward(seed):
+    """Disjoint key ranges per segment: gradients of every covered key and used row;
+    keys no range covers stay untouched. Bounds as in test_random_backward."""
+    from test_backward_gpu import _close
+    g, _, _ = _case(seed)
+    rng = np.random.default_rng(seed + 1)
+    ranges, total_k, covered, q, k, v = _range_inputs(rng, g, seed, disjoint=True)
+    do = _make_dout(g, seed)
+    plan = gva.Plan.from_ranges(g.cu_q, g.used_q, ranges, total_k, g.num_heads_q, g.num_heads_kv, g.head_dim)
+    dq, dk, dv = (t.float().cpu().numpy().astype(np.float64) for t in gpu_backward(g, q, k, v, do, plan=plan))
+    qn, kn, vn, don = (t.float().numpy() for t in (q, k, v, do))
+    ref = gva_oracle.attention_backward_ranges(qn, kn, vn, don, g.cu_q, g.used_q, ranges,
+                                               dq=np.full(qn.shape, FILL), dk=np.full(kn.shape, FILL),
+                                               dv=np.full(vn.shape, FILL))
+    fill32 = np.float64(np.float32(FILL))
+    rows = ~W.gap_rows(g.cu_q, g.used_q)
+    assert np.all(dq[~rows] == fill32) and np.all(dk[~covered] == fill32) and np.all(dv[~covered] == fill32)
+    _close("dQ", dq[rows], ref[0][rows], MAX_REL, 2 * RMS_REL, 1e-5)
+    _close("dK", dk[covered], ref[1][covered], MAX_REL, 2 * RMS_REL, 1e-5)
+    _close("dV", dv[covered], ref[2][covered], MAX_REL, 2 * RMS_REL, 1e-5)
