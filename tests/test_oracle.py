@@ -478,10 +478,28 @@ def pin_backward_ranges(orc):
     assert np.all(dk[[8, 11]] == 4.0) and np.all(dv[[8, 11]] == 5.0)  # rows no range covers
 
 
+def pin_used_flops(orc):
+    """Useful FLOPs are 2·d per score for QK^T plus 2·d per score for PV, summed over
+    every (used row, used key, query head): counted here one pair at a time, and checked
+    against a closed form (the tiny workload: 40·48 + 17·33 + 12·0 pairs, 4 heads,
+    d = 64)."""
+    rng = np.random.default_rng(17)
+    uq, uk = rng.integers(0, 9, size=5), rng.integers(0, 7, size=5)
+    hq, d = 3, 8
+    pairs = 0
+    for b in range(5):
+        for _ in range(int(uq[b])):
+            for _ in range(int(uk[b])):
+                pairs += 1
+    assert orc.used_flops(uq, uk, hq, d) == 2 * d * 2 * hq * pairs
+    g = W.tiny()
+    assert orc.used_flops(g.used_q, g.used_k, g.num_heads_q, g.head_dim) == 4 * 64 * 4 * (40 * 48 + 17 * 33)
+
+
 PINS = [pin_bruteforce, pin_default_scale, pin_dilution_golden, pin_zero_keys_closed_form,
         pin_single_key, pin_keyless_and_gap_rows, pin_pad_invariance, pin_sdpa_equal_lengths,
         pin_gqa_repeat, pin_key_permutation, pin_merge_union, pin_rows_match, pin_ranges, pin_causal,
-        pin_backward, pin_backward_causal, pin_backward_ranges]
+        pin_backward, pin_backward_causal, pin_backward_ranges, pin_used_flops]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -525,6 +543,7 @@ MUTANTS = {
     "backward_ranges_overwrite": ("np.add.at(dk_out, (idx, hk), s * (ds.T @ qs))",
                                   "dk_out[idx, hk] = s * (ds.T @ qs)"),
     "range_end_dropped": ("np.arange(int(st), int(st) + int(n))", "np.arange(int(st), int(st) + int(n) - 1)"),
+    "flops_one_product": ("return 4.0 * head_dim * num_heads_q", "return 2.0 * head_dim * num_heads_q"),
 }
 
 
