@@ -24,12 +24,22 @@
  *                                in the review of PR #302)
  *   total_q = cu_seqlens_q[B], total_k = cu_seqlens_k[B] (rows of the buffers).
  *
+ * Entry points:
+ *   plans        gva_plan (used prefixes), gva_plan_ranges (several key ranges per
+ *                segment), gva_plan_causal (block-causal), gva_plan_get_info,
+ *                gva_plan_inspect (the work lists, host only), gva_plan_destroy
+ *   forward      gva_forward, gva_forward_noalloc (no plan, no allocation)
+ *   merge        gva_lse_merge (FP32 LSE merge of partial results)
+ *   backward     gva_backward_workspace_size, gva_backward (dQ, dK, dV)
+ *   status       gva_device_status, gva_status_string, gva_last_error
+ *
  * Conventions:
  *   - Every function returns a gva_status and never throws. On failure,
  *     gva_last_error() gives a human-readable reason (thread-local).
- *   - gva_forward and gva_lse_merge are asynchronous on `stream`, allocate nothing,
- *     and do not synchronise the host. gva_plan allocates and uploads a small device
- *     work list once per geometry (from host ints: no device-to-host read).
+ *   - gva_forward, gva_lse_merge and gva_backward are asynchronous on `stream`,
+ *     allocate nothing, and do not synchronise the host. gva_plan allocates and
+ *     uploads a small device work list once per geometry (from host ints: no
+ *     device-to-host read).
  *   - The caller owns every tensor. A plan owns only its device work list and is
  *     released by gva_plan_destroy; no launch that uses it may still be in flight.
  *   - Two launches that share a plan may run concurrently: a plan holds no per-call
