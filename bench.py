@@ -27,6 +27,7 @@ import subprocess
 import sys
 import threading
 import time
+import types
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -59,6 +60,97 @@ def _describe(g):
             "heads_q": g.num_heads_q, "heads_kv": g.num_heads_kv, "head_dim": g.head_dim}
 
 
+LABELS = {
+    "long_replay": ("long joint video+LiDAR replay: 4 segments x 32768 q rows (used 60-100%) x 65536 keys "
+                    "(used 50-100%), Hq=32, Hkv=8, d=128, bf16, non-causal"),
+    "long_replay_small": "reduced long replay (profiling): 2 segments x 8192 q rows x 32768 keys, Hq=32, Hkv=8",
+    "cfg_text_cross": "CFG B=2 text cross-attention: 2 x 4096 q rows, text keys 700 / 20 of 1024, Hq=16, Hkv=8",
+    "multiview_causal": "multiview causal gapped replay: 7 segments, 2 visibility partitions + FP32 LSE merge",
+    "multiview_fused": "multiview causal gapped replay: 7 segments, 2 visibility partitions fused in one launch",
+    "multiview_blockcausal": ("multiview causal gapped replay: 7 segments, block-causal masking with 512-token "
+                              "frames in one launch (FLOPs count visible keys only)"),
+    "long_replay_bwd": ("backward (dQ, dK, dV) of the long joint video+LiDAR replay: 4 segments x 32768 q rows "
+                        "(used 60-100%) x 65536 keys (used 50-100%), Hq=32, Hkv=8, d=128, bf16; FLOPs = 2.5 x "
+                        "the forward's (five used-row products)"),
+    "multiview_fused_bwd": ("backward of the multiview causal gapped replay with its 2 visibility partitions as "
+                            "two key ranges per segment of one plan"),
+    "multiview_blockcausal_bwd": ("backward of the multiview causal gapped replay with 512-token block-causal "
+                                  "masking (FLOPs: 2.5 x the visible-key forward FLOPs)"),
+    "long_replay_small_bwd": "backward of the reduced long replay (profiling): 2 segments x 8192 q rows x 32768 keys",
+    "lse_merge_union": ("text + video LSE merge: 8192 q rows in 10 segments, each attending its own 1024 text and "
+                        "16384 video keys as 2 launches (FP32 partials) + FP32 LSE merge, one segment's text "
+                        "partition empty; Hq=Hkv=24, d=128"),
+    "lse_merge": ("the FP32 LSE merge alone on the text + video workload's partials: 8192 q rows in 10 "
+                  "segments, 2 FP32 partitions (one segment's text partition keyless), bf16 output, Hq=24, d=128"),
+    "tiny": "tiny: 3 segments, Hq=4, Hkv=2, d=64",
+}
+WORKLOADS = tuple(LABELS)
+
+
+def spec(name: str):
+    """The host-side description of a workload, shared by both arms: its geometries
+    (one per forward launch), the merged geometry of partitioned ones (`parts`), the
+    geometry and seed its Q / K / V are drawn from, and its options."""
+    from gapped_varlen_attention_gb300 import workloads as W
+    if name not in LABELS:
+        raise SystemExit(f"unknown workload {name}")
+    sp = types.SimpleNamespace(name=name, label=LABELS[name], parts=None, ranges=None, causal_block=0,
+                               backward=name.endswith("_bwd"), merge_only=False, k_pad_fill=None,
+                               part_kv_geoms=None, used_k_parts=None)
+    base = name[:-4] if sp.backward else name
+    if base in ("long_replay", "long_replay_small"):
+        g = W.long_replay() if base == "long_replay" else W.long_replay_small()
+        sp.geoms, sp.qkv_geom, sp.seed = [g], g, 1005 if base == "long_replay" else 1006
+    elif base == "cfg_text_cross":
+        g = W.cfg_text_cross()
+        sp.geoms, sp.qkv_geom, sp.seed, sp.k_pad_fill = [g], g, 1002, 0.0
+    elif base.startswith("multiview"):
+        full, parts = W.multiview_causal()
+        sp.qkv_geom, sp.seed = full, 1003
+        if base == "multiview_causal":
+            sp.geoms, sp.parts = parts, full
+        else:
+            sp.geoms = [full]
+        if base == "multiview_fused":
+            sp.ranges = [[(int(p.cu_k[b]), int(p.used_k[b])) for p in parts] for b in range(full.num_segments)]
+        if base == "multiview_blockcausal":
+            sp.causal_block = 512
+    elif base in ("lse_merge_union", "lse_merge"):
+        text, video, union, _ = W.lse_merge_union()
+        sp.parts, sp.qkv_geom, sp.seed = union, text, 1004
+        if base == "lse_merge_union":
+            sp.geoms, sp.part_kv_geoms = [text, video], [(text, 1004), (video, 2004)]
+        else:
+            sp.geoms, sp.merge_only, sp.used_k_parts = [union], True, [text.used_k, video.used_k]
+    else:
+        g = W.tiny()
+        sp.geoms, sp.qkv_geom, sp.seed = [g], g, 1001
+    return sp
+
+
+def spec_input_bytes(sp) -> int:
+    """Bytes of the step's device-resident inputs (whole buffers, gap rows included)."""
+    qg = sp.parts if sp.parts is not None else sp.geoms[0]
+    q = qg.total_q * qg.num_heads_q * qg.head_dim * 2
+    lse = qg.num_heads_q * qg.total_q * 4
+    if sp.merge_only:
+        return len(sp.used_k_parts) * (2 * q + lse)
+    kv_geoms = [g for g, _ in sp.part_kv_geoms] if sp.part_kv_geoms is not None else [sp.qkv_geom]
+    kv = sum(2 * g.total_k * g.num_heads_kv * g.head_dim * 2 for g in kv_geoms)
+    return q + kv + ((2 * q + lse) if sp.backward else 0)
+
+
+def spec_config(sp, per_step: dict, parallelism: str) -> dict:
+    """The `config` object of a bench line: the same for both arms of one workload."""
+    geom = sp.parts if sp.parts is not None else sp.geoms[0]
+    input_bytes = spec_input_bytes(sp)
+    return {"workload": sp.name, "description": sp.label, **_describe(geom), **per_step,
+            "l2": "inputs larger than L2 (no flush needed)" if input_bytes > 2 * 129e6
+            else "L2 flushed before every step (256 MB write, then a 256 MB read so that the write's dirty "
+                 "lines are written back before the step; outside the timed events)",
+            "parallelism": parallelism}
+
+
 class Workload:
     """Device-resident inputs and outputs of one workload, and its step."""
 
@@ -68,107 +160,23 @@ class Workload:
         self.name = name
         self.gva = gva
         dev = "cuda"
-        if name == "long_replay":
-            g = W.long_replay()
-            self.geoms = [g]
-            self.q, self.k, self.v = W.make_qkv(g, 1005 + seed_offset, device=dev)
-            self.parts = None
-            self.label = ("long joint video+LiDAR replay: 4 segments x 32768 q rows (used 60-100%) x 65536 keys "
-                          "(used 50-100%), Hq=32, Hkv=8, d=128, bf16, non-causal")
-        elif name == "long_replay_small":
-            g = W.long_replay_small()
-            self.geoms = [g]
-            self.q, self.k, self.v = W.make_qkv(g, 1006 + seed_offset, device=dev)
-            self.parts = None
-            self.label = "reduced long replay (profiling): 2 segments x 8192 q rows x 32768 keys, Hq=32, Hkv=8"
-        elif name == "cfg_text_cross":
-            g = W.cfg_text_cross()
-            self.geoms = [g]
-            self.q, self.k, self.v = W.make_qkv(g, 1002 + seed_offset, device=dev, k_pad_fill=0.0)
-            self.parts = None
-            self.label = "CFG B=2 text cross-attention: 2 x 4096 q rows, text keys 700 / 20 of 1024, Hq=16, Hkv=8"
-        elif name == "multiview_causal":
-            full, parts = W.multiview_causal()
-            self.geoms = parts
-            self.q, self.k, self.v = W.make_qkv(full, 1003 + seed_offset, device=dev)
-            self.parts = full
-            self.label = "multiview causal gapped replay: 7 segments, 2 visibility partitions + FP32 LSE merge"
-        elif name == "multiview_fused":
-            full, parts = W.multiview_causal()
-            self.geoms = [full]
-            self.q, self.k, self.v = W.make_qkv(full, 1003 + seed_offset, device=dev)
-            self.parts = None
-            self.ranges = [[(int(p.cu_k[b]), int(p.used_k[b])) for p in parts] for b in range(full.num_segments)]
-            self.label = "multiview causal gapped replay: 7 segments, 2 visibility partitions fused in one launch"
-        elif name == "multiview_blockcausal":
-            full, _ = W.multiview_causal()
-            self.geoms = [full]
-            self.q, self.k, self.v = W.make_qkv(full, 1003 + seed_offset, device=dev)
-            self.parts = None
-            self.causal_block = 512
-            self.label = ("multiview causal gapped replay: 7 segments, block-causal masking with 512-token frames "
-                          "in one launch (FLOPs count visible keys only)")
-        elif name == "long_replay_bwd":
-            g = W.long_replay()
-            self.geoms = [g]
-            self.q, self.k, self.v = W.make_qkv(g, 1005 + seed_offset, device=dev)
-            self.parts = None
+        sp = self.spec = spec(name)
+        self.label, self.geoms, self.parts = sp.label, sp.geoms, sp.parts
+        if sp.ranges is not None:
+            self.ranges = sp.ranges
+        if sp.causal_block:
+            self.causal_block = sp.causal_block
+        if sp.backward:
             self.backward = True
-            self.label = ("backward (dQ, dK, dV) of the long joint video+LiDAR replay: 4 segments x 32768 q rows "
-                          "(used 60-100%) x 65536 keys (used 50-100%), Hq=32, Hkv=8, d=128, bf16; FLOPs = 2.5 x "
-                          "the forward's (five used-row products)")
-        elif name == "multiview_fused_bwd":
-            full, parts = W.multiview_causal()
-            self.geoms = [full]
-            self.q, self.k, self.v = W.make_qkv(full, 1003 + seed_offset, device=dev)
-            self.parts = None
-            self.ranges = [[(int(p.cu_k[b]), int(p.used_k[b])) for p in parts] for b in range(full.num_segments)]
-            self.backward = True
-            self.label = ("backward of the multiview causal gapped replay with its 2 visibility partitions as two "
-                          "key ranges per segment of one plan")
-        elif name == "multiview_blockcausal_bwd":
-            full, _ = W.multiview_causal()
-            self.geoms = [full]
-            self.q, self.k, self.v = W.make_qkv(full, 1003 + seed_offset, device=dev)
-            self.parts = None
-            self.causal_block = 512
-            self.backward = True
-            self.label = ("backward of the multiview causal gapped replay with 512-token block-causal masking "
-                          "(FLOPs: 2.5 x the visible-key forward FLOPs)")
-        elif name == "long_replay_small_bwd":
-            g = W.long_replay_small()
-            self.geoms = [g]
-            self.q, self.k, self.v = W.make_qkv(g, 1006 + seed_offset, device=dev)
-            self.parts = None
-            self.backward = True
-            self.label = "backward of the reduced long replay (profiling): 2 segments x 8192 q rows x 32768 keys"
-        elif name == "lse_merge_union":
-            text, video, union, _ = W.lse_merge_union()
-            self.geoms = [text, video]
-            self.q, kt, vt = W.make_qkv(text, 1004 + seed_offset, device=dev)
-            kvid, vvid = W.make_qkv(video, 2004 + seed_offset, device=dev)[1:]
-            self.part_kv = [(kt, vt), (kvid, vvid)]
-            self.parts = union
-            self.label = ("text + video LSE merge: 8192 q rows in 10 segments, each attending its own 1024 text and "
-                          "16384 video keys as 2 launches (FP32 partials) + FP32 LSE merge, one segment's text "
-                          "partition empty; Hq=Hkv=24, d=128")
-        elif name == "lse_merge":
-            text, video, union, _ = W.lse_merge_union()
-            self.geoms = [union]
-            self.parts = union
+        if sp.merge_only:
             self.merge_only = True
-            self.used_k_parts = [text.used_k, video.used_k]
-            self.label = ("the FP32 LSE merge alone on the text + video workload's partials: 8192 q rows in 10 "
-                          "segments, 2 FP32 partitions (one segment's text partition keyless), bf16 output, "
-                          "Hq=24, d=128")
-        elif name == "tiny":
-            g = W.tiny()
-            self.geoms = [g]
-            self.q, self.k, self.v = W.make_qkv(g, 1001 + seed_offset, device=dev)
-            self.parts = None
-            self.label = "tiny: 3 segments, Hq=4, Hkv=2, d=64"
+            self.used_k_parts = sp.used_k_parts
+        elif sp.part_kv_geoms is not None:
+            self.q = W.make_qkv(sp.qkv_geom, sp.seed + seed_offset, device=dev)[0]
+            self.part_kv = [W.make_qkv(pg, s + seed_offset, device=dev)[1:] for pg, s in sp.part_kv_geoms]
         else:
-            raise SystemExit(f"unknown workload {name}")
+            self.q, self.k, self.v = W.make_qkv(sp.qkv_geom, sp.seed + seed_offset, device=dev,
+                                                k_pad_fill=sp.k_pad_fill)
         self.merge_only = getattr(self, "merge_only", False)
         if self.merge_only:
             self.plans = []
@@ -260,14 +268,10 @@ class Workload:
         for p in self.plans + ([self.merge_plan] if self.parts is not None else []):
             self.gva.device_status(p)
 
-    def config(self):
-        geom = self.parts if self.parts is not None else self.geoms[0]
+    def config(self, parallelism: str):
         per_step = {"algorithmic_bytes_per_step": self.work} if self.merge_only else \
             {"useful_flops_per_step": self.flops}
-        return {"workload": self.name, "description": self.label, **_describe(geom), **per_step,
-                "l2": "inputs larger than L2 (no flush needed)" if self.input_bytes() > 2 * 129e6
-                else "L2 flushed before every step (256 MB write, then a 256 MB read so that the write's dirty "
-                     "lines are written back before the step; outside the timed events)"}
+        return spec_config(self.spec, per_step, parallelism)
 
     def input_bytes(self):
         return sum(t.numel() * t.element_size() for t in self.inputs)
@@ -651,11 +655,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gva", "reference"], default="gva")
-    ap.add_argument("--workload", default="long_replay",
-                    choices=["long_replay", "long_replay_small", "cfg_text_cross", "multiview_causal",
-                             "multiview_fused", "multiview_blockcausal", "long_replay_bwd", "long_replay_small_bwd",
-                             "multiview_blockcausal_bwd", "multiview_fused_bwd", "lse_merge_union", "lse_merge",
-                             "tiny"])
+    ap.add_argument("--workload", default="long_replay", choices=list(WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     args = ap.parse_args()
@@ -696,13 +696,19 @@ def main():
     wl.check()
 
     flush = None
-    if wl.input_bytes() <= 2 * 129e6:
+    if spec_input_bytes(wl.spec) <= 2 * 129e6:
         flush = L2Flush()
 
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clocks:
-        clocks.wait_samples(1, 5.0)  # nvidia-smi is up before the timed region starts
+        # nvidia-smi is up before the timed region starts; the same steps keep running
+        # meanwhile so that the clocks do not drop while the device would otherwise idle
+        def keep_busy():
+            for _ in range(max(1, args.warmup)):
+                wl.step()
+            torch.cuda.synchronize()
+        clocks.wait_samples(1, 5.0, work=keep_busy)
         n_before = len(clocks.lines)
         torch.cuda.nvtx.range_push("timed")  # lets a profiler keep only the timed launches
         ms = time_steps(wl.step, args.steps, stream, flush)
@@ -788,7 +794,7 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16, the pages' segment shapes)",
-        "config": {**wl.config(), "parallelism": f"replicas x{world} (independent problems per GPU)"},
+        "config": wl.config(f"replicas x{world} (independent problems per GPU)"),
         ("pct_of_hbm_peak" if wl.bound == "hbm" else "pct_of_bf16_peak"): round(100.0 * value / world / peak, 2),
         "roofline": {
             "bound": wl.bound,
@@ -825,56 +831,37 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     from gapped_varlen_attention_gb300 import workloads as W
+    from oracle import gva_oracle
 
-    class HostWorkload:
-        pass
-
-    wl = HostWorkload()
-    wl.name = args.workload
-    if args.workload in ("long_replay", "long_replay_bwd"):
-        g = W.long_replay()
-        wl.geoms = [g]
-        seed = 1005
-    elif args.workload == "cfg_text_cross":
-        g = W.cfg_text_cross()
-        wl.geoms = [g]
-        seed = 1002
-    elif args.workload in ("multiview_causal", "multiview_fused", "multiview_fused_bwd"):
-        g, parts = W.multiview_causal()
-        wl.geoms = parts
-        seed = 1003
-    elif args.workload in ("multiview_blockcausal", "multiview_blockcausal_bwd"):
-        g, _ = W.multiview_causal()
-        wl.geoms = [g]
-        wl.causal_block = 512
-        seed = 1003
-    elif args.workload in ("long_replay_small", "long_replay_small_bwd"):
-        g = W.long_replay_small()
-        wl.geoms = [g]
-        seed = 1006
-    elif args.workload in ("lse_merge_union", "lse_merge"):
-        text, video, g, _ = W.lse_merge_union()
-        wl.geoms = [text, video]
-        seed = 1004
-    else:
-        g = W.tiny()
-        wl.geoms = [g]
-        seed = 1001
+    sp = spec(args.workload)
+    wl = types.SimpleNamespace(name=sp.name, geoms=sp.geoms, causal_block=sp.causal_block, backward=sp.backward)
     metric, unit = METRIC, UNIT
-    if args.workload == "lse_merge_union":
-        wl.q, kt, vt = W.make_qkv(text, seed)
-        wl.part_kv = [(kt, vt), W.make_qkv(video, 2004)[1:]]
-    elif args.workload == "lse_merge":
-        wl.merge_only, wl.parts, wl.used_k_parts = True, g, [text.used_k, video.used_k]
-        wl.partials = list(zip(*W.make_partials(g, wl.used_k_parts, 3004)))
+    if sp.merge_only:
+        wl.merge_only, wl.parts, wl.used_k_parts = True, sp.parts, sp.used_k_parts
+        wl.partials = list(zip(*W.make_partials(sp.parts, sp.used_k_parts, 3004)))
         metric, unit = "gapped-varlen FP32 LSE merge GB/s (algorithmic bytes: live partials, LSEs, output)", "GB/s"
+        per_step = {"algorithmic_bytes_per_step": merge_bytes(sp.parts, sp.used_k_parts, 2)}
     else:
-        wl.q, wl.k, wl.v = W.make_qkv(g, seed)
-    if args.workload in ("long_replay_bwd", "long_replay_small_bwd", "multiview_blockcausal_bwd",
-                         "multiview_fused_bwd"):
-        wl.backward = True
-        wl.d_out = torch.randn(wl.q.shape, generator=torch.Generator().manual_seed(2005)).bfloat16()
-        metric = "gapped-varlen attn bwd TFLOP/s (used rows, 2.5 x fwd FLOPs) & % of GB300 BF16 peak"
+        if sp.part_kv_geoms is not None:
+            wl.q = W.make_qkv(sp.qkv_geom, sp.seed)[0]
+            wl.part_kv = [W.make_qkv(pg, s)[1:] for pg, s in sp.part_kv_geoms]
+        else:
+            wl.q, wl.k, wl.v = W.make_qkv(sp.qkv_geom, sp.seed, k_pad_fill=sp.k_pad_fill)
+        # the workload's useful FLOPs, counted on the host: used (or visible) pairs x 4 d Hq
+        flops = 0.0
+        for g in sp.geoms:
+            if sp.causal_block:
+                pairs = sum(float(gva_oracle.causal_limits(int(g.used_q[b]), int(g.used_k[b]), sp.causal_block).sum())
+                            for b in range(g.num_segments))
+                flops += 4.0 * g.head_dim * g.num_heads_q * pairs
+            else:
+                flops += gva_oracle.used_flops(g.used_q, g.used_k, g.num_heads_q, g.head_dim)
+        if sp.backward:
+            wl.d_out = torch.randn(wl.q.shape, generator=torch.Generator().manual_seed(2005)).bfloat16()
+            metric = "gapped-varlen attn bwd TFLOP/s (used rows, 2.5 x fwd FLOPs) & % of GB300 BF16 peak"
+            flops *= 2.5
+        per_step = {"useful_flops_per_step": flops}
+    config = spec_config(sp, per_step, "FP64 oracle on the host cores (rank 0 only)")
     budget = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     for i in range(args.warmup):
         oracle_sample_rate(wl, budget, seed=i)
@@ -899,7 +886,7 @@ def run_reference(args, world, rank):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded N(0,1) bf16 widened to f64)",
-        "config": {"workload": args.workload},
+        "config": config,
         "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
                          "sample": descs[-1] + f"; {budget:.1f} s per step"},
         "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
