@@ -454,20 +454,23 @@ class L2Flush:
         torch.sum(self.clean, dim=0, out=self.acc)
 
 
-def time_steps(fn, steps: int, stream, flush=None) -> float:
+def time_steps(fn, steps: int, stream, flush=None, per_step=None) -> float:
     """Device milliseconds for `steps` calls of fn, CUDA events on `stream`. With a
     flush (an L2Flush, for inputs smaller than L2), it runs before every step, outside
     the events, so each step starts with a cold L2 and only the step is timed; a short
-    device-side sleep after it covers the host's time to issue the step."""
+    device-side sleep after it covers the host's time to issue the step. Without one the
+    steps run back to back, with an event between consecutive steps. `per_step`, if
+    given, receives each step's milliseconds."""
     if flush is None:
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
-        start.record(stream)
-        for _ in range(steps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        ev[0].record(stream)
+        for i in range(steps):
             fn()
-        end.record(stream)
-        end.synchronize()
-        return start.elapsed_time(end)
+            ev[i + 1].record(stream)
+        ev[-1].synchronize()
+        if per_step is not None:
+            per_step.extend(ev[i].elapsed_time(ev[i + 1]) for i in range(steps))
+        return ev[0].elapsed_time(ev[-1])
     pairs = []
     for _ in range(steps):
         flush()
@@ -480,6 +483,8 @@ def time_steps(fn, steps: int, stream, flush=None) -> float:
         b.record(stream)
         pairs.append((a, b))
     pairs[-1][1].synchronize()
+    if per_step is not None:
+        per_step.extend(a.elapsed_time(b) for a, b in pairs)
     return sum(a.elapsed_time(b) for a, b in pairs)
 
 
@@ -711,7 +716,8 @@ def main():
         clocks.wait_samples(1, 5.0, work=keep_busy)
         n_before = len(clocks.lines)
         torch.cuda.nvtx.range_push("timed")  # lets a profiler keep only the timed launches
-        ms = time_steps(wl.step, args.steps, stream, flush)
+        step_ms = []
+        ms = time_steps(wl.step, args.steps, stream, flush, step_ms)
         torch.cuda.synchronize()
         torch.cuda.nvtx.range_pop()
         clock_window = "timed region"
@@ -757,7 +763,8 @@ def main():
     e2e_ms = e2e_run.run(args.e2e_steps) / args.e2e_steps
     barrier()
 
-    ms_step, fwd_ms, e2e_ms = max_over_ranks([ms_step, fwd_ms, e2e_ms], dist, "cuda")
+    ms_step, fwd_ms, e2e_ms, med_ms = max_over_ranks([ms_step, fwd_ms, e2e_ms, float(np.median(step_ms))], dist,
+                                                     "cuda")
 
     if rank != 0:
         if dist is not None:
@@ -789,6 +796,7 @@ def main():
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms_step, 4),
+        "ms_per_step_median": round(med_ms, 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -796,6 +804,9 @@ def main():
         "data": "synthetic (seeded N(0,1) bf16, the pages' segment shapes)",
         "config": wl.config(f"replicas x{world} (independent problems per GPU)"),
         ("pct_of_hbm_peak" if wl.bound == "hbm" else "pct_of_bf16_peak"): round(100.0 * value / world / peak, 2),
+        **({} if wl.bound == "hbm" else {
+            "pct_of_bf16_peak_burst": round(100.0 * value / world / peaks["bf16_tflops"], 2),
+            "pct_of_bf16_peak_sustained": round(100.0 * value / world / peaks["bf16_tflops_sustained"], 2)}),
         "roofline": {
             "bound": wl.bound,
             "achieved": round(achieved, 2),
