@@ -44,7 +44,7 @@ class PlanInfo(ctypes.Structure):
 class WorkSummary(ctypes.Structure):
     _fields_ = [("num_work_items", ctypes.c_int32), ("num_key_blocks", ctypes.c_int32),
                 ("num_merge_units", ctypes.c_int32), ("num_bwd_items", ctypes.c_int32),
-                ("num_kv_units", ctypes.c_int32), ("reserved", ctypes.c_int32), ("used_flops", ctypes.c_double)]
+                ("num_kv_units", ctypes.c_int32), ("backward_ok", ctypes.c_int32), ("used_flops", ctypes.c_double)]
 
 
 _lib = None
@@ -78,8 +78,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
                                     ctypes.POINTER(vp)]
     lib.gva_backward_workspace_size.argtypes = [vp, ctypes.POINTER(ctypes.c_size_t)]
     lib.gva_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, vp, ctypes.c_size_t, f32, vp]
-    lib.gva_plan_inspect.argtypes = [pi32, pi32, pi32, pi32, i32, i32, i32, i32, i32, ctypes.POINTER(WorkSummary),
-                                     pi32, i32, pi32, i32, pi32, i32]
+    lib.gva_plan_inspect.argtypes = [pi32, pi32, pi32, pi32, i32, pi32, pi32, pi32, ctypes.c_int64, i32, i32, i32,
+                                     i32, ctypes.POINTER(WorkSummary), pi32, i32, pi32, i32, pi32, i32]
     for name in ("gva_plan", "gva_forward", "gva_lse_merge", "gva_plan_destroy", "gva_plan_get_info",
                  "gva_device_status", "gva_forward_noalloc", "gva_plan_ranges", "gva_plan_causal",
                  "gva_backward_workspace_size", "gva_backward", "gva_plan_inspect"):
@@ -105,18 +105,30 @@ KV_UNIT_FIELDS = ("key_row0", "keys", "q_row0", "q_used", "head_kv", "tile0", "k
 
 
 def inspect_plan(cu_seqlens_q, seqused_q, cu_seqlens_k, seqused_k, num_heads_q: int, num_heads_kv: int,
-                 head_dim: int, causal_block: int = 0) -> dict:
+                 head_dim: int, causal_block: int = 0, key_ranges=None, total_k: int = 0) -> dict:
     """``gva_plan_inspect``: the work lists a plan of this geometry holds, built on the
-    host (no CUDA call). Returns the counts, ``used_flops`` and three int32 arrays of 8
-    columns in the kernels' order: ``items`` (forward, fields ``WORK_ITEM_FIELDS``),
-    ``bwd_items`` (dQ, same fields) and ``kv_units`` (dK / dV, ``KV_UNIT_FIELDS``)."""
+    host (no CUDA call). With ``key_ranges`` (per segment a list of ``(start, length)``
+    K/V row ranges, as ``Plan.from_ranges``) the keys are those ranges and
+    ``cu_seqlens_k`` / ``seqused_k`` are not used. Returns the counts, ``backward_ok``,
+    ``used_flops`` and three int32 arrays of 8 columns in the kernels' order: ``items``
+    (forward, fields ``WORK_ITEM_FIELDS``), ``bwd_items`` (dQ, same fields) and
+    ``kv_units`` (dK / dV, ``KV_UNIT_FIELDS``)."""
     lib = load_library()
-    a = [_i32(x) for x in (cu_seqlens_q, seqused_q, cu_seqlens_k, seqused_k)]
-    n = int(a[1].shape[0])
+    q = [_i32(x) for x in (cu_seqlens_q, seqused_q)]
+    n = int(q[1].shape[0])
     p = lambda x: x.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))  # noqa: E731
+    if key_ranges is not None:
+        off = _i32(np.concatenate([[0], np.cumsum([len(r) for r in key_ranges])]))
+        flat = [x for r in key_ranges for x in r]
+        st = _i32([a for a, _ in flat]) if flat else _i32(np.zeros(1))
+        ln = _i32([b for _, b in flat]) if flat else _i32(np.zeros(1))
+        keys = [None, None, p(off), p(st), p(ln), int(total_k)]
+    else:
+        k = [_i32(x) for x in (cu_seqlens_k, seqused_k)]
+        keys = [p(k[0]), p(k[1]), None, None, None, 0]
     summ = WorkSummary()
-    args = [p(a[0]), p(a[1]), p(a[2]), p(a[3]), n, int(causal_block), int(num_heads_q), int(num_heads_kv),
-            int(head_dim), ctypes.byref(summ)]
+    args = [p(q[0]), p(q[1]), keys[0], keys[1], n, keys[2], keys[3], keys[4], keys[5], int(causal_block),
+            int(num_heads_q), int(num_heads_kv), int(head_dim), ctypes.byref(summ)]
     _check(lib, lib.gva_plan_inspect(*args, None, 0, None, 0, None, 0), "gva_plan_inspect")
     items = np.zeros((max(summ.num_work_items, 1), 8), np.int32)
     bwd = np.zeros((max(summ.num_bwd_items, 1), 8), np.int32)
@@ -125,7 +137,7 @@ def inspect_plan(cu_seqlens_q, seqused_q, cu_seqlens_k, seqused_k, num_heads_q: 
                                      summ.num_kv_units), "gva_plan_inspect")
     return {"num_work_items": summ.num_work_items, "num_key_blocks": summ.num_key_blocks,
             "num_merge_units": summ.num_merge_units, "num_bwd_items": summ.num_bwd_items,
-            "num_kv_units": summ.num_kv_units, "used_flops": summ.used_flops,
+            "num_kv_units": summ.num_kv_units, "backward_ok": bool(summ.backward_ok), "used_flops": summ.used_flops,
             "items": items[:summ.num_work_items], "bwd_items": bwd[:summ.num_bwd_items],
             "kv_units": kvu[:summ.num_kv_units]}
 

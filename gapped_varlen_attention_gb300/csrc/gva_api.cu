@@ -416,14 +416,13 @@ gva_status gva_plan_causal(const int32_t* cu_seqlens_q, const int32_t* seqused_q
                     out_plan);
 }
 
-gva_status gva_plan_ranges(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int32_t num_segments,
-                           const int32_t* key_range_offsets, const int32_t* key_range_starts,
-                           const int32_t* key_range_lengths, int64_t total_k, int32_t num_heads_q,
-                           int32_t num_heads_kv, int32_t head_dim, gva_plan_t* out_plan) {
-  if (out_plan == nullptr) return fail(GVA_ERR_INVALID_ARG, "out_plan is NULL");
-  *out_plan = nullptr;
-  gva_status s = validate_common(cu_seqlens_q, seqused_q, num_segments, num_heads_q, num_heads_kv, head_dim);
-  if (s != GVA_OK) return s;
+}  // extern "C"
+
+namespace {
+// Key ranges of gva_plan_ranges: offsets start at 0 and do not decrease, every range lies
+// in [0, total_k). *disjoint tells whether the non-empty ranges are pairwise disjoint.
+gva_status validate_ranges(int32_t num_segments, const int32_t* key_range_offsets, const int32_t* key_range_starts,
+                           const int32_t* key_range_lengths, int64_t total_k, bool* disjoint_out) {
   if (key_range_offsets == nullptr) return fail(GVA_ERR_INVALID_ARG, "key_range_offsets is NULL");
   if (total_k < 0 || total_k > INT32_MAX) return fail(GVA_ERR_INVALID_ARG, "total_k=%lld is out of range", (long long)total_k);
   if (key_range_offsets[0] != 0) return fail(GVA_ERR_INVALID_ARG, "key_range_offsets[0] must be 0");
@@ -448,33 +447,67 @@ gva_status gva_plan_ranges(const int32_t* cu_seqlens_q, const int32_t* seqused_q
   bool disjoint = true;
   for (size_t i = 1; i < spans.size(); ++i)
     if (static_cast<int64_t>(spans[i - 1].first) + spans[i - 1].second > spans[i].first) disjoint = false;
+  *disjoint_out = disjoint;
+  return GVA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+gva_status gva_plan_ranges(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int32_t num_segments,
+                           const int32_t* key_range_offsets, const int32_t* key_range_starts,
+                           const int32_t* key_range_lengths, int64_t total_k, int32_t num_heads_q,
+                           int32_t num_heads_kv, int32_t head_dim, gva_plan_t* out_plan) {
+  if (out_plan == nullptr) return fail(GVA_ERR_INVALID_ARG, "out_plan is NULL");
+  *out_plan = nullptr;
+  gva_status s = validate_common(cu_seqlens_q, seqused_q, num_segments, num_heads_q, num_heads_kv, head_dim);
+  if (s != GVA_OK) return s;
+  bool disjoint = false;
+  s = validate_ranges(num_segments, key_range_offsets, key_range_starts, key_range_lengths, total_k, &disjoint);
+  if (s != GVA_OK) return s;
   return build_plan(cu_seqlens_q, seqused_q, num_segments, key_range_offsets, key_range_starts, key_range_lengths,
                     total_k, num_heads_q, num_heads_kv, head_dim, 0, disjoint, out_plan);
 }
 
 gva_status gva_plan_inspect(const int32_t* cu_seqlens_q, const int32_t* seqused_q, const int32_t* cu_seqlens_k,
-                            const int32_t* seqused_k, int32_t num_segments, int32_t causal_block, int32_t num_heads_q,
-                            int32_t num_heads_kv, int32_t head_dim, gva_work_summary* summary, int32_t* items,
-                            int32_t items_capacity, int32_t* bwd_items, int32_t bwd_items_capacity,
-                            int32_t* kv_units, int32_t kv_units_capacity) {
+                            const int32_t* seqused_k, int32_t num_segments, const int32_t* key_range_offsets,
+                            const int32_t* key_range_starts, const int32_t* key_range_lengths, int64_t total_k,
+                            int32_t causal_block, int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim,
+                            gva_work_summary* summary, int32_t* items, int32_t items_capacity, int32_t* bwd_items,
+                            int32_t bwd_items_capacity, int32_t* kv_units, int32_t kv_units_capacity) {
   if (summary == nullptr) return fail(GVA_ERR_INVALID_ARG, "summary is NULL");
   if (causal_block < 0) return fail(GVA_ERR_INVALID_ARG, "causal_block=%d must be >= 0", causal_block);
   gva_status s = validate_common(cu_seqlens_q, seqused_q, num_segments, num_heads_q, num_heads_kv, head_dim);
   if (s != GVA_OK) return s;
-  if (cu_seqlens_k == nullptr || (num_segments > 0 && seqused_k == nullptr))
-    return fail(GVA_ERR_INVALID_ARG, "a geometry array is NULL");
-  s = validate_offsets(cu_seqlens_k, seqused_k, num_segments, "k");
-  if (s != GVA_OK) return s;
-  std::vector<int32_t> off(num_segments + 1), start(num_segments), len(num_segments);
-  for (int32_t b = 0; b <= num_segments; ++b) off[b] = b;
-  for (int32_t b = 0; b < num_segments; ++b) {
-    start[b] = cu_seqlens_k[b];
-    len[b] = seqused_k[b];
+  std::vector<int32_t> off, start, len;
+  bool backward_ok = true;
+  if (key_range_offsets != nullptr) {  // as gva_plan_ranges
+    if (causal_block > 0) return fail(GVA_ERR_INVALID_ARG, "block-causal plans take prefix keys, not ranges");
+    s = validate_ranges(num_segments, key_range_offsets, key_range_starts, key_range_lengths, total_k, &backward_ok);
+    if (s != GVA_OK) return s;
+    const int32_t n = key_range_offsets[num_segments];
+    off.assign(key_range_offsets, key_range_offsets + num_segments + 1);
+    start.assign(key_range_starts, key_range_starts + n);
+    len.assign(key_range_lengths, key_range_lengths + n);
+  } else {  // as gva_plan / gva_plan_causal
+    if (cu_seqlens_k == nullptr || (num_segments > 0 && seqused_k == nullptr))
+      return fail(GVA_ERR_INVALID_ARG, "a geometry array is NULL");
+    s = validate_offsets(cu_seqlens_k, seqused_k, num_segments, "k");
+    if (s != GVA_OK) return s;
+    off.resize(num_segments + 1);
+    start.resize(num_segments);
+    len.resize(num_segments);
+    for (int32_t b = 0; b <= num_segments; ++b) off[b] = b;
+    for (int32_t b = 0; b < num_segments; ++b) {
+      start[b] = cu_seqlens_k[b];
+      len[b] = seqused_k[b];
+    }
   }
   HostWork w;
   s = build_work(cu_seqlens_q, seqused_q, num_segments, off.data(), start.data(), len.data(), num_heads_q,
-                 num_heads_kv, head_dim, causal_block, true, w);
+                 num_heads_kv, head_dim, causal_block, backward_ok, w);
   if (s != GVA_OK) return s;
+  summary->backward_ok = backward_ok ? 1 : 0;
   summary->num_work_items = static_cast<int32_t>(w.items.size());
   summary->num_key_blocks = static_cast<int32_t>(w.blocks.size());
   summary->num_merge_units = static_cast<int32_t>(w.units.size());

@@ -189,18 +189,96 @@ def test_capacity_truncates_and_errors():
     p = lambda x: x.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))  # noqa: E731
     s = _lib.WorkSummary()
     one = np.full((2, 8), -5, np.int32)
-    st = lib.gva_plan_inspect(p(a[0]), p(a[1]), p(a[2]), p(a[3]), 4, 0, 8, 2, 128, ctypes.byref(s), p(one), 1,
-                              None, 0, None, 0)
-    assert st == 0 and s.num_work_items == full["num_work_items"]
+    geo = [p(a[0]), p(a[1]), p(a[2]), p(a[3]), 4, None, None, None, 0]
+
+    def call(*rest, geometry=geo):
+        return lib.gva_plan_inspect(*geometry, *rest)
+    assert call(0, 8, 2, 128, ctypes.byref(s), p(one), 1, None, 0, None, 0) == 0
+    assert s.num_work_items == full["num_work_items"] and s.backward_ok == 1
     assert np.array_equal(one[0], full["items"][0]) and np.all(one[1] == -5)
-    # NULL summary, negative block, bad geometry
-    assert lib.gva_plan_inspect(p(a[0]), p(a[1]), p(a[2]), p(a[3]), 4, 0, 8, 2, 128, None, None, 0, None, 0,
-                                None, 0) == 1
-    assert lib.gva_plan_inspect(p(a[0]), p(a[1]), p(a[2]), p(a[3]), 4, -1, 8, 2, 128, ctypes.byref(s), None, 0,
-                                None, 0, None, 0) == 1
+    # NULL summary, negative block, bad geometry, unsupported head_dim
+    assert call(0, 8, 2, 128, None, None, 0, None, 0, None, 0) == 1
+    assert call(-1, 8, 2, 128, ctypes.byref(s), None, 0, None, 0, None, 0) == 1
     bad = a[3].copy()
     bad[0] = a[2][1] - a[2][0] + 1  # used keys above the capacity
-    assert lib.gva_plan_inspect(p(a[0]), p(a[1]), p(a[2]), p(bad), 4, 0, 8, 2, 128, ctypes.byref(s), None, 0,
-                                None, 0, None, 0) == 1
-    assert lib.gva_plan_inspect(p(a[0]), p(a[1]), p(a[2]), p(a[3]), 4, 0, 8, 2, 96, ctypes.byref(s), None, 0,
-                                None, 0, None, 0) == 2
+    assert call(0, 8, 2, 128, ctypes.byref(s), None, 0, None, 0, None, 0,
+                geometry=[p(a[0]), p(a[1]), p(a[2]), p(bad), 4, None, None, None, 0]) == 1
+    assert call(0, 8, 2, 96, ctypes.byref(s), None, 0, None, 0, None, 0) == 2
+    # ranges: a range past total_k, and ranges with a causal block, are refused
+    off, st, ln = (np.ascontiguousarray(x, np.int32) for x in ([0, 1, 1, 1, 2], [0, 90], [50, 20]))
+    rgeo = [p(a[0]), p(a[1]), None, None, 4, p(off), p(st), p(ln)]
+    assert call(0, 8, 2, 128, ctypes.byref(s), None, 0, None, 0, None, 0, geometry=rgeo + [110]) == 0
+    assert call(0, 8, 2, 128, ctypes.byref(s), None, 0, None, 0, None, 0, geometry=rgeo + [100]) == 1
+    assert call(16, 8, 2, 128, ctypes.byref(s), None, 0, None, 0, None, 0, geometry=rgeo + [110]) == 1
+
+
+def _random_ranges(rng, nseg, total_k, disjoint):
+    if disjoint:
+        cuts = np.sort(rng.choice(np.arange(1, total_k), size=8 * nseg, replace=False))
+        pieces = [(int(cuts[2 * i]), int(cuts[2 * i + 1] - cuts[2 * i])) for i in range(4 * nseg)]
+        rng.shuffle(pieces)
+        out = []
+        for _ in range(nseg):
+            take = int(rng.integers(0, 5))
+            out.append(pieces[:take])
+            pieces = pieces[take:]
+        return out
+    out = []
+    for _ in range(nseg):
+        rr = []
+        for _ in range(int(rng.integers(0, 5))):
+            st = int(rng.integers(0, total_k))
+            rr.append((st, int(rng.integers(0, min(700, total_k - st) + 1))))
+        out.append(rr)
+    return out
+
+
+@pytest.mark.parametrize("seed", range(8))
+@pytest.mark.parametrize("disjoint", [True, False])
+def test_key_range_plans(seed, disjoint):
+    """gva_plan_ranges' lists: each range cut into blocks of at most 128 keys in order;
+    every item of a segment carries its segment's blocks and key count; FLOPs count the
+    concatenated keys; dK / dV units are the blocks (one per KV head) and exist only when
+    the non-empty ranges are disjoint."""
+    rng = np.random.default_rng(900 + seed)
+    hkv = int(rng.choice([1, 2, 4]))
+    g = W.random_geometry(rng, int(rng.integers(1, 6)), 700, 10, hkv * int(rng.choice([1, 2, 8])), hkv, 128)
+    total_k = 3000
+    ranges = _random_ranges(rng, g.num_segments, total_k, disjoint)
+    w = _lib.inspect_plan(g.cu_q, g.used_q, None, None, g.num_heads_q, g.num_heads_kv, g.head_dim,
+                          key_ranges=ranges, total_k=total_k)
+    spans = sorted((st, n) for rr in ranges for st, n in rr if n > 0)
+    overlap = any(a[0] + a[1] > b[0] for a, b in zip(spans, spans[1:]))
+    assert w["backward_ok"] == (not overlap)
+    blocks, seg_blk0 = [], []
+    for rr in ranges:
+        seg_blk0.append(len(blocks))
+        for st, n in rr:
+            blocks += [(st + o, min(BLOCK_KEYS, n - o)) for o in range(0, n, BLOCK_KEYS)]
+    assert w["num_key_blocks"] == len(blocks)
+    keys = [sum(n for _, n in rr) for rr in ranges]
+    assert w["used_flops"] == pytest.approx(
+        4.0 * g.head_dim * g.num_heads_q * sum(int(q) * k for q, k in zip(g.used_q, keys)), rel=1e-12)
+    seg_of = {}
+    for b in range(g.num_segments):
+        for r in range(int(g.cu_q[b]), int(g.cu_q[b] + g.used_q[b])):
+            seg_of[r] = b
+    covered = {}
+    for it in rec(w["items"], _lib.WORK_ITEM_FIELDS):
+        b = seg_of[it["q_row0"]]
+        nb = (seg_blk0[b + 1] if b + 1 < len(seg_blk0) else len(blocks)) - seg_blk0[b]
+        assert it["blk0"] == seg_blk0[b] and it["nblk"] == nb and it["k_len"] == keys[b]
+        for r in range(it["q_row0"], it["q_row0"] + it["q_rows"]):
+            assert (r, it["head_kv"]) not in covered
+            covered[(r, it["head_kv"])] = True
+    assert len(covered) == int(g.used_q.sum()) * g.num_heads_kv
+    units = rec(w["kv_units"], _lib.KV_UNIT_FIELDS)
+    if overlap:
+        assert units == [] and w["num_bwd_items"] == 0
+        return
+    want = sorted((blk[0], blk[1], int(g.cu_q[b]), int(g.used_q[b]), hk)
+                  for b in range(g.num_segments)
+                  for blk in blocks[seg_blk0[b]:(seg_blk0[b + 1] if b + 1 < len(seg_blk0) else len(blocks))]
+                  for hk in range(g.num_heads_kv))
+    got = sorted((u["key_row0"], u["keys"], u["q_row0"], u["q_used"], u["head_kv"]) for u in units)
+    assert got == want
