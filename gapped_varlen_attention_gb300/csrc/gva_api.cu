@@ -362,6 +362,37 @@ gva_status validate_common(const int32_t* cu_seqlens_q, const int32_t* seqused_q
   return validate_offsets(cu_seqlens_q, seqused_q, num_segments, "q");
 }
 
+// Key ranges of gva_plan_ranges: offsets start at 0 and do not decrease, every range lies
+// in [0, total_k). *disjoint tells whether the non-empty ranges are pairwise disjoint.
+gva_status validate_ranges(int32_t num_segments, const int32_t* key_range_offsets, const int32_t* key_range_starts,
+                           const int32_t* key_range_lengths, int64_t total_k, bool* disjoint_out) {
+  if (key_range_offsets == nullptr) return fail(GVA_ERR_INVALID_ARG, "key_range_offsets is NULL");
+  if (total_k < 0 || total_k > INT32_MAX) return fail(GVA_ERR_INVALID_ARG, "total_k=%lld is out of range", (long long)total_k);
+  if (key_range_offsets[0] != 0) return fail(GVA_ERR_INVALID_ARG, "key_range_offsets[0] must be 0");
+  for (int32_t b = 0; b < num_segments; ++b)
+    if (key_range_offsets[b + 1] < key_range_offsets[b])
+      return fail(GVA_ERR_INVALID_ARG, "key_range_offsets decreases at segment %d", b);
+  const int32_t num_ranges = key_range_offsets[num_segments];
+  if (num_ranges > 0 && (key_range_starts == nullptr || key_range_lengths == nullptr))
+    return fail(GVA_ERR_INVALID_ARG, "key range arrays are NULL");
+  for (int32_t r = 0; r < num_ranges; ++r) {
+    const int64_t st = key_range_starts[r], n = key_range_lengths[r];
+    if (st < 0 || n < 0 || st + n > total_k)
+      return fail(GVA_ERR_INVALID_ARG, "key range %d = [%lld, %lld) is outside [0, total_k=%lld)", r, (long long)st,
+                  (long long)(st + n), (long long)total_k);
+  }
+  // The backward needs every K/V row to belong to at most one range (a shared row would
+  // need its dK / dV summed across units): check that the non-empty ranges are disjoint.
+  std::vector<std::pair<int32_t, int32_t>> spans;
+  for (int32_t r = 0; r < num_ranges; ++r)
+    if (key_range_lengths[r] > 0) spans.push_back({key_range_starts[r], key_range_lengths[r]});
+  std::sort(spans.begin(), spans.end());
+  bool disjoint = true;
+  for (size_t i = 1; i < spans.size(); ++i)
+    if (static_cast<int64_t>(spans[i - 1].first) + spans[i - 1].second > spans[i].first) disjoint = false;
+  *disjoint_out = disjoint;
+  return GVA_OK;
+}
 }  // namespace
 
 namespace gva {
@@ -415,44 +446,6 @@ gva_status gva_plan_causal(const int32_t* cu_seqlens_q, const int32_t* seqused_q
                     cu_seqlens_k[num_segments], num_heads_q, num_heads_kv, head_dim, causal_block, true,
                     out_plan);
 }
-
-}  // extern "C"
-
-namespace {
-// Key ranges of gva_plan_ranges: offsets start at 0 and do not decrease, every range lies
-// in [0, total_k). *disjoint tells whether the non-empty ranges are pairwise disjoint.
-gva_status validate_ranges(int32_t num_segments, const int32_t* key_range_offsets, const int32_t* key_range_starts,
-                           const int32_t* key_range_lengths, int64_t total_k, bool* disjoint_out) {
-  if (key_range_offsets == nullptr) return fail(GVA_ERR_INVALID_ARG, "key_range_offsets is NULL");
-  if (total_k < 0 || total_k > INT32_MAX) return fail(GVA_ERR_INVALID_ARG, "total_k=%lld is out of range", (long long)total_k);
-  if (key_range_offsets[0] != 0) return fail(GVA_ERR_INVALID_ARG, "key_range_offsets[0] must be 0");
-  for (int32_t b = 0; b < num_segments; ++b)
-    if (key_range_offsets[b + 1] < key_range_offsets[b])
-      return fail(GVA_ERR_INVALID_ARG, "key_range_offsets decreases at segment %d", b);
-  const int32_t num_ranges = key_range_offsets[num_segments];
-  if (num_ranges > 0 && (key_range_starts == nullptr || key_range_lengths == nullptr))
-    return fail(GVA_ERR_INVALID_ARG, "key range arrays are NULL");
-  for (int32_t r = 0; r < num_ranges; ++r) {
-    const int64_t st = key_range_starts[r], n = key_range_lengths[r];
-    if (st < 0 || n < 0 || st + n > total_k)
-      return fail(GVA_ERR_INVALID_ARG, "key range %d = [%lld, %lld) is outside [0, total_k=%lld)", r, (long long)st,
-                  (long long)(st + n), (long long)total_k);
-  }
-  // The backward needs every K/V row to belong to at most one range (a shared row would
-  // need its dK / dV summed across units): check that the non-empty ranges are disjoint.
-  std::vector<std::pair<int32_t, int32_t>> spans;
-  for (int32_t r = 0; r < num_ranges; ++r)
-    if (key_range_lengths[r] > 0) spans.push_back({key_range_starts[r], key_range_lengths[r]});
-  std::sort(spans.begin(), spans.end());
-  bool disjoint = true;
-  for (size_t i = 1; i < spans.size(); ++i)
-    if (static_cast<int64_t>(spans[i - 1].first) + spans[i - 1].second > spans[i].first) disjoint = false;
-  *disjoint_out = disjoint;
-  return GVA_OK;
-}
-}  // namespace
-
-extern "C" {
 
 gva_status gva_plan_ranges(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int32_t num_segments,
                            const int32_t* key_range_offsets, const int32_t* key_range_starts,
