@@ -1,4 +1,5 @@
-"""FP64 CPU oracle for the gapped variable-length attention forward and its LSE merge.
+"""FP64 CPU oracle for the gapped variable-length attention forward, its LSE merge and
+its backward.
 
 TEST INFRASTRUCTURE ONLY. This module is the correctness reference that the CUDA
 path is checked against. Only ``tests/``, ``__graft_entry__.smoke()`` and the
@@ -37,6 +38,11 @@ sets of the same query rows:
 Block-causal masking within a segment (``causal_block``) restricts row i to keys
 j < (floor(pos / B) + 1) * B with pos = i + used_k - used_q: a single launch covers the
 causal replay that the visibility partitions of PR #312 split into maskless launches.
+
+The backward (``attention_backward``) is the gradient of that definition: with P the
+softmax and dO the output gradient, dP_ij = <dO_i, V_j>, D_i = <dO_i, O_i>,
+dS_ij = P_ij (dP_ij - D_i), dQ_i = s sum_j dS_ij K_j, dK_j = s sum_i dS_ij Q_i and
+dV_j = sum_i P_ij dO_i, the sums over i running over the query heads of the KV head.
 
 Score blocks are sized from a byte budget rather than a fixed row count (the
 review of PR #302 on the FP32 fallback's score block), so long segments do not
