@@ -5,7 +5,10 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <functional>
+#include <queue>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include <cudaTypedefs.h>
@@ -19,6 +22,7 @@ struct gva_plan {
   int32_t num_segments = 0, num_heads_q = 0, num_heads_kv = 0, head_dim = 0, group = 0, causal_block = 0;
   int64_t total_q = 0, total_k = 0;
   int32_t num_items = 0, num_units = 0, grid = 0;
+  int32_t num_item_slots = 0;  // entries of d_items: each CTA's items in the kernels' walk, padded
   double used_flops = 0.0;
   gva::WorkItem* d_items = nullptr;
   gva::KeyBlock* d_blocks = nullptr;
@@ -112,6 +116,83 @@ void free_plan(struct gva_plan* p) {
   delete p;
 }
 
+// Estimated run time of a forward item, in key blocks of a two-tile item. Measured per
+// item: 1.6 us per key block with two Q tiles, 1.38 us with one (its serial chain of
+// scores, softmax and PV is not hidden behind another tile's), and about 3 us for its
+// first copies and its epilogue.
+double item_cost(const gva::WorkItem& it) {
+  return 1.9 + (it.n_tiles == 2 ? 1.0 : 0.86) * it.nblk;
+}
+
+// The forward work list as the kernels walk it: CTA c reads entry item_index(r, c, grid)
+// in round r. Items are assigned to CTAs longest first, each to the CTA with the least
+// estimated work, and then single moves or swaps between the most and the least loaded
+// CTA are applied while they lower the larger of the two. Entries past the end of a
+// CTA's list are padding items (no Q tiles, no key blocks) that every role skips.
+std::vector<gva::WorkItem> balanced_layout(const std::vector<gva::WorkItem>& sorted, int grid) {
+  std::vector<gva::WorkItem> laid;
+  if (sorted.empty() || grid <= 0) return laid;
+  std::vector<double> cost(sorted.size());
+  for (size_t i = 0; i < sorted.size(); ++i) cost[i] = item_cost(sorted[i]);
+  std::vector<std::vector<int32_t>> lists(grid);
+  std::vector<double> load(grid, 0.0);
+  using Load = std::pair<double, int>;
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+  for (int c = 0; c < grid; ++c) heap.push({0.0, c});
+  for (size_t i = 0; i < sorted.size(); ++i) {
+    const Load top = heap.top();
+    heap.pop();
+    lists[top.second].push_back(static_cast<int32_t>(i));
+    load[top.second] = top.first + cost[i];
+    heap.push({load[top.second], top.second});
+  }
+  for (int iter = 0; iter < 4 * grid + 1000; ++iter) {
+    const int hi = static_cast<int>(std::max_element(load.begin(), load.end()) - load.begin());
+    const int lo = static_cast<int>(std::min_element(load.begin(), load.end()) - load.begin());
+    double best = load[hi] - 1e-9;
+    int bi = -1, bj = -1;  // bj < 0: move item bi of hi to lo; else swap it with item bj of lo
+    for (size_t a = 0; a < lists[hi].size(); ++a) {
+      const double ca = cost[lists[hi][a]];
+      if (std::max(load[hi] - ca, load[lo] + ca) < best) {
+        best = std::max(load[hi] - ca, load[lo] + ca);
+        bi = static_cast<int>(a);
+        bj = -1;
+      }
+      for (size_t b = 0; b < lists[lo].size(); ++b) {
+        const double d = ca - cost[lists[lo][b]];
+        if (d > 0.0 && std::max(load[hi] - d, load[lo] + d) < best) {
+          best = std::max(load[hi] - d, load[lo] + d);
+          bi = static_cast<int>(a);
+          bj = static_cast<int>(b);
+        }
+      }
+    }
+    if (bi < 0) break;
+    const int32_t a = lists[hi][bi];
+    lists[hi].erase(lists[hi].begin() + bi);
+    double d = cost[a];
+    if (bj >= 0) {
+      const int32_t b = lists[lo][bj];
+      lists[lo].erase(lists[lo].begin() + bj);
+      lists[hi].push_back(b);
+      d -= cost[b];
+    }
+    lists[lo].push_back(a);
+    load[hi] -= d;
+    load[lo] += d;
+  }
+  size_t rounds = 0;
+  for (auto& l : lists) {
+    std::sort(l.begin(), l.end());  // the sorted list's order: longest first
+    rounds = std::max(rounds, l.size());
+  }
+  laid.assign(rounds * grid, gva::WorkItem{});  // padding: n_tiles = nblk = 0
+  for (int c = 0; c < grid; ++c)
+    for (size_t r = 0; r < lists[c].size(); ++r)
+      laid[gva::item_index(static_cast<int>(r), c, grid)] = sorted[lists[c][r]];
+  return laid;
+}
+
 // Shared by gva_plan and gva_plan_ranges once the arguments are validated: segment b's
 // keys are the ranges range_off[b] .. range_off[b+1] of (range_start, range_len).
 // causal_block > 0 (block-causal, one prefix range per segment): each item only gets the
@@ -151,7 +232,7 @@ gva_status build_work(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
   const int32_t tokens_per_tile = gva::kTileRows / group;
   const int32_t tokens_per_item = tokens_per_tile * gva::kTilesPerItem;
   std::vector<gva::WorkItem> items;
-  std::vector<int64_t> cost;
+  std::vector<double> cost;
   std::vector<gva::MergeUnit>& units = w.units;
   double& flops = w.flops;
   // keys visible to the row at key position pos (block-causal)
@@ -187,7 +268,7 @@ gva_status build_work(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
           it.nblk = (last + gva::kBlockKeys - 1) / gva::kBlockKeys;
         }
         items.push_back(it);
-        cost.push_back(static_cast<int64_t>(it.nblk) * it.n_tiles * 4 + it.n_tiles);
+        cost.push_back(item_cost(it));
       }
     }
   }
@@ -291,13 +372,15 @@ gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
   p->num_units = static_cast<int32_t>(units.size());
   p->grid = std::min(p->num_items, sms);
   p->used_flops = flops;
+  const std::vector<gva::WorkItem> laid = balanced_layout(sorted, p->grid);
+  p->num_item_slots = static_cast<int32_t>(laid.size());
   if ((e = cudaMalloc(&p->d_error, sizeof(int))) != cudaSuccess || (e = cudaMemset(p->d_error, 0, sizeof(int))) != cudaSuccess) {
     free_plan(p);
     return cuda_fail(e, "allocating the plan's error word");
   }
-  if (!sorted.empty()) {
-    if ((e = cudaMalloc(&p->d_items, sorted.size() * sizeof(gva::WorkItem))) != cudaSuccess ||
-        (e = cudaMemcpy(p->d_items, sorted.data(), sorted.size() * sizeof(gva::WorkItem), cudaMemcpyHostToDevice)) !=
+  if (!laid.empty()) {
+    if ((e = cudaMalloc(&p->d_items, laid.size() * sizeof(gva::WorkItem))) != cudaSuccess ||
+        (e = cudaMemcpy(p->d_items, laid.data(), laid.size() * sizeof(gva::WorkItem), cudaMemcpyHostToDevice)) !=
             cudaSuccess) {
       free_plan(p);
       return cuda_fail(e, "uploading the work list");
@@ -549,7 +632,7 @@ gva_status gva_forward(gva_plan_t plan, const void* q, const void* k, const void
   gva::FwdParams prm{};
   prm.items = plan->d_items;
   prm.blocks = plan->d_blocks;
-  prm.num_items = plan->num_items;
+  prm.num_items = plan->num_item_slots;
   prm.out = out;
   prm.out_wide = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
   prm.lse = lse;

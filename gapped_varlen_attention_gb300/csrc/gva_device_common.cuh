@@ -38,12 +38,6 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, int* e
   }
 }
 
-// Persistent schedule: the items are sorted by decreasing cost; CTA c takes item
-// r * grid + c in even rounds and r * grid + (grid - 1 - c) in odd ones.
-__device__ __forceinline__ int item_index(int round, int cta, int grid) {
-  return (round & 1) ? round * grid + (grid - 1 - cta) : round * grid + cta;
-}
-
 __device__ __forceinline__ void prefetch_l1(const void* p) {
   asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }
