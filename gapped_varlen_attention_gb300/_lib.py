@@ -44,7 +44,8 @@ class PlanInfo(ctypes.Structure):
 class WorkSummary(ctypes.Structure):
     _fields_ = [("num_work_items", ctypes.c_int32), ("num_key_blocks", ctypes.c_int32),
                 ("num_merge_units", ctypes.c_int32), ("num_bwd_items", ctypes.c_int32),
-                ("num_kv_units", ctypes.c_int32), ("backward_ok", ctypes.c_int32), ("used_flops", ctypes.c_double)]
+                ("num_kv_units", ctypes.c_int32), ("backward_ok", ctypes.c_int32), ("used_flops", ctypes.c_double),
+                ("num_walk_entries", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 _lib = None
@@ -79,7 +80,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.gva_backward_workspace_size.argtypes = [vp, ctypes.POINTER(ctypes.c_size_t)]
     lib.gva_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, vp, ctypes.c_size_t, f32, vp]
     lib.gva_plan_inspect.argtypes = [pi32, pi32, pi32, pi32, i32, pi32, pi32, pi32, ctypes.c_int64, i32, i32, i32,
-                                     i32, ctypes.POINTER(WorkSummary), pi32, i32, pi32, i32, pi32, i32]
+                                     i32, i32, ctypes.POINTER(WorkSummary), pi32, i32, pi32, i32, pi32, i32, pi32,
+                                     i32]
     for name in ("gva_plan", "gva_forward", "gva_lse_merge", "gva_plan_destroy", "gva_plan_get_info",
                  "gva_device_status", "gva_forward_noalloc", "gva_plan_ranges", "gva_plan_causal",
                  "gva_backward_workspace_size", "gva_backward", "gva_plan_inspect"):
@@ -105,14 +107,15 @@ KV_UNIT_FIELDS = ("key_row0", "keys", "q_row0", "q_used", "head_kv", "tile0", "k
 
 
 def inspect_plan(cu_seqlens_q, seqused_q, cu_seqlens_k, seqused_k, num_heads_q: int, num_heads_kv: int,
-                 head_dim: int, causal_block: int = 0, key_ranges=None, total_k: int = 0) -> dict:
+                 head_dim: int, causal_block: int = 0, key_ranges=None, total_k: int = 0, grid: int = 152) -> dict:
     """``gva_plan_inspect``: the work lists a plan of this geometry holds, built on the
     host (no CUDA call). With ``key_ranges`` (per segment a list of ``(start, length)``
     K/V row ranges, as ``Plan.from_ranges``) the keys are those ranges and
     ``cu_seqlens_k`` / ``seqused_k`` are not used. Returns the counts, ``backward_ok``,
     ``used_flops`` and three int32 arrays of 8 columns in the kernels' order: ``items``
     (forward, fields ``WORK_ITEM_FIELDS``), ``bwd_items`` (dQ, same fields) and
-    ``kv_units`` (dK / dV, ``KV_UNIT_FIELDS``)."""
+    ``kv_units`` (dK / dV, ``KV_UNIT_FIELDS``), plus ``walk``: the forward list as a grid
+    of ``grid`` CTAs walks it (index into ``items``, -1 for padding)."""
     lib = load_library()
     q = [_i32(x) for x in (cu_seqlens_q, seqused_q)]
     n = int(q[1].shape[0])
@@ -128,17 +131,19 @@ def inspect_plan(cu_seqlens_q, seqused_q, cu_seqlens_k, seqused_k, num_heads_q: 
         keys = [p(k[0]), p(k[1]), None, None, None, 0]
     summ = WorkSummary()
     args = [p(q[0]), p(q[1]), keys[0], keys[1], n, keys[2], keys[3], keys[4], keys[5], int(causal_block),
-            int(num_heads_q), int(num_heads_kv), int(head_dim), ctypes.byref(summ)]
-    _check(lib, lib.gva_plan_inspect(*args, None, 0, None, 0, None, 0), "gva_plan_inspect")
+            int(num_heads_q), int(num_heads_kv), int(head_dim), int(grid), ctypes.byref(summ)]
+    _check(lib, lib.gva_plan_inspect(*args, None, 0, None, 0, None, 0, None, 0), "gva_plan_inspect")
     items = np.zeros((max(summ.num_work_items, 1), 8), np.int32)
+    walk = np.zeros(max(summ.num_walk_entries, 1), np.int32)
     bwd = np.zeros((max(summ.num_bwd_items, 1), 8), np.int32)
     kvu = np.zeros((max(summ.num_kv_units, 1), 8), np.int32)
-    _check(lib, lib.gva_plan_inspect(*args, p(items), summ.num_work_items, p(bwd), summ.num_bwd_items, p(kvu),
-                                     summ.num_kv_units), "gva_plan_inspect")
+    _check(lib, lib.gva_plan_inspect(*args, p(items), summ.num_work_items, p(walk), summ.num_walk_entries, p(bwd),
+                                     summ.num_bwd_items, p(kvu), summ.num_kv_units), "gva_plan_inspect")
     return {"num_work_items": summ.num_work_items, "num_key_blocks": summ.num_key_blocks,
             "num_merge_units": summ.num_merge_units, "num_bwd_items": summ.num_bwd_items,
             "num_kv_units": summ.num_kv_units, "backward_ok": bool(summ.backward_ok), "used_flops": summ.used_flops,
-            "items": items[:summ.num_work_items], "bwd_items": bwd[:summ.num_bwd_items],
+            "items": items[:summ.num_work_items], "walk": walk[:summ.num_walk_entries],
+            "bwd_items": bwd[:summ.num_bwd_items],
             "kv_units": kvu[:summ.num_kv_units]}
 
 

@@ -549,10 +549,12 @@ gva_status gva_plan_inspect(const int32_t* cu_seqlens_q, const int32_t* seqused_
                             const int32_t* seqused_k, int32_t num_segments, const int32_t* key_range_offsets,
                             const int32_t* key_range_starts, const int32_t* key_range_lengths, int64_t total_k,
                             int32_t causal_block, int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim,
-                            gva_work_summary* summary, int32_t* items, int32_t items_capacity, int32_t* bwd_items,
-                            int32_t bwd_items_capacity, int32_t* kv_units, int32_t kv_units_capacity) {
+                            int32_t grid, gva_work_summary* summary, int32_t* items, int32_t items_capacity,
+                            int32_t* walk, int32_t walk_capacity, int32_t* bwd_items, int32_t bwd_items_capacity,
+                            int32_t* kv_units, int32_t kv_units_capacity) {
   if (summary == nullptr) return fail(GVA_ERR_INVALID_ARG, "summary is NULL");
   if (causal_block < 0) return fail(GVA_ERR_INVALID_ARG, "causal_block=%d must be >= 0", causal_block);
+  if (grid < 1) return fail(GVA_ERR_INVALID_ARG, "grid=%d must be >= 1", grid);
   gva_status s = validate_common(cu_seqlens_q, seqused_q, num_segments, num_heads_q, num_heads_kv, head_dim);
   if (s != GVA_OK) return s;
   std::vector<int32_t> off, start, len;
@@ -584,6 +586,26 @@ gva_status gva_plan_inspect(const int32_t* cu_seqlens_q, const int32_t* seqused_
                  num_heads_kv, head_dim, causal_block, backward_ok, w);
   if (s != GVA_OK) return s;
   summary->backward_ok = backward_ok ? 1 : 0;
+  // the forward list as a grid of `grid` CTAs walks it: the index of each entry's item
+  // in the sorted list, -1 for padding
+  const std::vector<gva::WorkItem> laid =
+      balanced_layout(w.items, std::min<int32_t>(grid, static_cast<int32_t>(w.items.size())));
+  summary->num_walk_entries = static_cast<int32_t>(laid.size());
+  if (walk != nullptr && walk_capacity > 0) {
+    // items are unique by (first row, KV head)
+    std::vector<std::pair<std::pair<int32_t, int32_t>, int32_t>> key(w.items.size());
+    for (size_t i = 0; i < w.items.size(); ++i) key[i] = {{w.items[i].q_row0, w.items[i].head_kv}, static_cast<int32_t>(i)};
+    std::sort(key.begin(), key.end());
+    for (size_t e = 0; e < laid.size() && e < static_cast<size_t>(walk_capacity); ++e) {
+      if (laid[e].n_tiles == 0) {
+        walk[e] = -1;
+        continue;
+      }
+      const auto k = std::make_pair(laid[e].q_row0, laid[e].head_kv);
+      const auto it = std::lower_bound(key.begin(), key.end(), std::make_pair(k, INT32_MIN));
+      walk[e] = (it != key.end() && it->first == k) ? it->second : -2;
+    }
+  }
   summary->num_work_items = static_cast<int32_t>(w.items.size());
   summary->num_key_blocks = static_cast<int32_t>(w.blocks.size());
   summary->num_merge_units = static_cast<int32_t>(w.units.size());

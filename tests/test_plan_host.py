@@ -22,9 +22,50 @@ def _built():
     gva.build()
 
 
-def inspect(g, causal_block=0):
+SMS = 152
+
+
+def inspect(g, causal_block=0, grid=SMS):
     return _lib.inspect_plan(g.cu_q, g.used_q, g.cu_k, g.used_k, g.num_heads_q, g.num_heads_kv, g.head_dim,
-                             causal_block)
+                             causal_block, grid=grid)
+
+
+def item_index(r, c, grid):
+    """The kernels' walk: CTA c takes entry r * grid + c in even rounds, the mirror in odd."""
+    return r * grid + (grid - 1 - c if r & 1 else c)
+
+
+def est_cost(it):
+    """The plan's run-time estimate of a forward item, in key blocks of a two-tile item:
+    1.6 us per block with two Q tiles, 1.38 us with one, about 3 us per item."""
+    return 1.9 + (1.0 if it["n_tiles"] == 2 else 0.86) * it["nblk"]
+
+
+def check_walk(items, walk, grid):
+    """Every item is walked exactly once, a CTA's padding comes after its items, and no
+    CTA carries more than the average load plus one item."""
+    n = len(items)
+    if n == 0:
+        assert len(walk) == 0
+        return
+    grid = min(grid, n)
+    assert len(walk) % grid == 0
+    seen = np.zeros(n, int)
+    loads = []
+    for c in range(grid):
+        load, padded = 0.0, False
+        for r in range(len(walk) // grid):
+            e = int(walk[item_index(r, c, grid)])
+            if e < 0:
+                padded = True
+                continue
+            assert not padded, "an item after a CTA's padding"
+            seen[e] += 1
+            load += est_cost(items[e])
+        loads.append(load)
+    assert np.all(seen == 1)
+    costs = [est_cost(it) for it in items]
+    assert max(loads) <= sum(costs) / grid + max(costs) + 1e-9
 
 
 def rec(a, fields):
@@ -86,8 +127,9 @@ def check_work(g, B=0):
     items = rec(w["items"], _lib.WORK_ITEM_FIELDS)
     assert len(items) == w["num_work_items"]
     check_items(items, tpt * TILES_PER_ITEM, TILES_PER_ITEM)
-    cost = [it["nblk"] * it["n_tiles"] * 4 + it["n_tiles"] for it in items]
+    cost = [est_cost(it) for it in items]
     assert cost == sorted(cost, reverse=True), "forward items not longest first"
+    check_walk(items, w["walk"], SMS)
 
     # ---- dQ items: one Q tile each, sorted by key blocks
     bwd = rec(w["bwd_items"], _lib.WORK_ITEM_FIELDS)
@@ -154,6 +196,35 @@ def test_long_replay_counts():
     assert w["num_work_items"] == g.num_heads_kv * sum(-(-int(q) // tpi) for q in g.used_q)
 
 
+@pytest.mark.parametrize("grid", [1, 5, 152])
+def test_walk_on_small_grids(grid):
+    g = W.random_geometry(np.random.default_rng(40 + grid), 5, 900, 2000, 8, 2, 128)
+    w = inspect(g, 0, grid)
+    check_walk(rec(w["items"], _lib.WORK_ITEM_FIELDS), w["walk"], grid)
+
+
+def test_walk_balances_the_text_video_forward():
+    """960 items (720 of two tiles, 240 of one) on 152 CTAs: 48 CTAs must take 7 items.
+    The snake order of the sorted list puts 5 long and 2 short items on some CTAs; the
+    balanced walk's longest CTA carries at most the average plus one short item, and at
+    least 5 % less than the snake's."""
+    text, video, union, dead = W.lse_merge_union()
+    w = inspect(video)
+    items = rec(w["items"], _lib.WORK_ITEM_FIELDS)
+    costs = np.array([est_cost(it) for it in items])
+    snake = np.zeros(SMS)
+    for i, c in enumerate(costs):
+        r, k = divmod(i, SMS)
+        snake[k if r % 2 == 0 else SMS - 1 - k] += c
+    loads = np.zeros(SMS)
+    for e in range(len(w["walk"])):
+        if w["walk"][e] >= 0:
+            r, k = divmod(e, SMS)
+            loads[k if r % 2 == 0 else SMS - 1 - k] += costs[w["walk"][e]]
+    assert loads.max() <= costs.sum() / SMS + costs.min() + 1e-9
+    assert loads.max() < 0.95 * snake.max()
+
+
 @pytest.mark.parametrize("seed", range(6))
 @pytest.mark.parametrize("B", [0, 1, 7, 64, 128, 300])
 def test_random_geometries(seed, B):
@@ -191,8 +262,8 @@ def test_capacity_truncates_and_errors():
     one = np.full((2, 8), -5, np.int32)
     geo = [p(a[0]), p(a[1]), p(a[2]), p(a[3]), 4, None, None, None, 0]
 
-    def call(*rest, geometry=geo):
-        return lib.gva_plan_inspect(*geometry, *rest)
+    def call(block, hq, hkv, d, summ, items, cap, *rest, geometry=geo, grid=SMS):
+        return lib.gva_plan_inspect(*geometry, block, hq, hkv, d, grid, summ, items, cap, None, 0, *rest)
     assert call(0, 8, 2, 128, ctypes.byref(s), p(one), 1, None, 0, None, 0) == 0
     assert s.num_work_items == full["num_work_items"] and s.backward_ok == 1
     assert np.array_equal(one[0], full["items"][0]) and np.all(one[1] == -5)
@@ -204,6 +275,7 @@ def test_capacity_truncates_and_errors():
     assert call(0, 8, 2, 128, ctypes.byref(s), None, 0, None, 0, None, 0,
                 geometry=[p(a[0]), p(a[1]), p(a[2]), p(bad), 4, None, None, None, 0]) == 1
     assert call(0, 8, 2, 96, ctypes.byref(s), None, 0, None, 0, None, 0) == 2
+    assert call(0, 8, 2, 128, ctypes.byref(s), None, 0, None, 0, None, 0, grid=0) == 1
     # ranges: a range past total_k, and ranges with a causal block, are refused
     off, st, ln = (np.ascontiguousarray(x, np.int32) for x in ([0, 1, 1, 1, 2], [0, 90], [50, 20]))
     rgeo = [p(a[0]), p(a[1]), None, None, 4, p(off), p(st), p(ln)]
