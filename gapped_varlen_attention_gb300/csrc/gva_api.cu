@@ -124,16 +124,18 @@ double item_cost(const gva::WorkItem& it) {
   return 1.9 + (it.n_tiles == 2 ? 1.0 : 0.86) * it.nblk;
 }
 
-// The forward work list as the kernels walk it: CTA c reads entry item_index(r, c, grid)
-// in round r. Items are assigned to CTAs longest first, each to the CTA with the least
-// estimated work, and then single moves or swaps between the most and the least loaded
-// CTA are applied while they lower the larger of the two. Entries past the end of a
-// CTA's list are padding items (no Q tiles, no key blocks) that every role skips.
-std::vector<gva::WorkItem> balanced_layout(const std::vector<gva::WorkItem>& sorted, int grid) {
-  std::vector<gva::WorkItem> laid;
+// A work list as the kernels walk it: CTA c reads entry item_index(r, c, grid) in round r.
+// Work (sorted longest first by `cost_of`) is assigned to CTAs longest first, each to
+// the CTA with the least estimated work, and then single moves or swaps between the most
+// and the least loaded CTA are applied while they lower the larger of the two. Entries
+// past the end of a CTA's list are value-initialised padding (no tiles, no key blocks,
+// no keys), which every role of the forward, dQ and dK / dV kernels skips.
+template <typename T, typename Cost>
+std::vector<T> balanced_layout(const std::vector<T>& sorted, int grid, Cost cost_of) {
+  std::vector<T> laid;
   if (sorted.empty() || grid <= 0) return laid;
   std::vector<double> cost(sorted.size());
-  for (size_t i = 0; i < sorted.size(); ++i) cost[i] = item_cost(sorted[i]);
+  for (size_t i = 0; i < sorted.size(); ++i) cost[i] = cost_of(sorted[i]);
   std::vector<std::vector<int32_t>> lists(grid);
   std::vector<double> load(grid, 0.0);
   using Load = std::pair<double, int>;
@@ -186,7 +188,7 @@ std::vector<gva::WorkItem> balanced_layout(const std::vector<gva::WorkItem>& sor
     std::sort(l.begin(), l.end());  // the sorted list's order: longest first
     rounds = std::max(rounds, l.size());
   }
-  laid.assign(rounds * grid, gva::WorkItem{});  // padding: n_tiles = nblk = 0
+  laid.assign(rounds * grid, T{});
   for (int c = 0; c < grid; ++c)
     for (size_t r = 0; r < lists[c].size(); ++r)
       laid[gva::item_index(static_cast<int>(r), c, grid)] = sorted[lists[c][r]];
@@ -372,7 +374,7 @@ gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
   p->num_units = static_cast<int32_t>(units.size());
   p->grid = std::min(p->num_items, sms);
   p->used_flops = flops;
-  const std::vector<gva::WorkItem> laid = balanced_layout(sorted, p->grid);
+  const std::vector<gva::WorkItem> laid = balanced_layout(sorted, p->grid, item_cost);
   p->num_item_slots = static_cast<int32_t>(laid.size());
   if ((e = cudaMalloc(&p->d_error, sizeof(int))) != cudaSuccess || (e = cudaMemset(p->d_error, 0, sizeof(int))) != cudaSuccess) {
     free_plan(p);
@@ -403,20 +405,30 @@ gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
     }
   }
   p->backward_ok = backward;
-  p->num_bwd_items = static_cast<int32_t>(bwd_items.size());
-  p->num_kv_units = static_cast<int32_t>(kv_units.size());
-  p->bwd_grid = std::min(p->num_bwd_items, sms);
-  if (!bwd_items.empty()) {
-    if ((e = cudaMalloc(&p->d_bwd_items, bwd_items.size() * sizeof(gva::WorkItem))) != cudaSuccess ||
-        (e = cudaMemcpy(p->d_bwd_items, bwd_items.data(), bwd_items.size() * sizeof(gva::WorkItem),
+  p->bwd_grid = std::min(static_cast<int32_t>(bwd_items.size()), sms);
+  // Both backward lists balanced like the forward's. A dQ item is one Q tile over its
+  // key blocks (three products per block); a dK / dV unit is one key block over its Q
+  // tiles (four per tile). Each also pays a fixed cost of about two blocks or tiles.
+  // The dK / dV launch takes min(entries, SMs) CTAs: the same grid as below.
+  const std::vector<gva::WorkItem> bwd_laid =
+      balanced_layout(bwd_items, p->bwd_grid, [](const gva::WorkItem& it) { return 2.0 + it.nblk; });
+  const int32_t tpt = gva::kTileRows / group;
+  const std::vector<gva::KvUnit> kv_laid = balanced_layout(
+      kv_units, std::min(static_cast<int32_t>(kv_units.size()), sms),
+      [tpt](const gva::KvUnit& u) { return 2.0 + ((u.q_used + tpt - 1) / tpt - u.tile0); });
+  p->num_bwd_items = static_cast<int32_t>(bwd_laid.size());
+  p->num_kv_units = static_cast<int32_t>(kv_laid.size());
+  if (!bwd_laid.empty()) {
+    if ((e = cudaMalloc(&p->d_bwd_items, bwd_laid.size() * sizeof(gva::WorkItem))) != cudaSuccess ||
+        (e = cudaMemcpy(p->d_bwd_items, bwd_laid.data(), bwd_laid.size() * sizeof(gva::WorkItem),
                         cudaMemcpyHostToDevice)) != cudaSuccess) {
       free_plan(p);
       return cuda_fail(e, "uploading the backward work list");
     }
   }
-  if (!kv_units.empty()) {
-    if ((e = cudaMalloc(&p->d_kv_units, kv_units.size() * sizeof(gva::KvUnit))) != cudaSuccess ||
-        (e = cudaMemcpy(p->d_kv_units, kv_units.data(), kv_units.size() * sizeof(gva::KvUnit),
+  if (!kv_laid.empty()) {
+    if ((e = cudaMalloc(&p->d_kv_units, kv_laid.size() * sizeof(gva::KvUnit))) != cudaSuccess ||
+        (e = cudaMemcpy(p->d_kv_units, kv_laid.data(), kv_laid.size() * sizeof(gva::KvUnit),
                         cudaMemcpyHostToDevice)) != cudaSuccess) {
       free_plan(p);
       return cuda_fail(e, "uploading the dK / dV units");
@@ -589,7 +601,7 @@ gva_status gva_plan_inspect(const int32_t* cu_seqlens_q, const int32_t* seqused_
   // the forward list as a grid of `grid` CTAs walks it: the index of each entry's item
   // in the sorted list, -1 for padding
   const std::vector<gva::WorkItem> laid =
-      balanced_layout(w.items, std::min<int32_t>(grid, static_cast<int32_t>(w.items.size())));
+      balanced_layout(w.items, std::min<int32_t>(grid, static_cast<int32_t>(w.items.size())), item_cost);
   summary->num_walk_entries = static_cast<int32_t>(laid.size());
   if (walk != nullptr && walk_capacity > 0) {
     // items are unique by (first row, KV head)
