@@ -108,9 +108,8 @@ struct BwdParams {
 };
 
 // Persistent schedule: in round r, CTA c of a grid of `grid` takes the work-list entry
-// at r * grid + c in even rounds and r * grid + (grid - 1 - c) in odd ones. (The
-// forward's list is laid out on the host so that this walk hands each CTA the items it
-// was assigned; the backward's lists are sorted longest first.)
+// at r * grid + c in even rounds and r * grid + (grid - 1 - c) in odd ones. The host
+// lays every work list out so that this walk hands each CTA the work it was assigned.
 __host__ __device__ inline int item_index(int round, int cta, int grid) {
   return (round & 1) ? round * grid + (grid - 1 - cta) : round * grid + cta;
 }
