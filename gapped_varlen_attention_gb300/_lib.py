@@ -80,8 +80,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.gva_backward_workspace_size.argtypes = [vp, ctypes.POINTER(ctypes.c_size_t)]
     lib.gva_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, vp, ctypes.c_size_t, f32, vp]
     lib.gva_plan_inspect.argtypes = [pi32, pi32, pi32, pi32, i32, pi32, pi32, pi32, ctypes.c_int64, i32, i32, i32,
-                                     i32, i32, ctypes.POINTER(WorkSummary), pi32, i32, pi32, i32, pi32, i32, pi32,
-                                     i32]
+                                     i32, i32, i32, ctypes.POINTER(WorkSummary), pi32, i32, pi32, i32, pi32, i32,
+                                     pi32, i32]
     for name in ("gva_plan", "gva_forward", "gva_lse_merge", "gva_plan_destroy", "gva_plan_get_info",
                  "gva_device_status", "gva_forward_noalloc", "gva_plan_ranges", "gva_plan_causal",
                  "gva_backward_workspace_size", "gva_backward", "gva_plan_inspect"):
@@ -114,8 +114,9 @@ def inspect_plan(cu_seqlens_q, seqused_q, cu_seqlens_k, seqused_k, num_heads_q: 
     ``cu_seqlens_k`` / ``seqused_k`` are not used. Returns the counts, ``backward_ok``,
     ``used_flops`` and three int32 arrays of 8 columns in the kernels' order: ``items``
     (forward, fields ``WORK_ITEM_FIELDS``), ``bwd_items`` (dQ, same fields) and
-    ``kv_units`` (dK / dV, ``KV_UNIT_FIELDS``), plus ``walk``: the forward list as a grid
-    of ``grid`` CTAs walks it (index into ``items``, -1 for padding)."""
+    ``kv_units`` (dK / dV, ``KV_UNIT_FIELDS``), plus ``walk``, ``bwd_walk`` and
+    ``kv_walk``: each list as a grid of min(``grid``, its length) CTAs walks it (per
+    entry the index into the list, -1 for padding)."""
     lib = load_library()
     q = [_i32(x) for x in (cu_seqlens_q, seqused_q)]
     n = int(q[1].shape[0])
@@ -131,18 +132,26 @@ def inspect_plan(cu_seqlens_q, seqused_q, cu_seqlens_k, seqused_k, num_heads_q: 
         keys = [p(k[0]), p(k[1]), None, None, None, 0]
     summ = WorkSummary()
     args = [p(q[0]), p(q[1]), keys[0], keys[1], n, keys[2], keys[3], keys[4], keys[5], int(causal_block),
-            int(num_heads_q), int(num_heads_kv), int(head_dim), int(grid), ctypes.byref(summ)]
-    _check(lib, lib.gva_plan_inspect(*args, None, 0, None, 0, None, 0, None, 0), "gva_plan_inspect")
+            int(num_heads_q), int(num_heads_kv), int(head_dim), int(grid)]
+    _check(lib, lib.gva_plan_inspect(*args, 0, ctypes.byref(summ), None, 0, None, 0, None, 0, None, 0),
+           "gva_plan_inspect")
     items = np.zeros((max(summ.num_work_items, 1), 8), np.int32)
-    walk = np.zeros(max(summ.num_walk_entries, 1), np.int32)
     bwd = np.zeros((max(summ.num_bwd_items, 1), 8), np.int32)
     kvu = np.zeros((max(summ.num_kv_units, 1), 8), np.int32)
-    _check(lib, lib.gva_plan_inspect(*args, p(items), summ.num_work_items, p(walk), summ.num_walk_entries, p(bwd),
-                                     summ.num_bwd_items, p(kvu), summ.num_kv_units), "gva_plan_inspect")
+    walks = []
+    for kind in range(3):  # forward items, dQ items, dK / dV units
+        s2 = WorkSummary()
+        _check(lib, lib.gva_plan_inspect(*args, kind, ctypes.byref(s2), None, 0, None, 0, None, 0, None, 0),
+               "gva_plan_inspect")
+        walk = np.zeros(max(s2.num_walk_entries, 1), np.int32)
+        _check(lib, lib.gva_plan_inspect(*args, kind, ctypes.byref(s2), p(items), summ.num_work_items, p(walk),
+                                         s2.num_walk_entries, p(bwd), summ.num_bwd_items, p(kvu),
+                                         summ.num_kv_units), "gva_plan_inspect")
+        walks.append(walk[:s2.num_walk_entries])
     return {"num_work_items": summ.num_work_items, "num_key_blocks": summ.num_key_blocks,
             "num_merge_units": summ.num_merge_units, "num_bwd_items": summ.num_bwd_items,
             "num_kv_units": summ.num_kv_units, "backward_ok": bool(summ.backward_ok), "used_flops": summ.used_flops,
-            "items": items[:summ.num_work_items], "walk": walk[:summ.num_walk_entries],
+            "items": items[:summ.num_work_items], "walk": walks[0], "bwd_walk": walks[1], "kv_walk": walks[2],
             "bwd_items": bwd[:summ.num_bwd_items],
             "kv_units": kvu[:summ.num_kv_units]}
 

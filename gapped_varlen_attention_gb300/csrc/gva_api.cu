@@ -124,24 +124,29 @@ double item_cost(const gva::WorkItem& it) {
   return 1.9 + (it.n_tiles == 2 ? 1.0 : 0.86) * it.nblk;
 }
 
+// Backward work: a dQ item is one Q tile over its key blocks (three products per
+// block), a dK / dV unit one key block over its Q tiles (four per tile); each also pays
+// a fixed cost of about two blocks or tiles.
+double dq_item_cost(const gva::WorkItem& it) { return 2.0 + it.nblk; }
+double kv_unit_cost(const gva::KvUnit& u, int32_t tokens_per_tile) {
+  return 2.0 + ((u.q_used + tokens_per_tile - 1) / tokens_per_tile - u.tile0);
+}
+
 // A work list as the kernels walk it: CTA c reads entry item_index(r, c, grid) in round r.
-// Work (sorted longest first by `cost_of`) is assigned to CTAs longest first, each to
-// the CTA with the least estimated work, and then single moves or swaps between the most
-// and the least loaded CTA are applied while they lower the larger of the two. Entries
-// past the end of a CTA's list are value-initialised padding (no tiles, no key blocks,
-// no keys), which every role of the forward, dQ and dK / dV kernels skips.
-template <typename T, typename Cost>
-std::vector<T> balanced_layout(const std::vector<T>& sorted, int grid, Cost cost_of) {
-  std::vector<T> laid;
-  if (sorted.empty() || grid <= 0) return laid;
-  std::vector<double> cost(sorted.size());
-  for (size_t i = 0; i < sorted.size(); ++i) cost[i] = cost_of(sorted[i]);
+// Work (sorted longest first, with estimated costs `cost`) is assigned to CTAs longest
+// first, each to the CTA with the least estimated work, and then single moves or swaps
+// between the most and the least loaded CTA are applied while they lower the larger of
+// the two. Returns, per entry, the index of its work in the sorted list, or -1 for
+// padding past the end of a CTA's list.
+std::vector<int32_t> balanced_walk(const std::vector<double>& cost, int grid) {
+  std::vector<int32_t> walk;
+  if (cost.empty() || grid <= 0) return walk;
   std::vector<std::vector<int32_t>> lists(grid);
   std::vector<double> load(grid, 0.0);
   using Load = std::pair<double, int>;
   std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
   for (int c = 0; c < grid; ++c) heap.push({0.0, c});
-  for (size_t i = 0; i < sorted.size(); ++i) {
+  for (size_t i = 0; i < cost.size(); ++i) {
     const Load top = heap.top();
     heap.pop();
     lists[top.second].push_back(static_cast<int32_t>(i));
@@ -188,10 +193,23 @@ std::vector<T> balanced_layout(const std::vector<T>& sorted, int grid, Cost cost
     std::sort(l.begin(), l.end());  // the sorted list's order: longest first
     rounds = std::max(rounds, l.size());
   }
-  laid.assign(rounds * grid, T{});
+  walk.assign(rounds * grid, -1);
   for (int c = 0; c < grid; ++c)
-    for (size_t r = 0; r < lists[c].size(); ++r)
-      laid[gva::item_index(static_cast<int>(r), c, grid)] = sorted[lists[c][r]];
+    for (size_t r = 0; r < lists[c].size(); ++r) walk[gva::item_index(static_cast<int>(r), c, grid)] = lists[c][r];
+  return walk;
+}
+
+// The work laid out along balanced_walk; padding entries are value-initialised (no
+// tiles, no key blocks, no keys), which every role of the forward, dQ and dK / dV
+// kernels skips.
+template <typename T, typename Cost>
+std::vector<T> balanced_layout(const std::vector<T>& sorted, int grid, Cost cost_of) {
+  std::vector<double> cost(sorted.size());
+  for (size_t i = 0; i < sorted.size(); ++i) cost[i] = cost_of(sorted[i]);
+  const std::vector<int32_t> walk = balanced_walk(cost, grid);
+  std::vector<T> laid(walk.size(), T{});
+  for (size_t e = 0; e < walk.size(); ++e)
+    if (walk[e] >= 0) laid[e] = sorted[walk[e]];
   return laid;
 }
 
@@ -406,16 +424,13 @@ gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
   }
   p->backward_ok = backward;
   p->bwd_grid = std::min(static_cast<int32_t>(bwd_items.size()), sms);
-  // Both backward lists balanced like the forward's. A dQ item is one Q tile over its
-  // key blocks (three products per block); a dK / dV unit is one key block over its Q
-  // tiles (four per tile). Each also pays a fixed cost of about two blocks or tiles.
-  // The dK / dV launch takes min(entries, SMs) CTAs: the same grid as below.
-  const std::vector<gva::WorkItem> bwd_laid =
-      balanced_layout(bwd_items, p->bwd_grid, [](const gva::WorkItem& it) { return 2.0 + it.nblk; });
+  // Both backward lists balanced like the forward's. The dK / dV launch takes
+  // min(entries, SMs) CTAs: the same grid as below.
+  const std::vector<gva::WorkItem> bwd_laid = balanced_layout(bwd_items, p->bwd_grid, dq_item_cost);
   const int32_t tpt = gva::kTileRows / group;
-  const std::vector<gva::KvUnit> kv_laid = balanced_layout(
-      kv_units, std::min(static_cast<int32_t>(kv_units.size()), sms),
-      [tpt](const gva::KvUnit& u) { return 2.0 + ((u.q_used + tpt - 1) / tpt - u.tile0); });
+  const std::vector<gva::KvUnit> kv_laid =
+      balanced_layout(kv_units, std::min(static_cast<int32_t>(kv_units.size()), sms),
+                      [tpt](const gva::KvUnit& u) { return kv_unit_cost(u, tpt); });
   p->num_bwd_items = static_cast<int32_t>(bwd_laid.size());
   p->num_kv_units = static_cast<int32_t>(kv_laid.size());
   if (!bwd_laid.empty()) {
@@ -561,12 +576,13 @@ gva_status gva_plan_inspect(const int32_t* cu_seqlens_q, const int32_t* seqused_
                             const int32_t* seqused_k, int32_t num_segments, const int32_t* key_range_offsets,
                             const int32_t* key_range_starts, const int32_t* key_range_lengths, int64_t total_k,
                             int32_t causal_block, int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim,
-                            int32_t grid, gva_work_summary* summary, int32_t* items, int32_t items_capacity,
-                            int32_t* walk, int32_t walk_capacity, int32_t* bwd_items, int32_t bwd_items_capacity,
-                            int32_t* kv_units, int32_t kv_units_capacity) {
+                            int32_t grid, int32_t walk_list, gva_work_summary* summary, int32_t* items,
+                            int32_t items_capacity, int32_t* walk, int32_t walk_capacity, int32_t* bwd_items,
+                            int32_t bwd_items_capacity, int32_t* kv_units, int32_t kv_units_capacity) {
   if (summary == nullptr) return fail(GVA_ERR_INVALID_ARG, "summary is NULL");
   if (causal_block < 0) return fail(GVA_ERR_INVALID_ARG, "causal_block=%d must be >= 0", causal_block);
   if (grid < 1) return fail(GVA_ERR_INVALID_ARG, "grid=%d must be >= 1", grid);
+  if (walk_list < 0 || walk_list > 2) return fail(GVA_ERR_INVALID_ARG, "walk_list=%d is not 0, 1 or 2", walk_list);
   gva_status s = validate_common(cu_seqlens_q, seqused_q, num_segments, num_heads_q, num_heads_kv, head_dim);
   if (s != GVA_OK) return s;
   std::vector<int32_t> off, start, len;
@@ -598,26 +614,20 @@ gva_status gva_plan_inspect(const int32_t* cu_seqlens_q, const int32_t* seqused_
                  num_heads_kv, head_dim, causal_block, backward_ok, w);
   if (s != GVA_OK) return s;
   summary->backward_ok = backward_ok ? 1 : 0;
-  // the forward list as a grid of `grid` CTAs walks it: the index of each entry's item
-  // in the sorted list, -1 for padding
-  const std::vector<gva::WorkItem> laid =
-      balanced_layout(w.items, std::min<int32_t>(grid, static_cast<int32_t>(w.items.size())), item_cost);
-  summary->num_walk_entries = static_cast<int32_t>(laid.size());
-  if (walk != nullptr && walk_capacity > 0) {
-    // items are unique by (first row, KV head)
-    std::vector<std::pair<std::pair<int32_t, int32_t>, int32_t>> key(w.items.size());
-    for (size_t i = 0; i < w.items.size(); ++i) key[i] = {{w.items[i].q_row0, w.items[i].head_kv}, static_cast<int32_t>(i)};
-    std::sort(key.begin(), key.end());
-    for (size_t e = 0; e < laid.size() && e < static_cast<size_t>(walk_capacity); ++e) {
-      if (laid[e].n_tiles == 0) {
-        walk[e] = -1;
-        continue;
-      }
-      const auto k = std::make_pair(laid[e].q_row0, laid[e].head_kv);
-      const auto it = std::lower_bound(key.begin(), key.end(), std::make_pair(k, INT32_MIN));
-      walk[e] = (it != key.end() && it->first == k) ? it->second : -2;
-    }
+  // the chosen list as a grid of min(grid, its length) CTAs walks it
+  std::vector<double> cost;
+  if (walk_list == 0) {
+    for (const auto& it : w.items) cost.push_back(item_cost(it));
+  } else if (walk_list == 1) {
+    for (const auto& it : w.bwd_items) cost.push_back(dq_item_cost(it));
+  } else {
+    const int32_t tpt = gva::kTileRows / (num_heads_q / num_heads_kv);
+    for (const auto& u : w.kv_units) cost.push_back(kv_unit_cost(u, tpt));
   }
+  const std::vector<int32_t> laid = balanced_walk(cost, std::min<int32_t>(grid, static_cast<int32_t>(cost.size())));
+  summary->num_walk_entries = static_cast<int32_t>(laid.size());
+  if (walk != nullptr && walk_capacity > 0)
+    std::memcpy(walk, laid.data(), std::min<size_t>(laid.size(), walk_capacity) * sizeof(int32_t));
   summary->num_work_items = static_cast<int32_t>(w.items.size());
   summary->num_key_blocks = static_cast<int32_t>(w.blocks.size());
   summary->num_merge_units = static_cast<int32_t>(w.units.size());

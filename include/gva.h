@@ -257,21 +257,24 @@ GVA_API gva_status gva_backward(gva_plan_t plan, const void* q, const void* k, c
  * seqused_k, key_range_offsets NULL), or that of gva_plan_ranges (key_range_offsets,
  * key_range_starts, key_range_lengths and total_k; cu_seqlens_k / seqused_k are then
  * not read and causal_block must be 0). causal_block: 0 maskless, > 0 as
- * gva_plan_causal. grid (>= 1): the forward grid to lay the work list out for (the SM
- * count). Fills *summary (backward_ok: 0 for range plans whose non-empty ranges
+ * gva_plan_causal. grid (>= 1): the SM count the work lists are laid out for;
+ * walk_list selects the list `walk` describes (0 forward items, 1 dQ items, 2 dK / dV
+ * units). Fills *summary (backward_ok: 0 for range plans whose non-empty ranges
  * overlap, which gva_backward refuses) and copies at most *_capacity records of 8 int32
  * each into each non-NULL array, in the order the kernels take them:
  *   items     : forward work items {q_row0, q_rows, blk0, nblk, head_kv, n_tiles, k_len,
  *               q_pos0}, longest first;
- *   walk      : one int32 per entry of the forward list as the kernel walks it (CTA c
- *               reads entry r * grid + c in even rounds r, r * grid + grid - 1 - c in
- *               odd ones): the entry's index in items, or -1 for padding;
+ *   walk      : one int32 per entry of the chosen list as its kernel walks it (with
+ *               g = min(grid, the list's length) CTAs, CTA c reads entry r * g + c in
+ *               even rounds r and r * g + g - 1 - c in odd ones): the entry's index in
+ *               the sorted list, or -1 for padding;
  *   bwd_items : backward dQ items, same layout, one Q tile each;
  *   kv_units  : backward dK / dV units {key_row0, keys, q_row0, q_used, head_kv, tile0,
  *               key_pos0, pos_shift}, one per key block and KV head.
  * bwd_items and kv_units are empty when backward_ok is 0.
  * Errors: GVA_ERR_INVALID_ARG for a NULL summary, a negative causal_block, ranges with a
- * causal_block, grid < 1 or bad geometry; GVA_ERR_UNSUPPORTED as gva_plan.
+ * causal_block, grid < 1, walk_list outside 0 .. 2 or bad geometry; GVA_ERR_UNSUPPORTED
+ * as gva_plan.
  */
 typedef struct {
   int32_t num_work_items, num_key_blocks, num_merge_units, num_bwd_items, num_kv_units, backward_ok;
@@ -283,7 +286,8 @@ GVA_API gva_status gva_plan_inspect(const int32_t* cu_seqlens_q, const int32_t* 
                                     const int32_t* key_range_offsets, const int32_t* key_range_starts,
                                     const int32_t* key_range_lengths, int64_t total_k, int32_t causal_block,
                                     int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim, int32_t grid,
-                                    gva_work_summary* summary, int32_t* items, int32_t items_capacity,
+                                    int32_t walk_list, gva_work_summary* summary, int32_t* items,
+                                    int32_t items_capacity,
                                     int32_t* walk, int32_t walk_capacity, int32_t* bwd_items,
                                     int32_t bwd_items_capacity, int32_t* kv_units, int32_t kv_units_capacity);
 

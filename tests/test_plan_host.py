@@ -41,7 +41,15 @@ def est_cost(it):
     return 1.9 + (1.0 if it["n_tiles"] == 2 else 0.86) * it["nblk"]
 
 
-def check_walk(items, walk, grid):
+def dq_cost(it):
+    return 2.0 + it["nblk"]
+
+
+def kv_cost(u, tpt):
+    return 2.0 + (-(-u["q_used"] // tpt) - u["tile0"])
+
+
+def check_walk(items, walk, grid, cost=est_cost):
     """Every item is walked exactly once, a CTA's padding comes after its items, and no
     CTA carries more than the average load plus one item."""
     n = len(items)
@@ -61,10 +69,10 @@ def check_walk(items, walk, grid):
                 continue
             assert not padded, "an item after a CTA's padding"
             seen[e] += 1
-            load += est_cost(items[e])
+            load += cost(items[e])
         loads.append(load)
     assert np.all(seen == 1)
-    costs = [est_cost(it) for it in items]
+    costs = [cost(it) for it in items]
     assert max(loads) <= sum(costs) / grid + max(costs) + 1e-9
 
 
@@ -136,6 +144,7 @@ def check_work(g, B=0):
     check_items(bwd, tpt, 1)
     nb = [it["nblk"] for it in bwd]
     assert nb == sorted(nb, reverse=True), "dQ items not longest first"
+    check_walk(bwd, w["bwd_walk"], SMS, dq_cost)
 
     # ---- dK / dV units: one per (segment, KV head, key block), every used key once
     units = rec(w["kv_units"], _lib.KV_UNIT_FIELDS)
@@ -169,6 +178,7 @@ def check_work(g, B=0):
         assert not np.any(lim[:min(got["tile0"] * tpt, len(lim))] > u["key_pos0"])
     tiles = [-(-u["q_used"] // tpt) - u["tile0"] for u in units]
     assert tiles == sorted(tiles, reverse=True), "dK / dV units not longest first"
+    check_walk(units, w["kv_walk"], SMS, lambda u: kv_cost(u, tpt))
     return w
 
 
@@ -262,8 +272,8 @@ def test_capacity_truncates_and_errors():
     one = np.full((2, 8), -5, np.int32)
     geo = [p(a[0]), p(a[1]), p(a[2]), p(a[3]), 4, None, None, None, 0]
 
-    def call(block, hq, hkv, d, summ, items, cap, *rest, geometry=geo, grid=SMS):
-        return lib.gva_plan_inspect(*geometry, block, hq, hkv, d, grid, summ, items, cap, None, 0, *rest)
+    def call(block, hq, hkv, d, summ, items, cap, *rest, geometry=geo, grid=SMS, walk_list=0):
+        return lib.gva_plan_inspect(*geometry, block, hq, hkv, d, grid, walk_list, summ, items, cap, None, 0, *rest)
     assert call(0, 8, 2, 128, ctypes.byref(s), p(one), 1, None, 0, None, 0) == 0
     assert s.num_work_items == full["num_work_items"] and s.backward_ok == 1
     assert np.array_equal(one[0], full["items"][0]) and np.all(one[1] == -5)
@@ -276,6 +286,7 @@ def test_capacity_truncates_and_errors():
                 geometry=[p(a[0]), p(a[1]), p(a[2]), p(bad), 4, None, None, None, 0]) == 1
     assert call(0, 8, 2, 96, ctypes.byref(s), None, 0, None, 0, None, 0) == 2
     assert call(0, 8, 2, 128, ctypes.byref(s), None, 0, None, 0, None, 0, grid=0) == 1
+    assert call(0, 8, 2, 128, ctypes.byref(s), None, 0, None, 0, None, 0, walk_list=3) == 1
     # ranges: a range past total_k, and ranges with a causal block, are refused
     off, st, ln = (np.ascontiguousarray(x, np.int32) for x in ([0, 1, 1, 1, 2], [0, 90], [50, 20]))
     rgeo = [p(a[0]), p(a[1]), None, None, 4, p(off), p(st), p(ln)]
