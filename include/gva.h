@@ -260,8 +260,8 @@ GVA_API gva_status gva_backward(gva_plan_t plan, const void* q, const void* k, c
  * gva_plan_causal. grid (>= 1): the SM count the work lists are laid out for;
  * walk_list selects the list `walk` describes (0 forward items, 1 dQ items, 2 dK / dV
  * units). Fills *summary (backward_ok: 0 for range plans whose non-empty ranges
- * overlap, which gva_backward refuses) and copies at most *_capacity records of 8 int32
- * each into each non-NULL array, in the order the kernels take them:
+ * overlap, which gva_backward refuses) and copies at most *_capacity records into each
+ * non-NULL array (8 int32 per record; one per entry for walk):
  *   items     : forward work items {q_row0, q_rows, blk0, nblk, head_kv, n_tiles, k_len,
  *               q_pos0}, longest first;
  *   walk      : one int32 per entry of the chosen list as its kernel walks it (with
@@ -287,9 +287,9 @@ GVA_API gva_status gva_plan_inspect(const int32_t* cu_seqlens_q, const int32_t* 
                                     const int32_t* key_range_lengths, int64_t total_k, int32_t causal_block,
                                     int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim, int32_t grid,
                                     int32_t walk_list, gva_work_summary* summary, int32_t* items,
-                                    int32_t items_capacity,
-                                    int32_t* walk, int32_t walk_capacity, int32_t* bwd_items,
-                                    int32_t bwd_items_capacity, int32_t* kv_units, int32_t kv_units_capacity);
+                                    int32_t items_capacity, int32_t* walk, int32_t walk_capacity,
+                                    int32_t* bwd_items, int32_t bwd_items_capacity, int32_t* kv_units,
+                                    int32_t kv_units_capacity);
 
 /* Release a plan's device memory. NULL is accepted. Synchronous with respect to the
  * host only through cudaFree. */
