@@ -22,7 +22,6 @@ import hashlib
 import json
 import math
 import os
-import re
 import subprocess
 import sys
 import threading
@@ -39,12 +38,14 @@ import torch  # noqa: E402
 METRIC = "gapped-varlen attn fwd TFLOP/s (used rows) & % of GB300 BF16 peak; ms/launch"
 UNIT = "TFLOP/s"
 CSRC = os.path.join(ROOT, "gapped_varlen_attention_gb300", "csrc")
-# workload -> (ncu summary holding its DRAM bytes per launch, kernel source it was taken on)
-TRAFFIC_SUMMARIES = {
-    "long_replay": (os.path.join(ROOT, "profiles", "gva_fwd_kernel_long_replay.md"), os.path.join(CSRC, "gva_fwd.cu")),
-    "long_replay_bwd": (os.path.join(ROOT, "profiles", "gva_backward_long_replay.md"), os.path.join(CSRC, "gva_bwd.cu")),
-    "lse_merge": (os.path.join(ROOT, "profiles", "gva_lse_merge_kernel_text_video.md"),
-                  os.path.join(CSRC, "gva_merge.cu")),
+# DRAM bytes per launch of each workload's dominant kernel, as ncu measured them, with
+# the hash of the kernel sources they were measured on (written by hand from ncu output)
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "dram_traffic.json")
+# the sources behind each timed kernel: its .cu file and the device headers it includes
+KERNEL_SOURCES = {
+    "gva_fwd_kernel": ["gva_fwd.cu", "gva_device_common.cuh", "sm103_ptx.cuh", "gva_internal.h"],
+    "gva_backward": ["gva_bwd.cu", "gva_device_common.cuh", "sm103_ptx.cuh", "gva_internal.h"],
+    "gva_lse_merge_kernel": ["gva_merge.cu", "gva_device_common.cuh", "sm103_ptx.cuh", "gva_internal.h"],
 }
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
@@ -202,7 +203,7 @@ class Workload:
         self.flops = float(sum(p.info()["used_flops"] for p in self.plans))
         self.launches_per_step = len(self.geoms) + (0 if self.parts is None else 1)
         self.metric, self.unit, self.scale, self.bound = METRIC, UNIT, 1e12, "tensor"
-        self.kernel = "gva_fwd_kernel"
+        self.kernel = self.kernel_key = "gva_fwd_kernel"
         # the forward launch that dominates the step (most FLOPs)
         self.dominant = int(np.argmax([p.info()["used_flops"] for p in self.plans])) if self.plans else 0
         if getattr(self, "part_kv", None) is not None:
@@ -217,6 +218,7 @@ class Workload:
             self.metric = "gapped-varlen FP32 LSE merge GB/s (algorithmic bytes: live partials, LSEs, output)"
             self.unit, self.scale, self.bound = "GB/s", 1e9, "hbm"
             self.kernel = "gva_lse_merge_kernel<float, bf16>"
+            self.kernel_key = "gva_lse_merge_kernel"
         if getattr(self, "backward", False):
             # the forward's O and LSE are inputs of the backward (computed once, untimed)
             gva.forward(self.plans[0], self.q, self.k, self.v, self.out, self.lse)
@@ -229,6 +231,7 @@ class Workload:
             self.launches_per_step = 3  # rowsum(dO * O), dQ, dK / dV
             self.metric = "gapped-varlen attn bwd TFLOP/s (used rows, 2.5 x fwd FLOPs) & % of GB300 BF16 peak"
             self.kernel = "gva_backward (3 launches: rowsum, dQ, dK/dV)"
+            self.kernel_key = "gva_backward"
             self.inputs = [self.q, self.k, self.v, self.out, self.lse, self.d_out]
             self.outputs = list(self.grads)
         self.work = merge_bytes(self.parts, self.used_k_parts, self.out.element_size()) if self.merge_only \
@@ -263,6 +266,26 @@ class Workload:
         if getattr(self, "part_kv", None) is not None:
             return inputs[1 + 2 * i], inputs[2 + 2 * i]
         return inputs[1], inputs[2]
+
+    def dominant_bytes(self) -> float:
+        """Algorithmic HBM bytes of one launch of the dominant kernel (one backward call
+        for the backward): each used row and used key read or written once. Forward: Q,
+        O and the LSE of the used rows, K and V of the used keys. Backward: Q, O, dO and
+        dQ of the used rows, K, V, dK and dV of the used keys, the LSE read and D
+        written once and read twice. Merge: the metric's own bytes."""
+        if self.merge_only:
+            return float(self.work)
+        g = self.geoms[0 if getattr(self, "backward", False) else self.dominant]
+        hq, hkv, d = g.num_heads_q, g.num_heads_kv, g.head_dim
+        q_rows = float(np.sum(g.used_q))
+        if getattr(self, "ranges", None) is not None:
+            k_rows = float(sum(n for rs in self.ranges for _, n in rs))
+        else:
+            k_rows = float(np.sum(g.used_k))
+        if getattr(self, "backward", False):
+            return q_rows * hq * (4 * d * 2 + 4 * 4) + k_rows * hkv * 4 * d * 2
+        out = self.partials[self.dominant][0] if self.partials else self.out
+        return q_rows * hq * (d * 2 + d * out.element_size() + 4) + k_rows * hkv * 2 * d * 2
 
     def check(self):
         for p in self.plans + ([self.merge_plan] if self.parts is not None else []):
@@ -350,25 +373,26 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def source_hash(path: str) -> str:
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def kernel_source_hash(kernel: str) -> str:
+    """sha256[:16] over the kernel's sources (its .cu file, then the headers it includes)."""
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per launch (per step for the backward's three launches) from the
-    committed ncu summary, if it was taken on the current kernel source; else None."""
-    if workload not in TRAFFIC_SUMMARIES:
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes (read + write) per launch of the workload's dominant kernel (per call
+    for the backward's three launches), from the ncu record, if it was measured on the
+    current kernel sources; else None."""
+    if not os.path.exists(TRAFFIC_RECORD):
         return None
-    summary, source = TRAFFIC_SUMMARIES[workload]
-    if not os.path.exists(summary):
+    with open(TRAFFIC_RECORD) as f:
+        rec = json.load(f).get("records", {}).get(workload)
+    if not rec or rec.get("kernel") != kernel or rec.get("source_sha16") != kernel_source_hash(kernel):
         return None
-    text = open(summary).read()
-    h = re.search(r"kernel source sha256\[:16\][^:]*:\s*`?([0-9a-f]{16})", text)
-    t = re.search(r"dram bytes per full (?:launch|step)\s*[:|]\s*`?([0-9.eE+]+)", text)
-    if not h or not t or h.group(1) != source_hash(source):
-        return None
-    return float(t.group(1))
+    return float(rec["dram_bytes_per_launch"])
 
 
 class ClockSampler:
@@ -549,6 +573,31 @@ class E2EPipeline:
         end.synchronize()
         return start.elapsed_time(end)
 
+    def copy_rates(self, reps: int = 3):
+        """GB/s of one step's own copies run alone, nothing else on the device: the
+        host->device copy of its inputs and the device->host copy of its results (the
+        same row ranges and pinned buffers as the timed steps), each timed with events
+        on its copy stream. They tell how much of an end-to-end step the box's copy
+        rate sets."""
+        rates = []
+        for stream, copies in ((self.s_in, [(d, h, r) for d, h, r in zip(self.d_in[0], self.h_in, self.r_in)]),
+                               (self.s_out, [(h, d, r) for h, d, r in zip(self.h_out[0], self.d_out[0],
+                                                                          self.r_out)])):
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                for _ in range(reps):
+                    for dst, src, r in copies:
+                        copy_rows(dst, src, r)
+                b.record(stream)
+            b.synchronize()
+            rates.append(a.elapsed_time(b) / reps)
+        bi, bo = self.wl.copy_bytes()
+        return {"h2d_gbs": round(bi / (rates[0] * 1e-3) / 1e9, 1) if rates[0] > 0 else None,
+                "d2h_gbs": round(bo / (rates[1] * 1e-3) / 1e9, 1) if rates[1] > 0 else None,
+                "h2d_ms": round(rates[0], 4), "d2h_ms": round(rates[1], 4)}
+
 
 def max_over_ranks(values, dist, device):
     """Element-wise maximum of per-rank timings over all ranks (the slowest rank sets
@@ -654,6 +703,131 @@ def oracle_merge_rate(wl, budget_s: float, rng):
 
 # --------------------------------------------------------------------------------------
 
+# the other workloads the default run also measures (one entry each in `configs`):
+# the pages' remaining shapes, the fused and block-causal forms of the multiview replay,
+# the merge alone and the backward of the long replay
+CONFIG_WORKLOADS = ("tiny", "cfg_text_cross", "multiview_causal", "multiview_fused", "multiview_blockcausal",
+                    "lse_merge_union", "lse_merge", "long_replay_bwd")
+
+
+def measure(wl, steps: int, warmup: int, e2e_steps: int, stream, clock_index: int, barrier=lambda: None):
+    """Time one workload on this rank: `steps` steps (CUDA events per step), the
+    dominant kernel alone, the end-to-end steps through the public API, the pinned copy
+    rates, and the SM clocks during the timed region. Returns the raw numbers."""
+    for _ in range(warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    wl.check()
+    flush = L2Flush() if spec_input_bytes(wl.spec) <= 2 * 129e6 else None
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(clock_index) as clocks:
+        # nvidia-smi is up before the timed region starts; the same steps keep running
+        # meanwhile so that the clocks do not drop while the device would otherwise idle
+        def keep_busy():
+            for _ in range(max(1, warmup)):
+                wl.step()
+            torch.cuda.synchronize()
+        clocks.wait_samples(1, 5.0, work=keep_busy)
+        n_before = len(clocks.lines)
+        torch.cuda.nvtx.range_push("timed")  # lets a profiler keep only the timed launches
+        step_ms = []
+        ms = time_steps(wl.step, steps, stream, flush, step_ms)
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
+        window = "timed region"
+        if len(clocks.lines) - n_before < 3:
+            # a timed region shorter than the 200 ms sampling period: sample the same
+            # steps, untimed, right after it
+            def more():
+                for _ in range(4):
+                    wl.step()
+                torch.cuda.synchronize()
+            clocks.wait_samples(n_before + 3, 3.0, work=more)
+            window = ("timed region plus the same steps, untimed, right after it (the region is shorter than "
+                      "the sampling period)")
+    barrier()
+    # kernel-only time of the dominant launch (the forward with the most FLOPs; for the
+    # backward workload the whole backward call, for the merge workload the merge)
+    if getattr(wl, "backward", False) or wl.merge_only:
+        dominant = wl.step
+    else:
+        i = wl.dominant
+        dominant = lambda: wl.gva.forward(wl.plans[i], wl.q, *wl.kv_of(i),  # noqa: E731
+                                          *(wl.partials[i] if wl.partials else (wl.out, wl.lse)))
+    n_dom = max(3, steps // 2)
+    dom_ms = time_steps(dominant, n_dom, stream, flush) / n_dom
+    wl.check()
+    same_size_copy_gbs = None
+    if wl.bound == "hbm":
+        # context for an HBM-bound kernel of this size: a device copy moving the same
+        # bytes (half read, half written), timed the same way
+        src = torch.empty(int(wl.work // 2), dtype=torch.uint8, device="cuda")
+        dst = torch.empty_like(src)
+        copy_ms = time_steps(lambda: dst.copy_(src), 10, stream, flush) / 10
+        same_size_copy_gbs = wl.work / (copy_ms * 1e-3) / 1e9
+        del src, dst
+    # end to end through the public API: every step copies its inputs from pinned host
+    # memory and its results back, inside the timed region (pipelined over two buffers)
+    e2e_run = E2EPipeline(wl, stream)
+    e2e_run.run(1)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = e2e_run.run(e2e_steps) / e2e_steps
+    barrier()
+    copy = e2e_run.copy_rates()
+    del e2e_run
+    return {"ms_step": ms / steps, "med_ms": float(np.median(step_ms)), "dom_ms": dom_ms, "dom_launches": n_dom,
+            "e2e_ms": e2e_ms, "copy": copy, "clocks": {**clocks.summary(), "window": window},
+            "same_size_copy_gbs": same_size_copy_gbs, "l2_flushed": flush is not None}
+
+
+def roofline_of(wl, r, peaks, peak_src, traffic):
+    """The roofline entry of the dominant kernel. Its peak is the measured burst rate
+    when the kernel's own timed region (dom_launches x dom_ms) lasts under a second,
+    else the sustained one; both fractions are given for tensor-bound kernels."""
+    if getattr(wl, "backward", False) or wl.merge_only:
+        dom_work = wl.work
+    else:
+        dom_work = wl.plans[wl.dominant].info()["used_flops"]
+    achieved = dom_work / (r["dom_ms"] * 1e-3) / wl.scale
+    region_ms = r["dom_ms"] * r["dom_launches"]
+    out = {"bound": wl.bound, "achieved": round(achieved, 2)}
+    if wl.bound == "hbm":
+        peak = peaks["hbm_gbs"]
+        out.update(peak=peak, unit=wl.unit, frac=round(achieved / peak, 4),
+                   peak_source=f"{peak_src} HBM copy bandwidth (STREAM-style, read + write bytes)")
+    else:
+        sustained = region_ms > 1000.0
+        peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+        out.update(peak=peak, unit=wl.unit, frac=round(achieved / peak, 4),
+                   frac_burst=round(achieved / peaks["bf16_tflops"], 4),
+                   frac_sustained=round(achieved / peaks["bf16_tflops_sustained"], 4),
+                   peak_source=(f"{peak_src} {'sustained' if sustained else 'burst'} dense bf16 (cuBLAS): the "
+                                f"kernel's timed region ({r['dom_launches']} launches, {region_ms:.0f} ms) is "
+                                f"{'over' if sustained else 'under'} 1 s"))
+    out.update(traffic=traffic, kernel=wl.kernel, ms_per_launch=round(r["dom_ms"], 4),
+               launches_timed=r["dom_launches"])
+    alg = wl.dominant_bytes()
+    out["algorithmic_bytes"] = alg
+    if traffic is not None and alg > 0:
+        out["traffic_over_algorithmic"] = round(traffic / alg, 3)
+    if r["same_size_copy_gbs"] is not None:
+        out["same_size_copy_gbs"] = round(r["same_size_copy_gbs"], 1)
+    return out
+
+
+def e2e_of(wl, r, world):
+    bi, bo = wl.copy_bytes()
+    return {"value": round(job_rate(world, wl.work, r["e2e_ms"], wl.scale), 3), "unit": wl.unit,
+            "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo), "ms_per_step": round(r["e2e_ms"], 4),
+            "copy_gbs": r["copy"],
+            "copies": "pinned host buffers; every step copies its inputs in and its results out: the used rows of "
+                      "each [rows, heads, d] tensor (gap rows are neither inputs nor results) and whole LSE-shaped "
+                      "tensors; two device buffer sets and two copy streams overlap step i+1's input copy and step "
+                      "i-1's result copy with step i. copy_gbs: the same copies run alone on this box"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -663,6 +837,9 @@ def main():
     ap.add_argument("--workload", default="long_replay", choices=list(WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--configs", default="auto",
+                    help="comma-separated workloads measured after the main one and reported under `configs`; "
+                         "'auto': the other workloads for the default run, none otherwise; 'none': none")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -687,107 +864,61 @@ def main():
     if dist is not None:
         dist.barrier()
     gva.load_library()
-
-    wl = Workload(args.workload, seed_offset=rank)
     stream = torch.cuda.current_stream()
 
     def barrier():
         if dist is not None:
             dist.barrier()
 
-    for _ in range(args.warmup):
-        wl.step()
-    torch.cuda.synchronize()
-    wl.check()
-
-    flush = None
-    if spec_input_bytes(wl.spec) <= 2 * 129e6:
-        flush = L2Flush()
-
-    barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local_rank) as clocks:
-        # nvidia-smi is up before the timed region starts; the same steps keep running
-        # meanwhile so that the clocks do not drop while the device would otherwise idle
-        def keep_busy():
-            for _ in range(max(1, args.warmup)):
-                wl.step()
-            torch.cuda.synchronize()
-        clocks.wait_samples(1, 5.0, work=keep_busy)
-        n_before = len(clocks.lines)
-        torch.cuda.nvtx.range_push("timed")  # lets a profiler keep only the timed launches
-        step_ms = []
-        ms = time_steps(wl.step, args.steps, stream, flush, step_ms)
-        torch.cuda.synchronize()
-        torch.cuda.nvtx.range_pop()
-        clock_window = "timed region"
-        if len(clocks.lines) - n_before < 3:
-            # a timed region shorter than the 200 ms sampling period: sample the same
-            # steps, untimed, right after it
-            def more():
-                for _ in range(4):
-                    wl.step()
-                torch.cuda.synchronize()
-            clocks.wait_samples(n_before + 3, 3.0, work=more)
-            clock_window = ("timed region plus the same steps, untimed, right after it (the region is shorter "
-                            "than the sampling period)")
-    barrier()
-    ms_step = ms / args.steps
-    # kernel-only time of the dominant launch (the forward with the most FLOPs; for the
-    # backward workload the whole backward call, for the merge workload the merge) over
-    # the same kind of region
-    if getattr(wl, "backward", False) or wl.merge_only:
-        fwd_only = wl.step
+    if args.configs == "auto":
+        extra = [w for w in CONFIG_WORKLOADS if w != args.workload] if args.workload == "long_replay" else []
+    elif args.configs == "none":
+        extra = []
     else:
-        i = wl.dominant
-        fwd_only = lambda: wl.gva.forward(wl.plans[i], wl.q, *wl.kv_of(i),  # noqa: E731
-                                          *(wl.partials[i] if wl.partials else (wl.out, wl.lse)))
-    fwd_ms = time_steps(fwd_only, max(3, args.steps // 2), stream, flush) / max(3, args.steps // 2)
-    wl.check()
-    copy_gbs = None
-    if wl.bound == "hbm":
-        # context for an HBM-bound kernel of this size: a device copy moving the same
-        # bytes (half read, half written), timed the same way
-        src = torch.empty(int(wl.work // 2), dtype=torch.uint8, device="cuda")
-        dst = torch.empty_like(src)
-        copy_ms = time_steps(lambda: dst.copy_(src), 10, stream, flush) / 10
-        copy_gbs = wl.work / (copy_ms * 1e-3) / 1e9
-        del src, dst
+        extra = [w for w in args.configs.split(",") if w and w != args.workload]
+        for w in extra:
+            if w not in LABELS:
+                raise SystemExit(f"unknown workload {w}")
 
-    # end to end through the public API: every step copies its inputs from pinned host
-    # memory and its results back, inside the timed region (pipelined over two buffers)
-    e2e_run = E2EPipeline(wl, stream)
-    e2e_run.run(1)
-    torch.cuda.synchronize()
-    barrier()
-    e2e_ms = e2e_run.run(args.e2e_steps) / args.e2e_steps
-    barrier()
+    wl = Workload(args.workload, seed_offset=rank)
+    r = measure(wl, args.steps, args.warmup, args.e2e_steps, stream, local_rank, barrier)
+    r["ms_step"], r["dom_ms"], r["e2e_ms"], r["med_ms"] = max_over_ranks(
+        [r["ms_step"], r["dom_ms"], r["e2e_ms"], r["med_ms"]], dist, "cuda")
+    peaks, peak_src = load_peaks()
+    cpu = oracle_sample_rate(wl, args.cpu_budget_s) if rank == 0 else None
 
-    ms_step, fwd_ms, e2e_ms, med_ms = max_over_ranks([ms_step, fwd_ms, e2e_ms, float(np.median(step_ms))], dist,
-                                                     "cuda")
+    configs = {}
+    for name in extra:
+        # the main workload's buffers stay resident; each extra workload is built, timed
+        # and released in turn
+        w = Workload(name, seed_offset=rank)
+        rc = measure(w, args.steps, args.warmup, args.e2e_steps, stream, local_rank, barrier)
+        rc["ms_step"], rc["dom_ms"], rc["e2e_ms"], rc["med_ms"] = max_over_ranks(
+            [rc["ms_step"], rc["dom_ms"], rc["e2e_ms"], rc["med_ms"]], dist, "cuda")
+        value = job_rate(world, w.work, rc["ms_step"], w.scale)
+        configs[name] = {
+            "description": w.label, "metric": w.metric, "unit": w.unit,
+            "value": round(value, 3), "ms_per_step": round(rc["ms_step"], 4),
+            "ms_per_step_median": round(rc["med_ms"], 4),
+            ("algorithmic_bytes_per_step" if w.merge_only else "useful_flops_per_step"): w.work,
+            "roofline": roofline_of(w, rc, peaks, peak_src, recorded_traffic(name, w.kernel_key)),
+            "e2e": e2e_of(w, rc, world),
+            "gpu_launches": args.steps * w.launches_per_step,
+            "clocks": rc["clocks"],
+            "l2": "flushed before every step" if rc["l2_flushed"] else "inputs larger than L2",
+        }
+        del w
+        torch.cuda.empty_cache()
 
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
         return
 
-    peaks, peak_src = load_peaks()
-    sustained = args.steps * ms_step > 1000.0
-    if wl.bound == "hbm":
-        peak = peaks["hbm_gbs"]
-        peak_desc = f"{peak_src} HBM copy bandwidth (STREAM-style, read + write bytes)"
-    else:
-        peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
-        peak_desc = f"{peak_src} {'sustained' if sustained else 'burst'} dense bf16 (cuBLAS)"
-    value = job_rate(world, wl.work, ms_step, wl.scale)
-    if getattr(wl, "backward", False) or wl.merge_only:
-        dom_work = wl.work
-    else:
-        dom_work = wl.plans[wl.dominant].info()["used_flops"]
-    achieved = dom_work / (fwd_ms * 1e-3) / wl.scale
-    traffic = recorded_traffic(args.workload)
-    cpu_rate, cpu_desc, _, _ = oracle_sample_rate(wl, args.cpu_budget_s)
-    e2e_value = job_rate(world, wl.work, e2e_ms, wl.scale)
+    value = job_rate(world, wl.work, r["ms_step"], wl.scale)
+    peak_line = peaks["hbm_gbs"] if wl.bound == "hbm" else peaks[
+        "bf16_tflops_sustained" if args.steps * r["ms_step"] > 1000.0 else "bf16_tflops"]
+    cpu_rate, cpu_desc, _, _ = cpu
     line = {
         "metric": wl.metric,
         "value": round(value, 3),
@@ -795,42 +926,28 @@ def main():
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(ms_step, 4),
-        "ms_per_step_median": round(med_ms, 4),
+        "ms_per_step": round(r["ms_step"], 4),
+        "ms_per_step_median": round(r["med_ms"], 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16, the pages' segment shapes)",
         "config": wl.config(f"replicas x{world} (independent problems per GPU)"),
-        ("pct_of_hbm_peak" if wl.bound == "hbm" else "pct_of_bf16_peak"): round(100.0 * value / world / peak, 2),
+        ("pct_of_hbm_peak" if wl.bound == "hbm" else "pct_of_bf16_peak"): round(
+            100.0 * value / world / peak_line, 2),
         **({} if wl.bound == "hbm" else {
             "pct_of_bf16_peak_burst": round(100.0 * value / world / peaks["bf16_tflops"], 2),
             "pct_of_bf16_peak_sustained": round(100.0 * value / world / peaks["bf16_tflops_sustained"], 2)}),
-        "roofline": {
-            "bound": wl.bound,
-            "achieved": round(achieved, 2),
-            "peak": peak,
-            "unit": wl.unit,
-            "frac": round(achieved / peak, 4),
-            "traffic": traffic,
-            "kernel": wl.kernel,
-            "ms_per_launch": round(fwd_ms, 4),
-            "peak_source": peak_desc,
-            **({"same_size_copy_gbs": round(copy_gbs, 1)} if copy_gbs is not None else {}),
-        },
-        "e2e": {"value": round(e2e_value, 3), "unit": wl.unit,
-                "h2d_bytes_per_step": int(wl.copy_bytes()[0]), "d2h_bytes_per_step": int(wl.copy_bytes()[1]),
-                "ms_per_step": round(e2e_ms, 4),
-                "copies": "pinned host buffers; every step copies its inputs in and its results out: the used "
-                          "rows of each [rows, heads, d] tensor (gap rows are neither inputs nor results) and whole "
-                          "LSE-shaped tensors; two device buffer sets and two copy streams overlap step i+1's input "
-                          "copy and step i-1's result copy with step i"},
+        "roofline": roofline_of(wl, r, peaks, peak_src, recorded_traffic(args.workload, wl.kernel_key)),
+        "e2e": e2e_of(wl, r, world),
         "gpu_launches": args.steps * wl.launches_per_step,
-        "clocks": {**clocks.summary(), "window": clock_window},
+        "clocks": r["clocks"],
         "cpu_baseline": {"value": round(cpu_rate, 6), "unit": wl.unit, "cores": os.cpu_count(), "kind": "oracle",
                          "sample": cpu_desc},
     }
+    if configs:
+        line["configs"] = configs
     print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()

@@ -45,7 +45,7 @@ class WorkSummary(ctypes.Structure):
     _fields_ = [("num_work_items", ctypes.c_int32), ("num_key_blocks", ctypes.c_int32),
                 ("num_merge_units", ctypes.c_int32), ("num_bwd_items", ctypes.c_int32),
                 ("num_kv_units", ctypes.c_int32), ("backward_ok", ctypes.c_int32), ("used_flops", ctypes.c_double),
-                ("num_walk_entries", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("num_walk_entries", ctypes.c_int32), ("num_kv_segs", ctypes.c_int32)]
 
 
 _lib = None
@@ -81,7 +81,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.gva_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, vp, ctypes.c_size_t, f32, vp]
     lib.gva_plan_inspect.argtypes = [pi32, pi32, pi32, pi32, i32, pi32, pi32, pi32, ctypes.c_int64, i32, i32, i32,
                                      i32, i32, i32, ctypes.POINTER(WorkSummary), pi32, i32, pi32, i32, pi32, i32,
-                                     pi32, i32]
+                                     pi32, i32, pi32, i32]
     for name in ("gva_plan", "gva_forward", "gva_lse_merge", "gva_plan_destroy", "gva_plan_get_info",
                  "gva_device_status", "gva_forward_noalloc", "gva_plan_ranges", "gva_plan_causal",
                  "gva_backward_workspace_size", "gva_backward", "gva_plan_inspect"):
@@ -103,7 +103,8 @@ def _i32(a) -> np.ndarray:
 
 
 WORK_ITEM_FIELDS = ("q_row0", "q_rows", "blk0", "nblk", "head_kv", "n_tiles", "k_len", "q_pos0")
-KV_UNIT_FIELDS = ("key_row0", "keys", "q_row0", "q_used", "head_kv", "tile0", "key_pos0", "pos_shift")
+KV_UNIT_FIELDS = ("key_row0", "keys", "seg0", "n_tiles", "head_kv", "tile0", "key_pos0", "pos_shift")
+KV_SEG_FIELDS = ("q_row0", "q_used")
 
 
 def inspect_plan(cu_seqlens_q, seqused_q, cu_seqlens_k, seqused_k, num_heads_q: int, num_heads_kv: int,
@@ -114,7 +115,8 @@ def inspect_plan(cu_seqlens_q, seqused_q, cu_seqlens_k, seqused_k, num_heads_q: 
     ``cu_seqlens_k`` / ``seqused_k`` are not used. Returns the counts, ``backward_ok``,
     ``used_flops`` and three int32 arrays of 8 columns in the kernels' order: ``items``
     (forward, fields ``WORK_ITEM_FIELDS``), ``bwd_items`` (dQ, same fields) and
-    ``kv_units`` (dK / dV, ``KV_UNIT_FIELDS``), plus ``walk``, ``bwd_walk`` and
+    ``kv_units`` (dK / dV, ``KV_UNIT_FIELDS``), ``kv_segs`` (the segments the dK / dV
+    units list, 2 columns ``KV_SEG_FIELDS``), plus ``walk``, ``bwd_walk`` and
     ``kv_walk``: each list as a grid of min(``grid``, its length) CTAs walks it (per
     entry the index into the list, -1 for padding)."""
     lib = load_library()
@@ -133,27 +135,28 @@ def inspect_plan(cu_seqlens_q, seqused_q, cu_seqlens_k, seqused_k, num_heads_q: 
     summ = WorkSummary()
     args = [p(q[0]), p(q[1]), keys[0], keys[1], n, keys[2], keys[3], keys[4], keys[5], int(causal_block),
             int(num_heads_q), int(num_heads_kv), int(head_dim), int(grid)]
-    _check(lib, lib.gva_plan_inspect(*args, 0, ctypes.byref(summ), None, 0, None, 0, None, 0, None, 0),
+    _check(lib, lib.gva_plan_inspect(*args, 0, ctypes.byref(summ), None, 0, None, 0, None, 0, None, 0, None, 0),
            "gva_plan_inspect")
     items = np.zeros((max(summ.num_work_items, 1), 8), np.int32)
+    segs = np.zeros((max(summ.num_kv_segs, 1), 2), np.int32)
     bwd = np.zeros((max(summ.num_bwd_items, 1), 8), np.int32)
     kvu = np.zeros((max(summ.num_kv_units, 1), 8), np.int32)
     walks = []
     for kind in range(3):  # forward items, dQ items, dK / dV units
         s2 = WorkSummary()
-        _check(lib, lib.gva_plan_inspect(*args, kind, ctypes.byref(s2), None, 0, None, 0, None, 0, None, 0),
+        _check(lib, lib.gva_plan_inspect(*args, kind, ctypes.byref(s2), None, 0, None, 0, None, 0, None, 0, None, 0),
                "gva_plan_inspect")
         walk = np.zeros(max(s2.num_walk_entries, 1), np.int32)
         _check(lib, lib.gva_plan_inspect(*args, kind, ctypes.byref(s2), p(items), summ.num_work_items, p(walk),
                                          s2.num_walk_entries, p(bwd), summ.num_bwd_items, p(kvu),
-                                         summ.num_kv_units), "gva_plan_inspect")
+                                         summ.num_kv_units, p(segs), summ.num_kv_segs), "gva_plan_inspect")
         walks.append(walk[:s2.num_walk_entries])
     return {"num_work_items": summ.num_work_items, "num_key_blocks": summ.num_key_blocks,
             "num_merge_units": summ.num_merge_units, "num_bwd_items": summ.num_bwd_items,
             "num_kv_units": summ.num_kv_units, "backward_ok": bool(summ.backward_ok), "used_flops": summ.used_flops,
             "items": items[:summ.num_work_items], "walk": walks[0], "bwd_walk": walks[1], "kv_walk": walks[2],
             "bwd_items": bwd[:summ.num_bwd_items],
-            "kv_units": kvu[:summ.num_kv_units]}
+            "kv_units": kvu[:summ.num_kv_units], "kv_segs": segs[:summ.num_kv_segs]}
 
 
 class Plan:
@@ -361,9 +364,12 @@ def backward(plan: Plan, q, k, v, out, lse, d_out, dq, dk, dv, softmax_scale: fl
     return dq, dk, dv
 
 
-def device_status(plan: Plan):
-    """Synchronise and raise if a kernel of this plan recorded a device-side failure."""
-    _check(plan._lib, plan._lib.gva_device_status(plan.handle), "gva_device_status")
+def device_status(plan: Plan = None):
+    """Synchronise and raise if a kernel of this plan recorded a device-side failure;
+    without a plan, the same for the last ``forward_noalloc`` launch on the current
+    device (whose error word lives in the library's fixed scratch)."""
+    lib = plan._lib if plan is not None else load_library()
+    _check(lib, lib.gva_device_status(plan.handle if plan is not None else None), "gva_device_status")
 
 
 def forward_noalloc(cu_seqlens_q, seqused_q, cu_seqlens_k, seqused_k, num_heads_q: int, num_heads_kv: int,

@@ -6,6 +6,8 @@
 #include <cstdio>
 #include <cstring>
 #include <functional>
+#include <map>
+#include <mutex>
 #include <queue>
 #include <string>
 #include <utility>
@@ -15,6 +17,15 @@
 
 #include "gva.h"
 #include "gva_internal.h"
+
+// The tensor maps of the last call, keyed by the tensors' addresses: a plan is normally
+// called again and again on the same buffers, and encoding three or four maps costs
+// host time on every call of a short launch.
+struct MapCache {
+  const void* ptr[4] = {nullptr, nullptr, nullptr, nullptr};
+  CUtensorMap map[4];
+  bool valid = false;
+};
 
 struct gva_plan {
   int device = -1;
@@ -28,12 +39,14 @@ struct gva_plan {
   gva::KeyBlock* d_blocks = nullptr;
   gva::MergeUnit* d_units = nullptr;
   int* d_error = nullptr;
-  // backward work (plans from gva_plan only): one Q tile per dQ item, one key block of
-  // one KV head per dK / dV unit
-  bool backward_ok = false;
-  int32_t num_bwd_items = 0, num_kv_units = 0, bwd_grid = 0;
+  // backward work: one Q tile per dQ item; one piece of at most 128 K/V rows of one KV
+  // head per dK / dV unit, with the segments that attend it
+  int32_t num_bwd_items = 0, num_kv_units = 0, bwd_grid = 0, kv_grid = 0;
   gva::WorkItem* d_bwd_items = nullptr;
   gva::KvUnit* d_kv_units = nullptr;
+  gva::SegRef* d_kv_segs = nullptr;
+  std::mutex map_mutex;  // calls on one plan may come from several host threads
+  MapCache fwd_maps, bwd_maps;
 };
 
 namespace {
@@ -113,6 +126,7 @@ void free_plan(struct gva_plan* p) {
   if (p->d_error) cudaFree(p->d_error);
   if (p->d_bwd_items) cudaFree(p->d_bwd_items);
   if (p->d_kv_units) cudaFree(p->d_kv_units);
+  if (p->d_kv_segs) cudaFree(p->d_kv_segs);
   delete p;
 }
 
@@ -128,9 +142,7 @@ double item_cost(const gva::WorkItem& it) {
 // block), a dK / dV unit one key block over its Q tiles (four per tile); each also pays
 // a fixed cost of about two blocks or tiles.
 double dq_item_cost(const gva::WorkItem& it) { return 2.0 + it.nblk; }
-double kv_unit_cost(const gva::KvUnit& u, int32_t tokens_per_tile) {
-  return 2.0 + ((u.q_used + tokens_per_tile - 1) / tokens_per_tile - u.tile0);
-}
+double kv_unit_cost(const gva::KvUnit& u) { return 2.0 + u.n_tiles; }
 
 // A work list as the kernels walk it: CTA c reads entry item_index(r, c, grid) in round r.
 // Work (sorted longest first, with estimated costs `cost`) is assigned to CTAs longest
@@ -153,11 +165,19 @@ std::vector<int32_t> balanced_walk(const std::vector<double>& cost, int grid) {
     load[top.second] = top.first + cost[i];
     heap.push({load[top.second], top.second});
   }
+  // Each pass costs O(n log n) in the two lists' lengths: the best swap partner of an
+  // item of the most loaded CTA is found by binary search in the least loaded CTA's
+  // costs (the best exchange moves half the load gap).
+  std::vector<std::pair<double, int32_t>> lo_costs;
   for (int iter = 0; iter < 4 * grid + 1000; ++iter) {
     const int hi = static_cast<int>(std::max_element(load.begin(), load.end()) - load.begin());
     const int lo = static_cast<int>(std::min_element(load.begin(), load.end()) - load.begin());
+    const double gap = load[hi] - load[lo];
     double best = load[hi] - 1e-9;
     int bi = -1, bj = -1;  // bj < 0: move item bi of hi to lo; else swap it with item bj of lo
+    lo_costs.clear();
+    for (size_t b = 0; b < lists[lo].size(); ++b) lo_costs.push_back({cost[lists[lo][b]], static_cast<int32_t>(b)});
+    std::sort(lo_costs.begin(), lo_costs.end());
     for (size_t a = 0; a < lists[hi].size(); ++a) {
       const double ca = cost[lists[hi][a]];
       if (std::max(load[hi] - ca, load[lo] + ca) < best) {
@@ -165,16 +185,20 @@ std::vector<int32_t> balanced_walk(const std::vector<double>& cost, int grid) {
         bi = static_cast<int>(a);
         bj = -1;
       }
-      for (size_t b = 0; b < lists[lo].size(); ++b) {
-        const double d = ca - cost[lists[lo][b]];
+      // swap partners: costs just below and just above ca - gap / 2
+      const auto it = std::lower_bound(lo_costs.begin(), lo_costs.end(), std::make_pair(ca - 0.5 * gap, -1));
+      for (auto c = (it == lo_costs.begin() ? it : it - 1); c != lo_costs.end() && c <= it; ++c) {
+        const double d = ca - c->first;
         if (d > 0.0 && std::max(load[hi] - d, load[lo] + d) < best) {
           best = std::max(load[hi] - d, load[lo] + d);
           bi = static_cast<int>(a);
-          bj = static_cast<int>(b);
+          bj = c->second;
         }
       }
     }
-    if (bi < 0) break;
+    // stop when no exchange helps, or when the best one gains under 0.01 % of the
+    // largest load (long lists balance within that long before the pass limit)
+    if (bi < 0 || load[hi] - best < 1e-4 * load[hi]) break;
     const int32_t a = lists[hi][bi];
     lists[hi].erase(lists[hi].begin() + bi);
     double d = cost[a];
@@ -217,14 +241,14 @@ std::vector<T> balanced_layout(const std::vector<T>& sorted, int grid, Cost cost
 // keys are the ranges range_off[b] .. range_off[b+1] of (range_start, range_len).
 // causal_block > 0 (block-causal, one prefix range per segment): each item only gets the
 // key blocks its last row sees, and FLOPs count the visible keys of every row.
-// backward (every K/V row in at most one range, so each dK / dV row has one writer;
-// maskless, block-causal or ranges): also build the dQ items and the dK / dV units.
+// backward: also build the dQ items and the dK / dV units (every plan kind).
 struct HostWork {
   std::vector<gva::KeyBlock> blocks;
   std::vector<gva::WorkItem> items;  // forward, sorted longest first
   std::vector<gva::MergeUnit> units;
   std::vector<gva::WorkItem> bwd_items;
   std::vector<gva::KvUnit> kv_units;
+  std::vector<gva::SegRef> kv_segs;
   double flops = 0.0;
 };
 
@@ -306,7 +330,6 @@ gva_status build_work(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
     for (int32_t b = 0; b < num_segments; ++b) {
       const int32_t uq = seqused_q[b];
       const int32_t pos_shift = seg_keys[b] - uq;  // block-causal: key position of row 0
-      const int32_t n_q_tiles = (uq + tokens_per_tile - 1) / tokens_per_tile;
       for (int32_t hk = 0; hk < num_heads_kv; ++hk) {
         for (int32_t t0 = 0; t0 < uq; t0 += tokens_per_tile) {
           gva::WorkItem it{};
@@ -324,27 +347,87 @@ gva_status build_work(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
           }
           bwd_items.push_back(it);
         }
-        for (int32_t j = 0; j < seg_nblk[b]; ++j) {
-          const gva::KeyBlock& kb = blocks[seg_blk0[b] + j];
-          gva::KvUnit u{kb.row0, kb.valid, cu_seqlens_q[b], uq, hk, 0, j * gva::kBlockKeys, pos_shift};
-          if (causal_block > 0) {
-            // rows at key positions >= the start of the frame holding the block's first
-            // key see it; tiles before the first such row never do
-            const int64_t pos_min = (static_cast<int64_t>(u.key_pos0) / causal_block) * causal_block;
-            const int64_t row_min = std::max<int64_t>(0, pos_min - pos_shift);
-            u.tile0 = static_cast<int32_t>(std::min<int64_t>(row_min / tokens_per_tile, n_q_tiles));
-          }
-          kv_units.push_back(u);
-        }
       }
     }
     std::stable_sort(bwd_items.begin(), bwd_items.end(),
                      [](const gva::WorkItem& a, const gva::WorkItem& c) { return a.nblk > c.nblk; });
-    auto unit_tiles = [&](const gva::KvUnit& u) {
-      return (u.q_used + tokens_per_tile - 1) / tokens_per_tile - u.tile0;
+
+    // dK / dV units: pieces of at most kBlockKeys K/V rows, each with the segments that
+    // attend them (SegRef runs shared by every KV head), so every K/V row has one unit
+    // per KV head and a single writer.
+    std::vector<gva::SegRef>& segs = w.kv_segs;
+    struct Piece {
+      int32_t row0, keys, seg0, n_tiles, tile0, key_pos0, pos_shift;
     };
+    std::vector<Piece> pieces;
+    auto tiles_of = [&](int32_t rows) { return (rows + tokens_per_tile - 1) / tokens_per_tile; };
+    if (causal_block > 0) {
+      // one prefix range per segment: its key blocks, each attended by that segment only,
+      // from the first Q tile whose rows see the block's first key
+      for (int32_t b = 0; b < num_segments; ++b) {
+        const int32_t uq = seqused_q[b];
+        const int32_t pos_shift = seg_keys[b] - uq;
+        const int32_t seg0 = static_cast<int32_t>(segs.size());
+        if (uq > 0) segs.push_back({cu_seqlens_q[b], uq});
+        for (int32_t j = 0; j < seg_nblk[b]; ++j) {
+          const gva::KeyBlock& kb = blocks[seg_blk0[b] + j];
+          Piece pc{kb.row0, kb.valid, seg0, 0, 0, j * gva::kBlockKeys, pos_shift};
+          if (uq > 0) {
+            // rows at key positions >= the start of the frame holding the block's first
+            // key see it; tiles before the first such row never do
+            const int64_t pos_min = (static_cast<int64_t>(pc.key_pos0) / causal_block) * causal_block;
+            const int64_t row_min = std::max<int64_t>(0, pos_min - pos_shift);
+            pc.tile0 = static_cast<int32_t>(std::min<int64_t>(row_min / tokens_per_tile, tiles_of(uq)));
+            pc.n_tiles = tiles_of(uq) - pc.tile0;
+          }
+          pieces.push_back(pc);
+        }
+      }
+    } else {
+      // The union of every segment's key ranges, cut wherever a range starts or ends:
+      // within a piece the attending segments do not change. A segment with several
+      // ranges over the same rows attends them that many times and is listed so.
+      struct Edge {
+        int64_t x;
+        int32_t seg, delta;
+      };
+      std::vector<Edge> edges;
+      for (int32_t b = 0; b < num_segments; ++b)
+        for (int32_t r = range_off[b]; r < range_off[b + 1]; ++r)
+          if (range_len[r] > 0) {
+            edges.push_back({range_start[r], b, +1});
+            edges.push_back({static_cast<int64_t>(range_start[r]) + range_len[r], b, -1});
+          }
+      std::sort(edges.begin(), edges.end(), [](const Edge& a, const Edge& c) { return a.x < c.x; });
+      std::map<int32_t, int32_t> active;  // segment -> ranges of it covering the piece
+      for (size_t e = 0; e < edges.size();) {
+        const int64_t x = edges[e].x;
+        for (; e < edges.size() && edges[e].x == x; ++e) {
+          const int32_t m = (active[edges[e].seg] += edges[e].delta);
+          if (m == 0) active.erase(edges[e].seg);
+        }
+        if (active.empty() || e == edges.size()) continue;
+        const int64_t x1 = edges[e].x;  // the piece is rows [x, x1)
+        const int32_t seg0 = static_cast<int32_t>(segs.size());
+        int32_t n_tiles = 0;
+        for (const auto& am : active) {
+          const int32_t uq = seqused_q[am.first];
+          if (uq == 0) continue;  // no rows: contributes nothing
+          for (int32_t c = 0; c < am.second; ++c) {
+            segs.push_back({cu_seqlens_q[am.first], uq});
+            n_tiles += tiles_of(uq);
+          }
+        }
+        for (int64_t o = x; o < x1; o += gva::kBlockKeys)
+          pieces.push_back({static_cast<int32_t>(o), static_cast<int32_t>(std::min<int64_t>(gva::kBlockKeys, x1 - o)),
+                            seg0, n_tiles, 0, 0, 0});
+      }
+    }
+    for (int32_t hk = 0; hk < num_heads_kv; ++hk)
+      for (const Piece& pc : pieces)
+        kv_units.push_back({pc.row0, pc.keys, pc.seg0, pc.n_tiles, hk, pc.tile0, pc.key_pos0, pc.pos_shift});
     std::stable_sort(kv_units.begin(), kv_units.end(),
-                     [&](const gva::KvUnit& a, const gva::KvUnit& c) { return unit_tiles(a) > unit_tiles(c); });
+                     [](const gva::KvUnit& a, const gva::KvUnit& c) { return a.n_tiles > c.n_tiles; });
   }
   return GVA_OK;
 }
@@ -363,6 +446,7 @@ gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
   const std::vector<gva::MergeUnit>& units = w.units;
   const std::vector<gva::WorkItem>& bwd_items = w.bwd_items;
   const std::vector<gva::KvUnit>& kv_units = w.kv_units;
+  const std::vector<gva::SegRef>& kv_segs = w.kv_segs;
   const double flops = w.flops;
 
   // ---- device
@@ -422,15 +506,11 @@ gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
       return cuda_fail(e, "uploading the merge units");
     }
   }
-  p->backward_ok = backward;
+  // Both backward lists balanced like the forward's, each for the grid its launch takes.
   p->bwd_grid = std::min(static_cast<int32_t>(bwd_items.size()), sms);
-  // Both backward lists balanced like the forward's. The dK / dV launch takes
-  // min(entries, SMs) CTAs: the same grid as below.
+  p->kv_grid = std::min(static_cast<int32_t>(kv_units.size()), sms);
   const std::vector<gva::WorkItem> bwd_laid = balanced_layout(bwd_items, p->bwd_grid, dq_item_cost);
-  const int32_t tpt = gva::kTileRows / group;
-  const std::vector<gva::KvUnit> kv_laid =
-      balanced_layout(kv_units, std::min(static_cast<int32_t>(kv_units.size()), sms),
-                      [tpt](const gva::KvUnit& u) { return kv_unit_cost(u, tpt); });
+  const std::vector<gva::KvUnit> kv_laid = balanced_layout(kv_units, p->kv_grid, kv_unit_cost);
   p->num_bwd_items = static_cast<int32_t>(bwd_laid.size());
   p->num_kv_units = static_cast<int32_t>(kv_laid.size());
   if (!bwd_laid.empty()) {
@@ -449,6 +529,14 @@ gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
       return cuda_fail(e, "uploading the dK / dV units");
     }
   }
+  if (!kv_segs.empty()) {
+    if ((e = cudaMalloc(&p->d_kv_segs, kv_segs.size() * sizeof(gva::SegRef))) != cudaSuccess ||
+        (e = cudaMemcpy(p->d_kv_segs, kv_segs.data(), kv_segs.size() * sizeof(gva::SegRef),
+                        cudaMemcpyHostToDevice)) != cudaSuccess) {
+      free_plan(p);
+      return cuda_fail(e, "uploading the dK / dV units' segments");
+    }
+  }
   *out_plan = p;
   return ok();
 }
@@ -464,8 +552,9 @@ gva_status validate_common(const int32_t* cu_seqlens_q, const int32_t* seqused_q
   if (num_heads_q % num_heads_kv != 0)
     return fail(GVA_ERR_INVALID_ARG, "num_heads_q=%d is not divisible by num_heads_kv=%d", num_heads_q, num_heads_kv);
   const int32_t group = num_heads_q / num_heads_kv;
-  if (gva::kTileRows % group != 0)
-    return fail(GVA_ERR_UNSUPPORTED, "query heads per KV head (%d) must divide %d", group, gva::kTileRows);
+  // A Q tile folds floor(128 / group) tokens of the group's heads into its 128 rows.
+  if (group > gva::kTileRows)
+    return fail(GVA_ERR_UNSUPPORTED, "query heads per KV head (%d) must be at most %d", group, gva::kTileRows);
   if (head_dim != 64 && head_dim != 128)
     return fail(GVA_ERR_UNSUPPORTED, "head_dim=%d is not supported (64 or 128)", head_dim);
   if (num_heads_q > 256) return fail(GVA_ERR_UNSUPPORTED, "num_heads_q=%d is too large (at most 256)", num_heads_q);
@@ -473,9 +562,9 @@ gva_status validate_common(const int32_t* cu_seqlens_q, const int32_t* seqused_q
 }
 
 // Key ranges of gva_plan_ranges: offsets start at 0 and do not decrease, every range lies
-// in [0, total_k). *disjoint tells whether the non-empty ranges are pairwise disjoint.
+// in [0, total_k). Ranges may overlap, within a segment or across segments.
 gva_status validate_ranges(int32_t num_segments, const int32_t* key_range_offsets, const int32_t* key_range_starts,
-                           const int32_t* key_range_lengths, int64_t total_k, bool* disjoint_out) {
+                           const int32_t* key_range_lengths, int64_t total_k) {
   if (key_range_offsets == nullptr) return fail(GVA_ERR_INVALID_ARG, "key_range_offsets is NULL");
   if (total_k < 0 || total_k > INT32_MAX) return fail(GVA_ERR_INVALID_ARG, "total_k=%lld is out of range", (long long)total_k);
   if (key_range_offsets[0] != 0) return fail(GVA_ERR_INVALID_ARG, "key_range_offsets[0] must be 0");
@@ -491,16 +580,6 @@ gva_status validate_ranges(int32_t num_segments, const int32_t* key_range_offset
       return fail(GVA_ERR_INVALID_ARG, "key range %d = [%lld, %lld) is outside [0, total_k=%lld)", r, (long long)st,
                   (long long)(st + n), (long long)total_k);
   }
-  // The backward needs every K/V row to belong to at most one range (a shared row would
-  // need its dK / dV summed across units): check that the non-empty ranges are disjoint.
-  std::vector<std::pair<int32_t, int32_t>> spans;
-  for (int32_t r = 0; r < num_ranges; ++r)
-    if (key_range_lengths[r] > 0) spans.push_back({key_range_starts[r], key_range_lengths[r]});
-  std::sort(spans.begin(), spans.end());
-  bool disjoint = true;
-  for (size_t i = 1; i < spans.size(); ++i)
-    if (static_cast<int64_t>(spans[i - 1].first) + spans[i - 1].second > spans[i].first) disjoint = false;
-  *disjoint_out = disjoint;
   return GVA_OK;
 }
 }  // namespace
@@ -565,11 +644,10 @@ gva_status gva_plan_ranges(const int32_t* cu_seqlens_q, const int32_t* seqused_q
   *out_plan = nullptr;
   gva_status s = validate_common(cu_seqlens_q, seqused_q, num_segments, num_heads_q, num_heads_kv, head_dim);
   if (s != GVA_OK) return s;
-  bool disjoint = false;
-  s = validate_ranges(num_segments, key_range_offsets, key_range_starts, key_range_lengths, total_k, &disjoint);
+  s = validate_ranges(num_segments, key_range_offsets, key_range_starts, key_range_lengths, total_k);
   if (s != GVA_OK) return s;
   return build_plan(cu_seqlens_q, seqused_q, num_segments, key_range_offsets, key_range_starts, key_range_lengths,
-                    total_k, num_heads_q, num_heads_kv, head_dim, 0, disjoint, out_plan);
+                    total_k, num_heads_q, num_heads_kv, head_dim, 0, true, out_plan);
 }
 
 gva_status gva_plan_inspect(const int32_t* cu_seqlens_q, const int32_t* seqused_q, const int32_t* cu_seqlens_k,
@@ -578,7 +656,8 @@ gva_status gva_plan_inspect(const int32_t* cu_seqlens_q, const int32_t* seqused_
                             int32_t causal_block, int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim,
                             int32_t grid, int32_t walk_list, gva_work_summary* summary, int32_t* items,
                             int32_t items_capacity, int32_t* walk, int32_t walk_capacity, int32_t* bwd_items,
-                            int32_t bwd_items_capacity, int32_t* kv_units, int32_t kv_units_capacity) {
+                            int32_t bwd_items_capacity, int32_t* kv_units, int32_t kv_units_capacity,
+                            int32_t* kv_segs, int32_t kv_segs_capacity) {
   if (summary == nullptr) return fail(GVA_ERR_INVALID_ARG, "summary is NULL");
   if (causal_block < 0) return fail(GVA_ERR_INVALID_ARG, "causal_block=%d must be >= 0", causal_block);
   if (grid < 1) return fail(GVA_ERR_INVALID_ARG, "grid=%d must be >= 1", grid);
@@ -586,10 +665,9 @@ gva_status gva_plan_inspect(const int32_t* cu_seqlens_q, const int32_t* seqused_
   gva_status s = validate_common(cu_seqlens_q, seqused_q, num_segments, num_heads_q, num_heads_kv, head_dim);
   if (s != GVA_OK) return s;
   std::vector<int32_t> off, start, len;
-  bool backward_ok = true;
   if (key_range_offsets != nullptr) {  // as gva_plan_ranges
     if (causal_block > 0) return fail(GVA_ERR_INVALID_ARG, "block-causal plans take prefix keys, not ranges");
-    s = validate_ranges(num_segments, key_range_offsets, key_range_starts, key_range_lengths, total_k, &backward_ok);
+    s = validate_ranges(num_segments, key_range_offsets, key_range_starts, key_range_lengths, total_k);
     if (s != GVA_OK) return s;
     const int32_t n = key_range_offsets[num_segments];
     off.assign(key_range_offsets, key_range_offsets + num_segments + 1);
@@ -611,9 +689,9 @@ gva_status gva_plan_inspect(const int32_t* cu_seqlens_q, const int32_t* seqused_
   }
   HostWork w;
   s = build_work(cu_seqlens_q, seqused_q, num_segments, off.data(), start.data(), len.data(), num_heads_q,
-                 num_heads_kv, head_dim, causal_block, backward_ok, w);
+                 num_heads_kv, head_dim, causal_block, true, w);
   if (s != GVA_OK) return s;
-  summary->backward_ok = backward_ok ? 1 : 0;
+  summary->backward_ok = 1;
   // the chosen list as a grid of min(grid, its length) CTAs walks it
   std::vector<double> cost;
   if (walk_list == 0) {
@@ -621,8 +699,7 @@ gva_status gva_plan_inspect(const int32_t* cu_seqlens_q, const int32_t* seqused_
   } else if (walk_list == 1) {
     for (const auto& it : w.bwd_items) cost.push_back(dq_item_cost(it));
   } else {
-    const int32_t tpt = gva::kTileRows / (num_heads_q / num_heads_kv);
-    for (const auto& u : w.kv_units) cost.push_back(kv_unit_cost(u, tpt));
+    for (const auto& u : w.kv_units) cost.push_back(kv_unit_cost(u));
   }
   const std::vector<int32_t> laid = balanced_walk(cost, std::min<int32_t>(grid, static_cast<int32_t>(cost.size())));
   summary->num_walk_entries = static_cast<int32_t>(laid.size());
@@ -633,6 +710,7 @@ gva_status gva_plan_inspect(const int32_t* cu_seqlens_q, const int32_t* seqused_
   summary->num_merge_units = static_cast<int32_t>(w.units.size());
   summary->num_bwd_items = static_cast<int32_t>(w.bwd_items.size());
   summary->num_kv_units = static_cast<int32_t>(w.kv_units.size());
+  summary->num_kv_segs = static_cast<int32_t>(w.kv_segs.size());
   summary->used_flops = w.flops;
   static_assert(sizeof(gva::WorkItem) == 8 * sizeof(int32_t) && sizeof(gva::KvUnit) == 8 * sizeof(int32_t),
                 "8 int32 per exported record");
@@ -642,6 +720,9 @@ gva_status gva_plan_inspect(const int32_t* cu_seqlens_q, const int32_t* seqused_
   copy_out(items, items_capacity, w.items.data(), w.items.size());
   copy_out(bwd_items, bwd_items_capacity, w.bwd_items.data(), w.bwd_items.size());
   copy_out(kv_units, kv_units_capacity, w.kv_units.data(), w.kv_units.size());
+  static_assert(sizeof(gva::SegRef) == 2 * sizeof(int32_t), "2 int32 per exported segment");
+  if (kv_segs != nullptr && kv_segs_capacity > 0)
+    std::memcpy(kv_segs, w.kv_segs.data(), std::min<size_t>(w.kv_segs.size(), kv_segs_capacity) * sizeof(gva::SegRef));
   return ok();
 }
 
@@ -666,12 +747,29 @@ gva_status gva_forward(gva_plan_t plan, const void* q, const void* k, const void
     return fail(GVA_ERR_INVALID_ARG, "the plan was built on device %d, the current device is %d", plan->device, dev);
   const int32_t tokens_per_tile = gva::kTileRows / plan->group;
   CUtensorMap mq, mk, mv;
-  gva_status s;
-  const int64_t krows = has_keys ? plan->total_k : 1;
-  if ((s = make_map(&mq, q, plan->total_q, plan->num_heads_q, plan->head_dim, tokens_per_tile, plan->group, "Q")) != GVA_OK)
-    return s;
-  if ((s = make_map(&mk, k, krows, plan->num_heads_kv, plan->head_dim, gva::kBlockKeys, 1, "K")) != GVA_OK) return s;
-  if ((s = make_map(&mv, v, krows, plan->num_heads_kv, plan->head_dim, gva::kBlockKeys, 1, "V")) != GVA_OK) return s;
+  {
+    std::lock_guard<std::mutex> lock(plan->map_mutex);
+    MapCache& c = plan->fwd_maps;
+    if (!(c.valid && c.ptr[0] == q && c.ptr[1] == k && c.ptr[2] == v)) {
+      c.valid = false;
+      gva_status s;
+      const int64_t krows = has_keys ? plan->total_k : 1;
+      if ((s = make_map(&c.map[0], q, plan->total_q, plan->num_heads_q, plan->head_dim, tokens_per_tile, plan->group,
+                        "Q")) != GVA_OK)
+        return s;
+      if ((s = make_map(&c.map[1], k, krows, plan->num_heads_kv, plan->head_dim, gva::kBlockKeys, 1, "K")) != GVA_OK)
+        return s;
+      if ((s = make_map(&c.map[2], v, krows, plan->num_heads_kv, plan->head_dim, gva::kBlockKeys, 1, "V")) != GVA_OK)
+        return s;
+      c.ptr[0] = q;
+      c.ptr[1] = k;
+      c.ptr[2] = v;
+      c.valid = true;
+    }
+    mq = c.map[0];
+    mk = c.map[1];
+    mv = c.map[2];
+  }
   const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(plan->head_dim));
   gva::FwdParams prm{};
   prm.items = plan->d_items;
@@ -737,8 +835,6 @@ gva_status gva_lse_merge(gva_plan_t plan, int32_t num_parts, const void* const* 
 
 gva_status gva_backward_workspace_size(gva_plan_t plan, size_t* bytes) {
   if (plan == nullptr || bytes == nullptr) return fail(GVA_ERR_INVALID_ARG, "plan or bytes is NULL");
-  if (!plan->backward_ok)
-    return fail(GVA_ERR_UNSUPPORTED, "the backward needs each K/V row in at most one key range of the plan");
   *bytes = static_cast<size_t>(plan->num_heads_q) * static_cast<size_t>(plan->total_q) * sizeof(float);
   return ok();
 }
@@ -748,8 +844,6 @@ gva_status gva_backward(gva_plan_t plan, const void* q, const void* k, const voi
                         gva_dtype dkv_dtype, void* workspace, size_t workspace_bytes, float softmax_scale,
                         cudaStream_t stream) {
   if (plan == nullptr) return fail(GVA_ERR_INVALID_ARG, "plan is NULL");
-  if (!plan->backward_ok)
-    return fail(GVA_ERR_UNSUPPORTED, "the backward needs each K/V row in at most one key range of the plan");
   if ((dq_dtype != GVA_BF16 && dq_dtype != GVA_FP32) || (dkv_dtype != GVA_BF16 && dkv_dtype != GVA_FP32))
     return fail(GVA_ERR_INVALID_ARG, "bad gradient dtype");
   if (plan->num_bwd_items == 0 && plan->num_kv_units == 0) return ok();  // no used row and no used key
@@ -782,20 +876,40 @@ gva_status gva_backward(gva_plan_t plan, const void* q, const void* k, const voi
   const int64_t qrows = has_rows ? plan->total_q : 1;  // the maps need one row
   const int64_t krows = has_keys ? plan->total_k : 1;
   CUtensorMap mq, mk, mv, mdo;
-  gva_status s;
-  if ((s = make_map(&mq, q, qrows, plan->num_heads_q, plan->head_dim, tokens_per_tile, plan->group, "Q")) != GVA_OK)
-    return s;
-  if ((s = make_map(&mdo, d_out, qrows, plan->num_heads_q, plan->head_dim, tokens_per_tile,
-                    plan->group, "dO")) != GVA_OK)
-    return s;
-  if ((s = make_map(&mk, k, krows, plan->num_heads_kv, plan->head_dim, gva::kBlockKeys, 1, "K")) != GVA_OK) return s;
-  if ((s = make_map(&mv, v, krows, plan->num_heads_kv, plan->head_dim, gva::kBlockKeys, 1, "V")) != GVA_OK) return s;
+  {
+    std::lock_guard<std::mutex> lock(plan->map_mutex);
+    MapCache& c = plan->bwd_maps;
+    if (!(c.valid && c.ptr[0] == q && c.ptr[1] == k && c.ptr[2] == v && c.ptr[3] == d_out)) {
+      c.valid = false;
+      gva_status s;
+      if ((s = make_map(&c.map[0], q, qrows, plan->num_heads_q, plan->head_dim, tokens_per_tile, plan->group,
+                        "Q")) != GVA_OK)
+        return s;
+      if ((s = make_map(&c.map[1], k, krows, plan->num_heads_kv, plan->head_dim, gva::kBlockKeys, 1, "K")) != GVA_OK)
+        return s;
+      if ((s = make_map(&c.map[2], v, krows, plan->num_heads_kv, plan->head_dim, gva::kBlockKeys, 1, "V")) != GVA_OK)
+        return s;
+      if ((s = make_map(&c.map[3], d_out, qrows, plan->num_heads_q, plan->head_dim, tokens_per_tile, plan->group,
+                        "dO")) != GVA_OK)
+        return s;
+      c.ptr[0] = q;
+      c.ptr[1] = k;
+      c.ptr[2] = v;
+      c.ptr[3] = d_out;
+      c.valid = true;
+    }
+    mq = c.map[0];
+    mk = c.map[1];
+    mv = c.map[2];
+    mdo = c.map[3];
+  }
   const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(plan->head_dim));
   gva::BwdParams prm{};
   prm.items = plan->d_bwd_items;
   prm.blocks = plan->d_blocks;
   prm.num_items = plan->num_bwd_items;
   prm.kv_units = plan->d_kv_units;
+  prm.kv_segs = plan->d_kv_segs;
   prm.num_kv_units = plan->num_kv_units;
   prm.lse = lse;
   prm.dvec = static_cast<float*>(workspace);
@@ -813,7 +927,7 @@ gva_status gva_backward(gva_plan_t plan, const void* q, const void* k, const voi
   prm.error_flag = plan->d_error;
   e = gva::launch_backward(plan->head_dim, dq_dtype == GVA_FP32, dkv_dtype == GVA_FP32, prm, plan->d_units,
                            plan->num_units, out, d_out, static_cast<float*>(workspace), mq, mk, mv, mdo,
-                           plan->bwd_grid, stream);
+                           plan->bwd_grid, plan->kv_grid, plan->sm_count, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launching the backward kernels");
   return ok();
 }
@@ -840,7 +954,7 @@ gva_status gva_plan_get_info(gva_plan_t plan, gva_plan_info* info) {
 }
 
 gva_status gva_device_status(gva_plan_t plan) {
-  if (plan == nullptr) return fail(GVA_ERR_INVALID_ARG, "plan is NULL");
+  if (plan == nullptr) return static_cast<gva_status>(gva::noalloc_device_status());
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
   int word = 0;

@@ -63,14 +63,49 @@ __device__ __forceinline__ void zero_tile_row(uint8_t* tile, int row) {
   }
 }
 
+// Zero rows [filled, 128) of `n` 128-row tiles spaced `stride` bytes apart, with all
+// `nthreads` threads of the block. A folded Q / dO tile fills T * G rows (T =
+// floor(128 / G) tokens of G heads); when G does not divide 128 the copies never write
+// the remaining rows, which would otherwise meet zero weights (0 * NaN) in the MMAs.
+template <int D>
+__device__ __forceinline__ void zero_tile_tails(uint8_t* tile0, int stride, int n, int filled, int nthreads) {
+  const int pad = kTileRows - filled;
+  for (int x = threadIdx.x; x < n * pad * (D / 64) * 8; x += nthreads) {
+    const int piece = x % 8, rest = x / 8;
+    const int ch = rest % (D / 64), rest2 = rest / (D / 64);
+    const int r = filled + rest2 % pad, t = rest2 / pad;
+    *reinterpret_cast<uint4*>(tile0 + t * stride + ch * kChunkBytes + r * 128 + piece * 16) = make_uint4(0, 0, 0, 0);
+  }
+}
+
 __device__ __forceinline__ KvUnit load_unit(const KvUnit* units, int idx) {
   const int4* p = reinterpret_cast<const int4*>(units + idx);
   const int4 a = __ldg(p), b = __ldg(p + 1);
   KvUnit u;
-  u.key_row0 = a.x; u.keys = a.y; u.q_row0 = a.z; u.q_used = a.w;
+  u.key_row0 = a.x; u.keys = a.y; u.seg0 = a.z; u.n_tiles = a.w;
   u.head_kv = b.x; u.tile0 = b.y; u.key_pos0 = b.z; u.pos_shift = b.w;
   return u;
 }
+
+// The Q tiles of a dK / dV unit, in order: tiles tile0 .. of its first segment, then
+// every tile of each further segment. `next` must only be called while tiles remain.
+struct TileWalk {
+  const int2* segs;
+  int s, k;   // current SegRef and tile within its segment
+  int2 seg;   // (first token row, used rows) of that segment
+  __device__ __forceinline__ void start(const SegRef* list, const KvUnit& u) {
+    segs = reinterpret_cast<const int2*>(list);
+    s = u.seg0;
+    k = u.tile0;
+    seg = __ldg(segs + s);
+  }
+  __device__ __forceinline__ void next(int T) {
+    if (++k * T >= seg.y) {
+      k = 0;
+      seg = __ldg(segs + (++s));
+    }
+  }
+};
 
 // dK / dV kernel control block.
 struct BwdCtrl {
@@ -226,12 +261,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tmem_alloc(&ctrl.tmem_base, kBwdTmemCols);
     tmem_relinquish_alloc_permit();
   }
+  const int T = p.tokens_per_tile;
+  const int G = p.group;
+  zero_tile_tails<D>(sQ, C::kTileBytes, 2, T * G, kBwdThreads);  // the Q and dO tiles
+  fence_proxy_async_smem();
   tcgen05_fence_before();
   __syncthreads();
   tcgen05_fence_after();
   const uint32_t tmem = ctrl.tmem_base;
-  const int T = p.tokens_per_tile;
-  const int G = p.group;
+  const uint32_t q_tile_bytes = static_cast<uint32_t>(T * G) * D * 2;  // bytes one folded tile's copies bring
   // TMEM: two S buffers [0,128) and [128,256) (block m uses buffer m & 1), dP
   // [256,384), dQ [384,384+D). The dS of key half h (bf16 pairs) overwrites columns
   // [64h, 64h+32) of its block's S buffer. With S double-buffered, the products of
@@ -260,7 +298,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (leader) ok = wait_bar(&ctrl.a_empty, (q_it & 1) ^ 1, abort_flag, p.error_flag);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       if (leader) {
-        mbar_arrive_expect_tx(&ctrl.a_full, 2 * C::kTileBytes);
+        mbar_arrive_expect_tx(&ctrl.a_full, 2 * q_tile_bytes);
 #pragma unroll
         for (int ch = 0; ch < C::kChunks; ++ch) {
           tma_load_3d(sQ + ch * kChunkBytes, &map_q, &ctrl.a_full, ch * 64, it.q_row0, it.head_kv * G);
@@ -397,7 +435,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int idx = item_index(round, blockIdx.x, gridDim.x);
       if (idx >= p.num_items) break;
       const WorkItem it = load_item(p.items, idx);
-      const bool valid = tok < it.q_rows;
+      const bool valid = hl < G && tok < it.q_rows;
       const int64_t token = static_cast<int64_t>(it.q_row0) + tok;
       const int head = it.head_kv * G + hl;
       TOut* qrow = dq + (token * p.num_heads_q + head) * D + (D / 2) * wg;
@@ -505,20 +543,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tmem_alloc(&ctrl.tmem_base, kBwdTmemCols);
     tmem_relinquish_alloc_permit();
   }
+  const int T = p.tokens_per_tile;
+  const int G = p.group;
+  zero_tile_tails<D>(sSlots, C::kTileBytes, 4, T * G, kBwdThreads);  // both slots' Q and dO tiles
+  fence_proxy_async_smem();
   tcgen05_fence_before();
   __syncthreads();
   tcgen05_fence_after();
   const uint32_t tmem = ctrl.tmem_base;
-  const int T = p.tokens_per_tile;
-  const int G = p.group;
+  const uint32_t q_tile_bytes = static_cast<uint32_t>(T * G) * D * 2;  // bytes one folded tile's copies bring
   // TMEM: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [384,384+D). Column half h
   // (Q-tile rows 64h .. 64h+63) of S^T / dP^T is [64h, +64) / [128+64h, +64); its P^T
   // (bf16 pairs) overwrites [64h, +32) and its dS^T [128+64h, +32). P^T is ready before
   // dS^T, so dV += P^T dO runs while the compute threads still form dS^T; the next S^T
   // follows the dV products and the next dP^T the dK products.
   constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
-  // Q tiles of the unit: from the first one that sees the block (block-causal) to the end
-  auto n_tiles = [&](const KvUnit& u) { return (u.q_used + T - 1) / T - u.tile0; };
 
   if (warp == 0) {
     // As in the dQ kernel: lane 0 copies, the warp clears rows past the used keys of a
@@ -536,7 +575,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int idx = item_index(round, blockIdx.x, gridDim.x);
       if (idx >= p.num_kv_units) break;
       const KvUnit u = load_unit(p.kv_units, idx);
-      const int nqt = n_tiles(u);
+      const int nqt = u.n_tiles;
       if (nqt == 0) continue;
       if (leader) ok = wait_bar(&ctrl.a_empty, (kv_it & 1) ^ 1, abort_flag, p.error_flag);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
@@ -565,18 +604,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       ++kv_it;
+      TileWalk tw;
+      tw.start(p.kv_segs, u);
       for (int i = 0; i < nqt && ok; ++i) {
+        if (i > 0) tw.next(T);
         const uint32_t sl = ld & 1;
         if (leader) ok = wait_bar(&ctrl.r_empty[sl], ((ld >> 1) & 1) ^ 1, abort_flag, p.error_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         uint8_t* tq = sSlots + sl * 2 * C::kTileBytes;
         uint8_t* tdo = tq + C::kTileBytes;
-        const int t0 = u.q_row0 + (u.tile0 + i) * T;
-        const int vt = min(T, u.q_used - (u.tile0 + i) * T);  // used tokens of this tile
+        const int t0 = tw.seg.x + tw.k * T;
+        const int vt = min(T, tw.seg.y - tw.k * T);  // used tokens of this tile
         uint64_t* bar = vt == T ? &ctrl.r_full[sl] : &ctrl.zero_bar;
         if (leader) {
-          mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
+          mbar_arrive_expect_tx(bar, 2 * q_tile_bytes);
 #pragma unroll
           for (int ch = 0; ch < C::kChunks; ++ch) {
             tma_load_3d(tq + ch * kChunkBytes, &map_q, bar, ch * 64, t0, u.head_kv * G);
@@ -636,7 +678,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int idx = item_index(round, blockIdx.x, gridDim.x);
         if (idx >= p.num_kv_units) break;
         const KvUnit u = load_unit(p.kv_units, idx);
-        const int nqt = n_tiles(u);
+        const int nqt = u.n_tiles;
         if (nqt == 0) continue;
         ok = wait_bar(&ctrl.a_full, kv_it & 1, abort_flag, p.error_flag);
         if (ok) ok = wait_tile(qi);
@@ -706,7 +748,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int idx = item_index(round, blockIdx.x, gridDim.x);
       if (idx >= p.num_kv_units) break;
       const KvUnit u = load_unit(p.kv_units, idx);
-      const int nqt = n_tiles(u);
+      const int nqt = u.n_tiles;
       const bool key_valid = key < u.keys;
       const int64_t krow = static_cast<int64_t>(u.key_row0) + key;
       TOut* dkrow = dk + (krow * p.num_heads_kv + u.head_kv) * D + (D / 2) * wg;
@@ -720,22 +762,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       // log2-LSE and D of this half's Q-tile rows (loader threads tid < 64), fetched one
       // tile ahead; +inf LSE (P = 0) and D = 0 past the used rows
-      const int64_t lrow0 = static_cast<int64_t>(u.head_kv * G + rhl) * p.total_q + u.q_row0 + rtok;
-      auto fetch = [&](int i, float& xl_v, float& xd_v, int& lim_v) {
-        const int r = (u.tile0 + i) * T + rtok;  // row within the segment
-        const bool rvalid = r < u.q_used;
+      const int64_t lhead = static_cast<int64_t>(u.head_kv * G + rhl) * p.total_q;
+      TileWalk fw;  // the tile the next fetch reads
+      if (tid < 64 && nqt > 0) fw.start(p.kv_segs, u);
+      auto fetch = [&](float& xl_v, float& xd_v, int& lim_v) {
+        const int r = fw.k * T + rtok;  // row within the segment
+        const bool rvalid = rhl < G && r < fw.seg.y;  // (rows past T * G fold no head)
         lim_v = 0x7fffffff;
         if constexpr (kCausal) {
           const int pos = r + u.pos_shift;
           lim_v = pos < 0 ? 0 : (pos / p.causal_block + 1) * p.causal_block;
         }
-        const float l = rvalid && lim_v > 0 ? __ldg(p.lse + lrow0 + (r - rtok)) : -CUDART_INF_F;
+        const int64_t li = lhead + fw.seg.x + r;
+        const float l = rvalid && lim_v > 0 ? __ldg(p.lse + li) : -CUDART_INF_F;
         xl_v = l > -CUDART_INF_F ? l * kLog2e : CUDART_INF_F;  // +inf: P = 0
-        xd_v = rvalid ? __ldg(p.dvec + lrow0 + (r - rtok)) : 0.0f;
+        xd_v = rvalid ? __ldg(p.dvec + li) : 0.0f;
       };
       float nxl = 0.0f, nxd = 0.0f;
       int nlim = 0;
-      if (tid < 64) fetch(0, nxl, nxd, nlim);
+      if (tid < 64 && nqt > 0) fetch(nxl, nxd, nlim);
       for (int i = 0; i < nqt; ++i) {
         const int par = tiles & 1;
         ++tiles;
@@ -743,7 +788,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ctrl.xl[par][lrow] = nxl;
           ctrl.xd[par][lrow] = nxd;
           if constexpr (kCausal) ctrl.xlim[par][lrow] = nlim;
-          if (i + 1 < nqt) fetch(i + 1, nxl, nxd, nlim);
+          if (i + 1 < nqt) {
+            fw.next(T);
+            fetch(nxl, nxd, nlim);
+          }
         }
         const bool fine = __all_sync(0xffffffffu, wait_bar(&ctrl.s_full, sc & 1, abort_flag, p.error_flag));
         if (named_barrier_or(1 + wg, 128, !fine)) {
@@ -879,7 +927,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 template <int D, typename TQ, typename TKV, bool kCausal>
 cudaError_t launch_bwd_impl(const BwdParams& p, const MergeUnit* units, int32_t num_units, const void* out,
                             const void* d_out, float* dvec, const CUtensorMap& mq, const CUtensorMap& mk,
-                            const CUtensorMap& mv, const CUtensorMap& mdo, int dq_grid, int sms,
+                            const CUtensorMap& mv, const CUtensorMap& mdo, int dq_grid, int kv_grid, int sms,
                             cudaStream_t stream) {
   if (num_units > 0) {
     gva_bwd_dvec_kernel<D><<<min(num_units, sms * 8), 256, 0, stream>>>(
@@ -899,7 +947,7 @@ cudaError_t launch_bwd_impl(const BwdParams& p, const MergeUnit* units, int32_t 
     auto kkv = gva_bwd_dkdv_kernel<D, TKV, kCausal>;
     cudaError_t e = ensure_smem_limit<gva_bwd_dkdv_kernel<D, TKV, kCausal>>(BCfg<D>::kSmemDkv);
     if (e != cudaSuccess) return e;
-    kkv<<<min(p.num_kv_units, sms), kBwdThreads, BCfg<D>::kSmemDkv, stream>>>(mq, mk, mv, mdo, p);
+    kkv<<<kv_grid, kBwdThreads, BCfg<D>::kSmemDkv, stream>>>(mq, mk, mv, mdo, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -909,32 +957,29 @@ template <int D, bool kCausal>
 cudaError_t launch_bwd_dc(bool dq_f32, bool dkv_f32, const BwdParams& p, const MergeUnit* units, int32_t num_units,
                           const void* out, const void* d_out, float* dvec, const CUtensorMap& mq,
                           const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo, int dq_grid,
-                          int sms, cudaStream_t stream) {
+                          int kv_grid, int sms, cudaStream_t stream) {
   if (dq_f32) {
     return dkv_f32 ? launch_bwd_impl<D, float, float, kCausal>(p, units, num_units, out, d_out, dvec, mq, mk, mv, mdo,
-                                                               dq_grid, sms, stream)
+                                                               dq_grid, kv_grid, sms, stream)
                    : launch_bwd_impl<D, float, __nv_bfloat16, kCausal>(p, units, num_units, out, d_out, dvec, mq, mk,
-                                                                       mv, mdo, dq_grid, sms, stream);
+                                                                       mv, mdo, dq_grid, kv_grid, sms, stream);
   }
   return dkv_f32 ? launch_bwd_impl<D, __nv_bfloat16, float, kCausal>(p, units, num_units, out, d_out, dvec, mq, mk,
-                                                                     mv, mdo, dq_grid, sms, stream)
+                                                                     mv, mdo, dq_grid, kv_grid, sms, stream)
                  : launch_bwd_impl<D, __nv_bfloat16, __nv_bfloat16, kCausal>(p, units, num_units, out, d_out, dvec,
-                                                                             mq, mk, mv, mdo, dq_grid, sms, stream);
+                                                                             mq, mk, mv, mdo, dq_grid, kv_grid, sms, stream);
 }
 
 template <int D>
 cudaError_t launch_bwd_d(bool dq_f32, bool dkv_f32, const BwdParams& p, const MergeUnit* units, int32_t num_units,
                          const void* out, const void* d_out, float* dvec, const CUtensorMap& mq,
                          const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo, int dq_grid,
-                         cudaStream_t stream) {
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+                         int kv_grid, int sms, cudaStream_t stream) {
   if (p.causal_block > 0)
     return launch_bwd_dc<D, true>(dq_f32, dkv_f32, p, units, num_units, out, d_out, dvec, mq, mk, mv, mdo, dq_grid,
-                                  sms, stream);
+                                  kv_grid, sms, stream);
   return launch_bwd_dc<D, false>(dq_f32, dkv_f32, p, units, num_units, out, d_out, dvec, mq, mk, mv, mdo, dq_grid,
-                                 sms, stream);
+                                 kv_grid, sms, stream);
 }
 
 }  // namespace
@@ -942,12 +987,12 @@ cudaError_t launch_bwd_d(bool dq_f32, bool dkv_f32, const BwdParams& p, const Me
 cudaError_t launch_backward(int head_dim, bool dq_f32, bool dkv_f32, const BwdParams& p, const MergeUnit* units,
                             int32_t num_units, const void* out, const void* d_out, float* dvec,
                             const CUtensorMap& map_q, const CUtensorMap& map_k, const CUtensorMap& map_v,
-                            const CUtensorMap& map_do, int dq_grid, cudaStream_t stream) {
+                            const CUtensorMap& map_do, int dq_grid, int kv_grid, int sm_count, cudaStream_t stream) {
   if (head_dim == 128)
     return launch_bwd_d<128>(dq_f32, dkv_f32, p, units, num_units, out, d_out, dvec, map_q, map_k, map_v, map_do,
-                             dq_grid, stream);
+                             dq_grid, kv_grid, sm_count, stream);
   return launch_bwd_d<64>(dq_f32, dkv_f32, p, units, num_units, out, d_out, dvec, map_q, map_k, map_v, map_do,
-                          dq_grid, stream);
+                          dq_grid, kv_grid, sm_count, stream);
 }
 
 }  // namespace gva

@@ -37,17 +37,27 @@ struct alignas(8) KeyBlock {
   int32_t valid;
 };
 
-// One unit of the dK / dV kernel: one key block of one segment for one KV head, run
-// against every Q tile of the segment.
+// One unit of the dK / dV kernel: up to kBlockKeys consecutive K/V rows for one KV head,
+// run against every Q tile of every segment that attends them. The segments are a run
+// of SegRef entries; a segment whose key ranges cover the rows m times appears m times
+// (its rows attend each copy of those keys). Each K/V row belongs to exactly one unit
+// per KV head, so dK and dV have one writer and need no atomics, even when key ranges
+// of several segments (or of one segment) overlap.
 struct alignas(16) KvUnit {
   int32_t key_row0;  // global K/V row of the block's first key
-  int32_t keys;      // used keys in the block (1 .. kBlockKeys)
-  int32_t q_row0;    // global token row of the segment's first query
-  int32_t q_used;    // used query rows of the segment (0: dK = dV = 0)
+  int32_t keys;      // K/V rows in the block (1 .. kBlockKeys)
+  int32_t seg0;      // first SegRef of the unit's segments
+  int32_t n_tiles;   // Q tiles over all of them (0: no row attends the block, dK = dV = 0)
   int32_t head_kv;
-  int32_t tile0;     // first Q tile of the segment that sees the block (block-causal; else 0)
-  int32_t key_pos0;  // block-causal: index of the block's first key within the segment
+  int32_t tile0;     // first Q tile of the first segment that sees the block (block-causal; else 0)
+  int32_t key_pos0;  // block-causal (one segment): index of the block's first key within it
   int32_t pos_shift; // block-causal: key position of the segment's query row 0 (used_k - used_q)
+};
+
+// A segment attending a dK / dV unit's keys: its query rows (used rows > 0 only).
+struct alignas(8) SegRef {
+  int32_t q_row0;  // global token row of the segment's first query
+  int32_t q_used;  // used query rows
 };
 
 struct alignas(8) MergeUnit {
@@ -90,6 +100,7 @@ struct BwdParams {
   const KeyBlock* blocks;
   int32_t num_items;
   const KvUnit* kv_units;  // dK / dV work
+  const SegRef* kv_segs;   // the segments of each dK / dV unit
   int32_t num_kv_units;
   const float* lse;        // [Hq, total_q] from the forward
   const float* dvec;       // [Hq, total_q]: rowsum(dO * O)
@@ -127,11 +138,13 @@ cudaError_t launch_merge(bool in_f32, bool out_f32, const MergeParams& p, int sm
 int merge_smem_bytes(bool in_f32, int num_parts, int num_heads_q, int* ring_slots);
 int forward_smem_bytes(int head_dim);
 // Backward: rowsum(dO * O) over used rows, then dQ, then dK / dV (gva_bwd.cu).
-// Backward kernels take the block-causal variant when p.causal_block > 0.
+// Backward kernels take the block-causal variant when p.causal_block > 0. dq_grid and
+// kv_grid are the CTA counts the plan's dQ and dK / dV lists were laid out for.
 cudaError_t launch_backward(int head_dim, bool dq_f32, bool dkv_f32, const BwdParams& p, const MergeUnit* units,
                             int32_t num_units, const void* out, const void* d_out, float* dvec,
                             const CUtensorMap& map_q, const CUtensorMap& map_k, const CUtensorMap& map_v,
-                            const CUtensorMap& map_do, int dq_grid, cudaStream_t stream);
+                            const CUtensorMap& map_do, int dq_grid, int kv_grid, int sm_count,
+                            cudaStream_t stream);
 // Raise kernel K's dynamic shared-memory limit to `bytes`, once per device: the
 // attribute persists, and setting it on every launch is redundant work inside a CUDA
 // graph capture. One flag word per kernel instantiation (bit d: device d < 64).
@@ -150,5 +163,10 @@ inline cudaError_t ensure_smem_limit(int bytes) {
 
 // Set the calling thread's gva_last_error() text (defined in gva_api.cu).
 void set_last_error(const char* message);
+
+// Synchronise the current device, read and clear the error word of the last
+// gva_forward_noalloc launch on it (defined in gva_noalloc.cu; GVA_OK if none ran).
+// Returns a gva_status value.
+int noalloc_device_status();
 
 }  // namespace gva

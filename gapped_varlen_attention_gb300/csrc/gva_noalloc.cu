@@ -13,9 +13,16 @@
 // Set-up: the first call on a device (with that device current) resolves the array's
 // device address with cudaGetSymbolAddress and caches it; make that first call before
 // any stream capture. Each call then copies its work list into the array and clears
-// the error word, on the caller's stream. All calls share the one array, so calls
-// whose kernels overlap on the GPU (different streams, no ordering between them) race
-// on it and must be avoided; calls on one stream are ordered and safe.
+// the error word, on the caller's stream. The copy comes from a host staging array in
+// ordinary (pageable) memory, and the CUDA runtime starts such a copy only once the
+// stream's earlier work has finished: each call therefore waits on the host for the
+// work already queued on its stream. All calls share the one array, so calls whose
+// kernels overlap on the GPU (different streams, no ordering between them) race on it
+// and must be avoided; calls on one stream are ordered and safe.
+//
+// A bounded wait that times out inside the kernel leaves rows unwritten and sets the
+// error word; gva_device_status(NULL) reads (and clears) that word for the current
+// device after synchronising it.
 #include <algorithm>
 #include <cmath>
 #include <cstdarg>
@@ -87,6 +94,42 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
+namespace gva {
+
+// The error word of the last gva_forward_noalloc launch on the current device (behind
+// gva_device_status(NULL)): synchronise, read it, clear it. GVA_OK when no call has
+// run on this device yet.
+int noalloc_device_status() {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(GVA_ERR_UNSUPPORTED, "no usable CUDA device: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(GVA_ERR_UNSUPPORTED, "device ordinal %d is out of range", dev);
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    base = g_scratch_ptr[dev];
+  }
+  if (base == nullptr) {
+    set_last_error("");
+    return GVA_OK;
+  }
+  int* d_error = reinterpret_cast<int*>(static_cast<unsigned char*>(base) + kNoallocItemBytes + kNoallocBlockBytes);
+  if ((e = cudaDeviceSynchronize()) != cudaSuccess)
+    return fail(GVA_ERR_CUDA, "cudaDeviceSynchronize: %s", cudaGetErrorString(e));
+  int word = 0;
+  if ((e = cudaMemcpy(&word, d_error, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return fail(GVA_ERR_CUDA, "reading the no-alloc error word: %s", cudaGetErrorString(e));
+  if (word != 0) {
+    cudaMemset(d_error, 0, sizeof(int));
+    return fail(GVA_ERR_DEVICE_CHECK,
+                "a gva_forward_noalloc kernel recorded device error bits 0x%x (1 = bounded wait timed out)", word);
+  }
+  set_last_error("");
+  return GVA_OK;
+}
+
+}  // namespace gva
+
 extern "C" GVA_API gva_status gva_forward_noalloc(
     const int32_t* cu_seqlens_q, const int32_t* seqused_q, const int32_t* cu_seqlens_k, const int32_t* seqused_k,
     int32_t num_segments, int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim, const void* q, const void* k,
@@ -100,8 +143,8 @@ extern "C" GVA_API gva_status gva_forward_noalloc(
   if (num_heads_q <= 0 || num_heads_kv <= 0 || num_heads_q % num_heads_kv != 0)
     return fail(GVA_ERR_INVALID_ARG, "bad head counts (Hq=%d, Hkv=%d)", num_heads_q, num_heads_kv);
   const int32_t group = num_heads_q / num_heads_kv;
-  if (gva::kTileRows % group != 0)
-    return fail(GVA_ERR_UNSUPPORTED, "query heads per KV head (%d) must divide %d", group, gva::kTileRows);
+  if (group > gva::kTileRows)
+    return fail(GVA_ERR_UNSUPPORTED, "query heads per KV head (%d) must be at most %d", group, gva::kTileRows);
   if (head_dim != 64 && head_dim != 128) return fail(GVA_ERR_UNSUPPORTED, "head_dim=%d is not supported", head_dim);
   if (out_dtype != GVA_BF16 && out_dtype != GVA_FP32) return fail(GVA_ERR_INVALID_ARG, "bad out_dtype");
   if (!std::isfinite(softmax_scale)) return fail(GVA_ERR_INVALID_ARG, "softmax_scale is not finite");

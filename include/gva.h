@@ -96,7 +96,10 @@ typedef struct {
  *                                a first offset above 0 lets a visibility partition
  *                                address a sub-range of the same K/V buffers)
  *   seqused_q, seqused_k       : HOST int32 [num_segments], 0 <= used <= capacity
- *   num_heads_q % num_heads_kv == 0 and 128 % (num_heads_q / num_heads_kv) == 0
+ *   num_heads_q % num_heads_kv == 0, group g = num_heads_q / num_heads_kv <= 128,
+ *   num_heads_q <= 256; a 128-row Q tile folds floor(128 / g) tokens of the g query
+ *   heads of one KV head (GQA folding, PR #312 "Problem and behavior"), so any g up
+ *   to 128 is accepted (rows past floor(128 / g) * g of a tile are idle)
  *   head_dim in {64, 128}
  *
  * The plan is bound to the current CUDA device, which must be sm_103 (GB300).
@@ -204,8 +207,7 @@ GVA_API gva_status gva_lse_merge(gva_plan_t plan, int32_t num_parts, const void*
 /*
  * gva_backward_workspace_size - bytes of device workspace gva_backward needs.
  *
- * Writes Hq * total_q * 4 (one fp32 D value per row and query head) to *bytes. Returns
- * GVA_ERR_UNSUPPORTED for a range plan whose ranges overlap (see gva_backward).
+ * Writes Hq * total_q * 4 (one fp32 D value per row and query head) to *bytes.
  */
 GVA_API gva_status gva_backward_workspace_size(gva_plan_t plan, size_t* bytes);
 
@@ -222,9 +224,14 @@ GVA_API gva_status gva_backward_workspace_size(gva_plan_t plan, size_t* bytes);
  *   dK_j = s sum_{i, h of the KV group} dS_ij Q_i,   dV_j = sum_{i, h} P_ij dO_i
  * For plans from gva_plan (maskless), gva_plan_causal (the gradients of the block-causal
  * forward: P is zero past each row's key limit, and a row that sees no key gets dQ = 0)
- * and gva_plan_ranges (segment b's keys are its ranges, as in the forward). Every K/V
- * row must belong to at most one key range of the plan (one writer per dK / dV row): a
- * range plan whose non-empty ranges overlap is refused with GVA_ERR_UNSUPPORTED.
+ * and gva_plan_ranges (segment b's keys are its ranges, as in the forward). Key ranges
+ * may overlap, across segments or within one (TensorRT-LLM issue #18687, "additional
+ * notes": after an all-to-all the valid keys are not a prefix): a K/V row's dK / dV is
+ * then the sum of the contributions of every segment that attends it, counted once per
+ * range of that segment that covers the row, as the forward counts them. The plan cuts
+ * the union of the ranges where any range starts or ends and gives each piece (at most
+ * 128 rows) one unit per KV head that walks the Q tiles of all its attending segments,
+ * so each dK / dV row still has a single writer.
  *
  *   q, k, v   : DEVICE bf16, as given to gva_forward
  *   out, lse  : DEVICE, the forward's bf16 output [total_q, Hq, d] and fp32 LSE
@@ -238,7 +245,8 @@ GVA_API gva_status gva_backward_workspace_size(gva_plan_t plan, size_t* bytes);
  *   stream    : CUDA stream the kernels are enqueued on
  *
  * Rows written: dq on used rows (zero on the used rows of a keyless segment); dk / dv
- * on each segment's used keys (zero where the segment has no used row). Gap rows and
+ * on every K/V row some segment's keys include (zero where no attending segment has a
+ * used row). Gap rows and
  * K/V rows outside every segment's keys are not written; their contents (even NaN) do not affect any
  * written value. Every pointer 16-byte aligned; inputs must not alias outputs. No
  * atomics: the result is deterministic. Asynchronous; bounded device waits as for
@@ -259,9 +267,8 @@ GVA_API gva_status gva_backward(gva_plan_t plan, const void* q, const void* k, c
  * not read and causal_block must be 0). causal_block: 0 maskless, > 0 as
  * gva_plan_causal. grid (>= 1): the SM count the work lists are laid out for;
  * walk_list selects the list `walk` describes (0 forward items, 1 dQ items, 2 dK / dV
- * units). Fills *summary (backward_ok: 0 for range plans whose non-empty ranges
- * overlap, which gva_backward refuses) and copies at most *_capacity records into each
- * non-NULL array (8 int32 per record; one per entry for walk):
+ * units). Fills *summary (backward_ok: always 1) and copies at most *_capacity records
+ * into each non-NULL array (8 int32 per record; 2 for kv_segs; one per entry for walk):
  *   items     : forward work items {q_row0, q_rows, blk0, nblk, head_kv, n_tiles, k_len,
  *               q_pos0}, longest first;
  *   walk      : one int32 per entry of the chosen list as its kernel walks it (with
@@ -269,9 +276,11 @@ GVA_API gva_status gva_backward(gva_plan_t plan, const void* q, const void* k, c
  *               even rounds r and r * g + g - 1 - c in odd ones): the entry's index in
  *               the sorted list, or -1 for padding;
  *   bwd_items : backward dQ items, same layout, one Q tile each;
- *   kv_units  : backward dK / dV units {key_row0, keys, q_row0, q_used, head_kv, tile0,
- *               key_pos0, pos_shift}, one per key block and KV head.
- * bwd_items and kv_units are empty when backward_ok is 0.
+ *   kv_units  : backward dK / dV units {key_row0, keys, seg0, n_tiles, head_kv, tile0,
+ *               key_pos0, pos_shift}, one per piece of at most 128 K/V rows and KV head:
+ *               rows key_row0 .. key_row0 + keys, run against n_tiles Q tiles of the
+ *               segments kv_segs[seg0 ..] (starting at tile tile0 of the first);
+ *   kv_segs   : {q_row0, q_used} of the segments the units list (summary->num_kv_segs).
  * Errors: GVA_ERR_INVALID_ARG for a NULL summary, a negative causal_block, ranges with a
  * causal_block, grid < 1, walk_list outside 0 .. 2 or bad geometry; GVA_ERR_UNSUPPORTED
  * as gva_plan.
@@ -279,7 +288,7 @@ GVA_API gva_status gva_backward(gva_plan_t plan, const void* q, const void* k, c
 typedef struct {
   int32_t num_work_items, num_key_blocks, num_merge_units, num_bwd_items, num_kv_units, backward_ok;
   double used_flops;
-  int32_t num_walk_entries, reserved;
+  int32_t num_walk_entries, num_kv_segs;
 } gva_work_summary;
 GVA_API gva_status gva_plan_inspect(const int32_t* cu_seqlens_q, const int32_t* seqused_q,
                                     const int32_t* cu_seqlens_k, const int32_t* seqused_k, int32_t num_segments,
@@ -289,7 +298,7 @@ GVA_API gva_status gva_plan_inspect(const int32_t* cu_seqlens_q, const int32_t* 
                                     int32_t walk_list, gva_work_summary* summary, int32_t* items,
                                     int32_t items_capacity, int32_t* walk, int32_t walk_capacity,
                                     int32_t* bwd_items, int32_t bwd_items_capacity, int32_t* kv_units,
-                                    int32_t kv_units_capacity);
+                                    int32_t kv_units_capacity, int32_t* kv_segs, int32_t kv_segs_capacity);
 
 /* Release a plan's device memory. NULL is accepted. Synchronous with respect to the
  * host only through cudaFree. */
@@ -301,7 +310,11 @@ GVA_API gva_status gva_plan_get_info(gva_plan_t plan, gva_plan_info* info);
 /* Synchronise the device, read and clear the plan's device error word. Returns
  * GVA_ERR_DEVICE_CHECK if a kernel of this plan recorded a bounded-wait timeout or a
  * check failure since the last call, GVA_OK otherwise. For tests and debugging; it
- * is not needed on the fast path. */
+ * is not needed on the fast path.
+ * With plan = NULL it does the same for the error word of gva_forward_noalloc's
+ * scratch on the current device, which reports the last gva_forward_noalloc launch
+ * there (each call clears the word before its launch); GVA_OK if none has run, and
+ * GVA_ERR_UNSUPPORTED without a usable CUDA device. */
 GVA_API gva_status gva_device_status(gva_plan_t plan);
 
 /*
@@ -320,7 +333,7 @@ GVA_API gva_status gva_device_status(gva_plan_t plan);
  * Arguments: the geometry exactly as for gva_plan (HOST arrays, same rules), then the
  * tensors, scale and stream exactly as for gva_forward (the caller still owns and
  * passes inputs and outputs). A launch needing more than GVA_NOALLOC_MAX_WORK_ITEMS
- * work items (items = sum over segments of ceil(seqused_q / (256 / (Hq/Hkv))) * Hkv)
+ * work items (items = sum over segments of ceil(seqused_q / (2 * floor(128 / (Hq/Hkv)))) * Hkv)
  * or more than GVA_NOALLOC_MAX_KEY_BLOCKS key blocks (sum over segments of
  * ceil(seqused_k / 128)) is refused with GVA_ERR_INVALID_ARG before any GPU work.
  *
@@ -330,6 +343,15 @@ GVA_API gva_status gva_device_status(gva_plan_t plan);
  * on `stream`: calls on one stream are ordered, but calls whose kernels may overlap on
  * the GPU (different streams without ordering) race on the scratch and must not be
  * made.
+ *
+ * Host wait: the work list is copied from a host staging array in ordinary (pageable)
+ * memory, and the CUDA runtime starts such a copy only after the work already queued
+ * on `stream` has finished. Each call therefore blocks the calling thread until that
+ * earlier work is done (the kernel itself is then launched asynchronously).
+ *
+ * Device errors: a bounded wait that times out inside the kernel leaves rows
+ * unwritten and records it in the scratch's error word, not in the return value;
+ * gva_device_status(NULL) reads and clears that word for the current device.
  */
 #define GVA_NOALLOC_MAX_WORK_ITEMS 32768
 #define GVA_NOALLOC_MAX_KEY_BLOCKS 65536

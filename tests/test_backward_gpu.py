@@ -113,6 +113,11 @@ CASES = [  # (Hq, Hkv, d, seed)
     (4, 4, 64, 204),
     (16, 1, 128, 205),
     (128, 1, 64, 206),
+    # groups that do not divide the 128-row tile: floor(128 / g) tokens per tile
+    (12, 4, 128, 207),  # g = 3
+    (24, 4, 64, 208),   # g = 6
+    (12, 1, 128, 209),  # g = 12
+    (96, 1, 64, 210),   # g = 96: one token of 96 heads per tile
 ]
 
 
@@ -181,14 +186,14 @@ def test_deterministic():
         assert torch.equal(x, y)
 
 
-def test_overlapping_range_plans_are_refused():
-    """A K/V row in two ranges would need its dK / dV summed across units."""
+def test_overlapping_ranges_tiny():
+    """Two segments whose key ranges share rows 40 .. 47: those rows' dK / dV sum both
+    segments' contributions (the oracle's summed gradient)."""
     g = W.tiny()
-    rplan = gva.Plan.from_ranges(g.cu_q, g.used_q, [[(0, 48)], [(40, 33)], []], g.total_k, 4, 2, 64)
-    with pytest.raises(gva.GvaError, match="UNSUPPORTED"):
-        gva.backward_workspace_bytes(rplan)
-    ok = gva.Plan.from_ranges(g.cu_q, g.used_q, [[(0, 40)], [(40, 33)], []], g.total_k, 4, 2, 64)
-    assert gva.backward_workspace_bytes(ok) == 4 * g.total_q * 4
+    ranges = [[(0, 48)], [(40, 33)], []]
+    q, k, v = W.make_qkv(g, 1001)
+    do = _make_dout(g, 1001)
+    _check_ranges(g, ranges, _ranges_backward(g, ranges, g.total_k, q, k, v, do), q, k, v, do)
 
 
 def _ranges_backward(g, ranges, total_k, q, k, v, do):
@@ -209,12 +214,16 @@ def _check_ranges(g, ranges, got, q, k, v, do):
             covered[st:st + n] = True
     fill32 = np.float64(np.float32(FILL))
     assert np.all(dq[~dq_rows] == fill32) and np.all(dk[~covered] == fill32) and np.all(dv[~covered] == fill32)
-    for b, rr in enumerate(ranges):  # exact zeros: keyless segments' rows, row-less segments' keys
+    attended = np.zeros(kn.shape[0], bool)  # K/V rows some segment with used rows attends
+    for b, rr in enumerate(ranges):
+        if g.used_q[b]:
+            for st, n in rr:
+                attended[st:st + n] = True
+    for b, rr in enumerate(ranges):  # exact zeros: keyless segments' rows, keys no used row attends
         if g.used_q[b] and not sum(n for _, n in rr):
             assert np.all(dq[g.cu_q[b]:g.cu_q[b] + g.used_q[b]] == 0.0)
-        if not g.used_q[b]:
-            for st, n in rr:
-                assert np.all(dk[st:st + n] == 0.0) and np.all(dv[st:st + n] == 0.0)
+    idle = covered & ~attended
+    assert np.all(dk[idle] == 0.0) and np.all(dv[idle] == 0.0)
     _close("dQ", dq[dq_rows], ref[0][dq_rows])
     _close("dK", dk[covered], ref[1][covered])
     _close("dV", dv[covered], ref[2][covered])
@@ -237,6 +246,39 @@ def test_disjoint_key_ranges(hq, hkv, d, seed):
         ranges.append([(st, min(n, 400)) for st, n in pieces[:take]])
         pieces = pieces[take:]
     ranges[0] = []  # one keyless segment
+    gen = torch.Generator().manual_seed(seed)
+    q = torch.randn(g.total_q, hq, d, generator=gen).bfloat16()
+    k = torch.randn(total_k, hkv, d, generator=gen).bfloat16()
+    v = torch.randn(total_k, hkv, d, generator=gen).bfloat16()
+    do = _make_dout(g, seed)
+    covered = np.zeros(total_k, bool)
+    for rr in ranges:
+        for st, n in rr:
+            covered[st:st + n] = True
+    k[torch.from_numpy(~covered)] = float("nan")
+    v[torch.from_numpy(~covered)] = float("nan")
+    _check_ranges(g, ranges, _ranges_backward(g, ranges, total_k, q, k, v, do), q, k, v, do)
+
+
+@pytest.mark.parametrize("hq,hkv,d,seed", [(8, 2, 128, 821), (16, 16, 64, 822), (12, 4, 128, 823)])
+def test_overlapping_key_ranges(hq, hkv, d, seed):
+    """Key ranges that overlap freely: every segment attends one shared range (a common
+    prompt), plus up to three ranges of its own that may overlap other segments' ranges
+    or its own (one range listed twice). A K/V row's dK / dV is the sum over every
+    attending segment, counted once per covering range; rows no range covers stay
+    untouched (NaN inputs there)."""
+    rng = np.random.default_rng(seed)
+    g = W.random_geometry(rng, 5, 500, 10, hq, hkv, d)
+    total_k = 2000
+    shared = (int(rng.integers(0, 400)), int(rng.integers(1, 300)))
+    ranges = []
+    for b in range(g.num_segments):
+        rr = [shared]
+        for _ in range(int(rng.integers(0, 4))):
+            st = int(rng.integers(0, total_k - 1))
+            rr.append((st, int(rng.integers(0, min(400, total_k - st) + 1))))
+        ranges.append(rr)
+    ranges[-1].append(ranges[-1][-1])  # a range listed twice: its keys enter the softmax twice
     gen = torch.Generator().manual_seed(seed)
     q = torch.randn(g.total_q, hq, d, generator=gen).bfloat16()
     k = torch.randn(total_k, hkv, d, generator=gen).bfloat16()
@@ -280,6 +322,8 @@ CAUSAL_CASES = [  # (Hq, Hkv, d, causal block, seed)
     (8, 8, 64, 200, 604),
     (16, 1, 64, 128, 605),
     (4, 1, 128, 129, 606),
+    (12, 4, 128, 7, 607),  # g = 3
+    (24, 2, 64, 50, 608),  # g = 12
 ]
 
 
@@ -398,3 +442,29 @@ def test_multiview_block_causal_full_size_sampled():
                                                          do[sel].cpu(), [0, 1], [1], [0, n], [n])
             got = dq[sel].float().cpu().numpy().astype(np.float64)
             assert np.abs(got - dq_ref).max() <= MAX_REL * max(np.abs(dq_ref).max(), 1e-30)
+
+
+@pytest.mark.slow
+def test_long_replay_small_one_segment_and_kv_head_elementwise():
+    """dQ, dK and dV element by element at full size: the whole reduced long replay (2
+    segments of up to 8192 rows and 32768 keys, Hq = 32, Hkv = 8) runs through the
+    backward, and one whole segment of one KV head is checked against the oracle. Each
+    dK / dV unit there sums over the segment's ~190 Q tiles (32 tokens x 4 heads each),
+    so an error in one unit's accumulation or in any tile it streams shows up here,
+    which the sum identities at the larger size cannot localise."""
+    g = W.long_replay_small()
+    q, k, v = W.make_qkv(g, 1006, device="cuda", gap_fill=float("nan"))
+    do = _make_dout(g, 1006, device="cuda")
+    dq, dk, dv = gpu_backward(g, q, k, v, do)
+    b, hk = 0, int(np.random.default_rng(31).integers(0, g.num_heads_kv))
+    grp = g.num_heads_q // g.num_heads_kv
+    heads = slice(hk * grp, (hk + 1) * grp)
+    r0, nq, k0, nk = int(g.cu_q[b]), int(g.used_q[b]), int(g.cu_k[b]), int(g.used_k[b])
+    qs, dos = q[r0:r0 + nq, heads].cpu(), do[r0:r0 + nq, heads].cpu()
+    ks, vs = k[k0:k0 + nk, hk:hk + 1].cpu(), v[k0:k0 + nk, hk:hk + 1].cpu()
+    # the same problem with this KV head's group alone: Hq = grp, Hkv = 1
+    dq_ref, dk_ref, dv_ref = gva_oracle.attention_backward(qs, ks, vs, dos, [0, nq], [nq], [0, nk], [nk])
+    got = [t.float().cpu().numpy().astype(np.float64) for t in
+           (dq[r0:r0 + nq, heads], dk[k0:k0 + nk, hk:hk + 1], dv[k0:k0 + nk, hk:hk + 1])]
+    errs = (_close("dQ", got[0], dq_ref), _close("dK", got[1], dk_ref), _close("dV", got[2], dv_ref))
+    print(f"segment {b}, KV head {hk}: max err / max |ref|: dQ {errs[0]:.2e}  dK {errs[1]:.2e}  dV {errs[2]:.2e}")

@@ -68,3 +68,54 @@ def test_copy_rows_leaves_gaps():
     assert torch.all(dst[[0, 3, 4, 5, 9]] == -1.0)
     bench.copy_rows(dst, src, None)
     assert torch.equal(dst, src)
+
+
+def _roof_stub(work, dom_flops):
+    s = types.SimpleNamespace(bound="tensor", unit="TFLOP/s", scale=1e12, merge_only=False, work=work,
+                              kernel="gva_fwd_kernel", dominant=0)
+    s.plans = [types.SimpleNamespace(info=lambda: {"used_flops": dom_flops})]
+    s.dominant_bytes = lambda: 1.0e9
+    return s
+
+
+def test_roofline_peak_follows_the_kernels_own_timed_region():
+    """Burst peak when the dominant kernel's timed launches last under a second,
+    sustained above; both fractions are always given."""
+    peaks = {"bf16_tflops": 2000.0, "bf16_tflops_sustained": 1600.0, "hbm_gbs": 7000.0}
+    wl = _roof_stub(1e14, 1e14)
+    short = {"dom_ms": 60.0, "dom_launches": 10, "same_size_copy_gbs": None}  # 0.6 s
+    r = bench.roofline_of(wl, short, peaks, "measured", None)
+    assert r["peak"] == 2000.0 and "burst" in r["peak_source"]
+    assert r["achieved"] == pytest.approx(1e14 / 0.06 / 1e12, abs=0.01)  # rounded to 0.01
+    assert r["frac"] == r["frac_burst"] and r["frac_sustained"] == pytest.approx(r["achieved"] / 1600.0, abs=1e-4)
+    long = {"dom_ms": 60.0, "dom_launches": 20, "same_size_copy_gbs": None}  # 1.2 s
+    r = bench.roofline_of(wl, long, peaks, "measured", 2.0e9)
+    assert r["peak"] == 1600.0 and "sustained" in r["peak_source"]
+    assert r["traffic"] == 2.0e9 and r["traffic_over_algorithmic"] == 2.0
+
+
+def test_dominant_bytes_of_the_long_replay():
+    """Q, O (bf16) and LSE of the used rows plus K and V of the used keys: about 2.587 GB
+    for the long replay's used lengths."""
+    g = W.long_replay()
+    s = types.SimpleNamespace(merge_only=False, geoms=[g], dominant=0, partials=None,
+                              out=torch.empty(0, dtype=torch.bfloat16, device="meta"))
+    got = bench.Workload.dominant_bytes(s)
+    rows, keys = int(g.used_q.sum()), int(g.used_k.sum())
+    assert got == rows * 32 * (128 * 2 + 128 * 2 + 4) + keys * 8 * 2 * 128 * 2
+    assert got == pytest.approx(2.587e9, rel=1e-3)
+
+
+def test_recorded_traffic_needs_the_current_kernel_sources(tmp_path, monkeypatch):
+    import json
+    rec = tmp_path / "traffic.json"
+    monkeypatch.setattr(bench, "TRAFFIC_RECORD", str(rec))
+    assert bench.recorded_traffic("long_replay", "gva_fwd_kernel") is None  # no record
+    h = bench.kernel_source_hash("gva_fwd_kernel")
+    rec.write_text(json.dumps({"records": {"long_replay": {"kernel": "gva_fwd_kernel", "source_sha16": h,
+                                                           "dram_bytes_per_launch": 3.1e9}}}))
+    assert bench.recorded_traffic("long_replay", "gva_fwd_kernel") == 3.1e9
+    assert bench.recorded_traffic("long_replay", "gva_backward") is None  # another kernel
+    rec.write_text(json.dumps({"records": {"long_replay": {"kernel": "gva_fwd_kernel", "source_sha16": "0" * 16,
+                                                           "dram_bytes_per_launch": 3.1e9}}}))
+    assert bench.recorded_traffic("long_replay", "gva_fwd_kernel") is None  # taken on other sources

@@ -122,6 +122,12 @@ CASES = [  # (Hq, Hkv, d, out dtype, seed)
     (16, 8, 64, torch.float32, 26),
     (32, 8, 64, torch.bfloat16, 27),
     (128, 1, 128, torch.bfloat16, 28),
+    # groups that do not divide the 128-row tile: floor(128 / g) tokens per tile
+    (12, 4, 128, torch.bfloat16, 29),   # g = 3: 12 cross-attention heads split over 4 KV heads
+    (24, 4, 128, torch.float32, 30),    # g = 6
+    (12, 1, 64, torch.bfloat16, 31),    # g = 12
+    (40, 8, 128, torch.bfloat16, 32),   # g = 5
+    (100, 1, 128, torch.bfloat16, 33),  # g = 100: one token of 100 heads per tile
 ]
 
 

@@ -45,8 +45,8 @@ def dq_cost(it):
     return 2.0 + it["nblk"]
 
 
-def kv_cost(u, tpt):
-    return 2.0 + (-(-u["q_used"] // tpt) - u["tile0"])
+def kv_cost(u):
+    return 2.0 + u["n_tiles"]
 
 
 def check_walk(items, walk, grid, cost=est_cost):
@@ -85,6 +85,11 @@ def limits(uq, uk, B):
     if B == 0:
         return np.full(uq, uk, np.int64)
     return oracle.causal_limits(uq, uk, B).astype(np.int64)
+
+
+def kp_of(u):
+    """Index of a unit's first key within its segment (block-causal units carry it)."""
+    return u["key_pos0"]
 
 
 def check_work(g, B=0):
@@ -146,8 +151,10 @@ def check_work(g, B=0):
     assert nb == sorted(nb, reverse=True), "dQ items not longest first"
     check_walk(bwd, w["bwd_walk"], SMS, dq_cost)
 
-    # ---- dK / dV units: one per (segment, KV head, key block), every used key once
+    # ---- dK / dV units: one per (segment, KV head, key block), every used key once; each
+    # lists its one segment (if that has rows) and runs over its Q tiles from tile0
     units = rec(w["kv_units"], _lib.KV_UNIT_FIELDS)
+    segs = [tuple(int(x) for x in r) for r in w["kv_segs"]]
     want_units = []
     for b in range(nseg):
         n_tiles = -(-int(uq[b]) // tpt)
@@ -160,25 +167,30 @@ def check_work(g, B=0):
                     tile0 = 0
                 else:
                     tile0 = int(sees[0]) // tpt if sees.size else None
-                u = dict(key_row0=int(cu_k[b]) + kp, keys=min(BLOCK_KEYS, int(uk[b]) - kp), q_row0=int(cu_q[b]),
-                         q_used=int(uq[b]), head_kv=hk, key_pos0=kp, pos_shift=int(uk[b]) - int(uq[b]))
-                want_units.append((u, tile0, n_tiles, lim))
+                u = dict(key_row0=int(cu_k[b]) + kp, keys=min(BLOCK_KEYS, int(uk[b]) - kp), head_kv=hk,
+                         key_pos0=kp if B else 0, pos_shift=int(uk[b]) - int(uq[b]) if B else 0)
+                want_units.append((u, b, tile0, n_tiles, lim))
     assert len(units) == len(want_units)
     by_key = {(u["key_row0"], u["head_kv"]): u for u in units}
     assert len(by_key) == len(units), "a (key block, KV head) unit appears twice"
-    for u, tile0, n_tiles, lim in want_units:
+    for u, b, tile0, n_tiles, lim in want_units:
         got = by_key[(u["key_row0"], u["head_kv"])]
         assert {k: got[k] for k in u} == u
+        if uq[b] == 0:
+            assert got["n_tiles"] == 0  # no row attends the block: dK = dV = 0
+            continue
+        assert segs[got["seg0"]] == (int(cu_q[b]), int(uq[b]))
+        assert got["n_tiles"] == n_tiles - got["tile0"]
         if tile0 is not None:
             assert got["tile0"] == tile0
         else:  # no row sees the block: the unit may skip every tile, and skips no row that would
             assert got["tile0"] <= n_tiles
-            assert not np.any(lim[:got["tile0"] * tpt] > u["key_pos0"])
+            assert not np.any(lim[:got["tile0"] * tpt] > kp_of(u))
         # whatever the start tile, the rows it skips see no key of the block
-        assert not np.any(lim[:min(got["tile0"] * tpt, len(lim))] > u["key_pos0"])
-    tiles = [-(-u["q_used"] // tpt) - u["tile0"] for u in units]
+        assert not np.any(lim[:min(got["tile0"] * tpt, len(lim))] > kp_of(u))
+    tiles = [u["n_tiles"] for u in units]
     assert tiles == sorted(tiles, reverse=True), "dK / dV units not longest first"
-    check_walk(units, w["kv_walk"], SMS, lambda u: kv_cost(u, tpt))
+    check_walk(units, w["kv_walk"], SMS, kv_cost)
     return w
 
 
@@ -245,6 +257,18 @@ def test_random_geometries(seed, B):
     check_work(g, B)
 
 
+@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("B", [0, 5, 128])
+def test_random_geometries_groups_not_dividing_128(seed, B):
+    """GQA groups that do not divide the 128-row tile (g = 3 for 12 query heads over 4 KV
+    heads, ...): a tile folds floor(128 / g) tokens of the g heads."""
+    rng = np.random.default_rng(7200 + seed)
+    hkv = int(rng.choice([1, 2, 4]))
+    group = int(rng.choice([3, 5, 6, 12, 24, 100]))
+    g = W.random_geometry(rng, int(rng.integers(1, 7)), 700, 900, hkv * group, hkv, int(rng.choice([64, 128])))
+    check_work(g, B)
+
+
 def test_more_queries_than_keys_causal():
     """Rows whose key position is negative see nothing: they cost no key block."""
     cu = np.array([0, 300], np.int32)
@@ -273,7 +297,8 @@ def test_capacity_truncates_and_errors():
     geo = [p(a[0]), p(a[1]), p(a[2]), p(a[3]), 4, None, None, None, 0]
 
     def call(block, hq, hkv, d, summ, items, cap, *rest, geometry=geo, grid=SMS, walk_list=0):
-        return lib.gva_plan_inspect(*geometry, block, hq, hkv, d, grid, walk_list, summ, items, cap, None, 0, *rest)
+        return lib.gva_plan_inspect(*geometry, block, hq, hkv, d, grid, walk_list, summ, items, cap, None, 0, *rest,
+                                    None, 0)
     assert call(0, 8, 2, 128, ctypes.byref(s), p(one), 1, None, 0, None, 0) == 0
     assert s.num_work_items == full["num_work_items"] and s.backward_ok == 1
     assert np.array_equal(one[0], full["items"][0]) and np.all(one[1] == -5)
@@ -321,18 +346,21 @@ def _random_ranges(rng, nseg, total_k, disjoint):
 def test_key_range_plans(seed, disjoint):
     """gva_plan_ranges' lists: each range cut into blocks of at most 128 keys in order;
     every item of a segment carries its segment's blocks and key count; FLOPs count the
-    concatenated keys; dK / dV units are the blocks (one per KV head) and exist only when
-    the non-empty ranges are disjoint."""
+    concatenated keys. dK / dV units, for disjoint and overlapping ranges alike: every
+    K/V row some range covers lies in exactly one unit per KV head, no range boundary
+    falls inside a unit, and a unit lists exactly the segments (with rows) whose ranges
+    cover each of its rows, a segment once per covering range of its own."""
+    from collections import Counter
     rng = np.random.default_rng(900 + seed)
     hkv = int(rng.choice([1, 2, 4]))
     g = W.random_geometry(rng, int(rng.integers(1, 6)), 700, 10, hkv * int(rng.choice([1, 2, 8])), hkv, 128)
     total_k = 3000
     ranges = _random_ranges(rng, g.num_segments, total_k, disjoint)
+    if not disjoint and g.num_segments > 0 and ranges[0]:
+        ranges[0].append(ranges[0][0])  # one segment attends a range twice
     w = _lib.inspect_plan(g.cu_q, g.used_q, None, None, g.num_heads_q, g.num_heads_kv, g.head_dim,
                           key_ranges=ranges, total_k=total_k)
-    spans = sorted((st, n) for rr in ranges for st, n in rr if n > 0)
-    overlap = any(a[0] + a[1] > b[0] for a, b in zip(spans, spans[1:]))
-    assert w["backward_ok"] == (not overlap)
+    assert w["backward_ok"]
     blocks, seg_blk0 = [], []
     for rr in ranges:
         seg_blk0.append(len(blocks))
@@ -355,13 +383,62 @@ def test_key_range_plans(seed, disjoint):
             assert (r, it["head_kv"]) not in covered
             covered[(r, it["head_kv"])] = True
     assert len(covered) == int(g.used_q.sum()) * g.num_heads_kv
+
+    # ---- dK / dV units against a row-by-row count of the ranges covering each K/V row
+    tpt = TILE_ROWS // (g.num_heads_q // g.num_heads_kv)
+    cover = [Counter() for _ in range(total_k)]  # K/V row -> {segment: covering ranges}
+    bounds = set()
+    for b, rr in enumerate(ranges):
+        for st, n in rr:
+            if n > 0:
+                bounds |= {st, st + n}
+                for x in range(st, st + n):
+                    cover[x][b] += 1
+    seg_by_row0 = {int(g.cu_q[b]): b for b in range(g.num_segments) if g.used_q[b] > 0}
     units = rec(w["kv_units"], _lib.KV_UNIT_FIELDS)
-    if overlap:
-        assert units == [] and w["num_bwd_items"] == 0
-        return
-    want = sorted((blk[0], blk[1], int(g.cu_q[b]), int(g.used_q[b]), hk)
-                  for b in range(g.num_segments)
-                  for blk in blocks[seg_blk0[b]:(seg_blk0[b + 1] if b + 1 < len(seg_blk0) else len(blocks))]
-                  for hk in range(g.num_heads_kv))
-    got = sorted((u["key_row0"], u["keys"], u["q_row0"], u["q_used"], u["head_kv"]) for u in units)
-    assert got == want
+    segs = [tuple(int(v) for v in r) for r in w["kv_segs"]]
+    seen = Counter()
+    for u in units:
+        assert 1 <= u["keys"] <= BLOCK_KEYS and u["tile0"] == 0
+        assert not any(u["key_row0"] < x < u["key_row0"] + u["keys"] for x in bounds), "a unit crosses a boundary"
+        # the unit's segments: consecutive SegRefs whose tiles add up to n_tiles
+        listed, tiles, i = Counter(), 0, u["seg0"]
+        while tiles < u["n_tiles"]:
+            q_row0, q_used = segs[i]
+            listed[seg_by_row0[q_row0]] += 1
+            assert q_used == int(g.used_q[seg_by_row0[q_row0]])
+            tiles += -(-q_used // tpt)
+            i += 1
+        assert tiles == u["n_tiles"]
+        for x in range(u["key_row0"], u["key_row0"] + u["keys"]):
+            want = Counter({b: m for b, m in cover[x].items() if g.used_q[b] > 0})
+            assert listed == want, (x, listed, want)
+            seen[(x, u["head_kv"])] += 1
+    rows = [x for x in range(total_k) if cover[x]]
+    assert len(seen) == len(rows) * g.num_heads_kv and all(c == 1 for c in seen.values())
+    tiles = [u["n_tiles"] for u in units]
+    assert tiles == sorted(tiles, reverse=True)
+
+
+def test_plan_building_stays_fast_on_a_large_geometry():
+    """The host plan for half a million forward items (plus about a million dQ items and
+    the dK / dV units) is built in well under a few seconds: the balancer's passes cost
+    O(n log n) in the list lengths, not O(n^2)."""
+    import ctypes
+    import time
+    rng = np.random.default_rng(0)
+    b = 64
+    uq = rng.integers(1, 262144, size=b)
+    cu_q = np.concatenate([[0], np.cumsum(np.full(b, 262144))])
+    uk = rng.integers(1, 4096, size=b)
+    cu_k = np.concatenate([[0], np.cumsum(np.full(b, 4096))])
+    a = [_lib._i32(x) for x in (cu_q, uq, cu_k, uk)]
+    p = lambda x: x.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))  # noqa: E731
+    lib = _lib.load_library()
+    summ = _lib.WorkSummary()
+    t0 = time.perf_counter()
+    st = lib.gva_plan_inspect(p(a[0]), p(a[1]), p(a[2]), p(a[3]), b, None, None, None, 0, 0, 16, 16, 128, SMS, 0,
+                              ctypes.byref(summ), None, 0, None, 0, None, 0, None, 0, None, 0)
+    took = time.perf_counter() - t0
+    assert st == 0 and summ.num_work_items > 500_000
+    assert took < 5.0, f"plan inspection took {took:.2f} s"

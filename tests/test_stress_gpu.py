@@ -35,11 +35,28 @@ def _case(seed):
     return g, block, out_dtype
 
 
+ODD_SEEDS = range(6000, 6060)
+
+
+def _case_odd_group(seed):
+    """As _case, with a GQA group that does not divide the 128-row tile."""
+    rng = np.random.default_rng(seed)
+    hkv = int(rng.choice([1, 2]))
+    group = int(rng.choice([3, 5, 6, 7, 12, 24, 48, 96]))
+    d = int(rng.choice([64, 128]))
+    g = W.random_geometry(rng, int(rng.integers(1, 6)), 400, 600, hkv * group, hkv, d)
+    block = 0 if rng.random() < 0.5 else int(rng.integers(1, 300))
+    out_dtype = torch.float32 if rng.random() < 0.3 else torch.bfloat16
+    return g, block, out_dtype
+
+
 def _check_forward(g, o, l, o_ref, l_ref):
-    """O within O_TOL of the oracle, plus, for a bf16 output, that format's own rounding
-    of the exact value (half an ulp, at most 2^-9 relative): few-key rows average a
-    handful of N(0, 1) values, so |O| reaches 2-4, where half a bf16 ulp alone is 4-8e-3."""
-    rel = 2.0 ** -9 if o.dtype == torch.bfloat16 else 0.0
+    """O within O_TOL of the oracle. The one exception is a bf16 output element whose
+    exact value has |O_ref| >= 4: there half a bf16 ulp (8 significant bits, up to
+    2^-8 |O_ref|, at least 1.56e-2) exceeds O_TOL by itself, so that element may also
+    be off by the format's own rounding of the exact value. Few-key rows average a
+    handful of N(0, 1) values, so such outputs do occur in the sweep."""
+    rel = 2.0 ** -8 if o.dtype == torch.bfloat16 else 0.0
     o = o.float().cpu().numpy().astype(np.float64)
     l = l.cpu().numpy().astype(np.float64)
     gap = W.gap_rows(g.cu_q, g.used_q)
@@ -55,7 +72,9 @@ def _check_forward(g, o, l, o_ref, l_ref):
         o_live = o.transpose(1, 0, 2)[live]
         ref_live = o_ref.transpose(1, 0, 2)[live]
         assert np.all(np.isfinite(o_live))
-        assert np.all(np.abs(o_live - ref_live) <= O_TOL + rel * np.abs(ref_live))
+        allow = O_TOL + np.where(np.abs(ref_live) >= 4.0, rel * np.abs(ref_live), 0.0)
+        err = np.abs(o_live - ref_live)
+        assert np.all(err <= allow), f"max |O err| = {err.max():.3e} (over the bound: {int((err > allow).sum())})"
 
 
 @pytest.mark.parametrize("seed", SEEDS)
@@ -71,6 +90,31 @@ def test_random_forward(seed):
                                                 out=np.full(qn.shape, FILL),
                                                 lse=np.full((g.num_heads_q, g.total_q), FILL), causal_block=block)
     _check_forward(g, o, l, o_ref, l_ref)
+
+
+@pytest.mark.parametrize("seed", ODD_SEEDS)
+def test_random_forward_groups_not_dividing_128(seed):
+    g, block, out_dtype = _case_odd_group(seed)
+    q, k, v = W.make_qkv(g, seed, gap_fill=float("nan"))
+    plan = gva.Plan.from_geometry(g, causal_block=block)
+    o, l = W.make_outputs(g, FILL, device="cuda", out_dtype=out_dtype)
+    gva.forward(plan, q.cuda(), k.cuda(), v.cuda(), o, l)
+    gva.device_status(plan)
+    qn, kn, vn = (t.float().numpy() for t in (q, k, v))
+    o_ref, l_ref = gva_oracle.attention_forward(qn, kn, vn, g.cu_q, g.used_q, g.cu_k, g.used_k,
+                                                out=np.full(qn.shape, FILL),
+                                                lse=np.full((g.num_heads_q, g.total_q), FILL), causal_block=block)
+    _check_forward(g, o, l, o_ref, l_ref)
+
+
+@pytest.mark.parametrize("seed", ODD_SEEDS[::2])
+def test_random_backward_groups_not_dividing_128(seed):
+    """Bounds as in test_random_backward."""
+    g, block, _ = _case_odd_group(seed)
+    q, k, v = W.make_qkv(g, seed, gap_fill=float("nan"))
+    do = _make_dout(g, seed)
+    check_backward(g, gpu_backward(g, q, k, v, do, causal_block=block),
+                   oracle_backward(g, q, k, v, do, causal_block=block), MAX_REL, 2 * RMS_REL, 1e-5)
 
 
 @pytest.mark.parametrize("seed", SEEDS[::2])
@@ -145,14 +189,16 @@ def test_random_key_ranges_forward(seed):
     _check_forward(g, o, l, o_ref, l_ref)
 
 
+@pytest.mark.parametrize("disjoint", [True, False])
 @pytest.mark.parametrize("seed", SEEDS[1::3])
-def test_random_key_ranges_backward(seed):
-    """Disjoint key ranges per segment: gradients of every covered key and used row;
-    keys no range covers stay untouched. Bounds as in test_random_backward."""
+def test_random_key_ranges_backward(seed, disjoint):
+    """Key ranges per segment, disjoint or overlapping freely (a shared K/V row sums the
+    contributions of every range that covers it): gradients of every covered key and used
+    row; keys no range covers stay untouched. Bounds as in test_random_backward."""
     from test_backward_gpu import _close
     g, _, _ = _case(seed)
     rng = np.random.default_rng(seed + 1)
-    ranges, total_k, covered, q, k, v = _range_inputs(rng, g, seed, disjoint=True)
+    ranges, total_k, covered, q, k, v = _range_inputs(rng, g, seed, disjoint=disjoint)
     do = _make_dout(g, seed)
     plan = gva.Plan.from_ranges(g.cu_q, g.used_q, ranges, total_k, g.num_heads_q, g.num_heads_kv, g.head_dim)
     dq, dk, dv = (t.float().cpu().numpy().astype(np.float64) for t in gpu_backward(g, q, k, v, do, plan=plan))
