@@ -133,17 +133,6 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint64_t q_desc, uint6
   }
 }
 
-// The same product over keys 64h .. 64h + 63 only (A columns 32h .. 32h + 31, B rows
-// 64h .. 64h + 63): O += P V in two halves, each issued once its half of P is in TMEM.
-template <int D>
-__device__ __forceinline__ void issue_pv_part(uint32_t tmem_o, uint32_t tmem_p, uint64_t v_desc, int h,
-                                              uint32_t accumulate) {
-  constexpr uint32_t idesc = make_idesc_bf16(kTileRows, D, true);
-#pragma unroll
-  for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
-    umma_bf16_ts(tmem_o, tmem_p + kk * 8, v_desc + ((kk * 16 * 128) >> 4), idesc, kk > 4 * h ? 1u : accumulate);
-}
-
 // D[128 x D] (+)= A[128 x 128] B[128 x D] with A (bf16 pairs) in TMEM and B MN-major in
 // shared memory (O += P V in the forward; dQ += dS K, dV += P^T dO, dK += dS^T Q).
 template <int D>

@@ -66,7 +66,7 @@ struct Cfg {
 struct Ctrl {
   uint64_t q_full, q_empty;
   uint64_t kv_full[10], kv_empty[10];
-  uint64_t s_full[2], p_full[2][2], o_full[2];  // p_full[t][h]: P of keys 64h .. 64h+63 of tile t
+  uint64_t s_full[2], p_full[2], o_full[2];
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -100,8 +100,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&ctrl.s_full[t], 1);
-      mbar_init(&ctrl.p_full[t][0], 128);
-      mbar_init(&ctrl.p_full[t][1], 128);
+      mbar_init(&ctrl.p_full[t], 128);
       mbar_init(&ctrl.o_full[t], 1);
     }
     mbar_init(&ctrl.mma_done, 1);
@@ -218,15 +217,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t vseq = 2 * (blk + j) + 1;
           kseq = vseq + 1;  // K_{j+1}
           ok = wait_bar(&ctrl.kv_full[vseq % NS], (vseq / NS) & 1, abort_flag, p.error_flag);
-          if (ok) ok = wait_bar(&ctrl.p_full[0][0], pc0 & 1, abort_flag, p.error_flag);
-          if (!ok) break;
-          tcgen05_fence_after();
-          issue_pv_part<D>(tmem + col_o(0), tmem + col_s(0), v_desc(vseq % NS), 0, j > 0);
-          ok = wait_bar(&ctrl.p_full[0][1], pc0 & 1, abort_flag, p.error_flag);
+          if (ok) ok = wait_bar(&ctrl.p_full[0], pc0 & 1, abort_flag, p.error_flag);
           if (!ok) break;
           ++pc0;
           tcgen05_fence_after();
-          issue_pv_part<D>(tmem + col_o(0), tmem + col_s(0), v_desc(vseq % NS), 1, 1u);
+          issue_pv<D>(tmem + col_o(0), tmem + col_s(0), v_desc(vseq % NS), j > 0);
           if (!more) umma_commit(&ctrl.o_full[0]);
           if (more) {
             ok = wait_bar(&ctrl.kv_full[kseq % NS], (kseq / NS) & 1, abort_flag, p.error_flag);
@@ -236,15 +231,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_commit(&ctrl.s_full[0]);
           }
           if (two) {
-            ok = wait_bar(&ctrl.p_full[1][0], pc1 & 1, abort_flag, p.error_flag);
-            if (!ok) break;
-            tcgen05_fence_after();
-            issue_pv_part<D>(tmem + col_o(1), tmem + col_s(1), v_desc(vseq % NS), 0, j > 0);
-            ok = wait_bar(&ctrl.p_full[1][1], pc1 & 1, abort_flag, p.error_flag);
+            ok = wait_bar(&ctrl.p_full[1], pc1 & 1, abort_flag, p.error_flag);
             if (!ok) break;
             ++pc1;
             tcgen05_fence_after();
-            issue_pv_part<D>(tmem + col_o(1), tmem + col_s(1), v_desc(vseq % NS), 1, 1u);
+            issue_pv<D>(tmem + col_o(1), tmem + col_s(1), v_desc(vseq % NS), j > 0);
             if (!more) umma_commit(&ctrl.o_full[1]);
             if (more) {
               issue_qk<D>(tmem + col_s(1), q_desc[1], k_desc(kseq % NS));
@@ -312,8 +303,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int bc = p.causal_block;
         row_limit = pos < 0 ? 0 : min(it.k_len, (pos / bc + 1) * bc);
       }
+      const int row_keys = kCausal ? row_limit : it.k_len;
       float m_used = -CUDART_INF_F;
-      float l = 0.0f, lp = 0.0f;  // row sums of the unrounded and of the bf16-rounded P
+      // Row sums of the unrounded P (for the LSE) and of the bf16-rounded P that the PV
+      // product multiplies (for O). When a row's weight sits on a handful of keys, each
+      // key's rounding stays in O unless O is divided by the rounded sum (then its
+      // weights sum to one). A warp with a row that sees at most one block of keys sums
+      // both (uniform over the warp); other warps divide by l, which adds at most 2^-9
+      // |O| and averages over their keys.
+      float l = 0.0f, lp = 0.0f;
+      const bool few_keys = __any_sync(0xffffffffu, row_keys <= kBlockKeys);
       // used keys of each block (>= 1), fetched one block ahead so the load's latency
       // hides behind the wait for the scores
       int rem_next = load_block(p.blocks, it.blk0).valid;
@@ -372,25 +371,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_used = m_new;
         }
         // P = 2^(s*c - m) as bf16 pairs (column i holds keys 2i, 2i+1), stored to the
-        // first 64 columns of S_t in 16-column pieces as they are ready. Each key half is
-        // handed to the tensor core as soon as it is stored, so the PV product of keys
-        // 0-63 runs while keys 64-127 are being exponentiated.
+        // first 64 columns of S_t in 16-column pieces as they are ready.
         const uint64_t c2 = f32x2(c, c);
         // A row that has seen no key yet (block-causal only) has m = -inf and all P = 0.
         const float m_ref = (kCausal && m_used == -CUDART_INF_F) ? 0.0f : m_used;
         const uint64_t neg_m2 = f32x2(-m_ref, -m_ref);
-        // Two row sums. lp adds the same bf16-rounded P that the PV product multiplies,
-        // so the weights of O = sum_j P_j V_j / lp sum to one and O stays a convex
-        // combination of the V rows (summing the unrounded P instead leaves each
-        // weight's rounding uncompensated, which rows with a handful of keys do not
-        // average out). l adds the unrounded P, for the LSE: ln of the rounded sum
-        // would be off by up to 2^-9 when one key dominates.
-        float l0 = 0.0f, l1 = 0.0f, l2 = 0.0f, l3 = 0.0f;
         uint64_t acc0 = f32x2(0.0f, 0.0f), acc1 = acc0;
+        if (!few_keys) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int q16 = 2 * h; q16 < 2 * h + 2; ++q16) {
+          for (int q16 = 0; q16 < 4; ++q16) {
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -400,61 +389,72 @@ __global__ void __launch_bounds__(kThreads, 1)
               a = ex2_approx(a);
               b = ex2_approx(b);
               pk[i] = pack_bf16x2(a, b);
-              if (i & 1) {
-                add_bf16x2_f32(l2, l3, pk[i]);
-                acc1 = fadd2(acc1, f32x2(a, b));
-              } else {
-                add_bf16x2_f32(l0, l1, pk[i]);
-                acc0 = fadd2(acc0, f32x2(a, b));
-              }
+              if (i & 1) acc1 = fadd2(acc1, f32x2(a, b));
+              else acc0 = fadd2(acc0, f32x2(a, b));
             }
             tmem_st16(s_addr + q16 * 16, pk);
           }
-          if (h == 0) {
-            // Before the first PV product of this block reads O or V:
-            if (resc) {
-              // O rescaled. Complete: the S MMA just waited for was issued after this
-              // tile's previous PV.
-              // (16 columns at a time: the other key half's scores are still live)
-#pragma unroll 1
-              for (int ch = 0; ch < D / 16; ++ch) {
-                uint32_t o[16];
-                tmem_ld16_sync(o_addr + ch * 16, o);
+        } else {
+          float r0 = 0.0f, r1 = 0.0f;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f_resc);
-                tmem_st16(o_addr + ch * 16, o);
-              }
+          for (int q16 = 0; q16 < 4; ++q16) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int k2 = q16 * 32 + 2 * i;
+              float a, b;
+              f32x2_split(ffma2(f32x2(s[k2], s[k2 + 1]), c2, neg_m2), a, b);
+              a = ex2_approx(a);
+              b = ex2_approx(b);
+              pk[i] = pack_bf16x2(a, b);
+              // the two rounded values as fp32: the low one moves up 16 bits, the high
+              // one is already in place
+              r0 += __uint_as_float(pk[i] << 16);
+              r1 += __uint_as_float(pk[i] & 0xFFFF0000u);
+              if (i & 1) acc1 = fadd2(acc1, f32x2(a, b));
+              else acc0 = fadd2(acc0, f32x2(a, b));
             }
-            if (t == 0 && rem < kBlockKeys) {
-              // Keys past the used length in this V block (gap, padding or another
-              // segment) get P = 0, but 0 * NaN would still poison O: zero those rows
-              // of the staged V block before the PV MMA reads it.
-              const uint32_t vseq = 2 * (vb + j) + 1;  // ring sequence number of V_j
-              ok = __all_sync(0xffffffffu,
-                              wait_bar(&ctrl.kv_full[vseq % NS], (vseq / NS) & 1, abort_flag, p.error_flag));
-              if (!ok) break;
-              uint8_t* vbase = sKV + (vseq % NS) * C::kKVBytes;
-              const int n16 = (kBlockKeys - rem) * C::kChunks * 8;  // 16-byte pieces to clear
-              for (int i = row; i < n16; i += 128) {
-                const int r = rem + i / (C::kChunks * 8);
-                const int rest = i % (C::kChunks * 8);
-                *reinterpret_cast<uint4*>(vbase + (rest / 8) * C::kKVChunkBytes + r * 128 + (rest % 8) * 16) =
-                    make_uint4(0, 0, 0, 0);
-              }
-              fence_proxy_async_smem();
-            }
+            tmem_st16(s_addr + q16 * 16, pk);
           }
-          tmem_wait_st();
-          tcgen05_fence_before();
-          mbar_arrive(&ctrl.p_full[t][h]);
+          lp += r0 + r1;
         }
-        if (!ok) break;
-        lp += (l0 + l1) + (l2 + l3);
         {
           float la, lb;
           f32x2_split(fadd2(acc0, acc1), la, lb);
           l += la + lb;
         }
+        if (resc) {
+          // Complete: the S MMA just waited for was issued after this tile's previous PV.
+#pragma unroll
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t o[32];
+            tmem_ld32_sync(o_addr + ch * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f_resc);
+            tmem_st32(o_addr + ch * 32, o);
+          }
+        }
+        if (t == 0 && rem < kBlockKeys) {
+          // Keys past the used length in this V block (gap, padding or another
+          // segment) get P = 0, but 0 * NaN would still poison O: zero those rows of
+          // the staged V block before the PV MMA reads it.
+          const uint32_t vseq = 2 * (vb + j) + 1;  // ring sequence number of V_j
+          ok = __all_sync(0xffffffffu,
+                          wait_bar(&ctrl.kv_full[vseq % NS], (vseq / NS) & 1, abort_flag, p.error_flag));
+          if (!ok) break;
+          uint8_t* vbase = sKV + (vseq % NS) * C::kKVBytes;
+          const int n16 = (kBlockKeys - rem) * C::kChunks * 8;  // 16-byte pieces to clear
+          for (int i = row; i < n16; i += 128) {
+            const int r = rem + i / (C::kChunks * 8);
+            const int rest = i % (C::kChunks * 8);
+            *reinterpret_cast<uint4*>(vbase + (rest / 8) * C::kKVChunkBytes + r * 128 + (rest % 8) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        tmem_wait_st();
+        tcgen05_fence_before();
+        mbar_arrive(&ctrl.p_full[t]);
       }
       if (!ok) break;
       if (t == 0) vb += nblk;
@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++oc;
       tcgen05_fence_after();
       // l > 0 for every row with a key; a block-causal row that sees none gets 0 / -inf.
-      const float inv_l = l > 0.0f ? 1.0f / lp : 0.0f;
+      const float inv_l = l > 0.0f ? 1.0f / (few_keys ? lp : l) : 0.0f;
       const float lse_val = l > 0.0f ? (m_used + log2f(l)) * kLn2 : -CUDART_INF_F;
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {

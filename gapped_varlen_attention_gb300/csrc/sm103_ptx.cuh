@@ -124,17 +124,6 @@ __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]
       : "memory");
 }
 
-// 16 consecutive 32-bit columns of the thread's lane, then wait for completion.
-__device__ __forceinline__ void tmem_ld16_sync(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : GVA_R8(0), GVA_R8(8)
-      : "r"(taddr)
-      : "memory");
-}
-
 // 128 consecutive 32-bit columns of the thread's lane, then wait for completion.
 __device__ __forceinline__ void tmem_ld128_sync(uint32_t taddr, uint32_t (&r)[128]) {
   asm volatile(
@@ -368,17 +357,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
-}
-
-// lo += the bf16 in bits 0-15 of p, hi += the bf16 in bits 16-31: each widened exactly
-// and added with one fp32 rounding (the mixed-precision add of the sm_100 family).
-__device__ __forceinline__ void add_bf16x2_f32(float& lo, float& hi, uint32_t p) {
-  asm("{\n\t.reg .b16 a, b;\n\t"
-      "mov.b32 {a, b}, %2;\n\t"
-      "add.rn.f32.bf16 %0, a, %0;\n\t"
-      "add.rn.f32.bf16 %1, b, %1;\n\t}"
-      : "+f"(lo), "+f"(hi)
-      : "r"(p));
 }
 
 }  // namespace gva

@@ -1,9 +1,11 @@
 """Randomised parity sweep of the forward and the backward against the FP64 oracle.
 
 Each case draws a gapped geometry (empty segments, ragged tails, NaN in every gap row),
-a head layout (GQA group 1 to 16, d = 64 or 128), a mask (none, or block-causal with a
-random frame length) and an output dtype, and compares every used element. The
-feature tests pin each case family on its own; this sweep covers their combinations."""
+a head layout (GQA group 1 to 16, or a group that does not divide the 128-row tile,
+d = 64 or 128), a mask (none, or block-causal with a random frame length) and an output
+dtype, and compares every used element. Key-range cases draw ranges that are disjoint
+or overlap freely. The feature tests pin each case family on its own; this sweep
+covers their combinations."""
 import numpy as np
 import pytest
 import torch
