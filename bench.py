@@ -500,7 +500,7 @@ def time_steps(fn, steps: int, stream, flush=None, per_step=None) -> float:
         flush()
         # keep the device busy (outside the events) while the host issues the step, so
         # that a short step is timed from its first launch, not from the host's call
-        torch.cuda._sleep(100000)
+        torch.cuda._sleep(200000)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         fn()
