@@ -331,31 +331,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_st();
         }
         float s[128];
+        float mx;  // the row's largest score in this block: the load returns it
         {
           uint32_t raw[128];
-          tmem_ld128_sync(s_addr, raw);
+          mx = tmem_ld128_max_sync(s_addr, raw);
 #pragma unroll
           for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(raw[i]);
         }
         if constexpr (kCausal) {
           // Diagonal blocks: keys at or past the row's limit leave the softmax (the
-          // limit differs per row, so this is done on the registers).
+          // limit differs per row, so this is done on the registers, and the max taken
+          // again over what is left).
           const int lim = row_limit - j * kBlockKeys;
           if (__any_sync(0xffffffffu, lim < kBlockKeys)) {
 #pragma unroll
             for (int i = 0; i < 128; ++i) s[i] = (i < lim) ? s[i] : -CUDART_INF_F;
+            float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
+            float mx2 = fmax3(s[6], s[7], s[8]), mx3 = fmax3(s[9], s[10], s[11]);
+#pragma unroll
+            for (int i = 12; i < 124; i += 8) {
+              mx0 = fmax3(mx0, s[i], s[i + 1]);
+              mx1 = fmax3(mx1, s[i + 2], s[i + 3]);
+              mx2 = fmax3(mx2, s[i + 4], s[i + 5]);
+              mx3 = fmax3(mx3, s[i + 6], s[i + 7]);
+            }
+            mx = fmax3(fmax3(mx0, mx1, s[124]), fmax3(mx2, mx3, s[125]), fmaxf(s[126], s[127]));
           }
         }
-        float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
-        float mx2 = fmax3(s[6], s[7], s[8]), mx3 = fmax3(s[9], s[10], s[11]);
-#pragma unroll
-        for (int i = 12; i < 124; i += 8) {
-          mx0 = fmax3(mx0, s[i], s[i + 1]);
-          mx1 = fmax3(mx1, s[i + 2], s[i + 3]);
-          mx2 = fmax3(mx2, s[i + 4], s[i + 5]);
-          mx3 = fmax3(mx3, s[i + 6], s[i + 7]);
-        }
-        const float mx = fmax3(fmax3(mx0, mx1, s[124]), fmax3(mx2, mx3, s[125]), fmaxf(s[126], s[127]));
         const float m_new = fmaxf(m_used, mx * c);
         // O is rescaled when the row max grows by more than the threshold; the O update
         // itself comes after P is stored, when fewer registers are live.

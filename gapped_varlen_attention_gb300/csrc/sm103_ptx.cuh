@@ -143,6 +143,29 @@ __device__ __forceinline__ void tmem_ld128_sync(uint32_t taddr, uint32_t (&r)[12
       : "memory");
 }
 
+// The same load, which also returns the largest of the thread's 128 values (the
+// tcgen05.ld reduction form of sm_103a: max over the loaded columns, exact).
+__device__ __forceinline__ float tmem_ld128_max_sync(uint32_t taddr, uint32_t (&r)[128]) {
+  float m;
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x128.max.f32 {"
+      "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,"
+      "%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+      "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,"
+      "%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,"
+      "%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127"
+      "}, %128, [%129];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : GVA_R8(0), GVA_R8(8), GVA_R8(16), GVA_R8(24), GVA_R8(32), GVA_R8(40), GVA_R8(48), GVA_R8(56), GVA_R8(64), GVA_R8(72), GVA_R8(80), GVA_R8(88), GVA_R8(96), GVA_R8(104), GVA_R8(112), GVA_R8(120),
+        "=f"(m)
+      : "r"(taddr)
+      : "memory");
+  return m;
+}
+
 #define GVA_RA8(a, i) "=r"(a[i + 0]), "=r"(a[i + 1]), "=r"(a[i + 2]), "=r"(a[i + 3]), "=r"(a[i + 4]), \
                       "=r"(a[i + 5]), "=r"(a[i + 6]), "=r"(a[i + 7])
 
