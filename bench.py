@@ -373,12 +373,38 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def code_only(text: str) -> str:
+    """C / C++ / CUDA source without its comments, blank lines and trailing spaces
+    (string and character literals kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        ch = text[i]
+        if ch in "\"'":
+            j = i + 1
+            while j < n and text[j] != ch:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(ch)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
+
+
 def kernel_source_hash(kernel: str) -> str:
-    """sha256[:16] over the kernel's sources (its .cu file, then the headers it includes)."""
+    """sha256[:16] over the code of the kernel's sources (its .cu file, then the headers
+    it includes), comments left out: a comment edit leaves a recorded capture valid."""
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(CSRC, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(CSRC, name), encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode())
+        h.update(b"\0")
     return h.hexdigest()[:16]
 
 

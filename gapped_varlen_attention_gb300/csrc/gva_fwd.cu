@@ -13,8 +13,9 @@
 //   warp 1      TMEM allocator and MMA issuer (one thread): S_t = Q_t K^T into TMEM,
 //               O_t += P_t V with P_t read from TMEM (tcgen05 "A from TMEM" form).
 //   warps 2-5   softmax + epilogue of Q tile 0; warps 6-9 of Q tile 1. One thread owns
-//               one tile row (= one TMEM lane), so the row max and row sum are plain
-//               register reductions with no shuffles or shared memory.
+//               one tile row (= one TMEM lane): the row max comes with the row's TMEM
+//               load (its max-reducing form) and the row sum is a register reduction,
+//               with no shuffles or shared memory.
 // A work item is (segment, KV head, 2 x 128 folded rows): the g = Hq/Hkv query heads
 // of one KV head are folded into the tile's rows (128/g tokens x g heads), so each K/V
 // block feeds 256 rows. Two tiles ping-pong: while the softmax warps of one tile work,

@@ -119,3 +119,21 @@ def test_recorded_traffic_needs_the_current_kernel_sources(tmp_path, monkeypatch
     rec.write_text(json.dumps({"records": {"long_replay": {"kernel": "gva_fwd_kernel", "source_sha16": "0" * 16,
                                                            "dram_bytes_per_launch": 3.1e9}}}))
     assert bench.recorded_traffic("long_replay", "gva_fwd_kernel") is None  # taken on other sources
+
+
+def test_kernel_hash_covers_code_not_comments(tmp_path, monkeypatch):
+    """A comment edit keeps the hash (and so a recorded capture) valid; a code edit does
+    not. String literals that hold comment markers are code."""
+    src = 'int f() { return 1; }  // one\n/* block\n comment */\nconst char* s = "//x/*y*/";\n'
+    assert bench.code_only(src) == 'int f() { return 1; }\nconst char* s = "//x/*y*/";'
+    csrc = tmp_path / "csrc"
+    csrc.mkdir()
+    names = bench.KERNEL_SOURCES["gva_fwd_kernel"]
+    for n in names:
+        (csrc / n).write_text(src)
+    monkeypatch.setattr(bench, "CSRC", str(csrc))
+    h0 = bench.kernel_source_hash("gva_fwd_kernel")
+    (csrc / names[0]).write_text(src.replace("// one", "// one, reworded\n// and a second line"))
+    assert bench.kernel_source_hash("gva_fwd_kernel") == h0
+    (csrc / names[0]).write_text(src.replace("return 1", "return 2"))
+    assert bench.kernel_source_hash("gva_fwd_kernel") != h0
