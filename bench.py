@@ -564,9 +564,13 @@ class E2EPipeline:
         self.s_in, self.s_out = torch.cuda.Stream(), torch.cuda.Stream()
 
     def run(self, steps: int) -> float:
-        """Device milliseconds for `steps` end-to-end steps."""
+        """Device milliseconds for `steps` end-to-end steps. `self.compute_ms` receives
+        each step's own time on the compute stream (from the end of its waits for its
+        input copy and its buffers to the end of the step), so that the region's time
+        splits into compute under concurrent copies and what the copies add."""
         st = self.stream
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        bracket = []
         start.record(st)
         self.s_in.wait_stream(st)
         self.s_out.wait_stream(st)
@@ -584,7 +588,11 @@ class E2EPipeline:
             st.wait_event(loaded)
             if copied[b] is not None:
                 st.wait_event(copied[b])
+            a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
             self.wl.step(self.d_in[b], self.d_out[b])
+            z.record(st)
+            bracket.append((a, z))
             computed[b] = torch.cuda.Event()
             computed[b].record(st)
             with torch.cuda.stream(self.s_out):
@@ -597,6 +605,7 @@ class E2EPipeline:
         st.wait_stream(self.s_out)
         end.record(st)
         end.synchronize()
+        self.compute_ms = [a.elapsed_time(z) for a, z in bracket]
         return start.elapsed_time(end)
 
     def copy_rates(self, reps: int = 3):
@@ -799,12 +808,17 @@ def measure(wl, steps: int, warmup: int, e2e_steps: int, stream, clock_index: in
     e2e_run.run(1)
     torch.cuda.synchronize()
     barrier()
-    e2e_ms = e2e_run.run(e2e_steps) / e2e_steps
+    with ClockSampler(clock_index) as e2e_clocks:
+        e2e_clocks.wait_samples(1, 5.0, work=lambda: (e2e_run.run(1), torch.cuda.synchronize()))
+        e2e_ms = e2e_run.run(e2e_steps) / e2e_steps
+    e2e_compute_ms = float(np.mean(e2e_run.compute_ms))
     barrier()
     copy = e2e_run.copy_rates()
     del e2e_run
     return {"ms_step": ms / steps, "med_ms": float(np.median(step_ms)), "dom_ms": dom_ms, "dom_launches": n_dom,
-            "e2e_ms": e2e_ms, "copy": copy, "clocks": {**clocks.summary(), "window": window},
+            "e2e_ms": e2e_ms, "e2e_steps": e2e_steps, "e2e_compute_ms": e2e_compute_ms,
+            "e2e_clocks": e2e_clocks.summary(),
+            "copy": copy, "clocks": {**clocks.summary(), "window": window},
             "same_size_copy_gbs": same_size_copy_gbs, "l2_flushed": flush is not None}
 
 
@@ -848,10 +862,18 @@ def e2e_of(wl, r, world):
     return {"value": round(job_rate(world, wl.work, r["e2e_ms"], wl.scale), 3), "unit": wl.unit,
             "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo), "ms_per_step": round(r["e2e_ms"], 4),
             "copy_gbs": r["copy"],
+            "steps": r["e2e_steps"],
+            "compute_ms_per_step": round(r["e2e_compute_ms"], 4),
+            "resident_ms_per_step": round(r["ms_step"], 4),
+            "clocks": r["e2e_clocks"],
             "copies": "pinned host buffers; every step copies its inputs in and its results out: the used rows of "
                       "each [rows, heads, d] tensor (gap rows are neither inputs nor results) and whole LSE-shaped "
                       "tensors; two device buffer sets and two copy streams overlap step i+1's input copy and step "
-                      "i-1's result copy with step i. copy_gbs: the same copies run alone on this box"}
+                      "i-1's result copy with step i. copy_gbs: the same copies run alone on this box. "
+                      "compute_ms_per_step: each step's own time on the compute stream inside this region (the "
+                      "copies of other steps running beside it), against resident_ms_per_step, the same step "
+                      "with no copies; the first step's input copy and the last step's result copy have no step to "
+                      "hide behind, so they add (h2d_ms + d2h_ms) / steps per step; clocks: sampled during this region"}
 
 
 def main():
