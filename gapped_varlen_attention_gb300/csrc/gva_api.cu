@@ -746,11 +746,14 @@ gva_status gva_forward(gva_plan_t plan, const void* q, const void* k, const void
   if (dev != plan->device)
     return fail(GVA_ERR_INVALID_ARG, "the plan was built on device %d, the current device is %d", plan->device, dev);
   const int32_t tokens_per_tile = gva::kTileRows / plan->group;
-  CUtensorMap mq, mk, mv;
+  // bf16 output leaves full tiles through TMA stores, over a map laid out like Q's
+  const bool out_tma = out_dtype == GVA_BF16;
+  const void* o_key = out_tma ? out : nullptr;
+  CUtensorMap mq, mk, mv, mo;
   {
     std::lock_guard<std::mutex> lock(plan->map_mutex);
     MapCache& c = plan->fwd_maps;
-    if (!(c.valid && c.ptr[0] == q && c.ptr[1] == k && c.ptr[2] == v)) {
+    if (!(c.valid && c.ptr[0] == q && c.ptr[1] == k && c.ptr[2] == v && c.ptr[3] == o_key)) {
       c.valid = false;
       gva_status s;
       const int64_t krows = has_keys ? plan->total_k : 1;
@@ -761,14 +764,19 @@ gva_status gva_forward(gva_plan_t plan, const void* q, const void* k, const void
         return s;
       if ((s = make_map(&c.map[2], v, krows, plan->num_heads_kv, plan->head_dim, gva::kBlockKeys, 1, "V")) != GVA_OK)
         return s;
+      if (out_tma && (s = make_map(&c.map[3], out, plan->total_q, plan->num_heads_q, plan->head_dim,
+                                   tokens_per_tile, plan->group, "O")) != GVA_OK)
+        return s;
       c.ptr[0] = q;
       c.ptr[1] = k;
       c.ptr[2] = v;
+      c.ptr[3] = o_key;
       c.valid = true;
     }
     mq = c.map[0];
     mk = c.map[1];
     mv = c.map[2];
+    mo = out_tma ? c.map[3] : c.map[0];
   }
   const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(plan->head_dim));
   gva::FwdParams prm{};
@@ -777,6 +785,7 @@ gva_status gva_forward(gva_plan_t plan, const void* q, const void* k, const void
   prm.num_items = plan->num_item_slots;
   prm.out = out;
   prm.out_wide = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
+  prm.out_tma = out_tma ? 1 : 0;
   prm.lse = lse;
   prm.total_q = plan->total_q;
   prm.num_heads_q = plan->num_heads_q;
@@ -785,7 +794,7 @@ gva_status gva_forward(gva_plan_t plan, const void* q, const void* k, const void
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.causal_block = plan->causal_block;
   prm.error_flag = plan->d_error;
-  e = gva::launch_forward(plan->head_dim, out_dtype == GVA_FP32, prm, mq, mk, mv, plan->grid, stream);
+  e = gva::launch_forward(plan->head_dim, out_dtype == GVA_FP32, prm, mq, mk, mv, mo, plan->grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launching the forward kernel");
   return ok();
 }

@@ -21,6 +21,11 @@
 // block feeds 256 rows. Two tiles ping-pong: while the softmax warps of one tile work,
 // the tensor core runs the other tile's PV and next QK^T.
 //
+// The epilogue of a full tile with bf16 output stages O in shared memory (64 columns at
+// a time, in the 128-byte-swizzled layout a Q tile arrives in) and writes it with one TMA
+// store per 64 columns; each thread storing its own row would touch 32 lines per store
+// instruction. Partial tiles and fp32 output store rows directly.
+//
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 [384,384+d).
 // P_t (bf16, two per 32-bit column) overwrites the first 64 columns of S_t once S_t is
 // in registers.
@@ -57,12 +62,31 @@ struct Cfg {
   static constexpr int kQChunkBytes = kTileRows * 128;   // one 64-column chunk of a Q tile
   static constexpr int kKVChunkBytes = kBlockKeys * 128;
   // One ring of K/V slots, loaded in the order K_0, V_0, K_1, V_1, ... so the producer
-  // runs about two key blocks ahead of the tensor core.
-  static constexpr int kSlots = D == 64 ? 10 : 5;
-  static constexpr int kSmem = kTilesPerItem * kQBytes + kSlots * kKVBytes;
+  // runs two key blocks (five at d = 64) ahead of the tensor core.
+  static constexpr int kSlots = D == 64 ? 10 : 4;
+  static constexpr int kStageBytes = kTileRows * 128;   // 64 bf16 columns of a tile's O
+  static constexpr int kSmem = kTilesPerItem * kQBytes + kSlots * kKVBytes + kTilesPerItem * kStageBytes;
   static constexpr int kSmemAlloc = kSmem + 1024;        // slack for 1024-byte alignment
   static_assert(kSmemAlloc <= 227 * 1024, "shared memory budget");
 };
+
+// Named barrier over the 128 threads of softmax warpgroup t (ids 1 and 2).
+__device__ __forceinline__ void warpgroup_sync(int t) {
+  if (t == 0) asm volatile("bar.sync 1, 128;" ::: "memory");
+  else asm volatile("bar.sync 2, 128;" ::: "memory");
+}
+
+// TMA store of a 3-D box from shared memory, and the bulk-group waits around it.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int32_t c0, int32_t c1,
+                                             int32_t c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_addr(src)), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 struct Ctrl {
   uint64_t q_full, q_empty;
@@ -79,7 +103,8 @@ struct Ctrl {
 template <int D, typename TOut, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     gva_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                   const __grid_constant__ CUtensorMap map_v, const FwdParams p) {
+                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
+                   const FwdParams p) {
   using C = Cfg<D>;
   constexpr uint32_t NS = C::kSlots;
   extern __shared__ uint8_t smem_raw[];
@@ -87,6 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;                                          // 2 tiles
   uint8_t* sKV = sQ + kTilesPerItem * C::kQBytes;              // NS slots
+  uint8_t* sStage = sKV + NS * C::kKVBytes;                    // O staging, one per tile
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -267,6 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_addr = tmem_addr(tmem, lane_base, col_o(t));
     const float c = p.scale_log2;
     TOut* out = reinterpret_cast<TOut*>(p.out);
+    constexpr bool kBf16Out = sizeof(TOut) == 2;
+    const bool store_issuer = warp == kFirstSoftmaxWarp + 4 * t && lane == 0;  // TMA stores of tile t
     uint32_t sc = 0, oc = 0, vb = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
@@ -468,21 +496,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       // l > 0 for every row with a key; a block-causal row that sees none gets 0 / -inf.
       const float inv_l = l > 0.0f ? 1.0f / (few_keys ? lp : l) : 0.0f;
       const float lse_val = l > 0.0f ? (m_used + log2f(l)) * kLn2 : -CUDART_INF_F;
+      if (kBf16Out && p.out_tma && it.q_rows - t * T >= T) {
+        // a full tile: every one of its T * G rows is a used row of the segment
+        uint8_t* stage = sStage + t * C::kStageBytes;
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t o[32];
-        tmem_ld32_sync(o_addr + ch * 32, o);
-        float x[32];
+        for (int ch = 0; ch < C::kChunks; ++ch) {
+          warpgroup_sync(t);  // the previous store has finished reading the staging buffer
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(o[i]) * inv_l;
-        if (valid) {
-          if (p.out_wide) store_row32_wide<TOut>(orow + ch * 32, x);
-          else store_row32<TOut>(orow + ch * 32, x);
+          for (int h = 0; h < 2; ++h) {  // 32 columns: 4 of the row's eight 16-byte pieces
+            uint32_t o[32];
+            tmem_ld32_sync(o_addr + ch * 64 + h * 32, o);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint32_t w[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                w[k] = pack_bf16x2(__uint_as_float(o[8 * i + 2 * k]) * inv_l,
+                                   __uint_as_float(o[8 * i + 2 * k + 1]) * inv_l);
+              *reinterpret_cast<uint4*>(stage + row * 128 + (((h * 4 + i) ^ (row & 7)) << 4)) =
+                  make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+          fence_proxy_async_smem();
+          warpgroup_sync(t);
+          if (store_issuer) {
+            tma_store_3d(&map_o, stage, ch * 64, it.q_row0 + t * T, it.head_kv * G);
+            bulk_wait_read();
+          }
+        }
+      } else {
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t o[32];
+          tmem_ld32_sync(o_addr + ch * 32, o);
+          float x[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(o[i]) * inv_l;
+          if (valid) {
+            if (p.out_wide) store_row32_wide<TOut>(orow + ch * 32, x);
+            else store_row32<TOut>(orow + ch * 32, x);
+          }
         }
       }
       if (valid) *lrow = lse_val;
     }
     tmem_wait_st();
+    if (store_issuer) bulk_wait_all();  // this CTA's TMA stores are complete before it exits
   }
 
   tcgen05_fence_before();
@@ -495,11 +554,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, typename TOut, bool kCausal>
 cudaError_t launch_impl(const FwdParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                        int grid, cudaStream_t stream) {
+                        const CUtensorMap& mo, int grid, cudaStream_t stream) {
   auto kern = gva_fwd_kernel<D, TOut, kCausal>;
   cudaError_t e = ensure_smem_limit<gva_fwd_kernel<D, TOut, kCausal>>(Cfg<D>::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, Cfg<D>::kSmemAlloc, stream>>>(mq, mk, mv, p);
+  kern<<<grid, kThreads, Cfg<D>::kSmemAlloc, stream>>>(mq, mk, mv, mo, p);
   return cudaGetLastError();
 }
 
@@ -510,20 +569,21 @@ int forward_smem_bytes(int head_dim) {
 }
 
 cudaError_t launch_forward(int head_dim, bool out_f32, const FwdParams& p, const CUtensorMap& map_q,
-                           const CUtensorMap& map_k, const CUtensorMap& map_v, int grid, cudaStream_t stream) {
+                           const CUtensorMap& map_k, const CUtensorMap& map_v, const CUtensorMap& map_o, int grid,
+                           cudaStream_t stream) {
   const bool causal = p.causal_block > 0;
   if (head_dim == 128) {
     if (causal)
-      return out_f32 ? launch_impl<128, float, true>(p, map_q, map_k, map_v, grid, stream)
-                     : launch_impl<128, __nv_bfloat16, true>(p, map_q, map_k, map_v, grid, stream);
-    return out_f32 ? launch_impl<128, float, false>(p, map_q, map_k, map_v, grid, stream)
-                   : launch_impl<128, __nv_bfloat16, false>(p, map_q, map_k, map_v, grid, stream);
+      return out_f32 ? launch_impl<128, float, true>(p, map_q, map_k, map_v, map_o, grid, stream)
+                     : launch_impl<128, __nv_bfloat16, true>(p, map_q, map_k, map_v, map_o, grid, stream);
+    return out_f32 ? launch_impl<128, float, false>(p, map_q, map_k, map_v, map_o, grid, stream)
+                   : launch_impl<128, __nv_bfloat16, false>(p, map_q, map_k, map_v, map_o, grid, stream);
   }
   if (causal)
-    return out_f32 ? launch_impl<64, float, true>(p, map_q, map_k, map_v, grid, stream)
-                   : launch_impl<64, __nv_bfloat16, true>(p, map_q, map_k, map_v, grid, stream);
-  return out_f32 ? launch_impl<64, float, false>(p, map_q, map_k, map_v, grid, stream)
-                 : launch_impl<64, __nv_bfloat16, false>(p, map_q, map_k, map_v, grid, stream);
+    return out_f32 ? launch_impl<64, float, true>(p, map_q, map_k, map_v, map_o, grid, stream)
+                   : launch_impl<64, __nv_bfloat16, true>(p, map_q, map_k, map_v, map_o, grid, stream);
+  return out_f32 ? launch_impl<64, float, false>(p, map_q, map_k, map_v, map_o, grid, stream)
+                 : launch_impl<64, __nv_bfloat16, false>(p, map_q, map_k, map_v, map_o, grid, stream);
 }
 
 }  // namespace gva

@@ -78,6 +78,7 @@ struct FwdParams {
   float scale_log2;         // softmax scale * log2(e)
   int32_t causal_block;     // > 0: block-causal masking within each segment
   int32_t out_wide;         // out is 32-byte aligned: rows are stored with 32-byte stores
+  int32_t out_tma;          // bf16 out with a tensor map: full Q tiles leave through TMA stores
   int* error_flag;
 };
 
@@ -129,8 +130,10 @@ __host__ __device__ inline int item_index(int round, int cta, int grid) {
 constexpr int kErrWaitTimeout = 1;
 
 // Launchers (defined in gva_fwd.cu / gva_merge.cu). They return the launch error.
+// map_o (over out, laid out like map_q) is read only when p.out_tma is set.
 cudaError_t launch_forward(int head_dim, bool out_f32, const FwdParams& p, const CUtensorMap& map_q,
-                           const CUtensorMap& map_k, const CUtensorMap& map_v, int grid, cudaStream_t stream);
+                           const CUtensorMap& map_k, const CUtensorMap& map_v, const CUtensorMap& map_o, int grid,
+                           cudaStream_t stream);
 // The merge runs one persistent CTA per resident slot (as many as fit per SM x sm_count).
 cudaError_t launch_merge(bool in_f32, bool out_f32, const MergeParams& p, int sm_count, cudaStream_t stream);
 // Dynamic shared memory of the merge launch (and its chunk ring slots), or -1 when the

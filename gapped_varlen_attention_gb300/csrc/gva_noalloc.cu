@@ -276,7 +276,8 @@ extern "C" GVA_API gva_status gva_forward_noalloc(
   prm.tokens_per_tile = tpt;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.error_flag = d_error;
-  e = gva::launch_forward(head_dim, out_dtype == GVA_FP32, prm, mq, mk, mv, std::min(n, sms), stream);
+  // out_tma stays 0: rows leave through direct stores and no map over out is needed
+  e = gva::launch_forward(head_dim, out_dtype == GVA_FP32, prm, mq, mk, mv, mq, std::min(n, sms), stream);
   if (e != cudaSuccess) return fail(GVA_ERR_CUDA, "launching the forward kernel: %s", cudaGetErrorString(e));
   return GVA_OK;
 }
