@@ -23,6 +23,7 @@
 // host time on every call of a short launch.
 struct MapCache {
   const void* ptr[4] = {nullptr, nullptr, nullptr, nullptr};
+  int out_dtype = -1;  // the forward's output map (ptr[3]) depends on its dtype too
   CUtensorMap map[4];
   bool valid = false;
 };
@@ -88,18 +89,21 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// A 3-D bf16 tensor map over a packed [rows, heads, d] tensor, viewed as
-// (d, rows, heads) so that a box of (64, box_rows, box_heads) lands in shared memory
-// head-major: smem row = head_in_box * box_rows + row_in_box, 128 bytes per row.
+// A 3-D tensor map over a packed [rows, heads, d] tensor (bf16, or fp32 with `f32`),
+// viewed as (d, rows, heads) so that a box of (128 bytes of d, box_rows, box_heads)
+// lands in shared memory head-major: smem row = head_in_box * box_rows + row_in_box, 128
+// bytes per row.
 gva_status make_map(CUtensorMap* map, const void* base, int64_t rows, int32_t heads, int32_t d, uint32_t box_rows,
-                    uint32_t box_heads, const char* name) {
+                    uint32_t box_heads, const char* name, bool f32 = false) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return fail(GVA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t es = f32 ? 4 : 2;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(heads)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(heads) * d * 2, static_cast<cuuint64_t>(d) * 2};
-  cuuint32_t box[3] = {64, box_rows, box_heads};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(heads) * d * es, static_cast<cuuint64_t>(d) * es};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), box_rows, box_heads};
   cuuint32_t elem[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, elem,
+  CUresult r = enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                   const_cast<void*>(base), dims, strides, box, elem,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(GVA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name, (int)r);
@@ -746,14 +750,13 @@ gva_status gva_forward(gva_plan_t plan, const void* q, const void* k, const void
   if (dev != plan->device)
     return fail(GVA_ERR_INVALID_ARG, "the plan was built on device %d, the current device is %d", plan->device, dev);
   const int32_t tokens_per_tile = gva::kTileRows / plan->group;
-  // bf16 output leaves full tiles through TMA stores, over a map laid out like Q's
-  const bool out_tma = out_dtype == GVA_BF16;
-  const void* o_key = out_tma ? out : nullptr;
+  // full tiles leave through TMA stores, over a map of out laid out like Q's
   CUtensorMap mq, mk, mv, mo;
   {
     std::lock_guard<std::mutex> lock(plan->map_mutex);
     MapCache& c = plan->fwd_maps;
-    if (!(c.valid && c.ptr[0] == q && c.ptr[1] == k && c.ptr[2] == v && c.ptr[3] == o_key)) {
+    if (!(c.valid && c.ptr[0] == q && c.ptr[1] == k && c.ptr[2] == v && c.ptr[3] == out &&
+          c.out_dtype == static_cast<int>(out_dtype))) {
       c.valid = false;
       gva_status s;
       const int64_t krows = has_keys ? plan->total_k : 1;
@@ -764,19 +767,20 @@ gva_status gva_forward(gva_plan_t plan, const void* q, const void* k, const void
         return s;
       if ((s = make_map(&c.map[2], v, krows, plan->num_heads_kv, plan->head_dim, gva::kBlockKeys, 1, "V")) != GVA_OK)
         return s;
-      if (out_tma && (s = make_map(&c.map[3], out, plan->total_q, plan->num_heads_q, plan->head_dim,
-                                   tokens_per_tile, plan->group, "O")) != GVA_OK)
+      if ((s = make_map(&c.map[3], out, plan->total_q, plan->num_heads_q, plan->head_dim, tokens_per_tile,
+                        plan->group, "O", out_dtype == GVA_FP32)) != GVA_OK)
         return s;
       c.ptr[0] = q;
       c.ptr[1] = k;
       c.ptr[2] = v;
-      c.ptr[3] = o_key;
+      c.ptr[3] = out;
+      c.out_dtype = static_cast<int>(out_dtype);
       c.valid = true;
     }
     mq = c.map[0];
     mk = c.map[1];
     mv = c.map[2];
-    mo = out_tma ? c.map[3] : c.map[0];
+    mo = c.map[3];
   }
   const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(plan->head_dim));
   gva::FwdParams prm{};
@@ -785,7 +789,7 @@ gva_status gva_forward(gva_plan_t plan, const void* q, const void* k, const void
   prm.num_items = plan->num_item_slots;
   prm.out = out;
   prm.out_wide = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
-  prm.out_tma = out_tma ? 1 : 0;
+  prm.out_tma = 1;
   prm.lse = lse;
   prm.total_q = plan->total_q;
   prm.num_heads_q = plan->num_heads_q;

@@ -21,10 +21,10 @@
 // block feeds 256 rows. Two tiles ping-pong: while the softmax warps of one tile work,
 // the tensor core runs the other tile's PV and next QK^T.
 //
-// The epilogue of a full tile with bf16 output stages O in shared memory (64 columns at
-// a time, in the 128-byte-swizzled layout a Q tile arrives in) and writes it with one TMA
-// store per 64 columns; each thread storing its own row would touch 32 lines per store
-// instruction. Partial tiles and fp32 output store rows directly.
+// The epilogue of a full tile stages O in shared memory (128 bytes of every row at a
+// time: 64 bf16 or 32 fp32 columns, in the 128-byte-swizzled layout a Q tile arrives in)
+// and writes it with one TMA store per pass; each thread storing its own row would touch
+// 32 lines per store instruction. Partial tiles store rows directly.
 //
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 [384,384+d).
 // P_t (bf16, two per 32-bit column) overwrites the first 64 columns of S_t once S_t is
@@ -64,7 +64,7 @@ struct Cfg {
   // One ring of K/V slots, loaded in the order K_0, V_0, K_1, V_1, ... so the producer
   // runs two key blocks (five at d = 64) ahead of the tensor core.
   static constexpr int kSlots = D == 64 ? 10 : 4;
-  static constexpr int kStageBytes = kTileRows * 128;   // 64 bf16 columns of a tile's O
+  static constexpr int kStageBytes = kTileRows * 128;   // 128 bytes of each row of a tile's O
   static constexpr int kSmem = kTilesPerItem * kQBytes + kSlots * kKVBytes + kTilesPerItem * kStageBytes;
   static constexpr int kSmemAlloc = kSmem + 1024;        // slack for 1024-byte alignment
   static_assert(kSmemAlloc <= 227 * 1024, "shared memory budget");
@@ -496,31 +496,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       // l > 0 for every row with a key; a block-causal row that sees none gets 0 / -inf.
       const float inv_l = l > 0.0f ? 1.0f / (few_keys ? lp : l) : 0.0f;
       const float lse_val = l > 0.0f ? (m_used + log2f(l)) * kLn2 : -CUDART_INF_F;
-      if (kBf16Out && p.out_tma && it.q_rows - t * T >= T) {
-        // a full tile: every one of its T * G rows is a used row of the segment
+      if (p.out_tma && it.q_rows - t * T >= T) {
+        // a full tile: every one of its T * G rows is a used row of the segment. Each
+        // pass stages 128 bytes of every row: 64 bf16 or 32 fp32 columns.
+        constexpr int kCols = kBf16Out ? 64 : 32;
         uint8_t* stage = sStage + t * C::kStageBytes;
 #pragma unroll
-        for (int ch = 0; ch < C::kChunks; ++ch) {
+        for (int ch = 0; ch < D / kCols; ++ch) {
           warpgroup_sync(t);  // the previous store has finished reading the staging buffer
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {  // 32 columns: 4 of the row's eight 16-byte pieces
+          for (int h = 0; h < kCols / 32; ++h) {  // 32 columns per TMEM load
             uint32_t o[32];
-            tmem_ld32_sync(o_addr + ch * 64 + h * 32, o);
+            tmem_ld32_sync(o_addr + ch * kCols + h * 32, o);
+            constexpr int kPieces = kBf16Out ? 4 : 8;  // 16-byte pieces these columns fill
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < kPieces; ++i) {
               uint32_t w[4];
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
-                w[k] = pack_bf16x2(__uint_as_float(o[8 * i + 2 * k]) * inv_l,
-                                   __uint_as_float(o[8 * i + 2 * k + 1]) * inv_l);
-              *reinterpret_cast<uint4*>(stage + row * 128 + (((h * 4 + i) ^ (row & 7)) << 4)) =
+              for (int k = 0; k < 4; ++k) {
+                if constexpr (kBf16Out)
+                  w[k] = pack_bf16x2(__uint_as_float(o[8 * i + 2 * k]) * inv_l,
+                                     __uint_as_float(o[8 * i + 2 * k + 1]) * inv_l);
+                else
+                  w[k] = __float_as_uint(__uint_as_float(o[4 * i + k]) * inv_l);
+              }
+              *reinterpret_cast<uint4*>(stage + row * 128 + (((h * kPieces + i) ^ (row & 7)) << 4)) =
                   make_uint4(w[0], w[1], w[2], w[3]);
             }
           }
           fence_proxy_async_smem();
           warpgroup_sync(t);
           if (store_issuer) {
-            tma_store_3d(&map_o, stage, ch * 64, it.q_row0 + t * T, it.head_kv * G);
+            tma_store_3d(&map_o, stage, ch * kCols, it.q_row0 + t * T, it.head_kv * G);
             bulk_wait_read();
           }
         }

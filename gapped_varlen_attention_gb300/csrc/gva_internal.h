@@ -78,7 +78,7 @@ struct FwdParams {
   float scale_log2;         // softmax scale * log2(e)
   int32_t causal_block;     // > 0: block-causal masking within each segment
   int32_t out_wide;         // out is 32-byte aligned: rows are stored with 32-byte stores
-  int32_t out_tma;          // bf16 out with a tensor map: full Q tiles leave through TMA stores
+  int32_t out_tma;          // out has a tensor map: full Q tiles leave through TMA stores
   int* error_flag;
 };
 
