@@ -77,15 +77,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return fn;
 }
 
+// A map over a packed [rows, heads, d] tensor (bf16, or fp32 with `f32`) whose box is 128
+// bytes of d by box_rows by box_heads, 128-byte swizzled.
 bool encode(CUtensorMap* m, const void* base, int64_t rows, int32_t heads, int32_t d, uint32_t box_rows,
-            uint32_t box_heads) {
+            uint32_t box_heads, bool f32 = false) {
   auto enc = encoder();
   if (enc == nullptr) return false;
+  const cuuint64_t es = f32 ? 4 : 2;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(heads)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(heads) * d * 2, static_cast<cuuint64_t>(d) * 2};
-  cuuint32_t box[3] = {64, box_rows, box_heads};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(heads) * d * es, static_cast<cuuint64_t>(d) * es};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), box_rows, box_heads};
   cuuint32_t elem[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, elem,
+  return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+             dims, strides, box, elem,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -256,11 +260,13 @@ extern "C" GVA_API gva_status gva_forward_noalloc(
   e = cudaMemsetAsync(d_error, 0, sizeof(int), stream);
   if (e != cudaSuccess) return fail(GVA_ERR_CUDA, "clearing the error word: %s", cudaGetErrorString(e));
 
-  CUtensorMap mq, mk, mv;
+  // the maps are host structures passed with the launch: nothing is allocated for them
+  CUtensorMap mq, mk, mv, mo;
   const int64_t krows = total_k > 0 ? total_k : 1;
   if (!encode(&mq, q, total_q, num_heads_q, head_dim, tpt, group) ||
       !encode(&mk, k, krows, num_heads_kv, head_dim, gva::kBlockKeys, 1) ||
-      !encode(&mv, v, krows, num_heads_kv, head_dim, gva::kBlockKeys, 1))
+      !encode(&mv, v, krows, num_heads_kv, head_dim, gva::kBlockKeys, 1) ||
+      !encode(&mo, out, total_q, num_heads_q, head_dim, tpt, group, out_dtype == GVA_FP32))
     return fail(GVA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
   const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
   gva::FwdParams prm{};
@@ -269,6 +275,7 @@ extern "C" GVA_API gva_status gva_forward_noalloc(
   prm.num_items = n;
   prm.out = out;
   prm.out_wide = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
+  prm.out_tma = 1;
   prm.lse = lse;
   prm.total_q = total_q;
   prm.num_heads_q = num_heads_q;
@@ -276,8 +283,7 @@ extern "C" GVA_API gva_status gva_forward_noalloc(
   prm.tokens_per_tile = tpt;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.error_flag = d_error;
-  // out_tma stays 0: rows leave through direct stores and no map over out is needed
-  e = gva::launch_forward(head_dim, out_dtype == GVA_FP32, prm, mq, mk, mv, mq, std::min(n, sms), stream);
+  e = gva::launch_forward(head_dim, out_dtype == GVA_FP32, prm, mq, mk, mv, mo, std::min(n, sms), stream);
   if (e != cudaSuccess) return fail(GVA_ERR_CUDA, "launching the forward kernel: %s", cudaGetErrorString(e));
   return GVA_OK;
 }
