@@ -241,6 +241,36 @@ std::vector<T> balanced_layout(const std::vector<T>& sorted, int grid, Cost cost
   return laid;
 }
 
+// Units of the LSE merge (and of the backward's D = rowsum(dO * O) kernel): runs of at
+// most kMergeRows used rows of one segment. When 16-row units overflow one wave of the
+// merge's resident CTAs (about four per SM), the last wave can hold only a few units,
+// which then run on an otherwise idle GPU; the rows per unit are then chosen so that the
+// units fill the waves they need (each segment's last unit may be shorter: one unit of
+// slack per segment). Units that fit one wave keep 16 rows: smaller ones only add
+// per-unit work.
+void build_merge_units(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int32_t num_segments,
+                       int32_t resident, std::vector<gva::MergeUnit>& units) {
+  int64_t total = 0, n16 = 0;
+  for (int32_t b = 0; b < num_segments; ++b) {
+    total += seqused_q[b];
+    n16 += (seqused_q[b] + gva::kMergeRows - 1) / gva::kMergeRows;
+  }
+  int32_t rows = gva::kMergeRows;
+  if (resident > 0 && n16 > resident) {
+    const int64_t waves = (n16 + resident - 1) / resident;
+    const int64_t slots = waves * resident - num_segments;
+    if (slots >= resident / 2)
+      rows = static_cast<int32_t>(std::min<int64_t>(gva::kMergeRows, std::max<int64_t>(1, (total + slots - 1) / slots)));
+  }
+  units.clear();
+  for (int32_t b = 0; b < num_segments; ++b)
+    for (int32_t r0 = 0; r0 < seqused_q[b]; r0 += rows)
+      units.push_back({cu_seqlens_q[b] + r0, std::min(rows, seqused_q[b] - r0)});
+}
+
+// Merge CTAs resident at once per SM, as the merge launches them for its usual shapes.
+constexpr int32_t kMergeCtasPerSm = 4;
+
 // Shared by gva_plan and gva_plan_ranges once the arguments are validated: segment b's
 // keys are the ranges range_off[b] .. range_off[b+1] of (range_start, range_len).
 // causal_block > 0 (block-causal, one prefix range per segment): each item only gets the
@@ -281,7 +311,6 @@ gva_status build_work(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
   const int32_t tokens_per_item = tokens_per_tile * gva::kTilesPerItem;
   std::vector<gva::WorkItem> items;
   std::vector<double> cost;
-  std::vector<gva::MergeUnit>& units = w.units;
   double& flops = w.flops;
   // keys visible to the row at key position pos (block-causal)
   auto limit_at = [&](int64_t pos, int32_t keys) -> int32_t {
@@ -298,8 +327,6 @@ gva_status build_work(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
     } else {
       flops += 4.0 * head_dim * num_heads_q * static_cast<double>(uq) * static_cast<double>(seg_keys[b]);
     }
-    for (int32_t r0 = 0; r0 < uq; r0 += gva::kMergeRows)
-      units.push_back({cu_seqlens_q[b] + r0, std::min(gva::kMergeRows, uq - r0)});
     for (int32_t hk = 0; hk < num_heads_kv; ++hk) {
       for (int32_t t0 = 0; t0 < uq; t0 += tokens_per_item) {
         gva::WorkItem it{};
@@ -447,7 +474,6 @@ gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
   const int32_t group = num_heads_q / num_heads_kv;
   const std::vector<gva::KeyBlock>& blocks = w.blocks;
   const std::vector<gva::WorkItem>& sorted = w.items;
-  const std::vector<gva::MergeUnit>& units = w.units;
   const std::vector<gva::WorkItem>& bwd_items = w.bwd_items;
   const std::vector<gva::KvUnit>& kv_units = w.kv_units;
   const std::vector<gva::SegRef>& kv_segs = w.kv_segs;
@@ -464,6 +490,9 @@ gva_status build_plan(const int32_t* cu_seqlens_q, const int32_t* seqused_q, int
   if (major != 10 || minor != 3)
     return fail(GVA_ERR_UNSUPPORTED, "this library is built for sm_103a (GB300); device %d is sm_%d%d", dev, major,
                 minor);
+
+  build_merge_units(cu_seqlens_q, seqused_q, num_segments, kMergeCtasPerSm * sms, w.units);
+  const std::vector<gva::MergeUnit>& units = w.units;
 
   struct gva_plan* p = new struct gva_plan();
   p->device = dev;
@@ -711,6 +740,7 @@ gva_status gva_plan_inspect(const int32_t* cu_seqlens_q, const int32_t* seqused_
     std::memcpy(walk, laid.data(), std::min<size_t>(laid.size(), walk_capacity) * sizeof(int32_t));
   summary->num_work_items = static_cast<int32_t>(w.items.size());
   summary->num_key_blocks = static_cast<int32_t>(w.blocks.size());
+  build_merge_units(cu_seqlens_q, seqused_q, num_segments, kMergeCtasPerSm * grid, w.units);
   summary->num_merge_units = static_cast<int32_t>(w.units.size());
   summary->num_bwd_items = static_cast<int32_t>(w.bwd_items.size());
   summary->num_kv_units = static_cast<int32_t>(w.kv_units.size());

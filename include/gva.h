@@ -79,7 +79,8 @@ typedef struct {
   int32_t num_segments, num_heads_q, num_heads_kv, head_dim;
   int64_t total_q, total_k;
   int32_t num_work_items;   /* forward work items (segment, kv head, 2 x 128-row Q tiles) */
-  int32_t num_merge_units;  /* merge work units (up to 16 used rows of one segment) */
+  int32_t num_merge_units;  /* merge work units (up to 16 used rows of one segment, sized so
+                               that the units fill whole waves of about 4 CTAs per SM) */
   int32_t grid_ctas;        /* persistent CTAs one forward launch uses */
   int32_t sm_count;
   double used_flops;        /* 4 * d * Hq * sum_b seqused_q[b] * seqused_k[b] */
@@ -265,7 +266,8 @@ GVA_API gva_status gva_backward(gva_plan_t plan, const void* q, const void* k, c
  * seqused_k, key_range_offsets NULL), or that of gva_plan_ranges (key_range_offsets,
  * key_range_starts, key_range_lengths and total_k; cu_seqlens_k / seqused_k are then
  * not read and causal_block must be 0). causal_block: 0 maskless, > 0 as
- * gva_plan_causal. grid (>= 1): the SM count the work lists are laid out for;
+ * gva_plan_causal. grid (>= 1): the SM count the work lists (and the merge units,
+ * summary->num_merge_units) are laid out for;
  * walk_list selects the list `walk` describes (0 forward items, 1 dQ items, 2 dK / dV
  * units). Fills *summary (backward_ok: always 1) and copies at most *_capacity records
  * into each non-NULL array (8 int32 per record; 2 for kv_segs; one per entry for walk):

@@ -49,6 +49,26 @@ def kv_cost(u):
     return 2.0 + u["n_tiles"]
 
 
+MERGE_CTAS_PER_SM = 4
+
+
+def merge_rows(uq, sms):
+    """Rows per LSE-merge unit: 16 while 16-row units fit one wave of the merge's resident
+    CTAs (4 per SM); else the used rows are spread over the waves those units need,
+    keeping one unit per segment in reserve for the segments' last, shorter units (16
+    rows if that leaves under half a wave)."""
+    total = int(sum(int(q) for q in uq))
+    resident = MERGE_CTAS_PER_SM * sms
+    n16 = sum(-(-int(q) // MERGE_ROWS) for q in uq)
+    if n16 <= resident:
+        return MERGE_ROWS
+    waves = -(-n16 // resident)
+    slots = waves * resident - len(uq)
+    if slots < resident // 2:
+        return MERGE_ROWS
+    return min(MERGE_ROWS, max(1, -(-total // slots)))
+
+
 def check_walk(items, walk, grid, cost=est_cost):
     """Every item is walked exactly once, a CTA's padding comes after its items, and no
     CTA carries more than the average load plus one item."""
@@ -106,7 +126,16 @@ def check_work(g, B=0):
 
     # ---- counts
     assert w["num_key_blocks"] == sum(-(-int(k) // BLOCK_KEYS) for k in uk)
-    assert w["num_merge_units"] == sum(-(-int(q) // MERGE_ROWS) for q in uq)
+    rows = merge_rows(uq, SMS)
+    assert 1 <= rows <= MERGE_ROWS
+    assert w["num_merge_units"] == sum(-(-int(q) // rows) for q in uq)
+    # the units need no more waves of the merge's resident CTAs than 16-row units would,
+    # and 16-row units that fit one wave stay as they are
+    resident = MERGE_CTAS_PER_SM * SMS
+    sixteen = sum(-(-int(q) // MERGE_ROWS) for q in uq)
+    assert -(-w["num_merge_units"] // resident) <= max(1, -(-sixteen // resident))
+    if sixteen <= resident:
+        assert w["num_merge_units"] == sixteen
     pairs = sum(float(limits(int(uq[b]), int(uk[b]), B).sum()) for b in range(nseg))
     want = 4.0 * g.head_dim * g.num_heads_q * pairs
     assert w["used_flops"] == pytest.approx(want, rel=1e-12)
