@@ -38,12 +38,15 @@ def test_tiny_workload_fp32_output():
     check_full(g, o, l, o_ref, l_ref, W.TINY_SENTINEL)
 
 
+@pytest.mark.parametrize("hq,hkv,d", [(8, 2, 128), (12, 4, 128), (24, 1, 128), (5, 1, 64)])
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
-def test_output_only_16_byte_aligned(out_dtype):
-    """An output that is 16- but not 32-byte aligned takes the 16-byte store path; the
-    result is the same as through an aligned buffer, and the elements just before and
-    after the output stay untouched."""
-    g = W.random_geometry(np.random.default_rng(77), 4, 300, 500, 8, 2, 128)
+def test_output_only_16_byte_aligned(out_dtype, hq, hkv, d):
+    """An output that is 16- but not 32-byte aligned: full tiles leave through TMA stores
+    (which need 16 bytes), partial tiles through 16-byte row stores. The result is the
+    same as through an aligned buffer, and the elements just before and after the output
+    stay untouched. With groups that do not divide 128 (3, 24, 5) a TMA box covers only
+    the T * G rows of a tile that hold data."""
+    g = W.random_geometry(np.random.default_rng(77), 4, 300, 500, hq, hkv, d)
     q, k, v = W.make_qkv(g, 77)
     o_ref, l_ref = gpu_forward(g, q, k, v, out_dtype=out_dtype)
     pad = 16 // torch.tensor([], dtype=out_dtype).element_size()
