@@ -166,13 +166,14 @@ GVA_API gva_status gva_plan_causal(const int32_t* cu_seqlens_q, const int32_t* s
  * #18687 "actual behavior" (padded keys must not enter the softmax denominator).
  *
  *   q, k, v   : DEVICE bf16, layouts above, 16-byte aligned, must not alias out/lse
- *   out       : DEVICE, out_dtype (GVA_BF16 or GVA_FP32), [total_q, Hq, d]
- *   lse       : DEVICE fp32 [Hq, total_q]
+ *   out       : DEVICE, out_dtype (GVA_BF16 or GVA_FP32), [total_q, Hq, d], 16-byte
+ *               aligned (full tiles are written by TMA stores, which require it)
+ *   lse       : DEVICE fp32 [Hq, total_q], 16-byte aligned
  *   softmax_scale : s in the formula; <= 0 selects 1/sqrt(head_dim)
  *   stream    : CUDA stream the kernel is enqueued on
  *
- * Only used rows of out / lse are written. Asynchronous; returns GVA_ERR_CUDA if the
- * launch fails. Device-side waits are bounded; a timeout is recorded in the plan's
+ * Only used rows of out / lse are written. Asynchronous; returns GVA_ERR_INVALID_ARG for a
+ * NULL or misaligned pointer and GVA_ERR_CUDA if the launch fails. Device-side waits are bounded; a timeout is recorded in the plan's
  * error word (gva_device_status) instead of hanging.
  */
 GVA_API gva_status gva_forward(gva_plan_t plan, const void* q, const void* k, const void* v, void* out,
