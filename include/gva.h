@@ -323,7 +323,7 @@ GVA_API gva_status gva_device_status(gva_plan_t plan);
 /*
  * gva_forward_noalloc - gva_forward for callers that cannot allocate device memory.
  *
- * The paper has no counterpart for this entry point. It exists for callers that may
+ * The source pages have no counterpart for this entry point. It exists for callers that may
  * not call cudaMalloc: a serving runtime that hands out all device memory from its own
  * pool, code under a fixed memory budget, or a loop that must not take cudaMalloc's
  * implicit device synchronisation. gva_plan allocates a device work list; this call
